@@ -1,0 +1,350 @@
+"""Pins for the CPU oracle: it is checked against things other than itself.
+
+* hand-derived closed forms (tests/golden/closed_form.json);
+* a pure-Python brute force (oracle.brute) on tiny shapes, every position;
+* PyTorch's library scaled_dot_product_attention in fp64 on CPU, called the
+  two ways the decode page calls it (sliced cache with enable_gqa, section
+  4.1; full-length cache with the boolean mask arange(L) <= pos, section
+  2.1/2.3) and the way the prefill page calls it (is_causal for a prompt with
+  no prefix);
+* closed forms: position 0 returns V[0] exactly; identical keys or a zero
+  query return the mean of V[0..pos];
+* invariances: key-row permutation, GQA == repeat-KV MHA, prefill of one
+  token == a decode step, prefix prefill == tail rows of a full prefill.
+
+``test_planted_mistakes_are_caught`` plants plausible mistakes in the oracle
+(monkeypatching its named steps) and checks that the pins above catch each.
+"""
+
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+import torch.nn.functional as F
+
+import oracle
+from oracle import attention as oatt
+from oracle import brute
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "closed_form.json")
+
+
+def _nested(x):
+    if isinstance(x, list):
+        return np.array([_nested(e) for e in x], dtype=np.float64)
+    return float(x)  # handles "nan"
+
+
+def _rand(rng, shape, bf16=True):
+    x = rng.standard_normal(shape).astype(np.float32)
+    if bf16:
+        x = torch.from_numpy(x).to(torch.bfloat16).to(torch.float64).numpy()
+    return x.astype(np.float64)
+
+
+def _poison_after(cache, positions):
+    c = cache.copy()
+    for b, p in enumerate(positions):
+        c[b, :, int(p) + 1:, :] = np.nan
+    return c
+
+
+# ---------------------------------------------------------------- golden ----
+
+def test_golden_closed_forms():
+    with open(GOLDEN) as f:
+        g = json.load(f)
+    for case in g["decode"]:
+        out = oracle.decode(_nested(case["q"]), _nested(case["k_cache"]),
+                            _nested(case["v_cache"]), case["positions"], case["scale"])
+        np.testing.assert_allclose(out, _nested(case["expected"]), rtol=0, atol=1e-12,
+                                   err_msg=case["why"])
+    for case in g["prefill"]:
+        out = oracle.prefill(_nested(case["q"]), _nested(case["k"]), _nested(case["v"]),
+                             case["start_pos"], case["scale"])
+        np.testing.assert_allclose(out, _nested(case["expected"]), rtol=0, atol=1e-12,
+                                   err_msg=case["why"])
+
+
+# ------------------------------------------------------------ brute force ---
+
+@pytest.mark.parametrize("B,Hq,Hkv,D", [(1, 1, 1, 4), (2, 4, 2, 8), (1, 4, 1, 3), (2, 2, 2, 5)])
+def test_brute_force_decode_every_position(B, Hq, Hkv, D):
+    rng = np.random.default_rng(B * 100 + Hq * 10 + D)
+    L = 7
+    for pos in range(L):
+        positions = [pos] * B if B == 1 else [pos, (pos * 3) % L]
+        q = _rand(rng, (B, Hq, D))
+        kc = _rand(rng, (B, Hkv, L, D))
+        vc = _rand(rng, (B, Hkv, L, D))
+        scale = 1.0 / math.sqrt(D)
+        got = oracle.decode(q, kc, vc, positions, scale)
+        want = np.array(brute.decode(q.tolist(), kc.tolist(), vc.tolist(), positions, scale))
+        np.testing.assert_allclose(got, want, rtol=1e-12, atol=1e-12)
+
+
+@pytest.mark.parametrize("S,start_pos,Hq,Hkv,d", [(1, 0, 1, 1, 4), (4, 0, 2, 2, 3),
+                                                  (3, 2, 4, 2, 4), (5, 3, 2, 1, 2)])
+def test_brute_force_prefill(S, start_pos, Hq, Hkv, d):
+    rng = np.random.default_rng(S * 7 + start_pos)
+    T = start_pos + S
+    q = _rand(rng, (S, Hq, d))
+    k = _rand(rng, (T, Hkv, d))
+    v = _rand(rng, (T, Hkv, d))
+    got = oracle.prefill(q, k, v, start_pos, 0.37)
+    want = np.array(brute.prefill(q.tolist(), k.tolist(), v.tolist(), start_pos, 0.37))
+    np.testing.assert_allclose(got, want, rtol=1e-12, atol=1e-12)
+
+
+# ------------------------------------------------------ library SDPA pins ---
+
+def _sdpa_decode_sliced(q, kc, vc, positions, scale):
+    """The decode page's patched call, section 4.1, per sequence."""
+    outs = []
+    for b, p in enumerate(positions):
+        qq = torch.from_numpy(q[b]).view(1, q.shape[1], 1, q.shape[2])
+        kk = torch.from_numpy(kc[b, :, : int(p) + 1]).unsqueeze(0)
+        vv = torch.from_numpy(vc[b, :, : int(p) + 1]).unsqueeze(0)
+        o = F.scaled_dot_product_attention(qq, kk, vv, scale=scale, enable_gqa=True)
+        outs.append(o.view(q.shape[1], q.shape[2]).numpy())
+    return np.stack(outs)
+
+
+def _sdpa_decode_masked(q, kc, vc, positions, scale):
+    """The decode page's original call, section 2.1/2.3: full cache, bool mask."""
+    L = kc.shape[2]
+    outs = []
+    for b, p in enumerate(positions):
+        mask = (torch.arange(L) <= int(p)).view(1, L)
+        qq = torch.from_numpy(q[b]).view(1, q.shape[1], 1, q.shape[2])
+        kk = torch.from_numpy(kc[b]).unsqueeze(0)
+        vv = torch.from_numpy(vc[b]).unsqueeze(0)
+        o = F.scaled_dot_product_attention(qq, kk, vv, attn_mask=mask, scale=scale,
+                                           enable_gqa=True)
+        outs.append(o.view(q.shape[1], q.shape[2]).numpy())
+    return np.stack(outs)
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,D,L", [(1, 16, 8, 128, 300), (3, 8, 2, 64, 64),
+                                          (2, 8, 8, 32, 40), (2, 8, 1, 16, 33)])
+def test_library_sdpa_decode(B, Hq, Hkv, D, L):
+    rng = np.random.default_rng(L + Hq)
+    positions = [int(x) for x in rng.integers(0, L, size=B)]
+    positions[0] = L - 1
+    q = _rand(rng, (B, Hq, D))
+    kc = _rand(rng, (B, Hkv, L, D))
+    vc = _rand(rng, (B, Hkv, L, D))
+    scale = 1.0 / math.sqrt(D)
+    got = oracle.decode(q, kc, vc, positions, scale)
+    np.testing.assert_allclose(got, _sdpa_decode_sliced(q, kc, vc, positions, scale),
+                               rtol=1e-11, atol=1e-12)
+    np.testing.assert_allclose(got, _sdpa_decode_masked(q, kc, vc, positions, scale),
+                               rtol=1e-11, atol=1e-12)
+
+
+def test_masked_full_equals_sliced_with_poisoned_tail():
+    """Section 3 of the decode page: slicing 0..pos is the same as masking."""
+    rng = np.random.default_rng(5)
+    B, Hq, Hkv, D, L = 3, 4, 2, 16, 50
+    positions = [0, 17, 49]
+    q = _rand(rng, (B, Hq, D))
+    kc = _poison_after(_rand(rng, (B, Hkv, L, D)), positions)
+    vc = _poison_after(_rand(rng, (B, Hkv, L, D)), positions)
+    a = oracle.decode(q, kc, vc, positions, 0.25)
+    b = oracle.decode_masked_full(q, kc, vc, positions, 0.25)
+    assert np.all(np.isfinite(a))
+    np.testing.assert_allclose(a, b, rtol=1e-12, atol=1e-13)
+
+
+@pytest.mark.parametrize("S,H,d", [(37, 4, 64), (128, 2, 32)])
+def test_library_sdpa_prefill_no_prefix_is_causal(S, H, d):
+    """Decode page section 5 / prefill page: a prompt with no prefix is plain
+    is_causal attention."""
+    rng = np.random.default_rng(S)
+    q = _rand(rng, (S, H, d))
+    k = _rand(rng, (S, H, d))
+    v = _rand(rng, (S, H, d))
+    scale = 1.0 / math.sqrt(d)
+    got = oracle.prefill(q, k, v, 0, scale)
+    ref = F.scaled_dot_product_attention(
+        torch.from_numpy(q).transpose(0, 1).unsqueeze(0),
+        torch.from_numpy(k).transpose(0, 1).unsqueeze(0),
+        torch.from_numpy(v).transpose(0, 1).unsqueeze(0),
+        is_causal=True, scale=scale).squeeze(0).transpose(0, 1).numpy()
+    np.testing.assert_allclose(got, ref, rtol=1e-11, atol=1e-12)
+
+
+def test_library_sdpa_prefill_with_prefix_gqa():
+    """Prefix prefill: new token i sees keys 0..start_pos+i (bottom-right
+    aligned causal mask), GQA via enable_gqa."""
+    rng = np.random.default_rng(11)
+    S, start_pos, Hq, Hkv, d = 20, 13, 8, 2, 16
+    T = start_pos + S
+    q = _rand(rng, (S, Hq, d))
+    k = _rand(rng, (T, Hkv, d))
+    v = _rand(rng, (T, Hkv, d))
+    mask = torch.arange(T).view(1, T) <= (start_pos + torch.arange(S)).view(S, 1)
+    ref = F.scaled_dot_product_attention(
+        torch.from_numpy(q).transpose(0, 1).unsqueeze(0),
+        torch.from_numpy(k).transpose(0, 1).unsqueeze(0),
+        torch.from_numpy(v).transpose(0, 1).unsqueeze(0),
+        attn_mask=mask, scale=0.3, enable_gqa=True).squeeze(0).transpose(0, 1).numpy()
+    np.testing.assert_allclose(oracle.prefill(q, k, v, start_pos, 0.3), ref,
+                               rtol=1e-11, atol=1e-12)
+
+
+# ------------------------------------------------------------ closed forms ---
+
+def test_position_zero_is_v0_exactly():
+    rng = np.random.default_rng(0)
+    B, Hq, Hkv, D, L = 2, 8, 4, 128, 16
+    q = _rand(rng, (B, Hq, D)) * 50
+    kc = _poison_after(_rand(rng, (B, Hkv, L, D)), [0, 0])
+    vc = _poison_after(_rand(rng, (B, Hkv, L, D)), [0, 0])
+    out = oracle.decode(q, kc, vc, [0, 0], 1.0 / math.sqrt(D))
+    for b in range(B):
+        for h in range(Hq):
+            assert np.array_equal(out[b, h], vc[b, h // 2, 0])
+
+
+def test_identical_keys_or_zero_query_give_mean_of_v():
+    rng = np.random.default_rng(1)
+    B, Hq, Hkv, D, L = 1, 4, 2, 32, 64
+    pos = 40
+    kc = _rand(rng, (B, Hkv, L, D))
+    kc[:, :, : pos + 1, :] = kc[:, :, :1, :]       # every attended key equal
+    vc = _rand(rng, (B, Hkv, L, D))
+    q = _rand(rng, (B, Hq, D))
+    out = oracle.decode(q, kc, vc, [pos], 0.1)
+    mean = vc[0, :, : pos + 1, :].mean(axis=1)
+    for h in range(Hq):
+        np.testing.assert_allclose(out[0, h], mean[h // 2], rtol=1e-12, atol=1e-13)
+    kc2 = _rand(rng, (B, Hkv, L, D))
+    out0 = oracle.decode(np.zeros_like(q), kc2, vc, [pos], 0.1)
+    for h in range(Hq):
+        np.testing.assert_allclose(out0[0, h], mean[h // 2], rtol=1e-12, atol=1e-13)
+
+
+# -------------------------------------------------------------- invariances ---
+
+def test_key_row_permutation_invariance():
+    rng = np.random.default_rng(2)
+    B, Hq, Hkv, D, L = 1, 4, 2, 16, 30
+    pos = 25
+    q = _rand(rng, (B, Hq, D))
+    kc = _rand(rng, (B, Hkv, L, D))
+    vc = _rand(rng, (B, Hkv, L, D))
+    perm = rng.permutation(pos + 1)
+    kp, vp = kc.copy(), vc.copy()
+    kp[:, :, : pos + 1] = kc[:, :, perm]
+    vp[:, :, : pos + 1] = vc[:, :, perm]
+    np.testing.assert_allclose(oracle.decode(q, kc, vc, [pos], 0.2),
+                               oracle.decode(q, kp, vp, [pos], 0.2), rtol=1e-12, atol=1e-13)
+
+
+@pytest.mark.parametrize("g", [2, 4, 8])
+def test_gqa_equals_repeat_kv_mha(g):
+    rng = np.random.default_rng(g)
+    B, Hkv, D, L = 2, 2, 16, 20
+    Hq = g * Hkv
+    positions = [19, 6]
+    q = _rand(rng, (B, Hq, D))
+    kc = _rand(rng, (B, Hkv, L, D))
+    vc = _rand(rng, (B, Hkv, L, D))
+    gqa = oracle.decode(q, kc, vc, positions, 0.25)
+    mha = oracle.decode(q, np.repeat(kc, g, axis=1), np.repeat(vc, g, axis=1), positions, 0.25)
+    np.testing.assert_allclose(gqa, mha, rtol=0, atol=0)
+
+
+def test_prefill_one_token_equals_decode_step():
+    rng = np.random.default_rng(3)
+    start_pos, Hq, Hkv, d = 33, 8, 2, 64
+    T = start_pos + 1
+    q = _rand(rng, (1, Hq, d))
+    k = _rand(rng, (T, Hkv, d))
+    v = _rand(rng, (T, Hkv, d))
+    pre = oracle.prefill(q, k, v, start_pos, 0.125)
+    kc = k.transpose(1, 0, 2)[None]          # [1, Hkv, T, d]
+    vc = v.transpose(1, 0, 2)[None]
+    dec = oracle.decode(q, kc, vc, [start_pos], 0.125)
+    np.testing.assert_allclose(pre, dec, rtol=1e-13, atol=1e-14)
+
+
+def test_prefix_prefill_equals_tail_of_full_prefill():
+    rng = np.random.default_rng(4)
+    start_pos, S, H, d = 9, 7, 3, 8
+    T = start_pos + S
+    q_all = _rand(rng, (T, H, d))
+    k = _rand(rng, (T, H, d))
+    v = _rand(rng, (T, H, d))
+    full = oracle.prefill(q_all, k, v, 0, 0.35)
+    tail = oracle.prefill(q_all[start_pos:], k, v, start_pos, 0.35)
+    np.testing.assert_allclose(tail, full[start_pos:], rtol=1e-13, atol=1e-14)
+
+
+def test_kv_append_writes_only_the_target_rows():
+    B, Hkv, L, D = 3, 2, 9, 4
+    kc = np.full((B, Hkv, L, D), 7.0)
+    vc = np.full((B, Hkv, L, D), -7.0)
+    kn = np.arange(B * Hkv * D, dtype=np.float64).reshape(B, Hkv, D)
+    vn = -kn - 1
+    positions = [0, 8, 4]
+    k2, v2 = oracle.kv_append(kc, vc, kn, vn, positions)
+    want_k, want_v = kc.copy(), vc.copy()
+    for b, p in enumerate(positions):
+        want_k[b, :, p] = kn[b]
+        want_v[b, :, p] = vn[b]
+    assert np.array_equal(k2, want_k) and np.array_equal(v2, want_v)
+    assert np.all(kc == 7.0)  # inputs not modified
+
+
+def test_work_counts():
+    """Algorithmic bytes/flops used by the roofline: hand-counted small cases."""
+    # one sequence at position 3: 4 rows of K and V, 2 KV heads, D=2, bf16
+    assert oracle.decode_bytes([3], Hq=4, Hkv=2, D=2) == 2 * 2 * 4 * 2 * 2 + 2 * 4 * 2 * 2
+    assert oracle.decode_flops([3], Hq=4, D=2) == 4 * 2 * 4 * 4
+    # S=2, start_pos=1: token 0 sees 2 keys, token 1 sees 3 keys
+    assert oracle.prefill_flops(2, 1, H=1, d=2) == 4 * 2 * 5
+
+
+# ------------------------------------------------------- planted mistakes ---
+
+def _pins_pass():
+    """Re-run a compact set of the independent pins; False if any fails."""
+    try:
+        test_golden_closed_forms()
+        test_brute_force_decode_every_position(2, 4, 2, 8)
+        test_brute_force_prefill(3, 2, 4, 2, 4)
+        test_library_sdpa_decode(3, 8, 2, 64, 64)
+        test_library_sdpa_prefill_with_prefix_gqa()
+        test_position_zero_is_v0_exactly()
+    except (AssertionError, IndexError, ValueError):
+        return False
+    return True
+
+
+def test_pins_pass_on_the_real_oracle():
+    assert _pins_pass()
+
+
+@pytest.mark.parametrize("mutant", ["head_mod", "exclusive_range", "top_left_causal",
+                                    "dropped_scale", "keys_as_values", "no_normalise"])
+def test_planted_mistakes_are_caught(monkeypatch, mutant):
+    if mutant == "head_mod":          # h % Hkv instead of h // g
+        monkeypatch.setattr(oatt, "_kv_head", lambda h, g, Hkv: h % Hkv)
+    elif mutant == "exclusive_range":  # 0..pos-1 instead of 0..pos
+        monkeypatch.setattr(oatt, "_attended_rows", lambda p: range(0, max(p, 1)))
+    elif mutant == "top_left_causal":  # mask aligned to the top-left corner
+        monkeypatch.setattr(oatt, "_causal_keys", lambda s, i: range(0, i + 1))
+    elif mutant == "dropped_scale":
+        orig = oatt._attend
+        monkeypatch.setattr(oatt, "_attend", lambda q, K, V, scale: orig(q, K, V, 1.0))
+    elif mutant == "keys_as_values":
+        orig = oatt._attend
+        monkeypatch.setattr(oatt, "_attend", lambda q, K, V, scale: orig(q, K, K, scale))
+    elif mutant == "no_normalise":
+        monkeypatch.setattr(oatt, "_softmax", lambda s: np.exp(s - np.max(s)))
+    assert not _pins_pass(), f"mutant {mutant} slipped past every pin"
