@@ -1,0 +1,507 @@
+#!/usr/bin/env python
+"""Benchmark of the decode/prefill hot path on one GB300 (or N replicas).
+
+Default workload ("streaming"): B=1, Hq=16, Hkv=8, D=128, max_len=8192 bf16
+static cache; one step = 8192 consecutive decode steps from position 0, each
+attn_kv_append (write the step's K/V row) then attn_decode_step (attend rows
+0..pos).  The 16384 launches of a step are captured once into a CUDA graph and
+replayed; inputs for all 8192 positions are resident in HBM before timing.
+L2 is flushed (a 512 MB write) between timed steps, outside the timed events.
+
+value = algorithmic decode bytes (K and V rows 0..pos of every KV head, plus
+q and out) / device time of the step, in GB/s; `steps_per_s` is decode steps
+per second.  Extra legs: per-position decode time (warm and cold L2), the
+ragged B=64 batch, the B=256 g=8 stress batch, and the causal prefill
+workloads (TFLOP/s), each against its roofline.
+
+``--impl reference`` times the fp64 CPU oracle (the only reference this
+method has) on the host cores, on a bounded sample of the same workload.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+STEPS_STREAM = 8192
+HQ, HKV, D, L = 16, 8, 128, 8192
+METRIC = "decode-attn HBM GB/s (% of peak) & steps/s; causal prefill TFLOP/s"
+FLUSH_BYTES = 512 << 20
+
+
+def _args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-legs", action="store_true", help="skip the extra workload legs")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-worker", type=str, default=None, help=argparse.SUPPRESS)
+    return ap.parse_args()
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), float(p["bf16_tflops_sustained"]), "measured"
+    except Exception:
+        return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+def _decode_bytes_stream(steps=STEPS_STREAM):
+    import oracle
+    return sum(oracle.decode_bytes([p], HQ, HKV, D) for p in range(steps))
+
+
+# ------------------------------------------------------------- CPU oracle ---
+
+def cpu_worker(kind: str):
+    """Time the oracle, single-threaded, on a bounded sample of a workload."""
+    import numpy as np
+    import oracle
+    rng = np.random.default_rng(0)
+    if kind == "streaming":
+        sample = list(range(0, STEPS_STREAM, 64))  # every 64th position of the loop
+        k = rng.standard_normal((STEPS_STREAM, HKV, D)).astype(np.float32).astype(np.float64)
+        v = rng.standard_normal((STEPS_STREAM, HKV, D)).astype(np.float32).astype(np.float64)
+        q = rng.standard_normal((STEPS_STREAM, 1, HQ, D)).astype(np.float32).astype(np.float64)
+        kc = k.transpose(1, 0, 2)[None]
+        vc = v.transpose(1, 0, 2)[None]
+        t0 = time.perf_counter()
+        nbytes = 0
+        for p in sample:
+            oracle.decode(q[p], kc[:, :, : p + 1], vc[:, :, : p + 1], [p], 1.0 / math.sqrt(D))
+            nbytes += oracle.decode_bytes([p], HQ, HKV, D)
+        dt = time.perf_counter() - t0
+        print(json.dumps({"value": nbytes / dt / 1e9, "unit": "GB/s", "seconds": dt,
+                          "steps_per_s": len(sample) / dt,
+                          "sample": f"oracle.decode at every 64th position of the 8192-step loop "
+                                    f"({len(sample)} steps, positions 0..8128)"}))
+    else:
+        raise ValueError(kind)
+
+
+def run_cpu_baseline(kind="streaming"):
+    env = dict(os.environ)
+    for var in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+        env[var] = "1"
+    env["CUDA_VISIBLE_DEVICES"] = ""
+    r = subprocess.run([sys.executable, os.path.abspath(__file__), "--cpu-worker", kind],
+                       capture_output=True, text=True, env=env, timeout=600)
+    if r.returncode != 0:
+        return {"error": r.stderr[-400:]}
+    d = json.loads(r.stdout.strip().splitlines()[-1])
+    return {"value": d["value"], "unit": d["unit"], "cores": 1, "kind": "oracle",
+            "sample": d["sample"], "seconds": round(d["seconds"], 2),
+            "steps_per_s": d["steps_per_s"]}
+
+
+# -------------------------------------------------------------- clocks -----
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, mx, reasons = [], 0.0, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = max(mx, float(f[2]))
+            except ValueError:
+                continue
+            for n, val in zip(names, f[5:9]):
+                if val.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+# ------------------------------------------------------------ our arm ------
+
+def _dist():
+    import torch
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if ws > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        torch.cuda.set_device(local)
+    return ws, rank, local
+
+
+def _barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def _max_over_ranks(ws, x: float) -> float:
+    if ws == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+class Stream:
+    """The streaming job: 8192 x (append, decode) captured in one CUDA graph."""
+
+    def __init__(self, torch, ga, synth, decode_only=False, seed=0):
+        self.torch = torch
+        dev = torch.device("cuda")
+        self.q, self.k, self.v, self.pos = synth.streaming_inputs(
+            steps=STEPS_STREAM, Hq=HQ, Hkv=HKV, D=D, seed=seed, device=dev)
+        self.kc = torch.zeros((1, HKV, L, D), dtype=torch.bfloat16, device=dev)
+        self.vc = torch.zeros_like(self.kc)
+        self.ws = ga.decode_workspace(1, HQ, HKV, L, D, device=dev)
+        self.outs = torch.empty((STEPS_STREAM, 1, HQ, D), dtype=torch.bfloat16, device=dev)
+        self.scale = 1.0 / math.sqrt(D)
+        self.ga = ga
+        if decode_only:  # fill the cache once so every position has its rows
+            self._launch(append=True, decode=False)
+            torch.cuda.synchronize()
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            self._launch(append=not decode_only, decode=True)  # eager warm-up
+        torch.cuda.current_stream().wait_stream(s)
+        torch.cuda.synchronize()
+        self.graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.graph):
+            self._launch(append=not decode_only, decode=True)
+        torch.cuda.synchronize()
+        self.launches = STEPS_STREAM * (1 if decode_only else 2)
+
+    def _launch(self, append=True, decode=True):
+        ga = self.ga
+        for s in range(STEPS_STREAM):
+            if append:
+                ga.attn_kv_append(self.k[s], self.v[s], self.pos[s], self.kc, self.vc)
+            if decode:
+                ga.attn_decode_step(self.q[s], self.pos[s], self.kc, self.vc, self.scale,
+                                    out=self.outs[s], workspace=self.ws)
+
+    def replay(self):
+        self.graph.replay()
+
+
+def _time_graph(torch, fn, flush, reps, warm):
+    for _ in range(warm):
+        flush.zero_()
+        fn()
+    torch.cuda.synchronize()
+    times = []
+    for _ in range(reps):
+        flush.zero_()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record()
+        fn()
+        b.record()
+        b.synchronize()
+        times.append(a.elapsed_time(b))
+    return times
+
+
+def _per_position(torch, ga, st, flush, hbm):
+    """Decode time at fixed positions: warm (graph of R back-to-back launches,
+    cache in L2) and cold (each launch preceded by an L2 flush; flush-only
+    time subtracted)."""
+    import oracle
+    R = 50
+    res = {}
+    for p in (100, 1000, 4000, 8000):
+        pos = torch.full((1,), p, dtype=torch.int32, device="cuda")
+        out = torch.empty((1, HQ, D), dtype=torch.bfloat16, device="cuda")
+
+        def one():
+            ga.attn_decode_step(st.q[p], pos, st.kc, st.vc, st.scale, out=out, workspace=st.ws)
+        one()
+        torch.cuda.synchronize()
+        g_warm = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g_warm):
+            for _ in range(R):
+                one()
+        g_cold = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g_cold):
+            for _ in range(R):
+                flush.zero_()
+                one()
+        g_flush = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g_flush):
+            for _ in range(R):
+                flush.zero_()
+        warm = statistics.median(_time_graph(torch, g_warm.replay, flush, 5, 2)) / R
+        cold = (statistics.median(_time_graph(torch, g_cold.replay, flush, 5, 2)) -
+                statistics.median(_time_graph(torch, g_flush.replay, flush, 5, 2))) / R
+        nb = oracle.decode_bytes([p], HQ, HKV, D)
+        res[str(p)] = {"us_warm_l2": round(warm * 1e3, 3), "us_cold_l2": round(cold * 1e3, 3),
+                       "GBs_cold": round(nb / (cold * 1e-3) / 1e9, 1),
+                       "frac_cold": round(nb / (cold * 1e-3) / 1e9 / hbm, 3),
+                       "bytes": nb}
+    return res
+
+
+def _decode_leg(torch, ga, synth, name, flush, hbm):
+    import oracle
+    case = synth.generators.workload_case(name, seed=0, device="cuda")
+    B, Hq, Dd = case.q.shape
+    Hkv, Ll = case.k_cache.shape[1], case.k_cache.shape[2]
+    ga.attn_kv_append(case.k_new, case.v_new, case.positions, case.k_cache, case.v_cache)
+    ws = ga.decode_workspace(B, Hq, Hkv, Ll, Dd)
+    out = torch.empty_like(case.q)
+
+    def one():
+        ga.attn_decode_step(case.q, case.positions, case.k_cache, case.v_cache, case.scale,
+                            out=out, workspace=ws)
+    times = _time_graph(torch, one, flush, 10, 3)
+    ms = statistics.median(times)
+    pos = case.positions.cpu().tolist()
+    nb = oracle.decode_bytes(pos, Hq, Hkv, Dd)
+    fl = oracle.decode_flops(pos, Hq, Dd)
+    r = {"us": round(ms * 1e3, 2), "GBs": round(nb / (ms * 1e-3) / 1e9, 1),
+         "frac_hbm": round(nb / (ms * 1e-3) / 1e9 / hbm, 3),
+         "TFLOPs_fp32_cuda_core": round(fl / (ms * 1e-3) / 1e12, 2), "bytes": nb,
+         "shape": {"B": B, "Hq": Hq, "Hkv": Hkv, "D": Dd, "L": Ll}}
+    del case, ws, out
+    torch.cuda.empty_cache()
+    return r
+
+
+def _prefill_leg(torch, ga, synth, name, flush, tflops_peak):
+    import oracle
+    case = synth.generators.workload_case(name, seed=0, device="cuda")
+    S, Hq, d = case.q.shape
+    out = torch.empty_like(case.q)
+    try:
+        ga.attn_prefill_causal(case.q, case.k, case.v, case.start_pos, case.scale, out=out)
+    except ga.AttnError as e:
+        return {"unavailable": str(e)}
+
+    def one():
+        ga.attn_prefill_causal(case.q, case.k, case.v, case.start_pos, case.scale, out=out)
+    ms = statistics.median(_time_graph(torch, one, flush, 10, 3))
+    fl = oracle.prefill_flops(S, case.start_pos, Hq, d)
+    return {"us": round(ms * 1e3, 2), "TFLOPs": round(fl / (ms * 1e-3) / 1e12, 1),
+            "frac_tensor": round(fl / (ms * 1e-3) / 1e12 / tflops_peak, 3), "flops": fl,
+            "shape": {"S": S, "start_pos": case.start_pos, "H": Hq, "d": d}}
+
+
+def run_ours(args):
+    import torch
+    import gqa_decode_attention_place_gb300 as ga
+    import synth
+
+    ws, rank, local = _dist()
+    hbm, tf_burst, tf_sus, peak_src = _peaks()
+    ga.load_library()
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    st = Stream(torch, ga, synth)
+    nbytes = _decode_bytes_stream()
+
+    # ---- timed region: K replays of the streaming step -------------------
+    for _ in range(max(3, args.warmup)):
+        flush.zero_()
+        st.replay()
+    torch.cuda.synchronize()
+    _barrier(ws)
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local)
+    clocks.start()
+    t_wall = time.perf_counter()
+    ev = []
+    for _ in range(args.steps):
+        flush.zero_()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record()
+        st.replay()
+        b.record()
+        ev.append((a, b))
+    torch.cuda.synchronize()
+    _barrier(ws)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - t_wall
+    clk = clocks.stop()
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    ms = _max_over_ranks(ws, statistics.mean(step_ms))
+    status = ga.attn_read_device_status(st.ws)
+
+    # ---- end to end: host inputs -> device -> step -> host outputs --------
+    h_in = [t.cpu().pin_memory() for t in (st.q, st.k, st.v, st.pos)]
+    h_out = torch.empty(st.outs.shape, dtype=st.outs.dtype).pin_memory()
+    d_in = [st.q, st.k, st.v, st.pos]
+    e2e_ms = []
+    for i in range(args.warmup + args.steps):
+        flush.zero_()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record()
+        for h, dv in zip(h_in, d_in):
+            dv.copy_(h, non_blocking=True)
+        st.replay()
+        h_out.copy_(st.outs, non_blocking=True)
+        b.record()
+        b.synchronize()
+        if i >= args.warmup:
+            e2e_ms.append(a.elapsed_time(b))
+    e2e = _max_over_ranks(ws, statistics.mean(e2e_ms))
+    h2d = sum(t.numel() * t.element_size() for t in h_in)
+    d2h = h_out.numel() * h_out.element_size()
+
+    # ---- roofline of the dominant kernel: decode launches alone -----------
+    dec = Stream(torch, ga, synth, decode_only=True, seed=1)
+    dec_ms = statistics.mean(_time_graph(torch, dec.replay, flush, max(3, args.steps), 3))
+    dec_avg_us = dec_ms * 1e3 / STEPS_STREAM
+    achieved = nbytes / (dec_ms * 1e-3) / 1e9
+    del dec
+
+    value = ws * nbytes / (ms * 1e-3) / 1e9
+    line = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "GB/s",
+        "n_gpus": ws,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) bf16 q/k/v rows)",
+        "config": {"workload": "streaming decode loop: B=1, Hq=16, Hkv=8 (g=2), D=128, "
+                               "max_len=8192, 8192 append+decode steps from position 0",
+                   "B": 1, "Hq": HQ, "Hkv": HKV, "D": D, "max_len": L,
+                   "decode_steps_per_step": STEPS_STREAM,
+                   "l2": "512 MB L2 flush between timed steps; inside a step the 33.5 MB "
+                         "cache stays L2-resident, as the workload does on a 129 MB L2",
+                   "launch": "one CUDA graph of 8192 x (attn_kv_append, attn_decode_step)",
+                   "parallelism": f"replicas x{ws} (independent streams, no collective)"},
+        "steps_per_s": round(ws * STEPS_STREAM / (ms * 1e-3), 1),
+        "us_per_decode_step": round(ms * 1e3 / STEPS_STREAM, 3),
+        "wall_s": round(wall, 3),
+        "gpu_launches": args.steps * st.launches,
+        "device_status": status,
+        "e2e": {"value": round(ws * nbytes / (e2e * 1e-3) / 1e9, 2), "unit": "GB/s",
+                "ms_per_step": round(e2e, 3), "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "roofline": {"kernel": "decode_splitkv_kernel<2>", "bound": "hbm",
+                     "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
+                     "frac": round(achieved / hbm, 3), "traffic": None,
+                     "peak_source": f"{peak_src} hbm_gbs",
+                     "avg_launch_us": round(dec_avg_us, 3),
+                     "bytes_per_launch_avg": nbytes // STEPS_STREAM,
+                     "note": "decode launches alone over positions 0..8191 (graph), "
+                             "cache L2-resident within the loop"},
+    }
+    if clk:
+        line["clocks"] = clk
+    if rank == 0 and not args.no_legs:
+        legs = {"per_position": _per_position(torch, ga, st, flush, hbm)}
+        del st
+        torch.cuda.empty_cache()
+        for name in ("ragged", "stress"):
+            legs[name] = _decode_leg(torch, ga, synth, name, flush, hbm)
+        for name in ("prefill_prefix", "prefill"):
+            legs[name] = _prefill_leg(torch, ga, synth, name, flush, tf_burst)
+        line["legs"] = legs
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = run_cpu_baseline("streaming")
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def run_reference(args):
+    """The oracle, as it stands, timed on the host cores (rank 0 only)."""
+    if int(os.environ.get("RANK", "0")) != 0:
+        return
+    times, vals = [], []
+    info = None
+    for i in range(args.warmup + args.steps):
+        info = run_cpu_baseline("streaming")
+        if "error" in info:
+            print(json.dumps({"impl": "reference", "unavailable": info["error"][-200:]}))
+            return
+        if i >= args.warmup:
+            times.append(info["seconds"])
+            vals.append(info["value"])
+    value = statistics.mean(vals)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
+        "n_gpus": int(os.environ.get("WORLD_SIZE", "1")), "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(statistics.mean(times) * 1e3, 1),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded N(0,1))",
+        "config": {"workload": "streaming decode loop: B=1, Hq=16, Hkv=8 (g=2), D=128, "
+                               "max_len=8192, 8192 append+decode steps from position 0",
+                   "sample": info["sample"]},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1,
+                         "kind": "oracle", "sample": info["sample"]},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = _args()
+    if args.cpu_worker:
+        cpu_worker(args.cpu_worker)
+        return
+    if args.impl == "reference":
+        run_reference(args)
+        return
+    run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

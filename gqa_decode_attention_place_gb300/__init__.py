@@ -1,0 +1,196 @@
+"""Python binding of libgqa_attn.so (include/gqa_attn.h).
+
+Argument marshalling only: every function takes torch CUDA tensors, checks
+their dtype, shape, contiguity and device, and passes raw device pointers and
+the current CUDA stream to the C entry point of the same name.  All compute
+runs in the library's CUDA kernels; there is no fallback path, and a missing
+or unloadable library raises immediately.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import torch
+
+from . import _build
+
+__all__ = [
+    "AttnError", "load_library", "library_path",
+    "attn_kv_append", "attn_decode_workspace_size", "attn_decode_step",
+    "attn_prefill_causal", "attn_read_device_status", "attn_status_string",
+    "attn_last_cuda_error", "decode_workspace",
+]
+
+ATTN_OK = 0
+ATTN_DEV_BAD_POSITION = 0x1
+ATTN_DEV_TIMEOUT = 0x2
+
+_LIB: Optional[ctypes.CDLL] = None
+
+
+class AttnError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        msg = f"{where}: {attn_status_string(code)} (status {code})"
+        if code == 4:
+            msg += f", CUDA error {attn_last_cuda_error()}"
+        super().__init__(msg)
+
+
+def library_path() -> str:
+    return _build.LIBPATH
+
+
+def load_library(build_if_missing: bool = True) -> ctypes.CDLL:
+    """Load libgqa_attn.so (building it in-tree first if allowed and needed)."""
+    global _LIB
+    if _LIB is not None:
+        return _LIB
+    if not os.path.exists(_build.LIBPATH) or (build_if_missing and not _build.up_to_date()):
+        if not build_if_missing:
+            raise RuntimeError(f"{_build.LIBPATH} is missing; run __graft_entry__.build()")
+        _build.build()
+    lib = ctypes.CDLL(_build.LIBPATH)
+    vp, i32, sz, f32 = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t, ctypes.c_float
+    lib.attn_kv_append.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, vp]
+    lib.attn_kv_append.restype = i32
+    lib.attn_decode_workspace_size.argtypes = [i32, i32, i32, i32, i32]
+    lib.attn_decode_workspace_size.restype = sz
+    lib.attn_decode_step.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, i32, f32, vp, vp, sz, vp]
+    lib.attn_decode_step.restype = i32
+    lib.attn_prefill_causal.argtypes = [vp, vp, vp, i32, i32, i32, i32, i32, f32, vp, vp]
+    lib.attn_prefill_causal.restype = i32
+    lib.attn_read_device_status.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32), vp]
+    lib.attn_read_device_status.restype = i32
+    lib.attn_status_string.argtypes = [i32]
+    lib.attn_status_string.restype = ctypes.c_char_p
+    lib.attn_last_cuda_error.argtypes = []
+    lib.attn_last_cuda_error.restype = i32
+    _LIB = lib
+    return lib
+
+
+def attn_status_string(code: int) -> str:
+    return load_library().attn_status_string(int(code)).decode()
+
+
+def attn_last_cuda_error() -> int:
+    return int(load_library().attn_last_cuda_error())
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _check(t: torch.Tensor, name: str, dtype, ndim: int):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dims, got shape {tuple(t.shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def _raise(code: int, where: str):
+    if code != ATTN_OK:
+        raise AttnError(code, where)
+
+
+def attn_kv_append(k_new, v_new, positions, k_cache, v_cache, stream=None) -> None:
+    """Write k_new/v_new [B,Hkv,D] into row positions[b] of k_cache/v_cache
+    [B,Hkv,L,D] (bf16, in place)."""
+    for t, n in ((k_new, "k_new"), (v_new, "v_new")):
+        _check(t, n, torch.bfloat16, 3)
+    for t, n in ((k_cache, "k_cache"), (v_cache, "v_cache")):
+        _check(t, n, torch.bfloat16, 4)
+    _check(positions, "positions", torch.int32, 1)
+    B, Hkv, L, D = k_cache.shape
+    if tuple(v_cache.shape) != (B, Hkv, L, D) or tuple(k_new.shape) != (B, Hkv, D) \
+            or tuple(v_new.shape) != (B, Hkv, D) or positions.shape[0] != B:
+        raise ValueError("attn_kv_append: inconsistent shapes")
+    code = load_library().attn_kv_append(
+        k_new.data_ptr(), v_new.data_ptr(), positions.data_ptr(), k_cache.data_ptr(),
+        v_cache.data_ptr(), B, Hkv, L, D, _stream(stream))
+    _raise(code, "attn_kv_append")
+
+
+def attn_decode_workspace_size(B: int, Hq: int, Hkv: int, L: int, D: int) -> int:
+    return int(load_library().attn_decode_workspace_size(B, Hq, Hkv, L, D))
+
+
+def decode_workspace(B: int, Hq: int, Hkv: int, L: int, D: int, device=None) -> torch.Tensor:
+    """A zero-filled workspace tensor of the size attn_decode_step needs."""
+    n = attn_decode_workspace_size(B, Hq, Hkv, L, D)
+    if n == 0:
+        raise AttnError(2, "attn_decode_workspace_size")
+    return torch.zeros(n, dtype=torch.uint8, device=device or "cuda")
+
+
+def attn_decode_step(q, positions, k_cache, v_cache, scale: float, out=None, workspace=None,
+                     stream=None) -> torch.Tensor:
+    """out[b,h] = softmax(scale q[b,h].K[b,h//g,0..pos_b]) V[b,h//g,0..pos_b]."""
+    _check(q, "q", torch.bfloat16, 3)
+    _check(positions, "positions", torch.int32, 1)
+    for t, n in ((k_cache, "k_cache"), (v_cache, "v_cache")):
+        _check(t, n, torch.bfloat16, 4)
+    B, Hq, D = q.shape
+    Hkv, L = k_cache.shape[1], k_cache.shape[2]
+    if tuple(k_cache.shape) != (B, Hkv, L, D) or tuple(v_cache.shape) != (B, Hkv, L, D) \
+            or positions.shape[0] != B:
+        raise ValueError("attn_decode_step: inconsistent shapes")
+    if out is None:
+        out = torch.empty_like(q)
+    else:
+        _check(out, "out", torch.bfloat16, 3)
+        if tuple(out.shape) != (B, Hq, D):
+            raise ValueError("attn_decode_step: out has the wrong shape")
+    if workspace is None:
+        workspace = decode_workspace(B, Hq, Hkv, L, D, device=q.device)
+    code = load_library().attn_decode_step(
+        q.data_ptr(), positions.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
+        B, Hq, Hkv, L, D, float(scale), out.data_ptr(), workspace.data_ptr(),
+        workspace.numel() * workspace.element_size(), _stream(stream))
+    _raise(code, "attn_decode_step")
+    return out
+
+
+def attn_prefill_causal(q, k, v, start_pos: int, scale: float, out=None,
+                        stream=None) -> torch.Tensor:
+    """Causal prefill: q [S,Hq,d] new tokens, k/v [start_pos+S,Hkv,d]."""
+    _check(q, "q", torch.bfloat16, 3)
+    _check(k, "k", torch.bfloat16, 3)
+    _check(v, "v", torch.bfloat16, 3)
+    S, Hq, d = q.shape
+    T, Hkv = k.shape[0], k.shape[1]
+    if T != start_pos + S or tuple(v.shape) != tuple(k.shape) or k.shape[2] != d:
+        raise ValueError("attn_prefill_causal: inconsistent shapes")
+    if out is None:
+        out = torch.empty_like(q)
+    else:
+        _check(out, "out", torch.bfloat16, 3)
+    code = load_library().attn_prefill_causal(
+        q.data_ptr(), k.data_ptr(), v.data_ptr(), S, int(start_pos), Hq, Hkv, d, float(scale),
+        out.data_ptr(), _stream(stream))
+    _raise(code, "attn_prefill_causal")
+    return out
+
+
+def attn_read_device_status(workspace, stream=None) -> int:
+    """Synchronise, read and clear the decode workspace's device status bits."""
+    bits = ctypes.c_uint32(0)
+    code = load_library().attn_read_device_status(workspace.data_ptr(), ctypes.byref(bits),
+                                                  _stream(stream))
+    if code not in (0, 5):
+        raise AttnError(code, "attn_read_device_status")
+    return int(bits.value)

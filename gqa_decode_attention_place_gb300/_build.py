@@ -1,0 +1,95 @@
+"""Build libgqa_attn.so in-tree with nvcc for sm_103a (GB300).
+
+Each ``csrc/*.cu`` file is compiled to an object in parallel, then linked into
+``lib/libgqa_attn.so`` (CUDA runtime linked statically).  Rebuilds only when a
+source or header is newer than the library.  ``-Xptxas -v`` output (registers,
+spills, shared memory) is kept in ``_build/ptxas.log``.
+"""
+
+from __future__ import annotations
+
+import concurrent.futures as cf
+import glob
+import os
+import shutil
+import subprocess
+import sys
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+ROOT = os.path.dirname(PKG)
+CSRC = os.path.join(PKG, "csrc")
+INCLUDE = os.path.join(ROOT, "include")
+BUILD = os.path.join(ROOT, "_build")
+LIBDIR = os.path.join(PKG, "lib")
+LIBNAME = "libgqa_attn.so"
+LIBPATH = os.path.join(LIBDIR, LIBNAME)
+
+ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
+NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
+                     "--expt-relaxed-constexpr", "-Xptxas", "-v", "-I", INCLUDE, "-I", CSRC]
+
+
+def _nvcc() -> str:
+    for cand in (os.environ.get("NVCC"), shutil.which("nvcc"), "/usr/local/cuda/bin/nvcc"):
+        if cand and os.path.exists(cand):
+            return cand
+    raise RuntimeError("nvcc not found: the CUDA toolkit is required to build libgqa_attn.so")
+
+
+def _sources():
+    return sorted(glob.glob(os.path.join(CSRC, "*.cu")))
+
+
+def _deps():
+    return (_sources() + glob.glob(os.path.join(CSRC, "*.cuh")) + glob.glob(os.path.join(CSRC, "*.h"))
+            + glob.glob(os.path.join(INCLUDE, "*.h")) + [os.path.abspath(__file__)])
+
+
+def up_to_date() -> bool:
+    if not os.path.exists(LIBPATH):
+        return False
+    t = os.path.getmtime(LIBPATH)
+    return all(os.path.getmtime(p) <= t for p in _deps())
+
+
+def _compile(nvcc: str, src: str):
+    obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")
+    cmd = [nvcc] + NVCC_FLAGS + ["-c", src, "-o", obj]
+    r = subprocess.run(cmd, capture_output=True, text=True)
+    return src, obj, r.returncode, r.stdout + r.stderr, " ".join(cmd)
+
+
+def build(force: bool = False, verbose: bool = False) -> str:
+    """Compile and link the library; return its path."""
+    if not force and up_to_date():
+        return LIBPATH
+    nvcc = _nvcc()
+    os.makedirs(BUILD, exist_ok=True)
+    os.makedirs(LIBDIR, exist_ok=True)
+    srcs = _sources()
+    logs = []
+    with cf.ThreadPoolExecutor(max_workers=max(1, min(len(srcs), os.cpu_count() or 4))) as ex:
+        results = list(ex.map(lambda s: _compile(nvcc, s), srcs))
+    failed = False
+    for src, obj, rc, out, cmd in results:
+        logs.append(f"$ {cmd}\n{out}")
+        if rc != 0:
+            failed = True
+            sys.stderr.write(f"nvcc failed on {src}:\n{out}\n")
+    with open(os.path.join(BUILD, "ptxas.log"), "w") as f:
+        f.write("\n".join(logs))
+    if failed:
+        raise RuntimeError("CUDA compilation failed (see _build/ptxas.log)")
+    tmp = LIBPATH + ".tmp"
+    link = [nvcc] + ARCH + ["-shared", "-o", tmp] + [r[1] for r in results]
+    r = subprocess.run(link, capture_output=True, text=True)
+    if r.returncode != 0:
+        raise RuntimeError(f"link failed:\n{r.stdout}{r.stderr}")
+    os.replace(tmp, LIBPATH)
+    if verbose:
+        print(f"built {LIBPATH}")
+    return LIBPATH
+
+
+if __name__ == "__main__":
+    build(force="--force" in sys.argv, verbose=True)

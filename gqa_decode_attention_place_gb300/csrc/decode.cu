@@ -1,0 +1,544 @@
+// decode.cu -- split-KV decode attention over a static KV cache with GQA.
+//
+// What it computes ("MiniCPM4 `forward_step` Attention Performance Fix",
+// sections 3 and 4.1): for every sequence b and query head h,
+//   out[b,h,:] = softmax_j(scale * q[b,h,:] . K[b,h/g,j,:]) V[b,h/g,j,:]
+// over cache rows j = 0..positions[b] only (the slice replaces the
+// full-length boolean mask of section 2.1, so the work follows position+1 and
+// not max_len, sections 2.4 and 6.4).
+//
+// How (GB300 design, not the page's: the page calls PyTorch SDPA):
+//  * The attended rows of every (sequence, KV head) pair -- a "segment" -- are
+//    cut into 64-row tiles.  All tiles of all segments form one flat list,
+//    and CTA c of the persistent grid (one CTA per SM) takes the contiguous
+//    range [c*T/G, (c+1)*T/G) of it.  The split is computed on the device from
+//    `positions`, so the launch does not depend on the positions and the
+//    load is balanced to within one tile however ragged the batch is.
+//  * One producer thread streams K and V tiles with 1-D bulk copies (TMA) into
+//    a 4-stage shared-memory ring guarded by mbarriers.  Each tile is read
+//    from HBM once and serves all g query heads of its KV head.
+//  * Eight consumer warps each take 8 keys of a tile, two at a time (one per
+//    half-warp; a lane holds 8 of the 128 dims).  q.k partial sums of the g
+//    heads are reduced across the 16 lanes with a transposing butterfly
+//    (each shuffle step halves the number of heads still carried), and the
+//    softmax is kept online in fp32 (running max and sum per head, in base 2
+//    with scale*log2(e) folded into q).
+//  * When a CTA finishes its part of a segment it merges its warps.  If it
+//    covered the whole segment it writes the output; otherwise it stores a
+//    partial (max, sum, unnormalised o) and takes a ticket; the CTA that
+//    arrives last combines the partials of that segment and writes the output
+//    (the split-KV combine pass, fused, with no spin-wait).
+#include <cfloat>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace gqa {
+namespace {
+
+constexpr int kD = 128;
+constexpr int kTile = 64;                          // keys per pipeline stage
+constexpr int kStages = 4;
+constexpr int kCWarps = 8;                         // consumer warps
+constexpr int kKeysPerWarp = kTile / kCWarps;      // 8
+constexpr int kIters = kKeysPerWarp / 2;           // 4 (two keys per warp step)
+constexpr int kThreads = (kCWarps + 1) * 32;       // + one producer warp
+constexpr int kConsumers = kCWarps * 32;
+constexpr int kRowBytes = kD * 2;
+constexpr int kTileBytes = kTile * kRowBytes;      // 16 KB
+constexpr int kMaxB = 8192;
+constexpr int kMaxGrid = 1024;
+constexpr float kLog2e = 1.4426950408889634f;
+
+struct Params {
+  const uint16_t* q;
+  const int32_t* positions;
+  const uint8_t* k_cache;
+  const uint8_t* v_cache;
+  uint16_t* out;
+  uint32_t* status;
+  uint32_t* counters;
+  float* part_ml;
+  float* part_o;
+  int B, Hq, Hkv, L;
+  float qscale;  // scale * log2(e)
+};
+
+__device__ __forceinline__ void consumer_bar() {
+  asm volatile("bar.sync 1, %0;" ::"n"(kConsumers) : "memory");
+}
+
+// Position of flat tile t within (sequence, KV head, tile) order.
+struct Walk {
+  int b, kvh, k, ntiles, n;  // n = attended rows of sequence b
+};
+
+__device__ __forceinline__ void walk_init(Walk& w, long long t, const int* prefix,
+                                          const int32_t* positions, int B, int Hkv) {
+  int lo = 0, hi = B - 1;  // largest b with Hkv*prefix[b] <= t
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if ((long long)Hkv * prefix[mid] <= t) lo = mid; else hi = mid - 1;
+  }
+  w.b = lo;
+  w.ntiles = prefix[lo + 1] - prefix[lo];
+  const long long off = t - (long long)Hkv * prefix[lo];
+  w.kvh = (int)(off / w.ntiles);
+  w.k = (int)(off % w.ntiles);
+  w.n = positions[lo] + 1;
+}
+
+__device__ __forceinline__ void walk_next(Walk& w, const int* prefix, const int32_t* positions,
+                                          int B, int Hkv) {
+  if (++w.k < w.ntiles) return;
+  w.k = 0;
+  if (++w.kvh < Hkv) return;
+  w.kvh = 0;
+  do { ++w.b; } while (w.b < B && prefix[w.b + 1] == prefix[w.b]);
+  if (w.b < B) {
+    w.ntiles = prefix[w.b + 1] - prefix[w.b];
+    w.n = positions[w.b] + 1;
+  }
+}
+
+// CTA whose tile range [c*T/G, (c+1)*T/G) contains flat tile t.
+__device__ __forceinline__ int cta_of(long long t, long long T, int G) {
+  return (int)(((unsigned long long)(t + 1) * G + T - 1) / T) - 1;
+}
+
+template <int G> struct Log2;
+template <> struct Log2<1> { static constexpr int v = 0; };
+template <> struct Log2<2> { static constexpr int v = 1; };
+template <> struct Log2<4> { static constexpr int v = 2; };
+template <> struct Log2<8> { static constexpr int v = 3; };
+
+// Sum of acc[h] over the 16 lanes of a half-warp, for every head at once.
+// Step with offset `off` keeps half of the heads and ships the other half to
+// the partner lane, so after log2(G) steps each lane carries one head:
+// head = l16 >> (4 - log2 G).  The remaining steps are a plain butterfly.
+template <int G>
+__device__ __forceinline__ float reduce16(float (&acc)[G], int l16) {
+  constexpr int LG = Log2<G>::v;
+#pragma unroll
+  for (int st = 0; st < LG; ++st) {
+    const int off = 8 >> st;
+    const int n = G >> (st + 1);
+    const bool upper = (l16 & off) != 0;
+#pragma unroll
+    for (int i = 0; i < n; ++i) {
+      const float keep = upper ? acc[n + i] : acc[i];
+      const float send = upper ? acc[i] : acc[n + i];
+      acc[i] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+    }
+  }
+  float v = acc[0];
+#pragma unroll
+  for (int off = 8 >> LG; off >= 1; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+  return v;
+}
+
+__device__ __forceinline__ void unpack8(const uint4& u, float (&f)[8]) {
+  f[0] = bf16lo(u.x); f[1] = bf16hi(u.x);
+  f[2] = bf16lo(u.y); f[3] = bf16hi(u.y);
+  f[4] = bf16lo(u.z); f[5] = bf16hi(u.z);
+  f[6] = bf16lo(u.w); f[7] = bf16hi(u.w);
+}
+
+template <int G>
+__global__ void __launch_bounds__(kThreads, 1) decode_splitkv_kernel(const Params p) {
+  constexpr int LG = Log2<G>::v;
+  extern __shared__ __align__(1024) uint8_t smem[];
+  uint8_t* stages = smem;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kStages * 2 * kTileBytes);
+  int* misc = reinterpret_cast<int*>(bars + 2 * kStages);  // [0] abort [1] last [8..15] scan
+  float* merge_ml = reinterpret_cast<float*>(misc + 16);   // [kCWarps][G][2]
+  float* merge_o = merge_ml + kCWarps * G * 2;             // [kCWarps][G][kD]
+  int* prefix = reinterpret_cast<int*>(merge_o + kCWarps * G * kD);  // [B+1]
+
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5, lane = tid & 31;
+  const int B = p.B, Hkv = p.Hkv, L = p.L;
+  volatile int* abort_flag = misc;
+
+  if (tid == 0) {
+#pragma unroll
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(smem_u32(&bars[s]), 1);                // full: producer arrival + bytes
+      mbar_init(smem_u32(&bars[kStages + s]), kCWarps);  // empty: one arrival per warp
+    }
+    misc[0] = 0;
+    misc[1] = 0;
+    fence_mbar_init();
+  }
+
+  // ---- tiles per sequence and their exclusive prefix sum (every CTA) ------
+  int carry = 0;
+  for (int base = 0; base < B; base += kConsumers) {
+    const int b = base + tid;
+    int v = 0;
+    if (tid < kConsumers && b < B) {
+      const int pos = p.positions[b];
+      if (pos >= 0 && pos < L) {
+        v = pos / kTile + 1;  // ceil((pos + 1) / kTile)
+      } else if (b % gridDim.x == blockIdx.x) {
+        // out-of-range position: flag it and make the sequence's output NaN
+        set_status(p.status, ATTN_DEV_BAD_POSITION);
+        uint4 nan4 = make_uint4(0x7fc07fc0u, 0x7fc07fc0u, 0x7fc07fc0u, 0x7fc07fc0u);
+        uint4* o4 = reinterpret_cast<uint4*>(p.out + (size_t)b * p.Hq * kD);
+        for (int i = 0; i < p.Hq * kD / 8; ++i) o4[i] = nan4;
+      }
+    }
+    int x = v;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, x, off);
+      if (lane >= off) x += y;
+    }
+    if (lane == 31 && warp < kCWarps) misc[8 + warp] = x;
+    __syncthreads();
+    int before = 0, chunk = 0;
+#pragma unroll
+    for (int w = 0; w < kCWarps; ++w) {
+      const int s = misc[8 + w];
+      before += (w < warp) ? s : 0;
+      chunk += s;
+    }
+    if (tid < kConsumers && b < B) prefix[b] = carry + before + x - v;
+    carry += chunk;
+    __syncthreads();
+  }
+  if (tid == 0) prefix[B] = carry;
+  __syncthreads();
+
+  const long long T = (long long)Hkv * carry;  // total tiles
+  const int Gd = gridDim.x;
+  const long long t0 = T * blockIdx.x / Gd;
+  const long long t1 = T * (blockIdx.x + 1) / Gd;
+  if (t0 >= t1) return;
+
+  // ------------------------------------------------------------- producer --
+  if (warp == kCWarps) {
+    if (lane == 0) {
+      Walk w;
+      walk_init(w, t0, prefix, p.positions, B, Hkv);
+      long long i = 0;
+      for (long long t = t0; t < t1; ++t, ++i) {
+        const int s = (int)(i % kStages);
+        const uint32_t u = (uint32_t)(i / kStages);
+        if (i >= kStages && !mbar_wait(smem_u32(&bars[kStages + s]), (u & 1u) ^ 1u, abort_flag)) {
+          *abort_flag = 1;
+          set_status(p.status, ATTN_DEV_TIMEOUT);
+          break;
+        }
+        const int rows = min(kTile, w.n - w.k * kTile);
+        const uint32_t bytes = (uint32_t)rows * kRowBytes;
+        const size_t row0 = ((size_t)w.b * Hkv + w.kvh) * (size_t)L + (size_t)w.k * kTile;
+        const uint32_t full = smem_u32(&bars[s]);
+        mbar_arrive_expect_tx(full, 2u * bytes);
+        bulk_g2s(smem_u32(stages + (size_t)s * 2 * kTileBytes), p.k_cache + row0 * kRowBytes,
+                 bytes, full);
+        bulk_g2s(smem_u32(stages + (size_t)s * 2 * kTileBytes + kTileBytes),
+                 p.v_cache + row0 * kRowBytes, bytes, full);
+        walk_next(w, prefix, p.positions, B, Hkv);
+      }
+    }
+    return;
+  }
+
+  // ------------------------------------------------------------ consumers --
+  const int half = lane >> 4, l16 = lane & 15;
+  const int hd = l16 >> (4 - LG);  // head whose score this lane ends up with
+  Walk w;
+  walk_init(w, t0, prefix, p.positions, B, Hkv);
+
+  float qf[G][8], o[G][8];
+  float m_run = -INFINITY, l_run = 0.f;
+
+  auto load_q = [&]() {
+    const uint16_t* qb = p.q + ((size_t)w.b * p.Hq + (size_t)w.kvh * G) * kD + l16 * 8;
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+      const uint4 u = *reinterpret_cast<const uint4*>(qb + (size_t)h * kD);
+      float f[8];
+      unpack8(u, f);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) qf[h][j] = f[j] * p.qscale;
+    }
+  };
+  auto reset_acc = [&]() {
+    m_run = -INFINITY;
+    l_run = 0.f;
+#pragma unroll
+    for (int h = 0; h < G; ++h)
+#pragma unroll
+      for (int j = 0; j < 8; ++j) o[h][j] = 0.f;
+  };
+  load_q();
+  reset_acc();
+
+  long long i = 0;
+  for (long long t = t0; t < t1; ++t, ++i) {
+    const int s = (int)(i % kStages);
+    const uint32_t u = (uint32_t)(i / kStages);
+    if (!mbar_wait(smem_u32(&bars[s]), u & 1u, abort_flag)) {
+      *abort_flag = 1;
+      set_status(p.status, ATTN_DEV_TIMEOUT);
+      break;
+    }
+    const int rows = min(kTile, w.n - w.k * kTile);
+    const uint8_t* Ks = stages + (size_t)s * 2 * kTileBytes;
+    const uint8_t* Vs = Ks + kTileBytes;
+
+    // scores of this warp's 8 keys (two per step), log2 domain
+    float sc[kIters];
+#pragma unroll
+    for (int it = 0; it < kIters; ++it) {
+      const int key = warp * kKeysPerWarp + it * 2 + half;
+      const uint4 kv = *reinterpret_cast<const uint4*>(Ks + key * kRowBytes + l16 * 16);
+      float kf[8];
+      unpack8(kv, kf);
+      float acc[G];
+#pragma unroll
+      for (int h = 0; h < G; ++h) {
+        float a = 0.f;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) a = fmaf(qf[h][j], kf[j], a);
+        acc[h] = a;
+      }
+      const float sv = reduce16<G>(acc, l16);
+      sc[it] = (key < rows) ? sv : -INFINITY;
+    }
+
+    // online softmax update for head hd
+    float mx = sc[0];
+#pragma unroll
+    for (int it = 1; it < kIters; ++it) mx = fmaxf(mx, sc[it]);
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+    const float m_new = fmaxf(m_run, mx);
+    const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
+    const float alpha = ex2(m_run - m_use);
+    float pr[kIters], ps = 0.f;
+#pragma unroll
+    for (int it = 0; it < kIters; ++it) {
+      pr[it] = ex2(sc[it] - m_use);
+      ps += pr[it];
+    }
+    ps += __shfl_xor_sync(0xffffffffu, ps, 16);
+    l_run = l_run * alpha + ps;
+    m_run = m_new;
+
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+      const float a = __shfl_sync(0xffffffffu, alpha, h << (4 - LG));
+#pragma unroll
+      for (int j = 0; j < 8; ++j) o[h][j] *= a;
+    }
+
+    // o += p * v
+#pragma unroll
+    for (int it = 0; it < kIters; ++it) {
+      const int key = warp * kKeysPerWarp + it * 2 + half;
+      const uint4 vv = *reinterpret_cast<const uint4*>(Vs + key * kRowBytes + l16 * 16);
+      float ph[G];
+#pragma unroll
+      for (int h = 0; h < G; ++h)
+        ph[h] = __shfl_sync(0xffffffffu, pr[it], (half << 4) | (h << (4 - LG)));
+      if (key < rows) {
+        float vf[8];
+        unpack8(vv, vf);
+#pragma unroll
+        for (int h = 0; h < G; ++h)
+#pragma unroll
+          for (int j = 0; j < 8; ++j) o[h][j] = fmaf(ph[h], vf[j], o[h][j]);
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(smem_u32(&bars[kStages + s]));
+
+    // ---- end of this CTA's part of the segment: merge and emit ------------
+    if (w.k == w.ntiles - 1 || t == t1 - 1) {
+      const int seg = w.b * Hkv + w.kvh;
+      const long long seg_t0 = (long long)Hkv * prefix[w.b] + (long long)w.kvh * w.ntiles;
+      const long long seg_t1 = seg_t0 + w.ntiles;
+      const bool whole = seg_t0 >= t0 && seg_t1 <= t1;
+      const int ct = tid;  // 0..255
+
+#pragma unroll
+      for (int h = 0; h < G; ++h)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) o[h][j] += __shfl_xor_sync(0xffffffffu, o[h][j], 16);
+      if (half == 0) {
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+          float4* dst = reinterpret_cast<float4*>(merge_o + ((warp * G + h) * kD + l16 * 8));
+          dst[0] = make_float4(o[h][0], o[h][1], o[h][2], o[h][3]);
+          dst[1] = make_float4(o[h][4], o[h][5], o[h][6], o[h][7]);
+        }
+        if (l16 == (hd << (4 - LG))) {
+          merge_ml[(warp * G + hd) * 2 + 0] = m_run;
+          merge_ml[(warp * G + hd) * 2 + 1] = l_run;
+        }
+      }
+      consumer_bar();
+
+      const int slot = blockIdx.x + seg;
+      uint16_t* out_seg = p.out + ((size_t)w.b * p.Hq + (size_t)w.kvh * G) * kD;
+      for (int idx = ct; idx < G * kD; idx += kConsumers) {
+        const int h = idx / kD, d = idx % kD;
+        float M = -INFINITY;
+#pragma unroll
+        for (int ww = 0; ww < kCWarps; ++ww) M = fmaxf(M, merge_ml[(ww * G + h) * 2]);
+        float Ls = 0.f, Os = 0.f;
+#pragma unroll
+        for (int ww = 0; ww < kCWarps; ++ww) {
+          const float e = ex2(merge_ml[(ww * G + h) * 2] - M);
+          Ls = fmaf(merge_ml[(ww * G + h) * 2 + 1], e, Ls);
+          Os = fmaf(merge_o[(ww * G + h) * kD + d], e, Os);
+        }
+        if (whole) {
+          __nv_bfloat16 r = __float2bfloat16_rn(Os / Ls);
+          out_seg[h * kD + d] = *reinterpret_cast<uint16_t*>(&r);
+        } else {
+          p.part_o[((size_t)slot * G + h) * kD + d] = Os;
+          if (d == 0) {
+            p.part_ml[((size_t)slot * G + h) * 2 + 0] = M;
+            p.part_ml[((size_t)slot * G + h) * 2 + 1] = Ls;
+          }
+        }
+      }
+      if (!whole) {
+        const int c_first = cta_of(seg_t0, T, Gd);
+        const int c_last = cta_of(seg_t1 - 1, T, Gd);
+        consumer_bar();
+        if (ct == 0) {
+          __threadfence();
+          const unsigned old = atomicAdd(&p.counters[seg], 1u);
+          misc[1] = (old == (unsigned)(c_last - c_first)) ? 1 : 0;
+        }
+        consumer_bar();
+        if (misc[1]) {
+          __threadfence();
+          for (int idx = ct; idx < G * kD; idx += kConsumers) {
+            const int h = idx / kD, d = idx % kD;
+            float M = -INFINITY;
+            for (int c = c_first; c <= c_last; ++c)
+              M = fmaxf(M, __ldcg(&p.part_ml[((size_t)(c + seg) * G + h) * 2]));
+            float Ls = 0.f, Os = 0.f;
+            for (int c = c_first; c <= c_last; ++c) {
+              const size_t sl = (size_t)(c + seg) * G + h;
+              const float e = ex2(__ldcg(&p.part_ml[sl * 2]) - M);
+              Ls = fmaf(__ldcg(&p.part_ml[sl * 2 + 1]), e, Ls);
+              Os = fmaf(__ldcg(&p.part_o[sl * kD + d]), e, Os);
+            }
+            __nv_bfloat16 r = __float2bfloat16_rn(Os / Ls);
+            out_seg[h * kD + d] = *reinterpret_cast<uint16_t*>(&r);
+          }
+          if (ct == 0) p.counters[seg] = 0u;  // ready for the next launch
+        }
+      }
+      consumer_bar();  // merge buffers are free again
+      reset_acc();
+    }
+    walk_next(w, prefix, p.positions, B, Hkv);
+    if (w.k == 0 && t + 1 < t1) load_q();
+  }
+
+  if (*abort_flag) {
+    // give copies that may still be in flight time to land before exit
+    const uint64_t t_start = globaltimer_ns();
+    while (globaltimer_ns() - t_start < 2000000ull) {
+    }
+  }
+}
+
+int g_num_sms[64];
+
+int num_sms() {
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64) dev = 0;
+  if (g_num_sms[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+      n = 148;
+    g_num_sms[dev] = n;
+  }
+  return g_num_sms[dev];
+}
+
+template <int G>
+size_t smem_bytes(int B) {
+  return (size_t)kStages * 2 * kTileBytes + 2 * kStages * sizeof(uint64_t) + 16 * sizeof(int) +
+         (size_t)kCWarps * G * 2 * sizeof(float) + (size_t)kCWarps * G * kD * sizeof(float) +
+         (size_t)(B + 1) * sizeof(int);
+}
+
+template <int G>
+cudaError_t launch_g(const Params& p, cudaStream_t stream) {
+  const size_t smem = smem_bytes<G>(kMaxB);
+  static bool configured[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev >= 0 && dev < 64 && !configured[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(decode_splitkv_kernel<G>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    configured[dev] = true;
+  }
+  const int grid = min(kMaxGrid, num_sms());
+  decode_splitkv_kernel<G><<<grid, kThreads, smem_bytes<G>(p.B), stream>>>(p);
+  return cudaGetLastError();
+}
+
+size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+}  // namespace
+
+DecodeWorkspace decode_workspace_layout(int B, int Hq, int Hkv, int D) {
+  DecodeWorkspace w{};
+  const int g = Hq / Hkv;
+  w.slots = kMaxGrid + B * Hkv;
+  w.status_off = 0;
+  w.counters_off = 256;
+  w.ml_off = align256(w.counters_off + (size_t)B * Hkv * sizeof(uint32_t));
+  w.o_off = align256(w.ml_off + (size_t)w.slots * g * 2 * sizeof(float));
+  w.total = align256(w.o_off + (size_t)w.slots * g * D * sizeof(float));
+  return w;
+}
+
+bool decode_supported(int B, int Hq, int Hkv, int L, int D) {
+  const int g = Hq / Hkv;
+  return D == kD && (g == 1 || g == 2 || g == 4 || g == 8) && B >= 1 && B <= kMaxB && L >= 1 &&
+         L <= (1 << 24);
+}
+
+cudaError_t launch_decode(const void* q, const int32_t* positions, const void* k_cache,
+                          const void* v_cache, int B, int Hq, int Hkv, int L, int D,
+                          float scale, void* out, void* workspace, cudaStream_t stream) {
+  const DecodeWorkspace ws = decode_workspace_layout(B, Hq, Hkv, D);
+  uint8_t* base = static_cast<uint8_t*>(workspace);
+  Params p;
+  p.q = static_cast<const uint16_t*>(q);
+  p.positions = positions;
+  p.k_cache = static_cast<const uint8_t*>(k_cache);
+  p.v_cache = static_cast<const uint8_t*>(v_cache);
+  p.out = static_cast<uint16_t*>(out);
+  p.status = reinterpret_cast<uint32_t*>(base + ws.status_off);
+  p.counters = reinterpret_cast<uint32_t*>(base + ws.counters_off);
+  p.part_ml = reinterpret_cast<float*>(base + ws.ml_off);
+  p.part_o = reinterpret_cast<float*>(base + ws.o_off);
+  p.B = B;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.L = L;
+  p.qscale = scale * kLog2e;
+  switch (Hq / Hkv) {
+    case 1: return launch_g<1>(p, stream);
+    case 2: return launch_g<2>(p, stream);
+    case 4: return launch_g<4>(p, stream);
+    case 8: return launch_g<8>(p, stream);
+  }
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace gqa

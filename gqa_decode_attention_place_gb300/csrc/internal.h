@@ -1,0 +1,30 @@
+// internal.h -- launchers behind the C ABI (host side).  Arguments reaching
+// these have been validated by capi.cu.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace gqa {
+
+cudaError_t launch_kv_append(const void* k_new, const void* v_new, const int32_t* positions,
+                             void* k_cache, void* v_cache, int B, int Hkv, int L, int D,
+                             cudaStream_t stream);
+
+// Decode workspace layout (bytes), shared by the size query and the launcher.
+struct DecodeWorkspace {
+  size_t status_off, counters_off, ml_off, o_off, total;
+  int slots;
+};
+DecodeWorkspace decode_workspace_layout(int B, int Hq, int Hkv, int D);
+
+cudaError_t launch_decode(const void* q, const int32_t* positions, const void* k_cache,
+                          const void* v_cache, int B, int Hq, int Hkv, int L, int D,
+                          float scale, void* out, void* workspace, cudaStream_t stream);
+
+cudaError_t launch_prefill(const void* q, const void* k, const void* v, int S, int start_pos,
+                           int Hq, int Hkv, int d, float scale, void* out,
+                           cudaStream_t stream);
+
+}  // namespace gqa

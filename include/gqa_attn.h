@@ -1,0 +1,156 @@
+/*
+ * gqa_attn.h -- C ABI of libgqa_attn.so: in-place static-KV-cache GQA decode
+ * attention and causal prefill over a cached prefix, for NVIDIA GB300
+ * (sm_103a).
+ *
+ * Where the operations come from (page title, section):
+ *   - "MiniCPM4 `forward_step` Attention Performance Fix", section 4.1: each
+ *     decode step writes the new key/value row of every KV head in place into
+ *     a preallocated static cache [B, Hkv, max_len, D] at position_id, then
+ *     attends the query heads (GQA, enable_gqa) over cache rows
+ *     0..position_id only -- no boolean mask and no full-length copy
+ *     (section 3).  Sections 2.4 and 6.4: the per-step cost must grow with
+ *     position_id + 1, not with max_len.
+ *   - "step14_3 -- batched attention", sections "problem" and
+ *     "F.scaled_dot_product_attention": prefill of S new tokens whose K/V
+ *     include the cached prefix, token-major layout [tokens, heads, d_head].
+ *
+ * Conventions shared by every call:
+ *   - All tensor pointers are DEVICE pointers owned by the caller.  The library
+ *     never allocates, frees or keeps device memory.
+ *   - Tensors are bf16 (raw 16-bit storage, `const void*`), dense, row-major,
+ *     with the shapes given per call.  Every tensor pointer must be 16-byte
+ *     aligned.
+ *   - GQA: query head h reads KV head h / g, g = Hq / Hkv (contiguous groups,
+ *     the repeat-KV convention).
+ *   - Every call is asynchronous on `stream` and returns an int status
+ *     (ATTN_OK or an ATTN_ERR_* code).  Argument errors are found on the host
+ *     before anything is launched; nothing is then written.  ATTN_ERR_CUDA means
+ *     a launch failed; attn_last_cuda_error() returns the CUDA error code.
+ *   - Errors that only the device can see (a position outside [0, max_len))
+ *     never trap: the affected sequence is skipped, decode writes NaN to its
+ *     output rows, and a bit is set in the device status word kept in the
+ *     decode workspace (read it with attn_read_device_status).
+ */
+#ifndef GQA_ATTN_H
+#define GQA_ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Return codes. */
+#define ATTN_OK                0
+#define ATTN_ERR_INVALID_ARG   1  /* null pointer, non-positive size, Hq % Hkv != 0,
+                                     pointer not 16-byte aligned, start_pos < 0 */
+#define ATTN_ERR_UNSUPPORTED   2  /* a size this build has no kernel for (see each call) */
+#define ATTN_ERR_WORKSPACE     3  /* workspace null or smaller than attn_decode_workspace_size() */
+#define ATTN_ERR_CUDA          4  /* a CUDA runtime call or launch failed */
+#define ATTN_ERR_DEVICE        5  /* attn_read_device_status: the device flagged a fault */
+
+/* Bits of the device status word (attn_read_device_status(..., &bits)). */
+#define ATTN_DEV_BAD_POSITION  0x1u  /* some positions[b] was outside [0, max_len) */
+#define ATTN_DEV_TIMEOUT       0x2u  /* a pipeline wait gave up (the kernel returned early) */
+
+/*
+ * attn_kv_append -- the in-place cache write of the decode page, section 4.1
+ * (key_cache[:, :, position_id, :] = key_states; same for values), with one
+ * position per sequence.
+ *
+ *   k_new, v_new : [B, Hkv, D] bf16, the new rows.
+ *   positions    : [B] int32, device memory; row positions[b] of every KV head
+ *                  of sequence b is overwritten.
+ *   k_cache,
+ *   v_cache      : [B, Hkv, L, D] bf16, modified in place.  Every other byte
+ *                  is left untouched (bit-exact copy of the new rows).
+ *   D            : multiple of 8 (16-byte rows), 8 <= D <= 256.
+ *
+ * A position outside [0, L) skips that sequence's write (no other effect;
+ * attn_decode_step with the same positions reports it).
+ */
+int attn_kv_append(const void* k_new, const void* v_new, const int32_t* positions,
+                   void* k_cache, void* v_cache,
+                   int B, int Hkv, int L, int D, cudaStream_t stream);
+
+/*
+ * attn_decode_workspace_size -- bytes of device workspace attn_decode_step
+ * needs for these sizes (split-KV partial results, per-(sequence, KV head)
+ * arrival counters and the device status word).  Returns 0 if the sizes are
+ * invalid or unsupported.  The workspace must be zero-filled before its first
+ * use (e.g. cudaMemsetAsync).  Every call leaves its arrival counters at zero
+ * again, so later calls with the same (B, Hq, Hkv, D) can reuse it as is; zero
+ * it again before using it with other sizes, or after a call that reported
+ * ATTN_DEV_TIMEOUT.  Calls that share a workspace must not overlap in time.
+ */
+size_t attn_decode_workspace_size(int B, int Hq, int Hkv, int L, int D);
+
+/*
+ * attn_decode_step -- sliced decode attention of the decode page, sections 3
+ * and 4.1: for every sequence b and query head h,
+ *     out[b,h,:] = softmax_j(scale * q[b,h,:] . K[b,h/g,j,:]) V[b,h/g,j,:]
+ * over j = 0..positions[b] inclusive.  Rows above positions[b] are never read
+ * (they may hold anything, NaN included).  Call attn_kv_append first for the
+ * step's new row (the page writes the row, then attends).
+ *
+ *   q         : [B, Hq, D] bf16 (one query token per sequence).
+ *   positions : [B] int32, device memory.
+ *   k_cache,
+ *   v_cache   : [B, Hkv, L, D] bf16.
+ *   scale     : fp32 score scale (the page's default is 1/sqrt(D)).
+ *   out       : [B, Hq, D] bf16 (= [B, Hq*D]), fp32 softmax and accumulation,
+ *               rounded to nearest even.
+ *   workspace : device buffer of at least attn_decode_workspace_size(...)
+ *               bytes, zero-filled before first use (see above).
+ *
+ * Supported: D == 128; g = Hq / Hkv in {1, 2, 4, 8}; 1 <= B <= 8192;
+ * 1 <= L <= 2^24.  Work is split over the attended rows only, so the cost of
+ * a step follows sum_b (positions[b] + 1), not B * L.
+ */
+int attn_decode_step(const void* q, const int32_t* positions,
+                     const void* k_cache, const void* v_cache,
+                     int B, int Hq, int Hkv, int L, int D, float scale,
+                     void* out, void* workspace, size_t workspace_bytes,
+                     cudaStream_t stream);
+
+/*
+ * attn_prefill_causal -- causal prefill over a cached prefix (prefill page,
+ * section "F.scaled_dot_product_attention"; decode page section 5: batch
+ * prefill is causal).  New token i (absolute position start_pos + i) attends
+ * keys 0..start_pos + i: the causal mask aligned to the bottom-right corner.
+ *
+ *   q         : [S, Hq, d] bf16, the S new tokens (token-major).
+ *   k, v      : [start_pos + S, Hkv, d] bf16, cached prefix rows first.
+ *   out       : [S, Hq, d] bf16 (= [S, Hq*d]).
+ *
+ * Supported: d == 64; g = Hq / Hkv >= 1; S >= 0 (S == 0 does nothing);
+ * start_pos >= 0; start_pos + S < 2^31.  QK^T and PV run on the tcgen05
+ * tensor cores (bf16 operands, fp32 accumulation in tensor memory).
+ */
+int attn_prefill_causal(const void* q, const void* k, const void* v,
+                        int S, int start_pos, int Hq, int Hkv, int d, float scale,
+                        void* out, cudaStream_t stream);
+
+/*
+ * attn_read_device_status -- synchronise `stream`, read the device status
+ * word from a decode workspace into *bits (ATTN_DEV_* flags), clear it, and
+ * return ATTN_OK if no bit was set, ATTN_ERR_DEVICE if one was, or
+ * ATTN_ERR_INVALID_ARG / ATTN_ERR_CUDA.  `bits` may be NULL.
+ */
+int attn_read_device_status(void* workspace, uint32_t* bits, cudaStream_t stream);
+
+/* Human-readable name of a status code (static string; never NULL). */
+const char* attn_status_string(int status);
+
+/* CUDA error code (cudaError_t as int) of the last ATTN_ERR_CUDA on this host
+ * thread, 0 if none. */
+int attn_last_cuda_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GQA_ATTN_H */

@@ -1,0 +1,203 @@
+"""Decode step (attn_kv_append then attn_decode_step) against the fp64 oracle.
+
+Covers the five decode workloads' shapes (the single step at position 100,
+the 8192-step streaming loop, the ragged B=64 batch, the B=256 g=8 stress
+batch with peaky keys), tile/split boundaries, position 0, out-of-range
+positions, NaN-poisoned rows past each position (any over-read would show up
+as NaN), every supported group size, workspace reuse, and the largest batch.
+"""
+
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import gqa_decode_attention_place_gb300 as ga
+import oracle
+import synth
+from _helpers import assert_attn_close, bits, f64
+
+pytestmark = pytest.mark.gpu
+
+
+def _oracle_rows(case, bs, heads=None):
+    """Oracle output for sequences `bs` (all heads, or `heads`), computed from
+    the pre-append cache and the new rows (call before the kernels run)."""
+    Hq = case.q.shape[1]
+    Hkv = case.k_cache.shape[1]
+    out = {}
+    for b in bs:
+        p = int(case.positions[b])
+        kc = f64(case.k_cache[b:b + 1, :, : p + 1])
+        vc = f64(case.v_cache[b:b + 1, :, : p + 1])
+        kc, vc = oracle.kv_append(kc, vc, f64(case.k_new[b:b + 1]), f64(case.v_new[b:b + 1]), [p])
+        hs = list(range(Hq)) if heads is None else heads
+        rows = oracle.decode_rows(f64(case.q[b:b + 1]), kc, vc, [p], case.scale,
+                                  [(0, h) for h in hs])
+        for h, r in zip(hs, rows):
+            out[(b, h)] = r
+    assert Hkv >= 1
+    return out
+
+
+def _run_step(case, workspace=None):
+    ga.attn_kv_append(case.k_new, case.v_new, case.positions, case.k_cache, case.v_cache)
+    out = ga.attn_decode_step(case.q, case.positions, case.k_cache, case.v_cache, case.scale,
+                              workspace=workspace)
+    torch.cuda.synchronize()
+    return out
+
+
+def _check(case, want, out, what):
+    keys = sorted(want)
+    got = np.stack([f64(out[b, h]) for b, h in keys])
+    ref = np.stack([want[k] for k in keys])
+    return assert_attn_close(got, ref, what)
+
+
+def test_single_step_workload():
+    """B=1, Hq=16, Hkv=8, rows 0..99 filled, new row at position 100."""
+    case = synth.generators.workload_case("single_step", seed=1, device="cuda")
+    want = _oracle_rows(case, [0])
+    out = _run_step(case)
+    _check(case, want, out, "single_step")
+
+
+@pytest.mark.parametrize("g", [1, 2, 4, 8])
+def test_tile_and_split_boundaries_poisoned(g):
+    Hkv = 2
+    positions = [0, 1, 62, 63, 64, 65, 127, 128, 129, 1000, 4095, 4096, 8191]
+    case = synth.decode_case(B=len(positions), Hq=g * Hkv, Hkv=Hkv, D=128, L=8192,
+                             positions=positions, fill="all", poison=True, seed=g,
+                             device="cuda")
+    want = _oracle_rows(case, range(len(positions)))
+    out = _run_step(case)
+    _check(case, want, out, f"boundaries g={g}")
+
+
+def test_position_zero_is_v0_bit_exact():
+    case = synth.decode_case(B=3, Hq=16, Hkv=8, D=128, L=64, positions=[0, 0, 0],
+                             fill="all", poison=True, seed=5, device="cuda")
+    out = _run_step(case)
+    for h in range(16):
+        assert torch.equal(bits(out[:, h]), bits(case.v_new[:, h // 2]))
+
+
+def test_ragged_workload_sampled():
+    """B=64, Hq=32, Hkv=8, positions uniform in [0, 8191], every row N(0,1)."""
+    case = synth.generators.workload_case("ragged", seed=2, device="cuda")
+    pos = case.positions.cpu().numpy()
+    order = np.argsort(pos)
+    bs = sorted(set([int(order[0]), int(order[1]), int(order[-1]), int(order[-2])] +
+                    [int(x) for x in np.random.default_rng(0).choice(64, 8, replace=False)]))
+    want = _oracle_rows(case, bs)
+    out = _run_step(case)
+    assert torch.isfinite(out.float()).all()
+    _check(case, want, out, "ragged")
+
+
+def test_ragged_small_full_oracle_poisoned():
+    case = synth.decode_case(B=16, Hq=32, Hkv=8, D=128, L=700, positions="uniform",
+                             fill="all", poison=True, seed=9, device="cuda")
+    want = _oracle_rows(case, range(16))
+    out = _run_step(case)
+    _check(case, want, out, "ragged small")
+
+
+def test_stress_workload_sampled():
+    """B=256, Hq=64, Hkv=8 (g=8), all at position 8191, 1% of key rows x8."""
+    case = synth.generators.workload_case("stress", seed=3, device="cuda")
+    bs = [0, 97, 255]
+    want = _oracle_rows(case, bs)
+    out = _run_step(case)
+    assert torch.isfinite(out.float()).all()
+    _check(case, want, out, "stress")
+    del case
+    torch.cuda.empty_cache()
+
+
+def test_peaky_keys_small_full_oracle():
+    case = synth.decode_case(B=4, Hq=64, Hkv=8, D=128, L=1500, positions=[1499, 700, 64, 3],
+                             fill="all", peaky=0.01, poison=True, seed=4, device="cuda")
+    want = _oracle_rows(case, range(4))
+    out = _run_step(case)
+    _check(case, want, out, "peaky")
+
+
+def test_streaming_workload_sampled_steps():
+    """8192 consecutive append+decode steps from position 0 (B=1, Hq=16, Hkv=8)."""
+    steps, Hq, Hkv, D, L = 8192, 16, 8, 128, 8192
+    q, k, v, pos = synth.streaming_inputs(steps=steps, Hq=Hq, Hkv=Hkv, D=D, seed=11,
+                                          device="cuda")
+    kc = torch.zeros((1, Hkv, L, D), dtype=torch.bfloat16, device="cuda")
+    vc = torch.zeros_like(kc)
+    ws = ga.decode_workspace(1, Hq, Hkv, L, D)
+    outs = torch.empty((steps, 1, Hq, D), dtype=torch.bfloat16, device="cuda")
+    scale = 1.0 / math.sqrt(D)
+    for s in range(steps):
+        ga.attn_kv_append(k[s], v[s], pos[s], kc, vc)
+        ga.attn_decode_step(q[s], pos[s], kc, vc, scale, out=outs[s], workspace=ws)
+    torch.cuda.synchronize()
+    assert ga.attn_read_device_status(ws) == 0
+    kk = f64(k[:, 0])   # [steps, Hkv, D]: row s of the cache is step s's k
+    vv = f64(v[:, 0])
+    for s in [0, 1, 63, 64, 65, 100, 1000, 4000, 8000, 8191]:
+        # cache state after the appends of steps 0..s: row j holds step j's k/v
+        kc_o = kk[: s + 1].transpose(1, 0, 2)[None]
+        vc_o = vv[: s + 1].transpose(1, 0, 2)[None]
+        want = oracle.decode(f64(q[s]), kc_o, vc_o, [s], scale)
+        assert_attn_close(f64(outs[s]), want, f"streaming step {s}")
+
+
+def test_out_of_range_positions_flag_and_nan():
+    case = synth.decode_case(B=4, Hq=16, Hkv=8, D=128, L=256, positions=[10, 256, -3, 255],
+                             fill="all", seed=6, device="cuda")
+    ws = ga.decode_workspace(4, 16, 8, 256, 128)
+    want = _oracle_rows(case, [0, 3])
+    out = _run_step(case, workspace=ws)
+    assert torch.isnan(out[1].float()).all() and torch.isnan(out[2].float()).all()
+    _check(case, want, out, "valid rows next to invalid ones")
+    assert ga.attn_read_device_status(ws) & ga.ATTN_DEV_BAD_POSITION
+    assert ga.attn_read_device_status(ws) == 0  # cleared by the read
+
+
+def test_workspace_reuse_across_calls():
+    """Counters are left at zero, so one workspace serves call after call of
+    the same sizes (re-zeroed when the sizes change)."""
+    ws = ga.decode_workspace(32, 32, 8, 4096, 128)
+    for seed, (B, positions) in enumerate([(32, "uniform"), (32, [4095] * 32),
+                                           (32, "uniform"), (5, [4095, 0, 64, 2000, 3]),
+                                           (5, [3, 4095, 64, 2000, 1])]):
+        if seed == 3:
+            ws.zero_()
+        case = synth.decode_case(B=B, Hq=32, Hkv=8, D=128, L=4096, positions=positions,
+                                 fill="all", poison=True, seed=100 + seed, device="cuda")
+        want = _oracle_rows(case, range(min(B, 6)))
+        out = _run_step(case, workspace=ws)
+        _check(case, want, out, f"reuse call {seed}")
+    assert ga.attn_read_device_status(ws) == 0
+
+
+def test_max_batch_tiny_positions():
+    """B=8192 (the largest batch): exercises the multi-chunk position scan."""
+    B, L = 8192, 4
+    case = synth.decode_case(B=B, Hq=8, Hkv=4, D=128, L=L, positions="uniform", fill="all",
+                             poison=True, seed=12, device="cuda")
+    bs = [0, 1, 255, 256, 4097, 8191]
+    want = _oracle_rows(case, bs)
+    out = _run_step(case)
+    assert torch.isfinite(out.float()).all()
+    _check(case, want, out, "B=8192")
+
+
+def test_single_row_cache_and_odd_scale():
+    case = synth.decode_case(B=2, Hq=4, Hkv=1, D=128, L=1, positions=[0, 0], fill="all",
+                             seed=13, device="cuda", scale=3.7)
+    want = _oracle_rows(case, [0, 1])
+    out = _run_step(case)
+    _check(case, want, out, "L=1")
+    case = synth.decode_case(B=2, Hq=8, Hkv=2, D=128, L=300, positions=[299, 150],
+                             fill="all", seed=14, device="cuda", scale=0.01)
+    want = _oracle_rows(case, [0, 1])
+    _check(case, want, _run_step(case), "scale 0.01")
