@@ -10,8 +10,8 @@
 // How (GB300 design, not the page's: the page calls PyTorch SDPA):
 //  * The attended rows of every (sequence, KV head) pair -- a "segment" -- are
 //    cut into 64-row tiles.  All tiles of all segments form one flat list,
-//    and CTA c of the persistent grid (one CTA per SM) takes the contiguous
-//    range [c*T/G, (c+1)*T/G) of it.  The split is computed on the device from
+//    and CTA c of the persistent grid (one CTA per SM; G = min(grid, T)) takes
+//    the contiguous range [c*T/G, (c+1)*T/G) of it.  The split is computed on the device from
 //    `positions`, so the launch does not depend on the positions and the
 //    load is balanced to within one tile however ragged the batch is.
 //  * One producer thread streams K and V tiles with 1-D bulk copies (TMA) into
@@ -211,10 +211,12 @@ __global__ void __launch_bounds__(kThreads, 1) decode_splitkv_kernel(const Param
   __syncthreads();
 
   const long long T = (long long)Hkv * carry;  // total tiles
-  const int Gd = gridDim.x;
+  // Only min(grid, T) CTAs take work, so every working CTA gets >= 1 tile and
+  // the CTAs covering a segment are exactly cta_of(first)..cta_of(last).
+  const int Gd = (int)min((long long)gridDim.x, T);
+  if ((int)blockIdx.x >= Gd) return;
   const long long t0 = T * blockIdx.x / Gd;
   const long long t1 = T * (blockIdx.x + 1) / Gd;
-  if (t0 >= t1) return;
 
   // ------------------------------------------------------------- producer --
   if (warp == kCWarps) {

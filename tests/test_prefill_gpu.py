@@ -1,0 +1,94 @@
+"""Causal prefill over a cached prefix (tcgen05 kernel) against the fp64 oracle.
+
+Covers both prefill workloads (512 new tokens over a 2048-token prefix; 2048
+tokens from scratch; 32 heads of d=64), query tiles and prefixes that are not
+multiples of the 128-row tile, a single new token, GQA head sharing and the
+empty problem.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import gqa_decode_attention_place_gb300 as ga
+import oracle
+import synth
+from _helpers import assert_attn_close, f64
+
+pytestmark = pytest.mark.gpu
+
+
+def _run(case):
+    out = ga.attn_prefill_causal(case.q, case.k, case.v, case.start_pos, case.scale)
+    torch.cuda.synchronize()
+    return out
+
+
+def _full_check(case, what):
+    want = oracle.prefill(f64(case.q), f64(case.k), f64(case.v), case.start_pos, case.scale)
+    got = f64(_run(case))
+    return assert_attn_close(got, want, what)
+
+
+def _sampled_check(case, rows, what):
+    want = oracle.prefill_rows(f64(case.q), f64(case.k), f64(case.v), case.start_pos,
+                               case.scale, rows)
+    out = _run(case)
+    got = np.stack([f64(out[i, h]) for i, h in rows])
+    assert torch.isfinite(out.float()).all()
+    return assert_attn_close(got, want, what)
+
+
+@pytest.mark.parametrize("S,start_pos,Hq,Hkv", [
+    (128, 0, 1, 1),      # one tile, no prefix
+    (1, 0, 2, 2),        # a single token
+    (100, 0, 2, 2),      # ragged single tile
+    (129, 0, 2, 1),      # tile + 1 row, GQA g=2
+    (300, 37, 4, 4),     # prefix not tile aligned
+    (1, 500, 4, 2),      # one new token over a prefix (== a decode step)
+    (128, 128, 2, 2),    # everything tile aligned
+    (200, 127, 8, 2),    # GQA g=4, prefix one short of a tile
+    (64, 129, 3, 1),     # g=3
+])
+def test_small_cases_full_oracle(S, start_pos, Hq, Hkv):
+    case = synth.prefill_case(S=S, start_pos=start_pos, Hq=Hq, Hkv=Hkv, d=64,
+                              seed=S + start_pos, device="cuda")
+    _full_check(case, f"S={S} start_pos={start_pos} Hq={Hq} Hkv={Hkv}")
+
+
+def test_prefill_prefix_workload():
+    """32 heads, d=64, 2048 cached prefix tokens + 512 new tokens."""
+    case = synth.generators.workload_case("prefill_prefix", seed=1, device="cuda")
+    rng = np.random.default_rng(1)
+    rows = [(int(i), int(h)) for i, h in zip(rng.integers(0, 512, 600), rng.integers(0, 32, 600))]
+    rows += [(i, 5) for i in range(512)] + [(0, h) for h in range(32)] + [(511, h) for h in range(32)]
+    _sampled_check(case, rows, "prefill_prefix")
+
+
+def test_prefill_workload():
+    """32 heads, d=64, 2048 tokens, no prefix (plain causal attention)."""
+    case = synth.generators.workload_case("prefill", seed=2, device="cuda")
+    rng = np.random.default_rng(2)
+    rows = [(int(i), int(h)) for i, h in zip(rng.integers(0, 2048, 800), rng.integers(0, 32, 800))]
+    rows += [(i, 17) for i in range(0, 2048, 3)] + [(0, h) for h in range(32)]
+    rows += [(2047, h) for h in range(32)] + [(127, 0), (128, 0), (1023, 31)]
+    _sampled_check(case, rows, "prefill")
+
+
+def test_first_token_is_v0_and_empty_problem():
+    case = synth.prefill_case(S=5, start_pos=0, Hq=2, Hkv=2, d=64, seed=9, device="cuda")
+    out = _run(case)
+    # token 0 sees key 0 only: softmax over one entry is exactly 1
+    assert torch.equal(out[0].view(torch.int16), case.v[0].view(torch.int16))
+    empty = synth.prefill_case(S=0, start_pos=10, Hq=2, Hkv=2, d=64, seed=1, device="cuda")
+    ga.attn_prefill_causal(empty.q, empty.k, empty.v, empty.start_pos, empty.scale)
+
+
+def test_prefill_matches_decode_path():
+    """One new token over a prefix through both kernels (both against the
+    oracle's definition, and against each other)."""
+    start_pos, H, D = 1000, 8, 64
+    case = synth.prefill_case(S=1, start_pos=start_pos, Hq=H, Hkv=H, d=D, seed=4, device="cuda")
+    out = _run(case)
+    want = oracle.prefill(f64(case.q), f64(case.k), f64(case.v), start_pos, case.scale)
+    assert_attn_close(f64(out), want, "S=1 prefill")
