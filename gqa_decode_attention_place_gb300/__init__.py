@@ -21,7 +21,7 @@ __all__ = [
     "AttnError", "load_library", "library_path",
     "attn_kv_append", "attn_decode_workspace_size", "attn_decode_step",
     "attn_prefill_causal", "attn_read_device_status", "attn_status_string",
-    "attn_last_cuda_error", "decode_workspace",
+    "attn_last_cuda_error", "decode_workspace", "attn_decode_step_noalloc",
 ]
 
 ATTN_OK = 0
@@ -61,6 +61,8 @@ def load_library(build_if_missing: bool = True) -> ctypes.CDLL:
     lib.attn_decode_workspace_size.restype = sz
     lib.attn_decode_step.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, i32, f32, vp, vp, sz, vp]
     lib.attn_decode_step.restype = i32
+    lib.attn_decode_step_noalloc.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, i32, f32, vp, vp]
+    lib.attn_decode_step_noalloc.restype = i32
     lib.attn_prefill_causal.argtypes = [vp, vp, vp, i32, i32, i32, i32, i32, f32, vp, vp]
     lib.attn_prefill_causal.restype = i32
     lib.attn_read_device_status.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32), vp]
@@ -162,6 +164,32 @@ def attn_decode_step(q, positions, k_cache, v_cache, scale: float, out=None, wor
         B, Hq, Hkv, L, D, float(scale), out.data_ptr(), workspace.data_ptr(),
         workspace.numel() * workspace.element_size(), _stream(stream))
     _raise(code, "attn_decode_step")
+    return out
+
+
+def attn_decode_step_noalloc(q, positions, k_cache, v_cache, scale: float, out=None,
+                             stream=None) -> torch.Tensor:
+    """attn_decode_step using the library's built-in scratch instead of a
+    workspace, so the call allocates no device memory."""
+    _check(q, "q", torch.bfloat16, 3)
+    _check(positions, "positions", torch.int32, 1)
+    for t, n in ((k_cache, "k_cache"), (v_cache, "v_cache")):
+        _check(t, n, torch.bfloat16, 4)
+    B, Hq, D = q.shape
+    Hkv, L = k_cache.shape[1], k_cache.shape[2]
+    if tuple(k_cache.shape) != (B, Hkv, L, D) or tuple(v_cache.shape) != (B, Hkv, L, D) \
+            or positions.shape[0] != B:
+        raise ValueError("attn_decode_step_noalloc: inconsistent shapes")
+    if out is None:
+        out = torch.empty_like(q)
+    else:
+        _check(out, "out", torch.bfloat16, 3)
+        if tuple(out.shape) != (B, Hq, D):
+            raise ValueError("attn_decode_step_noalloc: out has the wrong shape")
+    code = load_library().attn_decode_step_noalloc(
+        q.data_ptr(), positions.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
+        B, Hq, Hkv, L, D, float(scale), out.data_ptr(), _stream(stream))
+    _raise(code, "attn_decode_step_noalloc")
     return out
 
 

@@ -62,6 +62,22 @@ int attn_decode_step(const void* q, const int32_t* positions, const void* k_cach
                                         out, workspace, stream));
 }
 
+int attn_decode_step_noalloc(const void* q, const int32_t* positions, const void* k_cache,
+                             const void* v_cache, int B, int Hq, int Hkv, int L, int D,
+                             float scale, void* out, cudaStream_t stream) {
+  if (!q || !positions || !k_cache || !v_cache || !out) return ATTN_ERR_INVALID_ARG;
+  if (B <= 0 || Hq <= 0 || Hkv <= 0 || L <= 0 || D <= 0 || Hq % Hkv != 0)
+    return ATTN_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out) ||
+      (reinterpret_cast<uintptr_t>(positions) & 3u))
+    return ATTN_ERR_INVALID_ARG;
+  if (!gqa::decode_supported(B, Hq, Hkv, L, D)) return ATTN_ERR_UNSUPPORTED;
+  if (gqa::decode_workspace_layout(B, Hq, Hkv, D).total > gqa::noalloc_scratch_bytes())
+    return ATTN_ERR_WORKSPACE;  // beyond the built-in scratch
+  return cuda_status(gqa::launch_decode_noalloc(q, positions, k_cache, v_cache, B, Hq, Hkv, L,
+                                                D, scale, out, stream));
+}
+
 int attn_prefill_causal(const void* q, const void* k, const void* v, int S, int start_pos,
                         int Hq, int Hkv, int d, float scale, void* out, cudaStream_t stream) {
   if (S < 0 || start_pos < 0 || Hq <= 0 || Hkv <= 0 || d <= 0 || Hq % Hkv != 0)

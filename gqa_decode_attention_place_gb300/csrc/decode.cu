@@ -544,3 +544,56 @@ cudaError_t launch_decode(const void* q, const int32_t* positions, const void* k
 }
 
 }  // namespace gqa
+
+// ---------------------------------------------------------------------------
+// attn_decode_step_noalloc: the same decode, with its split-KV scratch in a
+// fixed device array instead of a caller-provided workspace, for callers
+// that cannot allocate device memory.
+// ---------------------------------------------------------------------------
+namespace gqa {
+namespace {
+
+// Upper bound of the built-in scratch; covers every decode size whose
+// attn_decode_workspace_size() is at most this (B=256, Hq=64, Hkv=8 needs
+// about 12.8 MB).  Every GPU that loads the library keeps this much device
+// memory until the process exits.
+constexpr size_t kNoAllocScratchBytes = (size_t)16 << 20;
+static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
+
+// Device address of g_noalloc_scratch, looked up once per device (with that
+// device current).  In host code the array's name is only a stand-in, never a
+// usable device address.
+void* noalloc_scratch(cudaError_t* err) {
+  static void* addr[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess && (dev < 0 || dev >= 64)) e = cudaErrorInvalidDevice;
+  if (e == cudaSuccess && !addr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e == cudaSuccess) addr[dev] = p;
+  }
+  *err = e;
+  return e == cudaSuccess ? addr[dev] : nullptr;
+}
+
+}  // namespace
+
+size_t noalloc_scratch_bytes() { return kNoAllocScratchBytes; }
+
+cudaError_t launch_decode_noalloc(const void* q, const int32_t* positions, const void* k_cache,
+                                  const void* v_cache, int B, int Hq, int Hkv, int L, int D,
+                                  float scale, void* out, cudaStream_t stream) {
+  cudaError_t e = cudaSuccess;
+  uint8_t* scratch = static_cast<uint8_t*>(noalloc_scratch(&e));
+  if (!scratch) return e;
+  // The array keeps the previous call's contents: the status word and the
+  // arrival counters must start at zero (the partials need no clearing).
+  const DecodeWorkspace ws = decode_workspace_layout(B, Hq, Hkv, D);
+  e = cudaMemsetAsync(scratch, 0, ws.ml_off, stream);
+  if (e != cudaSuccess) return e;
+  return launch_decode(q, positions, k_cache, v_cache, B, Hq, Hkv, L, D, scale, out, scratch,
+                       stream);
+}
+
+}  // namespace gqa

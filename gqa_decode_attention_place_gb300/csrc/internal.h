@@ -23,6 +23,12 @@ cudaError_t launch_decode(const void* q, const int32_t* positions, const void* k
                           const void* v_cache, int B, int Hq, int Hkv, int L, int D,
                           float scale, void* out, void* workspace, cudaStream_t stream);
 
+// Allocation-free decode: scratch in a fixed device array (decode.cu).
+size_t noalloc_scratch_bytes();
+cudaError_t launch_decode_noalloc(const void* q, const int32_t* positions, const void* k_cache,
+                                  const void* v_cache, int B, int Hq, int Hkv, int L, int D,
+                                  float scale, void* out, cudaStream_t stream);
+
 cudaError_t launch_prefill(const void* q, const void* k, const void* v, int S, int start_pos,
                            int Hq, int Hkv, int d, float scale, void* out,
                            cudaStream_t stream);
