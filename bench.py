@@ -46,6 +46,10 @@ def _args():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-legs", action="store_true", help="skip the extra workload legs")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--only", type=str, default=None,
+                    help="run one workload a few times and exit (for ncu captures): "
+                         "streaming_sample, single_step, ragged, stress, prefill, prefill_prefix")
+    ap.add_argument("--reps", type=int, default=3, help="launches per --only run")
     ap.add_argument("--cpu-worker", type=str, default=None, help=argparse.SUPPRESS)
     return ap.parse_args()
 
@@ -492,8 +496,54 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def run_only(args):
+    """A few launches of one workload, nothing else (for profiler captures)."""
+    import torch
+    import gqa_decode_attention_place_gb300 as ga
+    import synth
+    torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+    ga.load_library()
+    name = args.only
+    if name == "streaming_sample":
+        # the streaming loop at every 64th position: cache filled by a plain
+        # copy, then attn_kv_append + attn_decode_step at each sampled position
+        q, k, v, pos = synth.streaming_inputs(steps=STEPS_STREAM, Hq=HQ, Hkv=HKV, D=D, seed=0,
+                                              device="cuda")
+        kc = k[:, 0].transpose(0, 1).contiguous().unsqueeze(0)
+        vc = v[:, 0].transpose(0, 1).contiguous().unsqueeze(0)
+        ws = ga.decode_workspace(1, HQ, HKV, L, D)
+        out = torch.empty((1, HQ, D), dtype=torch.bfloat16, device="cuda")
+        for _ in range(args.reps):
+            for p in range(0, STEPS_STREAM, 64):
+                ga.attn_kv_append(k[p], v[p], pos[p], kc, vc)
+                ga.attn_decode_step(q[p], pos[p], kc, vc, 1.0 / math.sqrt(D), out=out,
+                                    workspace=ws)
+        torch.cuda.synchronize()
+        print(json.dumps({"only": name, "launches_per_rep": 2 * STEPS_STREAM // 64}))
+        return
+    w = synth.generators.WORKLOADS[name]
+    case = synth.generators.workload_case(name, seed=0, device="cuda")
+    if w["kind"] == "decode":
+        B, Hq, Dd = case.q.shape
+        ws = ga.decode_workspace(B, Hq, case.k_cache.shape[1], case.k_cache.shape[2], Dd)
+        out = torch.empty_like(case.q)
+        ga.attn_kv_append(case.k_new, case.v_new, case.positions, case.k_cache, case.v_cache)
+        for _ in range(args.reps):
+            ga.attn_decode_step(case.q, case.positions, case.k_cache, case.v_cache, case.scale,
+                                out=out, workspace=ws)
+    else:
+        out = torch.empty_like(case.q)
+        for _ in range(args.reps):
+            ga.attn_prefill_causal(case.q, case.k, case.v, case.start_pos, case.scale, out=out)
+    torch.cuda.synchronize()
+    print(json.dumps({"only": name, "reps": args.reps}))
+
+
 def main():
     args = _args()
+    if args.only:
+        run_only(args)
+        return
     if args.cpu_worker:
         cpu_worker(args.cpu_worker)
         return
