@@ -22,6 +22,7 @@ __all__ = [
     "attn_kv_append", "attn_decode_workspace_size", "attn_decode_step",
     "attn_prefill_causal", "attn_read_device_status", "attn_status_string",
     "attn_last_cuda_error", "decode_workspace", "attn_decode_step_noalloc",
+    "attn_decode_step_append",
 ]
 
 ATTN_OK = 0
@@ -61,6 +62,9 @@ def load_library(build_if_missing: bool = True) -> ctypes.CDLL:
     lib.attn_decode_workspace_size.restype = sz
     lib.attn_decode_step.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, i32, f32, vp, vp, sz, vp]
     lib.attn_decode_step.restype = i32
+    lib.attn_decode_step_append.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, f32,
+                                            vp, vp, sz, vp]
+    lib.attn_decode_step_append.restype = i32
     lib.attn_decode_step_noalloc.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, i32, f32, vp, vp]
     lib.attn_decode_step_noalloc.restype = i32
     lib.attn_prefill_causal.argtypes = [vp, vp, vp, i32, i32, i32, i32, i32, f32, vp, vp]
@@ -164,6 +168,37 @@ def attn_decode_step(q, positions, k_cache, v_cache, scale: float, out=None, wor
         B, Hq, Hkv, L, D, float(scale), out.data_ptr(), workspace.data_ptr(),
         workspace.numel() * workspace.element_size(), _stream(stream))
     _raise(code, "attn_decode_step")
+    return out
+
+
+def attn_decode_step_append(q, k_new, v_new, positions, k_cache, v_cache, scale: float,
+                            out=None, workspace=None, stream=None) -> torch.Tensor:
+    """attn_kv_append followed by attn_decode_step, in one launch."""
+    _check(q, "q", torch.bfloat16, 3)
+    for t, n in ((k_new, "k_new"), (v_new, "v_new")):
+        _check(t, n, torch.bfloat16, 3)
+    _check(positions, "positions", torch.int32, 1)
+    for t, n in ((k_cache, "k_cache"), (v_cache, "v_cache")):
+        _check(t, n, torch.bfloat16, 4)
+    B, Hq, D = q.shape
+    Hkv, L = k_cache.shape[1], k_cache.shape[2]
+    if tuple(k_cache.shape) != (B, Hkv, L, D) or tuple(v_cache.shape) != (B, Hkv, L, D) \
+            or tuple(k_new.shape) != (B, Hkv, D) or tuple(v_new.shape) != (B, Hkv, D) \
+            or positions.shape[0] != B:
+        raise ValueError("attn_decode_step_append: inconsistent shapes")
+    if out is None:
+        out = torch.empty_like(q)
+    else:
+        _check(out, "out", torch.bfloat16, 3)
+        if tuple(out.shape) != (B, Hq, D):
+            raise ValueError("attn_decode_step_append: out has the wrong shape")
+    if workspace is None:
+        workspace = decode_workspace(B, Hq, Hkv, L, D, device=q.device)
+    code = load_library().attn_decode_step_append(
+        q.data_ptr(), k_new.data_ptr(), v_new.data_ptr(), positions.data_ptr(),
+        k_cache.data_ptr(), v_cache.data_ptr(), B, Hq, Hkv, L, D, float(scale), out.data_ptr(),
+        workspace.data_ptr(), workspace.numel() * workspace.element_size(), _stream(stream))
+    _raise(code, "attn_decode_step_append")
     return out
 
 

@@ -58,8 +58,27 @@ int attn_decode_step(const void* q, const int32_t* positions, const void* k_cach
   if (!workspace || !aligned16(workspace) ||
       workspace_bytes < gqa::decode_workspace_layout(B, Hq, Hkv, D).total)
     return ATTN_ERR_WORKSPACE;
-  return cuda_status(gqa::launch_decode(q, positions, k_cache, v_cache, B, Hq, Hkv, L, D, scale,
-                                        out, workspace, stream));
+  return cuda_status(gqa::launch_decode(q, nullptr, nullptr, positions, k_cache, v_cache, B, Hq,
+                                        Hkv, L, D, scale, out, workspace, stream));
+}
+
+int attn_decode_step_append(const void* q, const void* k_new, const void* v_new,
+                            const int32_t* positions, void* k_cache, void* v_cache, int B,
+                            int Hq, int Hkv, int L, int D, float scale, void* out,
+                            void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  if (!q || !k_new || !v_new || !positions || !k_cache || !v_cache || !out)
+    return ATTN_ERR_INVALID_ARG;
+  if (B <= 0 || Hq <= 0 || Hkv <= 0 || L <= 0 || D <= 0 || Hq % Hkv != 0)
+    return ATTN_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k_new) || !aligned16(v_new) || !aligned16(k_cache) ||
+      !aligned16(v_cache) || !aligned16(out) || (reinterpret_cast<uintptr_t>(positions) & 3u))
+    return ATTN_ERR_INVALID_ARG;
+  if (!gqa::decode_supported(B, Hq, Hkv, L, D)) return ATTN_ERR_UNSUPPORTED;
+  if (!workspace || !aligned16(workspace) ||
+      workspace_bytes < gqa::decode_workspace_layout(B, Hq, Hkv, D).total)
+    return ATTN_ERR_WORKSPACE;
+  return cuda_status(gqa::launch_decode(q, k_new, v_new, positions, k_cache, v_cache, B, Hq, Hkv,
+                                        L, D, scale, out, workspace, stream));
 }
 
 int attn_decode_step_noalloc(const void* q, const int32_t* positions, const void* k_cache,

@@ -10,15 +10,17 @@
 // How (GB300 design, not the page's: the page calls PyTorch SDPA):
 //  * The attended rows of every (sequence, KV head) pair -- a "segment" -- are
 //    cut into 64-row tiles.  All tiles of all segments form one flat list,
-//    and CTA c of the persistent grid (one CTA per SM; G = min(grid, T)) takes
-//    the contiguous range [c*T/G, (c+1)*T/G) of it.  The split is computed on the device from
+//    and CTA c of the persistent grid (one CTA per SM; G = min(grid, T)
+//    working CTAs, or one per segment when segments average <= 8 tiles)
+//    takes the contiguous range [c*T/G, (c+1)*T/G) of it.  The split is computed on the device from
 //    `positions`, so the launch does not depend on the positions and the
 //    load is balanced to within one tile however ragged the batch is.
 //  * One producer thread streams K and V tiles with 1-D bulk copies (TMA) into
 //    a 4-stage shared-memory ring guarded by mbarriers.  Each tile is read
 //    from HBM once and serves all g query heads of its KV head.
-//  * Eight consumer warps each take 8 keys of a tile, two at a time (one per
-//    half-warp; a lane holds 8 of the 128 dims).  q.k partial sums of the g
+//  * 16 consumer warps (8 for g=8) each take 4 (8) keys of a tile, two at a
+//    time (one per half-warp; a lane holds 8 of the 128 dims, as fp32 pairs
+//    for the packed fma.rn.f32x2).  q.k partial sums of the g
 //    heads are reduced across the 16 lanes with a transposing butterfly
 //    (each shuffle step halves the number of heads still carried), and the
 //    softmax is kept online in fp32 (running max and sum per head, in base 2
@@ -39,22 +41,21 @@ namespace {
 constexpr int kD = 128;
 constexpr int kTile = 64;                          // keys per pipeline stage
 constexpr int kStages = 4;
-constexpr int kCWarps = 8;                         // consumer warps
-constexpr int kKeysPerWarp = kTile / kCWarps;      // 8
-constexpr int kIters = kKeysPerWarp / 2;           // 4 (two keys per warp step)
-constexpr int kThreads = (kCWarps + 1) * 32;       // + one producer warp
-constexpr int kConsumers = kCWarps * 32;
 constexpr int kRowBytes = kD * 2;
 constexpr int kTileBytes = kTile * kRowBytes;      // 16 KB
 constexpr int kMaxB = 8192;
 constexpr int kMaxGrid = 1024;
+constexpr int kMiscInts = 32;                      // [0] abort [1] last [8..8+NW) scan
+constexpr int kWholeTiles = 8;                     // segments this short are not split
 constexpr float kLog2e = 1.4426950408889634f;
 
 struct Params {
   const uint16_t* q;
+  const uint8_t* k_new;  // [B, Hkv, D] rows to append at positions[b], or null
+  const uint8_t* v_new;
   const int32_t* positions;
-  const uint8_t* k_cache;
-  const uint8_t* v_cache;
+  uint8_t* k_cache;  // written only by the fused append (row positions[b])
+  uint8_t* v_cache;
   uint16_t* out;
   uint32_t* status;
   uint32_t* counters;
@@ -64,8 +65,23 @@ struct Params {
   float qscale;  // scale * log2(e)
 };
 
+// Consumer warps per CTA: more warps hide the latency of the shuffle chains;
+// g=8 keeps 8 warps (its q and o registers would not fit 16).
+template <int G> struct Cfg {
+  static constexpr int NW = (G >= 8) ? 8 : 16;
+  static constexpr int kThreads = (NW + 1) * 32;   // + one producer warp
+  static constexpr int kConsumers = NW * 32;
+  static constexpr int kKeysPerWarp = kTile / NW;  // 4 or 8
+  static constexpr int kIters = kKeysPerWarp / 2;  // two keys per warp step
+  // registers per thread that still let one CTA of kThreads fit the SM
+  // (the register file is handed out as if the block were a multiple of
+  // 128 threads)
+  static constexpr int kMaxRegs = (65536 / ((kThreads + 127) / 128 * 128)) & ~7;
+};
+
+template <int NC>
 __device__ __forceinline__ void consumer_bar() {
-  asm volatile("bar.sync 1, %0;" ::"n"(kConsumers) : "memory");
+  asm volatile("bar.sync 1, %0;" ::"n"(NC) : "memory");
 }
 
 // Position of flat tile t within (sequence, KV head, tile) order.
@@ -137,23 +153,59 @@ __device__ __forceinline__ float reduce16(float (&acc)[G], int l16) {
   return v;
 }
 
-__device__ __forceinline__ void unpack8(const uint4& u, float (&f)[8]) {
-  f[0] = bf16lo(u.x); f[1] = bf16hi(u.x);
-  f[2] = bf16lo(u.y); f[3] = bf16hi(u.y);
-  f[4] = bf16lo(u.z); f[5] = bf16hi(u.z);
-  f[6] = bf16lo(u.w); f[7] = bf16hi(u.w);
+// Packed fp32 pair arithmetic (fma.rn.f32x2: two IEEE fp32 FMAs, one issue).
+struct f2 {
+  unsigned long long r;
+};
+__device__ __forceinline__ f2 mk2(float lo, float hi) {
+  f2 x;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(x.r) : "f"(lo), "f"(hi));
+  return x;
+}
+__device__ __forceinline__ void brk2(f2 x, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(x.r));
+}
+__device__ __forceinline__ f2 fma2(f2 a, f2 b, f2 c) {
+  f2 d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d.r) : "l"(a.r), "l"(b.r), "l"(c.r));
+  return d;
+}
+__device__ __forceinline__ f2 mul2(f2 a, f2 b) {
+  f2 d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d.r) : "l"(a.r), "l"(b.r));
+  return d;
+}
+
+// 8 bf16 (one 16-byte vector) -> 4 fp32 pairs (dims 2i, 2i+1).
+__device__ __forceinline__ void unpack8x2(const uint4& u, f2 (&f)[4]) {
+  f[0] = mk2(bf16lo(u.x), bf16hi(u.x));
+  f[1] = mk2(bf16lo(u.y), bf16hi(u.y));
+  f[2] = mk2(bf16lo(u.z), bf16hi(u.z));
+  f[3] = mk2(bf16lo(u.w), bf16hi(u.w));
 }
 
 template <int G>
-__global__ void __launch_bounds__(kThreads, 1) decode_splitkv_kernel(const Params p) {
+size_t smem_bytes(int B) {
+  constexpr int NW = Cfg<G>::NW;
+  return (size_t)kStages * 2 * kTileBytes + 2 * kStages * sizeof(uint64_t) +
+         kMiscInts * sizeof(int) + (size_t)NW * G * 2 * sizeof(float) +
+         (size_t)NW * G * kD * sizeof(float) + (size_t)(B + 1) * sizeof(int);
+}
+
+template <int G>
+__global__ void __maxnreg__(Cfg<G>::kMaxRegs) decode_splitkv_kernel(const Params p) {
   constexpr int LG = Log2<G>::v;
+  constexpr int NW = Cfg<G>::NW;
+  constexpr int NC = Cfg<G>::kConsumers;
+  constexpr int KPW = Cfg<G>::kKeysPerWarp;
+  constexpr int IT = Cfg<G>::kIters;
   extern __shared__ __align__(1024) uint8_t smem[];
   uint8_t* stages = smem;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kStages * 2 * kTileBytes);
-  int* misc = reinterpret_cast<int*>(bars + 2 * kStages);  // [0] abort [1] last [8..15] scan
-  float* merge_ml = reinterpret_cast<float*>(misc + 16);   // [kCWarps][G][2]
-  float* merge_o = merge_ml + kCWarps * G * 2;             // [kCWarps][G][kD]
-  int* prefix = reinterpret_cast<int*>(merge_o + kCWarps * G * kD);  // [B+1]
+  int* misc = reinterpret_cast<int*>(bars + 2 * kStages);
+  float* merge_ml = reinterpret_cast<float*>(misc + kMiscInts);  // [NW][G][2]
+  float* merge_o = merge_ml + NW * G * 2;                         // [NW][G][kD]
+  int* prefix = reinterpret_cast<int*>(merge_o + NW * G * kD);    // [B+1]
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
@@ -163,20 +215,25 @@ __global__ void __launch_bounds__(kThreads, 1) decode_splitkv_kernel(const Param
   if (tid == 0) {
 #pragma unroll
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(smem_u32(&bars[s]), 1);                // full: producer arrival + bytes
-      mbar_init(smem_u32(&bars[kStages + s]), kCWarps);  // empty: one arrival per warp
+      mbar_init(smem_u32(&bars[s]), 1);             // full: producer arrival + bytes
+      mbar_init(smem_u32(&bars[kStages + s]), NW);  // empty: one arrival per consumer warp
     }
     misc[0] = 0;
     misc[1] = 0;
     fence_mbar_init();
   }
+  // Launched with programmatic stream serialisation: everything above may run
+  // while the previous kernel on the stream finishes; nothing written by it
+  // (cache rows, positions, workspace counters) is read before this wait.
+  grid_dependency_wait();
+  grid_dependents_launch();
 
   // ---- tiles per sequence and their exclusive prefix sum (every CTA) ------
   int carry = 0;
-  for (int base = 0; base < B; base += kConsumers) {
+  for (int base = 0; base < B; base += NC) {
     const int b = base + tid;
     int v = 0;
-    if (tid < kConsumers && b < B) {
+    if (tid < NC && b < B) {
       const int pos = p.positions[b];
       if (pos >= 0 && pos < L) {
         v = pos / kTile + 1;  // ceil((pos + 1) / kTile)
@@ -194,16 +251,16 @@ __global__ void __launch_bounds__(kThreads, 1) decode_splitkv_kernel(const Param
       const int y = __shfl_up_sync(0xffffffffu, x, off);
       if (lane >= off) x += y;
     }
-    if (lane == 31 && warp < kCWarps) misc[8 + warp] = x;
+    if (lane == 31 && warp < NW) misc[8 + warp] = x;
     __syncthreads();
     int before = 0, chunk = 0;
 #pragma unroll
-    for (int w = 0; w < kCWarps; ++w) {
+    for (int w = 0; w < NW; ++w) {
       const int s = misc[8 + w];
       before += (w < warp) ? s : 0;
       chunk += s;
     }
-    if (tid < kConsumers && b < B) prefix[b] = carry + before + x - v;
+    if (tid < NC && b < B) prefix[b] = carry + before + x - v;
     carry += chunk;
     __syncthreads();
   }
@@ -211,15 +268,21 @@ __global__ void __launch_bounds__(kThreads, 1) decode_splitkv_kernel(const Param
   __syncthreads();
 
   const long long T = (long long)Hkv * carry;  // total tiles
-  // Only min(grid, T) CTAs take work, so every working CTA gets >= 1 tile and
-  // the CTAs covering a segment are exactly cta_of(first)..cta_of(last).
-  const int Gd = (int)min((long long)gridDim.x, T);
+  // Working CTAs: all of the grid, except when segments are short (on
+  // average <= kWholeTiles tiles): then one CTA per segment, because a split
+  // segment costs a partial round trip through L2, more than a few tiles.
+  // Never more than T, so every working CTA gets >= 1 tile and the CTAs
+  // covering a segment are exactly cta_of(first)..cta_of(last).
+  const long long nseg = (long long)B * Hkv;
+  long long gw = min((long long)gridDim.x, T);
+  if (T <= (long long)kWholeTiles * nseg) gw = min(gw, nseg);
+  const int Gd = (int)gw;
   if ((int)blockIdx.x >= Gd) return;
   const long long t0 = T * blockIdx.x / Gd;
   const long long t1 = T * (blockIdx.x + 1) / Gd;
 
   // ------------------------------------------------------------- producer --
-  if (warp == kCWarps) {
+  if (warp == NW) {
     if (lane == 0) {
       Walk w;
       walk_init(w, t0, prefix, p.positions, B, Hkv);
@@ -233,14 +296,36 @@ __global__ void __launch_bounds__(kThreads, 1) decode_splitkv_kernel(const Param
           break;
         }
         const int rows = min(kTile, w.n - w.k * kTile);
-        const uint32_t bytes = (uint32_t)rows * kRowBytes;
         const size_t row0 = ((size_t)w.b * Hkv + w.kvh) * (size_t)L + (size_t)w.k * kTile;
         const uint32_t full = smem_u32(&bars[s]);
-        mbar_arrive_expect_tx(full, 2u * bytes);
-        bulk_g2s(smem_u32(stages + (size_t)s * 2 * kTileBytes), p.k_cache + row0 * kRowBytes,
-                 bytes, full);
-        bulk_g2s(smem_u32(stages + (size_t)s * 2 * kTileBytes + kTileBytes),
-                 p.v_cache + row0 * kRowBytes, bytes, full);
+        const uint32_t sK = smem_u32(stages + (size_t)s * 2 * kTileBytes);
+        const uint32_t sV = sK + kTileBytes;
+        // Fused append: the segment's last tile ends with row pos = n-1,
+        // which comes from k_new/v_new (copied into the tile and, by this
+        // thread, into the cache).  No other CTA reads that row.
+        const bool fresh = p.k_new != nullptr && w.k == w.ntiles - 1;
+        const int cache_rows = fresh ? rows - 1 : rows;
+        mbar_arrive_expect_tx(full, 2u * (uint32_t)rows * kRowBytes);
+        if (cache_rows > 0) {
+          const uint32_t bytes = (uint32_t)cache_rows * kRowBytes;
+          bulk_g2s(sK, p.k_cache + row0 * kRowBytes, bytes, full);
+          bulk_g2s(sV, p.v_cache + row0 * kRowBytes, bytes, full);
+        }
+        if (fresh) {
+          const size_t src = ((size_t)w.b * Hkv + w.kvh) * kRowBytes;
+          const uint32_t off = (uint32_t)cache_rows * kRowBytes;
+          bulk_g2s(sK + off, p.k_new + src, kRowBytes, full);
+          bulk_g2s(sV + off, p.v_new + src, kRowBytes, full);
+          const uint4* kn = reinterpret_cast<const uint4*>(p.k_new + src);
+          const uint4* vn = reinterpret_cast<const uint4*>(p.v_new + src);
+          uint4* kd = reinterpret_cast<uint4*>(p.k_cache + (row0 + cache_rows) * kRowBytes);
+          uint4* vd = reinterpret_cast<uint4*>(p.v_cache + (row0 + cache_rows) * kRowBytes);
+#pragma unroll
+          for (int c = 0; c < kRowBytes / 16; ++c) {
+            kd[c] = kn[c];
+            vd[c] = vn[c];
+          }
+        }
         walk_next(w, prefix, p.positions, B, Hkv);
       }
     }
@@ -253,7 +338,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_splitkv_kernel(const Param
   Walk w;
   walk_init(w, t0, prefix, p.positions, B, Hkv);
 
-  float qf[G][8], o[G][8];
+  f2 qf[G][4];   // q[h][8 lane dims] as 4 pairs, pre-scaled by scale*log2(e)
+  f2 o[G][4];    // unnormalised output accumulators, same layout
   float m_run = -INFINITY, l_run = 0.f;
 
   auto load_q = [&]() {
@@ -261,10 +347,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_splitkv_kernel(const Param
 #pragma unroll
     for (int h = 0; h < G; ++h) {
       const uint4 u = *reinterpret_cast<const uint4*>(qb + (size_t)h * kD);
-      float f[8];
-      unpack8(u, f);
+      const uint32_t wd[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
-      for (int j = 0; j < 8; ++j) qf[h][j] = f[j] * p.qscale;
+      for (int j = 0; j < 4; ++j)
+        qf[h][j] = mk2(bf16lo(wd[j]) * p.qscale, bf16hi(wd[j]) * p.qscale);
     }
   };
   auto reset_acc = [&]() {
@@ -273,7 +359,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_splitkv_kernel(const Param
 #pragma unroll
     for (int h = 0; h < G; ++h)
 #pragma unroll
-      for (int j = 0; j < 8; ++j) o[h][j] = 0.f;
+      for (int j = 0; j < 4; ++j) o[h][j] = mk2(0.f, 0.f);
   };
   load_q();
   reset_acc();
@@ -291,21 +377,23 @@ __global__ void __launch_bounds__(kThreads, 1) decode_splitkv_kernel(const Param
     const uint8_t* Ks = stages + (size_t)s * 2 * kTileBytes;
     const uint8_t* Vs = Ks + kTileBytes;
 
-    // scores of this warp's 8 keys (two per step), log2 domain
-    float sc[kIters];
+    // scores of this warp's keys (two per step), log2 domain
+    float sc[IT];
 #pragma unroll
-    for (int it = 0; it < kIters; ++it) {
-      const int key = warp * kKeysPerWarp + it * 2 + half;
+    for (int it = 0; it < IT; ++it) {
+      const int key = warp * KPW + it * 2 + half;
       const uint4 kv = *reinterpret_cast<const uint4*>(Ks + key * kRowBytes + l16 * 16);
-      float kf[8];
-      unpack8(kv, kf);
+      f2 kf[4];
+      unpack8x2(kv, kf);
       float acc[G];
 #pragma unroll
       for (int h = 0; h < G; ++h) {
-        float a = 0.f;
+        f2 a = mul2(qf[h][0], kf[0]);
 #pragma unroll
-        for (int j = 0; j < 8; ++j) a = fmaf(qf[h][j], kf[j], a);
-        acc[h] = a;
+        for (int j = 1; j < 4; ++j) a = fma2(qf[h][j], kf[j], a);
+        float lo, hi;
+        brk2(a, lo, hi);
+        acc[h] = lo + hi;
       }
       const float sv = reduce16<G>(acc, l16);
       sc[it] = (key < rows) ? sv : -INFINITY;
@@ -314,14 +402,14 @@ __global__ void __launch_bounds__(kThreads, 1) decode_splitkv_kernel(const Param
     // online softmax update for head hd
     float mx = sc[0];
 #pragma unroll
-    for (int it = 1; it < kIters; ++it) mx = fmaxf(mx, sc[it]);
+    for (int it = 1; it < IT; ++it) mx = fmaxf(mx, sc[it]);
     mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
     const float m_new = fmaxf(m_run, mx);
     const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
     const float alpha = ex2(m_run - m_use);
-    float pr[kIters], ps = 0.f;
+    float pr[IT], ps = 0.f;
 #pragma unroll
-    for (int it = 0; it < kIters; ++it) {
+    for (int it = 0; it < IT; ++it) {
       pr[it] = ex2(sc[it] - m_use);
       ps += pr[it];
     }
@@ -332,26 +420,29 @@ __global__ void __launch_bounds__(kThreads, 1) decode_splitkv_kernel(const Param
 #pragma unroll
     for (int h = 0; h < G; ++h) {
       const float a = __shfl_sync(0xffffffffu, alpha, h << (4 - LG));
+      const f2 a2 = mk2(a, a);
 #pragma unroll
-      for (int j = 0; j < 8; ++j) o[h][j] *= a;
+      for (int j = 0; j < 4; ++j) o[h][j] = mul2(o[h][j], a2);
     }
 
     // o += p * v
 #pragma unroll
-    for (int it = 0; it < kIters; ++it) {
-      const int key = warp * kKeysPerWarp + it * 2 + half;
+    for (int it = 0; it < IT; ++it) {
+      const int key = warp * KPW + it * 2 + half;
       const uint4 vv = *reinterpret_cast<const uint4*>(Vs + key * kRowBytes + l16 * 16);
       float ph[G];
 #pragma unroll
       for (int h = 0; h < G; ++h)
         ph[h] = __shfl_sync(0xffffffffu, pr[it], (half << 4) | (h << (4 - LG)));
       if (key < rows) {
-        float vf[8];
-        unpack8(vv, vf);
+        f2 vf[4];
+        unpack8x2(vv, vf);
 #pragma unroll
-        for (int h = 0; h < G; ++h)
+        for (int h = 0; h < G; ++h) {
+          const f2 p2 = mk2(ph[h], ph[h]);
 #pragma unroll
-          for (int j = 0; j < 8; ++j) o[h][j] = fmaf(ph[h], vf[j], o[h][j]);
+          for (int j = 0; j < 4; ++j) o[h][j] = fma2(p2, vf[j], o[h][j]);
+        }
       }
     }
     __syncwarp();
@@ -363,36 +454,46 @@ __global__ void __launch_bounds__(kThreads, 1) decode_splitkv_kernel(const Param
       const long long seg_t0 = (long long)Hkv * prefix[w.b] + (long long)w.kvh * w.ntiles;
       const long long seg_t1 = seg_t0 + w.ntiles;
       const bool whole = seg_t0 >= t0 && seg_t1 <= t1;
-      const int ct = tid;  // 0..255
+      const int ct = tid;
 
+      // both half-warps hold partial o for the same (m, l): add them
 #pragma unroll
       for (int h = 0; h < G; ++h)
 #pragma unroll
-        for (int j = 0; j < 8; ++j) o[h][j] += __shfl_xor_sync(0xffffffffu, o[h][j], 16);
+        for (int j = 0; j < 4; ++j) {
+          float lo, hi;
+          brk2(o[h][j], lo, hi);
+          lo += __shfl_xor_sync(0xffffffffu, lo, 16);
+          hi += __shfl_xor_sync(0xffffffffu, hi, 16);
+          o[h][j] = mk2(lo, hi);
+        }
       if (half == 0) {
 #pragma unroll
         for (int h = 0; h < G; ++h) {
+          float f[8];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) brk2(o[h][j], f[2 * j], f[2 * j + 1]);
           float4* dst = reinterpret_cast<float4*>(merge_o + ((warp * G + h) * kD + l16 * 8));
-          dst[0] = make_float4(o[h][0], o[h][1], o[h][2], o[h][3]);
-          dst[1] = make_float4(o[h][4], o[h][5], o[h][6], o[h][7]);
+          dst[0] = make_float4(f[0], f[1], f[2], f[3]);
+          dst[1] = make_float4(f[4], f[5], f[6], f[7]);
         }
         if (l16 == (hd << (4 - LG))) {
           merge_ml[(warp * G + hd) * 2 + 0] = m_run;
           merge_ml[(warp * G + hd) * 2 + 1] = l_run;
         }
       }
-      consumer_bar();
+      consumer_bar<NC>();
 
       const int slot = blockIdx.x + seg;
       uint16_t* out_seg = p.out + ((size_t)w.b * p.Hq + (size_t)w.kvh * G) * kD;
-      for (int idx = ct; idx < G * kD; idx += kConsumers) {
+      for (int idx = ct; idx < G * kD; idx += NC) {
         const int h = idx / kD, d = idx % kD;
         float M = -INFINITY;
 #pragma unroll
-        for (int ww = 0; ww < kCWarps; ++ww) M = fmaxf(M, merge_ml[(ww * G + h) * 2]);
+        for (int ww = 0; ww < NW; ++ww) M = fmaxf(M, merge_ml[(ww * G + h) * 2]);
         float Ls = 0.f, Os = 0.f;
 #pragma unroll
-        for (int ww = 0; ww < kCWarps; ++ww) {
+        for (int ww = 0; ww < NW; ++ww) {
           const float e = ex2(merge_ml[(ww * G + h) * 2] - M);
           Ls = fmaf(merge_ml[(ww * G + h) * 2 + 1], e, Ls);
           Os = fmaf(merge_o[(ww * G + h) * kD + d], e, Os);
@@ -411,26 +512,54 @@ __global__ void __launch_bounds__(kThreads, 1) decode_splitkv_kernel(const Param
       if (!whole) {
         const int c_first = cta_of(seg_t0, T, Gd);
         const int c_last = cta_of(seg_t1 - 1, T, Gd);
-        consumer_bar();
+        consumer_bar<NC>();
         if (ct == 0) {
-          __threadfence();
-          const unsigned old = atomicAdd(&p.counters[seg], 1u);
+          // release: this CTA's partial (ordered before by the barrier) is
+          // visible to whoever acquires the counter; acquire: the last
+          // arrival sees every other CTA's partial
+          unsigned old;
+          asm volatile("atom.add.acq_rel.gpu.u32 %0, [%1], 1;"
+                       : "=r"(old)
+                       : "l"(&p.counters[seg])
+                       : "memory");
           misc[1] = (old == (unsigned)(c_last - c_first)) ? 1 : 0;
         }
-        consumer_bar();
+        consumer_bar<NC>();
         if (misc[1]) {
-          __threadfence();
-          for (int idx = ct; idx < G * kD; idx += kConsumers) {
+          // last to arrive: merge the segment's partials.  Batches of 8
+          // independent loads keep several L2 round trips in flight.
+          for (int idx = ct; idx < G * kD; idx += NC) {
             const int h = idx / kD, d = idx % kD;
-            float M = -INFINITY;
-            for (int c = c_first; c <= c_last; ++c)
-              M = fmaxf(M, __ldcg(&p.part_ml[((size_t)(c + seg) * G + h) * 2]));
-            float Ls = 0.f, Os = 0.f;
-            for (int c = c_first; c <= c_last; ++c) {
-              const size_t sl = (size_t)(c + seg) * G + h;
-              const float e = ex2(__ldcg(&p.part_ml[sl * 2]) - M);
-              Ls = fmaf(__ldcg(&p.part_ml[sl * 2 + 1]), e, Ls);
-              Os = fmaf(__ldcg(&p.part_o[sl * kD + d]), e, Os);
+            float M = -INFINITY, Ls = 0.f, Os = 0.f;
+            for (int c0 = c_first; c0 <= c_last; c0 += 8) {
+              float mm[8], ll[8], oo[8];
+#pragma unroll
+              for (int uu = 0; uu < 8; ++uu) {
+                const int c = c0 + uu;
+                if (c <= c_last) {
+                  const size_t sl = (size_t)(c + seg) * G + h;
+                  mm[uu] = __ldcg(&p.part_ml[sl * 2]);
+                  ll[uu] = __ldcg(&p.part_ml[sl * 2 + 1]);
+                  oo[uu] = __ldcg(&p.part_o[sl * kD + d]);
+                } else {
+                  mm[uu] = -INFINITY;
+                  ll[uu] = 0.f;
+                  oo[uu] = 0.f;
+                }
+              }
+              float Mb = M;
+#pragma unroll
+              for (int uu = 0; uu < 8; ++uu) Mb = fmaxf(Mb, mm[uu]);
+              const float sc0 = ex2(M - Mb);  // M = -inf on the first batch: 0
+              Ls *= sc0;
+              Os *= sc0;
+#pragma unroll
+              for (int uu = 0; uu < 8; ++uu) {
+                const float e = ex2(mm[uu] - Mb);
+                Ls = fmaf(ll[uu], e, Ls);
+                Os = fmaf(oo[uu], e, Os);
+              }
+              M = Mb;
             }
             __nv_bfloat16 r = __float2bfloat16_rn(Os / Ls);
             out_seg[h * kD + d] = *reinterpret_cast<uint16_t*>(&r);
@@ -438,7 +567,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_splitkv_kernel(const Param
           if (ct == 0) p.counters[seg] = 0u;  // ready for the next launch
         }
       }
-      consumer_bar();  // merge buffers are free again
+      consumer_bar<NC>();  // merge buffers are free again
       reset_acc();
     }
     walk_next(w, prefix, p.positions, B, Hkv);
@@ -469,13 +598,6 @@ int num_sms() {
 }
 
 template <int G>
-size_t smem_bytes(int B) {
-  return (size_t)kStages * 2 * kTileBytes + 2 * kStages * sizeof(uint64_t) + 16 * sizeof(int) +
-         (size_t)kCWarps * G * 2 * sizeof(float) + (size_t)kCWarps * G * kD * sizeof(float) +
-         (size_t)(B + 1) * sizeof(int);
-}
-
-template <int G>
 cudaError_t launch_g(const Params& p, cudaStream_t stream) {
   const size_t smem = smem_bytes<G>(kMaxB);
   static bool configured[64] = {};
@@ -487,9 +609,8 @@ cudaError_t launch_g(const Params& p, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     configured[dev] = true;
   }
-  const int grid = min(kMaxGrid, num_sms());
-  decode_splitkv_kernel<G><<<grid, kThreads, smem_bytes<G>(p.B), stream>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(decode_splitkv_kernel<G>, dim3(min(kMaxGrid, num_sms())),
+                    dim3(Cfg<G>::kThreads), smem_bytes<G>(p.B), stream, p);
 }
 
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
@@ -514,16 +635,19 @@ bool decode_supported(int B, int Hq, int Hkv, int L, int D) {
          L <= (1 << 24);
 }
 
-cudaError_t launch_decode(const void* q, const int32_t* positions, const void* k_cache,
-                          const void* v_cache, int B, int Hq, int Hkv, int L, int D,
-                          float scale, void* out, void* workspace, cudaStream_t stream) {
+cudaError_t launch_decode(const void* q, const void* k_new, const void* v_new,
+                          const int32_t* positions, const void* k_cache, const void* v_cache,
+                          int B, int Hq, int Hkv, int L, int D, float scale, void* out,
+                          void* workspace, cudaStream_t stream) {
   const DecodeWorkspace ws = decode_workspace_layout(B, Hq, Hkv, D);
   uint8_t* base = static_cast<uint8_t*>(workspace);
   Params p;
   p.q = static_cast<const uint16_t*>(q);
+  p.k_new = static_cast<const uint8_t*>(k_new);
+  p.v_new = static_cast<const uint8_t*>(v_new);
   p.positions = positions;
-  p.k_cache = static_cast<const uint8_t*>(k_cache);
-  p.v_cache = static_cast<const uint8_t*>(v_cache);
+  p.k_cache = static_cast<uint8_t*>(const_cast<void*>(k_cache));
+  p.v_cache = static_cast<uint8_t*>(const_cast<void*>(v_cache));
   p.out = static_cast<uint16_t*>(out);
   p.status = reinterpret_cast<uint32_t*>(base + ws.status_off);
   p.counters = reinterpret_cast<uint32_t*>(base + ws.counters_off);
@@ -592,8 +716,8 @@ cudaError_t launch_decode_noalloc(const void* q, const int32_t* positions, const
   const DecodeWorkspace ws = decode_workspace_layout(B, Hq, Hkv, D);
   e = cudaMemsetAsync(scratch, 0, ws.ml_off, stream);
   if (e != cudaSuccess) return e;
-  return launch_decode(q, positions, k_cache, v_cache, B, Hq, Hkv, L, D, scale, out, scratch,
-                       stream);
+  return launch_decode(q, nullptr, nullptr, positions, k_cache, v_cache, B, Hq, Hkv, L, D, scale,
+                       out, scratch, stream);
 }
 
 }  // namespace gqa

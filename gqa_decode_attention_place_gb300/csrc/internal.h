@@ -19,9 +19,12 @@ struct DecodeWorkspace {
 };
 DecodeWorkspace decode_workspace_layout(int B, int Hq, int Hkv, int D);
 
-cudaError_t launch_decode(const void* q, const int32_t* positions, const void* k_cache,
-                          const void* v_cache, int B, int Hq, int Hkv, int L, int D,
-                          float scale, void* out, void* workspace, cudaStream_t stream);
+// k_new/v_new null: attention only.  Non-null: the rows are appended at
+// positions[b] inside the same launch (kv append fused into decode).
+cudaError_t launch_decode(const void* q, const void* k_new, const void* v_new,
+                          const int32_t* positions, const void* k_cache, const void* v_cache,
+                          int B, int Hq, int Hkv, int L, int D, float scale, void* out,
+                          void* workspace, cudaStream_t stream);
 
 // Allocation-free decode: scratch in a fixed device array (decode.cu).
 size_t noalloc_scratch_bytes();

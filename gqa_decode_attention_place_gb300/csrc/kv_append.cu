@@ -13,6 +13,8 @@ __global__ void __launch_bounds__(256) kv_append_kernel(
     const uint4* __restrict__ k_new, const uint4* __restrict__ v_new,
     const int32_t* __restrict__ positions, uint4* __restrict__ k_cache,
     uint4* __restrict__ v_cache, int B, int Hkv, int L, int vec_per_row) {
+  grid_dependency_wait();
+  grid_dependents_launch();
   const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   const long long total = (long long)B * Hkv * vec_per_row;
   if (i >= total) return;
@@ -33,10 +35,10 @@ cudaError_t launch_kv_append(const void* k_new, const void* v_new, const int32_t
   const long long total = (long long)B * Hkv * vec_per_row;
   const int threads = 256;
   const long long blocks = (total + threads - 1) / threads;
-  kv_append_kernel<<<(unsigned)blocks, threads, 0, stream>>>(
-      static_cast<const uint4*>(k_new), static_cast<const uint4*>(v_new), positions,
-      static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache), B, Hkv, L, vec_per_row);
-  return cudaGetLastError();
+  return launch_pdl(kv_append_kernel, dim3((unsigned)blocks), dim3(threads), 0, stream,
+                    static_cast<const uint4*>(k_new), static_cast<const uint4*>(v_new),
+                    positions, static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache), B,
+                    Hkv, L, vec_per_row);
 }
 
 }  // namespace gqa

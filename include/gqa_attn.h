@@ -23,6 +23,9 @@
  *     aligned.
  *   - GQA: query head h reads KV head h / g, g = Hq / Hkv (contiguous groups,
  *     the repeat-KV convention).
+ *   - Kernels are launched with programmatic stream serialisation: a launch
+ *     may start its prologue while the previous kernel on `stream` drains,
+ *     and waits for that kernel's writes before reading any input.
  *   - Every call is asynchronous on `stream` and returns an int status
  *     (ATTN_OK or an ATTN_ERR_* code).  Argument errors are found on the host
  *     before anything is launched; nothing is then written.  ATTN_ERR_CUDA means
@@ -115,6 +118,31 @@ int attn_decode_step(const void* q, const int32_t* positions,
                      int B, int Hq, int Hkv, int L, int D, float scale,
                      void* out, void* workspace, size_t workspace_bytes,
                      cudaStream_t stream);
+
+/*
+ * attn_decode_step_append -- one decode step of the decode page, section 4.1,
+ * in one launch: the cache write of attn_kv_append followed by the attention
+ * of attn_decode_step.  Results are those of the two calls in that order:
+ * row positions[b] of every KV head of sequence b becomes k_new/v_new
+ * (bit-exact) and out is attention over rows 0..positions[b], the new row
+ * included.  The new rows are fed to the attention straight from k_new/v_new
+ * and written to the cache in the same launch.
+ *
+ *   q            : [B, Hq, D] bf16.
+ *   k_new, v_new : [B, Hkv, D] bf16.
+ *   positions    : [B] int32, device memory.
+ *   k_cache,
+ *   v_cache      : [B, Hkv, L, D] bf16, row positions[b] written in place.
+ *   out, workspace, scale and supported sizes: as attn_decode_step.
+ *
+ * A position outside [0, L) writes nothing for that sequence, gives NaN
+ * output rows and sets ATTN_DEV_BAD_POSITION.
+ */
+int attn_decode_step_append(const void* q, const void* k_new, const void* v_new,
+                            const int32_t* positions, void* k_cache, void* v_cache,
+                            int B, int Hq, int Hkv, int L, int D, float scale,
+                            void* out, void* workspace, size_t workspace_bytes,
+                            cudaStream_t stream);
 
 /*
  * attn_decode_step_noalloc -- attn_decode_step without a workspace argument.

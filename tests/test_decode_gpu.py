@@ -201,3 +201,73 @@ def test_single_row_cache_and_odd_scale():
                              fill="all", seed=14, device="cuda", scale=0.01)
     want = _oracle_rows(case, [0, 1])
     _check(case, want, _run_step(case), "scale 0.01")
+
+
+# ---- fused append + decode (attn_decode_step_append) ------------------------
+
+def _fused_step(case, workspace=None):
+    out = ga.attn_decode_step_append(case.q, case.k_new, case.v_new, case.positions,
+                                     case.k_cache, case.v_cache, case.scale, workspace=workspace)
+    torch.cuda.synchronize()
+    return out
+
+
+@pytest.mark.parametrize("g", [1, 2, 4, 8])
+def test_fused_append_decode_boundaries_poisoned(g):
+    Hkv = 2
+    positions = [0, 1, 62, 63, 64, 65, 127, 128, 129, 1000, 4095, 4096, 8191]
+    case = synth.decode_case(B=len(positions), Hq=g * Hkv, Hkv=Hkv, D=128, L=8192,
+                             positions=positions, fill="all", poison=True, seed=20 + g,
+                             device="cuda")
+    want = _oracle_rows(case, range(len(positions)))
+    pos = case.positions.cpu().numpy()
+    wk, wv = oracle.kv_append(bits(case.k_cache).cpu().numpy(), bits(case.v_cache).cpu().numpy(),
+                              bits(case.k_new).cpu().numpy(), bits(case.v_new).cpu().numpy(), pos)
+    out = _fused_step(case)
+    _check(case, want, out, f"fused g={g}")
+    assert np.array_equal(bits(case.k_cache).cpu().numpy(), wk)
+    assert np.array_equal(bits(case.v_cache).cpu().numpy(), wv)
+
+
+def test_fused_position_zero_and_bad_positions():
+    case = synth.decode_case(B=4, Hq=16, Hkv=8, D=128, L=64, positions=[0, 64, 0, -1],
+                             fill="all", poison=True, seed=31, device="cuda")
+    k_before = bits(case.k_cache).clone()
+    ws = ga.decode_workspace(4, 16, 8, 64, 128)
+    out = _fused_step(case, workspace=ws)
+    for h in range(16):
+        assert torch.equal(bits(out[0, h]), bits(case.v_new[0, h // 2]))
+        assert torch.equal(bits(out[2, h]), bits(case.v_new[2, h // 2]))
+    assert torch.isnan(out[1].float()).all() and torch.isnan(out[3].float()).all()
+    assert torch.equal(bits(case.k_cache[1]), k_before[1])
+    assert torch.equal(bits(case.k_cache[3]), k_before[3])
+    assert ga.attn_read_device_status(ws) & ga.ATTN_DEV_BAD_POSITION
+
+
+def test_fused_streaming_loop_matches_two_call_loop():
+    """The streaming workload through the fused call; sampled steps against
+    the oracle and every step against the append-then-decode pair."""
+    steps, Hq, Hkv, D, L = 1500, 16, 8, 128, 2048
+    q, k, v, pos = synth.streaming_inputs(steps=steps, Hq=Hq, Hkv=Hkv, D=D, seed=12,
+                                          device="cuda")
+    scale = 1.0 / math.sqrt(D)
+    caches = [torch.full((1, Hkv, L, D), float("nan"), dtype=torch.bfloat16, device="cuda")
+              for _ in range(4)]
+    ws = [ga.decode_workspace(1, Hq, Hkv, L, D) for _ in range(2)]
+    outs = [torch.empty((steps, 1, Hq, D), dtype=torch.bfloat16, device="cuda") for _ in range(2)]
+    for s in range(steps):
+        ga.attn_decode_step_append(q[s], k[s], v[s], pos[s], caches[0], caches[1], scale,
+                                   out=outs[0][s], workspace=ws[0])
+        ga.attn_kv_append(k[s], v[s], pos[s], caches[2], caches[3])
+        ga.attn_decode_step(q[s], pos[s], caches[2], caches[3], scale, out=outs[1][s],
+                            workspace=ws[1])
+    torch.cuda.synchronize()
+    assert torch.equal(bits(caches[0][:, :, :steps]), bits(caches[2][:, :, :steps]))
+    assert torch.equal(bits(caches[1][:, :, :steps]), bits(caches[3][:, :, :steps]))
+    assert torch.equal(bits(outs[0]), bits(outs[1]))
+    kk, vv = f64(k[:, 0]), f64(v[:, 0])
+    for s in [0, 63, 64, 777, 1499]:
+        kc_o = kk[: s + 1].transpose(1, 0, 2)[None]
+        vc_o = vv[: s + 1].transpose(1, 0, 2)[None]
+        want = oracle.decode(f64(q[s]), kc_o, vc_o, [s], scale)
+        assert_attn_close(f64(outs[0][s]), want, f"fused streaming step {s}")
