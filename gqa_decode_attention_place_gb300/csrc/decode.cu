@@ -153,29 +153,6 @@ __device__ __forceinline__ float reduce16(float (&acc)[G], int l16) {
   return v;
 }
 
-// Packed fp32 pair arithmetic (fma.rn.f32x2: two IEEE fp32 FMAs, one issue).
-struct f2 {
-  unsigned long long r;
-};
-__device__ __forceinline__ f2 mk2(float lo, float hi) {
-  f2 x;
-  asm("mov.b64 %0, {%1, %2};" : "=l"(x.r) : "f"(lo), "f"(hi));
-  return x;
-}
-__device__ __forceinline__ void brk2(f2 x, float& lo, float& hi) {
-  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(x.r));
-}
-__device__ __forceinline__ f2 fma2(f2 a, f2 b, f2 c) {
-  f2 d;
-  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d.r) : "l"(a.r), "l"(b.r), "l"(c.r));
-  return d;
-}
-__device__ __forceinline__ f2 mul2(f2 a, f2 b) {
-  f2 d;
-  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d.r) : "l"(a.r), "l"(b.r));
-  return d;
-}
-
 // 8 bf16 (one 16-byte vector) -> 4 fp32 pairs (dims 2i, 2i+1).
 __device__ __forceinline__ void unpack8x2(const uint4& u, f2 (&f)[4]) {
   f[0] = mk2(bf16lo(u.x), bf16hi(u.x));

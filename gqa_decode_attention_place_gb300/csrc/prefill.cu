@@ -8,18 +8,24 @@
 // 0..start_pos+i (causal mask aligned to the bottom-right corner), query head
 // h reads KV head h/g.  out [S,Hq,d] bf16.
 //
-// How (one CTA per (128-token query tile, query head); longest tiles first):
-//  * warp 0, one thread: TMA (cp.async.bulk.tensor, 128-byte swizzle) loads the
-//    Q tile once and streams 128-key K and V tiles through a 2-stage ring.
+// How: one CTA per (pair of 128-token query tiles, query head), longest pairs
+// first.  Each K/V tile loaded serves both query tiles.
+//  * warp 0, one thread: TMA (cp.async.bulk.tensor, 128-byte swizzle) loads
+//    the two Q tiles once and streams 128-key K and V tiles through a 3-stage
+//    ring (4 stages).
 //  * warp 1, one thread: issues tcgen05.mma (bf16 in, fp32 accumulate in
-//    tensor memory): S = Q K^T into 128 TMEM columns, then O_tile = P V into
-//    one of two 64-column TMEM buffers.  S of tile i+1 is issued as soon as
-//    the softmax has read S of tile i, so QK^T overlaps the softmax.
-//  * warps 4-7 (128 threads, thread r owns query row r): read the S row from
-//    TMEM, mask the causal diagonal, keep the online softmax (running max and
-//    sum in base 2), write P as bf16 into shared memory in the 128-byte
-//    swizzled K-major layout the MMA reads, and fold each finished O_tile into
-//    a register accumulator: O = O * exp2(m_old - m_new) + O_tile.
+//    tensor memory).  Per K/V tile i: S_A = Q_A K^T and S_B = Q_B K^T (128
+//    TMEM columns each), then O_A += P_A V and O_B += P_B V for tile i-1,
+//    with P read from tensor memory (64 columns of bf16 pairs per tile) and
+//    O kept in tensor memory for the whole key loop.  While one query tile's
+//    softmax runs, the tensor core works on the other tile.
+//  * warps 2-5 (tile A) and 6-9 (tile B), thread r owns query row r (TMEM
+//    lane quarter warp % 4): read the whole S row from TMEM into registers in
+//    one round trip, mask the causal diagonal, keep the online softmax in
+//    base 2, write P as bf16 pairs into tensor memory (tcgen05.st).  The
+//    running max is raised only when a row's max grows by more than 2^8
+//    (then O is rescaled in TMEM); otherwise P may reach 2^8, harmless in
+//    fp32 sums and bf16 P.
 //  Scores never leave the SM (no S or P in HBM).
 #include <cuda.h>
 
@@ -29,36 +35,39 @@
 namespace gqa {
 namespace {
 
-constexpr int kBM = 128;   // query rows per CTA (MMA M)
+constexpr int kBM = 128;   // query rows per tile (MMA M)
 constexpr int kBN = 128;   // keys per tile (MMA N of QK^T, K of PV)
 constexpr int kHD = 64;    // head dim (MMA K of QK^T, N of PV)
-constexpr int kKVStages = 2;
-constexpr int kPThreads = 256;
+constexpr int kQT = 2;     // query tiles per CTA
+constexpr int kKVStages = 4;
+constexpr int kPThreads = 320;             // 10 warps
 constexpr int kTileBytes = kBM * kHD * 2;  // 16 KB: a 128 x 64 bf16 tile
-constexpr uint32_t kTmemCols = 256;        // S: 128, O_tile x2: 2 x 64
+constexpr uint32_t kTmemCols = 512;        // S: 2 x 128, P: 2 x 64, O: 2 x 64
+constexpr uint32_t kTmemP = 256;           // P of tile x at 256 + 64x (bf16 pairs)
+constexpr uint32_t kTmemO = 384;           // O of tile x at 384 + 64x
+constexpr float kLazyTau = 8.0f;           // keep a stale max up to 2^8 below
 
 // shared memory map (offsets from a 1024-byte aligned base)
-constexpr int kOffQ = 0;
-constexpr int kOffKV = kOffQ + kTileBytes;                     // stage s: K, then V
-constexpr int kOffP = kOffKV + kKVStages * 2 * kTileBytes;     // P: keys 0-63, 64-127
-constexpr int kOffBar = kOffP + 2 * kTileBytes;
-constexpr int kSmemBytes = kOffBar + 256 + 1024;               // + alignment slack
+constexpr int kOffQ = 0;                                        // tile X at X * 16 KB
+constexpr int kOffKV = kOffQ + kQT * kTileBytes;                // stage s: K, then V
+constexpr int kOffBar = kOffKV + kKVStages * 2 * kTileBytes;
+constexpr int kSmemBytes = kOffBar + 256 + 1024;                // + alignment slack
 
 // barrier slots
 constexpr int kBarQ = 0;
-constexpr int kBarKVFull = 1;                 // + stage
+constexpr int kBarKVFull = 1;                     // + stage
 constexpr int kBarKVEmpty = kBarKVFull + kKVStages;
-constexpr int kBarSFull = kBarKVEmpty + kKVStages;
-constexpr int kBarSFree = kBarSFull + 1;
-constexpr int kBarPFull = kBarSFree + 1;
-constexpr int kBarPVDone = kBarPFull + 1;     // + buffer (2)
-constexpr int kNumBars = kBarPVDone + 2;
+constexpr int kBarSFull = kBarKVEmpty + kKVStages;  // + tile
+constexpr int kBarSFree = kBarSFull + kQT;
+constexpr int kBarPFull = kBarSFree + kQT;    // + tile
+constexpr int kBarPVDone = kBarPFull + kQT;   // + tile
+constexpr int kNumBars = kBarPVDone + kQT;
 
 __device__ unsigned int g_prefill_timeouts;   // diagnostic: waits that gave up
 
 struct PrefillParams {
   uint16_t* out;
-  int S, start_pos, Hq, Hkv, g, n_qt;
+  int S, start_pos, Hq, Hkv, g, n_pairs;
   float scale_log2;  // scale * log2(e)
 };
 
@@ -97,6 +106,18 @@ __device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t adesc, uint64_t
       : "memory");
 }
 
+// D[tmem] (+)= A[tmem] * B[smem desc]: A (M x 16, bf16 pairs in 8 columns,
+// row m in lane m) read from tensor memory.
+__device__ __forceinline__ void tc_mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc,
+                                          uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // 32 consecutive TMEM columns of this warp's 32 lanes -> 32 registers per thread.
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
   uint32_t r[32];
@@ -114,8 +135,57 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
   for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// 32 registers per thread -> 32 consecutive TMEM columns of this warp's lanes.
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+      "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+      "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
+      "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
+      "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])), "r"(__float_as_uint(v[8])),
+      "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
+      "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
+      "r"(__float_as_uint(v[15])), "r"(__float_as_uint(v[16])), "r"(__float_as_uint(v[17])),
+      "r"(__float_as_uint(v[18])), "r"(__float_as_uint(v[19])), "r"(__float_as_uint(v[20])),
+      "r"(__float_as_uint(v[21])), "r"(__float_as_uint(v[22])), "r"(__float_as_uint(v[23])),
+      "r"(__float_as_uint(v[24])), "r"(__float_as_uint(v[25])), "r"(__float_as_uint(v[26])),
+      "r"(__float_as_uint(v[27])), "r"(__float_as_uint(v[28])), "r"(__float_as_uint(v[29])),
+      "r"(__float_as_uint(v[30])), "r"(__float_as_uint(v[31]))
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const float (&v)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
+      "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
+      "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
+      "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])), "r"(__float_as_uint(v[8])),
+      "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
+      "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
+      "r"(__float_as_uint(v[15]))
+      : "memory");
+}
+
 __device__ __forceinline__ void tmem_ld_wait() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_st_wait() {
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
 // Shared-memory matrix descriptor of a tcgen05 operand in the 128-byte
@@ -163,11 +233,15 @@ __global__ void __launch_bounds__(kPThreads, 1)
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int h = blockIdx.x % p.Hq;
-  const int qt = p.n_qt - 1 - (int)(blockIdx.x / p.Hq);  // longest (last) tiles first
-  const int q0 = qt * kBM;
+  const int pair = p.n_pairs - 1 - (int)(blockIdx.x / p.Hq);  // longest pairs first
+  const int q0 = pair * kQT * kBM;
   const int kvh = h / p.g;
-  const int q_last = min(q0 + kBM, p.S);              // one past the last valid row
-  const int n_tiles = (p.start_pos + q_last + kBN - 1) / kBN;
+  // key tiles each query tile needs (0 if the tile holds no query row)
+  auto ntile = [&](int x) -> int {
+    const int r0 = q0 + x * kBM;
+    return r0 < p.S ? (p.start_pos + min(r0 + kBM, p.S) + kBN - 1) / kBN : 0;
+  };
+  const int n_tiles = max(ntile(0), ntile(1));
 
   if (tid == 0) {
     mbar_init(bar(kBarQ), 1);
@@ -175,11 +249,12 @@ __global__ void __launch_bounds__(kPThreads, 1)
       mbar_init(bar(kBarKVFull + s), 1);
       mbar_init(bar(kBarKVEmpty + s), 1);
     }
-    mbar_init(bar(kBarSFull), 1);
-    mbar_init(bar(kBarSFree), 128);
-    mbar_init(bar(kBarPFull), 128);
-    mbar_init(bar(kBarPVDone + 0), 1);
-    mbar_init(bar(kBarPVDone + 1), 1);
+    for (int x = 0; x < kQT; ++x) {
+      mbar_init(bar(kBarSFull + x), 1);
+      mbar_init(bar(kBarSFree + x), 128);
+      mbar_init(bar(kBarPFull + x), 128);
+      mbar_init(bar(kBarPVDone + x), 1);
+    }
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -194,16 +269,16 @@ __global__ void __launch_bounds__(kPThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_holder;
-  const uint32_t tm_S = tmem;            // columns [0, 128)
-  const uint32_t tm_O0 = tmem + 128;     // columns [128, 192)
+  // TMEM columns: S of tile x [128x, +128); P of tile x [256+64x, +64);
+  // O of tile x [384+64x, +64)
   const uint32_t sQ = base + kOffQ;
-  const uint32_t sP = base + kOffP;
 
   if (warp == 0) {
     // ------------------------------------------------------ TMA producer --
     if (lane == 0) {
-      mbar_arrive_expect_tx(bar(kBarQ), kTileBytes);
-      tma_load_3d(sQ, &tm_q, 0, h, q0, bar(kBarQ));
+      mbar_arrive_expect_tx(bar(kBarQ), kQT * kTileBytes);
+      for (int x = 0; x < kQT; ++x)
+        tma_load_3d(sQ + x * kTileBytes, &tm_q, 0, h, q0 + x * kBM, bar(kBarQ));
       for (int i = 0; i < n_tiles; ++i) {
         const int s = i % kKVStages;
         const uint32_t u = (uint32_t)(i / kKVStages);
@@ -219,147 +294,177 @@ __global__ void __launch_bounds__(kPThreads, 1)
     if (lane == 0) {
       constexpr uint32_t idesc_qk = make_idesc(kBM, kBN, false);
       constexpr uint32_t idesc_pv = make_idesc(kBM, kHD, true);
-      auto issue_s = [&](int i) -> bool {
-        const int s = i % kKVStages;
-        if (!wait_or_abort(bar(kBarKVFull + s), (uint32_t)(i / kKVStages) & 1u, abort_flag))
-          return false;
+      auto issue_pv = [&](int x, int j) -> bool {  // O_x (+)= P_x V_j
+        if (!wait_or_abort(bar(kBarPFull + x), (uint32_t)j & 1u, abort_flag)) return false;
         tc_fence_after();
-        const uint32_t sK = base + kOffKV + s * 2 * kTileBytes;
-#pragma unroll
-        for (int k = 0; k < kHD / 16; ++k)
-          tc_mma(tm_S, sw128_desc(sQ + k * 32), sw128_desc(sK + k * 32), idesc_qk, k > 0);
-        tc_commit(bar(kBarSFull));
-        return true;
-      };
-      bool ok = wait_or_abort(bar(kBarQ), 0, abort_flag) && issue_s(0);
-      for (int i = 0; ok && i < n_tiles; ++i) {
-        if (i + 1 < n_tiles) {
-          // the softmax has read S_i: issue S_{i+1} while it works on tile i
-          ok = wait_or_abort(bar(kBarSFree), (uint32_t)i & 1u, abort_flag) && issue_s(i + 1);
-          if (!ok) break;
-        }
-        if (!wait_or_abort(bar(kBarPFull), (uint32_t)i & 1u, abort_flag)) break;
-        tc_fence_after();
-        const int s = i % kKVStages;
-        const uint32_t sV = base + kOffKV + s * 2 * kTileBytes + kTileBytes;
-        const uint32_t tm_O = tm_O0 + (uint32_t)(i & 1) * kHD;
+        const uint32_t sV = base + kOffKV + (j % kKVStages) * 2 * kTileBytes + kTileBytes;
+        // A = P from TMEM (16 keys = 8 columns of bf16 pairs per MMA)
 #pragma unroll
         for (int k = 0; k < kBN / 16; ++k)
-          tc_mma(tm_O, sw128_desc(sP + (k >> 2) * kTileBytes + (k & 3) * 32),
-                 sw128_desc(sV + k * 16 * 128), idesc_pv, k > 0);
-        tc_commit(bar(kBarPVDone + (i & 1)));
-        tc_commit(bar(kBarKVEmpty + s));
+          tc_mma_ts(tmem + kTmemO + 64 * x, tmem + kTmemP + 64 * x + 8 * k,
+                    sw128_desc(sV + k * 16 * 128), idesc_pv, (j > 0 || k > 0) ? 1u : 0u);
+        tc_commit(bar(kBarPVDone + x));
+        return true;
+      };
+      bool ok = wait_or_abort(bar(kBarQ), 0, abort_flag);
+      for (int i = 0; ok && i < n_tiles; ++i) {
+        const int s = i % kKVStages;
+        if (!wait_or_abort(bar(kBarKVFull + s), (uint32_t)(i / kKVStages) & 1u, abort_flag)) break;
+        const uint32_t sK = base + kOffKV + s * 2 * kTileBytes;
+        for (int x = 0; ok && x < kQT; ++x) {
+          if (i >= ntile(x)) continue;
+          // the softmax has read S_x of tile i-1
+          if (i > 0 && !wait_or_abort(bar(kBarSFree + x), (uint32_t)(i - 1) & 1u, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+#pragma unroll
+          for (int k = 0; k < kHD / 16; ++k)
+            tc_mma(tmem + 128 * x, sw128_desc(sQ + x * kTileBytes + k * 32),
+                   sw128_desc(sK + k * 32), idesc_qk, k > 0);
+          tc_commit(bar(kBarSFull + x));
+        }
+        if (!ok) break;
+        if (i > 0) {
+          for (int x = 0; ok && x < kQT; ++x)
+            if (i - 1 < ntile(x)) ok = issue_pv(x, i - 1);
+          tc_commit(bar(kBarKVEmpty + (i - 1) % kKVStages));
+        }
       }
+      for (int x = 0; ok && x < kQT; ++x)
+        if (n_tiles - 1 < ntile(x)) ok = issue_pv(x, n_tiles - 1);
     }
-  } else if (warp >= 4) {
+  } else {
     // ------------------------------------------- softmax / epilogue (r) --
-    const int r = (warp - 4) * 32 + lane;              // query row of this thread
-    const uint32_t lane_off = (uint32_t)((warp - 4) * 32) << 16;
-    const int qpos = p.start_pos + q0 + r;             // absolute position of the row
-    float m_run = -INFINITY, l_run = 0.f, alpha_prev = 0.f;
-    float o[kHD];
-#pragma unroll
-    for (int j = 0; j < kHD; ++j) o[j] = 0.f;
-
-    auto fold = [&](int i) -> bool {  // o = o * alpha_prev + O_tile_i
-      if (!wait_or_abort(bar(kBarPVDone + (i & 1)), (uint32_t)(i >> 1) & 1u, abort_flag))
-        return false;
+    const int x = (warp - 2) >> 2;                      // query tile of this warpgroup
+    const int sub = warp & 3;                           // TMEM lane quarter
+    const int r = sub * 32 + lane;                      // row within the tile
+    const uint32_t lane_off = (uint32_t)(sub * 32) << 16;
+    const uint32_t tm_S = tmem + 128 * x + lane_off;
+    const uint32_t tm_O = tmem + kTmemO + 64 * x + lane_off;
+    const uint32_t tm_P = tmem + kTmemP + 64 * x + lane_off;
+    const int row = q0 + x * kBM + r;                   // query token index
+    const int qpos = p.start_pos + row;                 // its absolute position
+    const float c = p.scale_log2;
+    float m_run = -INFINITY, l_run = 0.f;
+    const int nt = ntile(x);
+    bool ok = true;
+    auto wait_pv = [&](int j) -> bool {  // PV_x of tile j done
+      if (!wait_or_abort(bar(kBarPVDone + x), (uint32_t)j & 1u, abort_flag)) return false;
       tc_fence_after();
-      const uint32_t tm_O = tm_O0 + (uint32_t)(i & 1) * kHD + lane_off;
-      float t0[32], t1[32];
-      tmem_ld32(tm_O, t0);
-      tmem_ld32(tm_O + 32, t1);
-      tmem_ld_wait();
-#pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        o[j] = fmaf(o[j], alpha_prev, t0[j]);
-        o[32 + j] = fmaf(o[32 + j], alpha_prev, t1[j]);
-      }
       return true;
     };
 
-    bool ok = true;
-    for (int i = 0; i < n_tiles; ++i) {
-      if (!wait_or_abort(bar(kBarSFull), (uint32_t)i & 1u, abort_flag)) { ok = false; break; }
+    for (int i = 0; i < nt; ++i) {
+      if (!wait_or_abort(bar(kBarSFull + x), (uint32_t)i & 1u, abort_flag)) { ok = false; break; }
       tc_fence_after();
+      const int kbase = i * kBN;
+      const bool diag = kbase + kBN - 1 > qpos;
+
+      // the whole S row in one round trip
       float sv[kBN];
-      {
-        float c[32];
 #pragma unroll
-        for (int cc = 0; cc < kBN / 32; ++cc) {
-          tmem_ld32(tm_S + lane_off + cc * 32, c);
-#pragma unroll
-          for (int j = 0; j < 32; ++j) sv[cc * 32 + j] = c[j];
-        }
+      for (int cc = 0; cc < kBN / 32; ++cc) {
+        float* dst = sv + cc * 32;
+        tmem_ld32(tm_S + cc * 32, *reinterpret_cast<float(*)[32]>(dst));
       }
       tmem_ld_wait();
       tc_fence_before();
-      mbar_arrive(bar(kBarSFree));
+      mbar_arrive(bar(kBarSFree + x));       // S_x may be overwritten
 
-      // causal mask (only tiles reaching past this row's position) and max
-      const int kbase = i * kBN;
-      float mx = -INFINITY;
-      if (kbase + kBN - 1 > qpos) {
+      // scale (packed pairs) and mask; 8 independent running maxima
+      const f2 c2 = mk2(c, c);
 #pragma unroll
-        for (int j = 0; j < kBN; ++j) {
-          sv[j] = (kbase + j <= qpos) ? sv[j] * p.scale_log2 : -INFINITY;
-          mx = fmaxf(mx, sv[j]);
+      for (int j = 0; j < kBN; j += 2) {
+        const f2 t = mul2(mk2(sv[j], sv[j + 1]), c2);
+        brk2(t, sv[j], sv[j + 1]);
+      }
+      if (diag) {
+#pragma unroll
+        for (int j = 0; j < kBN; ++j) sv[j] = (kbase + j > qpos) ? -INFINITY : sv[j];
+      }
+      float mx8[8];
+#pragma unroll
+      for (int a = 0; a < 8; ++a) mx8[a] = sv[a];
+#pragma unroll
+      for (int j = 8; j < kBN; ++j) mx8[j & 7] = fmaxf(mx8[j & 7], sv[j]);
+      const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                             fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+
+      // PV of tile i-1 done: O is stable and P_x may be overwritten
+      if (i > 0 && !wait_pv(i - 1)) { ok = false; break; }
+      if (mx > m_run + kLazyTau) {  // first tile, or the max grew by > 2^8
+        const float alpha = ex2(m_run - mx);
+        m_run = mx;
+        l_run *= alpha;
+        if (i > 0) {
+#pragma unroll 1
+          for (int cc = 0; cc < kHD / 16; ++cc) {
+            float o[16];
+            tmem_ld16(tm_O + cc * 16, o);
+            tmem_ld_wait();
+#pragma unroll
+            for (int j = 0; j < 16; ++j) o[j] *= alpha;
+            tmem_st16(tm_O + cc * 16, o);
+          }
         }
-      } else {
+      }
+
+      // P = 2^(s*c - m) (exactly 0 where masked: 2^-inf) as bf16 pairs into
+      // TMEM: column q of P holds keys 2q (low half) and 2q+1 (high half)
+      const f2 m2 = mk2(-m_run, -m_run);
+      f2 rs2[4];
 #pragma unroll
-        for (int j = 0; j < kBN; ++j) {
-          sv[j] *= p.scale_log2;
-          mx = fmaxf(mx, sv[j]);
+      for (int a = 0; a < 4; ++a) rs2[a] = mk2(0.f, 0.f);
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        float pw[32];
+#pragma unroll
+        for (int q = 0; q < 32; ++q) {
+          const int j = half * 64 + 2 * q;
+          float lo, hi;
+          brk2(add2(mk2(sv[j], sv[j + 1]), m2), lo, hi);
+          lo = ex2(lo);
+          hi = ex2(hi);
+          rs2[q & 3] = add2(rs2[q & 3], mk2(lo, hi));
+          pw[q] = __uint_as_float(pack_bf16x2(lo, hi));
         }
+        tmem_st32(tm_P + half * 32, pw);
       }
-      const float m_new = fmaxf(m_run, mx);
-      const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
-      const float alpha = ex2(m_run - m_use);
-      float rs = 0.f;
-#pragma unroll
-      for (int j = 0; j < kBN; ++j) {
-        sv[j] = ex2(sv[j] - m_use);
-        rs += sv[j];
+      {
+        f2 t = add2(add2(rs2[0], rs2[1]), add2(rs2[2], rs2[3]));
+        float lo, hi;
+        brk2(t, lo, hi);
+        l_run += lo + hi;
       }
-      l_run = l_run * alpha + rs;
-      m_run = m_new;
-
-      // PV_{i-1} finished: fold it, and P's buffer is free again
-      if (i > 0 && !fold(i - 1)) { ok = false; break; }
-
-      // P row r -> shared memory, 128-byte swizzle: 16-byte chunk c of row r
-      // sits at chunk position c ^ (r % 8); keys 0-63 and 64-127 in two tiles
-#pragma unroll
-      for (int c = 0; c < kBN / 8; ++c) {
-        const uint32_t w0 = pack_bf16x2(sv[c * 8 + 0], sv[c * 8 + 1]);
-        const uint32_t w1 = pack_bf16x2(sv[c * 8 + 2], sv[c * 8 + 3]);
-        const uint32_t w2 = pack_bf16x2(sv[c * 8 + 4], sv[c * 8 + 5]);
-        const uint32_t w3 = pack_bf16x2(sv[c * 8 + 6], sv[c * 8 + 7]);
-        const uint32_t addr =
-            sP + (c >> 3) * kTileBytes + r * 128 + (((c & 7) ^ (r & 7)) << 4);
-        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(w0), "r"(w1),
-                     "r"(w2), "r"(w3)
-                     : "memory");
-      }
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(bar(kBarPFull));
-      alpha_prev = alpha;
+      mbar_arrive(bar(kBarPFull + x));       // P_x (and any O rescale) ready
     }
-    if (ok) ok = fold(n_tiles - 1);
 
-    // epilogue: normalise and store row r (128 contiguous bytes)
-    if (q0 + r < p.S) {
+    // epilogue: O / l for row r (128 contiguous bytes)
+    if (nt > 0) {
+      if (ok) ok = wait_pv(nt - 1);
+      tc_fence_after();
       const float inv = ok ? 1.f / l_run : __int_as_float(0x7fc00000);
-      uint4* dst = reinterpret_cast<uint4*>(p.out + ((size_t)(q0 + r) * p.Hq + h) * kHD);
+      uint4* dst = reinterpret_cast<uint4*>(p.out + ((size_t)row * p.Hq + h) * kHD);
 #pragma unroll
-      for (int c = 0; c < kHD / 8; ++c) {
-        uint4 v;
-        v.x = pack_bf16x2(o[c * 8 + 0] * inv, o[c * 8 + 1] * inv);
-        v.y = pack_bf16x2(o[c * 8 + 2] * inv, o[c * 8 + 3] * inv);
-        v.z = pack_bf16x2(o[c * 8 + 4] * inv, o[c * 8 + 5] * inv);
-        v.w = pack_bf16x2(o[c * 8 + 6] * inv, o[c * 8 + 7] * inv);
-        dst[c] = v;
+      for (int cc = 0; cc < kHD / 32; ++cc) {
+        float o[32];
+        tmem_ld32(tm_O + cc * 32, o);
+        tmem_ld_wait();
+        if (row < p.S) {
+#pragma unroll
+          for (int q8 = 0; q8 < 4; ++q8) {
+            uint4 w;
+            w.x = pack_bf16x2(o[q8 * 8 + 0] * inv, o[q8 * 8 + 1] * inv);
+            w.y = pack_bf16x2(o[q8 * 8 + 2] * inv, o[q8 * 8 + 3] * inv);
+            w.z = pack_bf16x2(o[q8 * 8 + 4] * inv, o[q8 * 8 + 5] * inv);
+            w.w = pack_bf16x2(o[q8 * 8 + 6] * inv, o[q8 * 8 + 7] * inv);
+            dst[cc * 4 + q8] = w;
+          }
+        }
       }
     }
   }
@@ -444,9 +549,9 @@ cudaError_t launch_prefill(const void* q, const void* k, const void* v, int S, i
   p.Hq = Hq;
   p.Hkv = Hkv;
   p.g = Hq / Hkv;
-  p.n_qt = (S + kBM - 1) / kBM;
+  p.n_pairs = (S + kQT * kBM - 1) / (kQT * kBM);
   p.scale_log2 = scale * 1.4426950408889634f;
-  const long long blocks = (long long)p.n_qt * Hq;
+  const long long blocks = (long long)p.n_pairs * Hq;
   if (blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
   prefill_tcgen05_kernel<<<(unsigned)blocks, kPThreads, kSmemBytes, stream>>>(mq, mk, mv, p);
   return cudaGetLastError();
