@@ -5,38 +5,45 @@
 //   out[b,h,:] = softmax_j(scale * q[b,h,:] . K[b,h/g,j,:]) V[b,h/g,j,:]
 // over cache rows j = 0..positions[b] only (the slice replaces the
 // full-length boolean mask of section 2.1, so the work follows position+1 and
-// not max_len, sections 2.4 and 6.4).
+// not max_len, sections 2.4 and 6.4).  Optionally the step's new K/V row is
+// appended in the same launch (the page writes the row, then attends).
 //
 // How (GB300 design, not the page's: the page calls PyTorch SDPA):
 //  * The attended rows of every (sequence, KV head) pair -- a "segment" -- are
-//    cut into 64-row tiles.  All tiles of all segments form one flat list,
-//    and CTA c of the persistent grid (one CTA per SM; G = min(grid, T)
-//    working CTAs, or one per segment when segments average <= 8 tiles)
-//    takes the contiguous range [c*T/G, (c+1)*T/G) of it.  The split is computed on the device from
-//    `positions`, so the launch does not depend on the positions and the
-//    load is balanced to within one tile however ragged the batch is.
-//  * One producer thread streams K and V tiles with 1-D bulk copies (TMA) into
-//    a 4-stage shared-memory ring guarded by mbarriers.  Each tile is read
-//    from HBM once and serves all g query heads of its KV head.
+//    cut into 64-row tiles.  One producer thread streams K and V tiles with
+//    1-D bulk copies (TMA) into a 4-stage shared-memory ring guarded by
+//    mbarriers.  Each tile is read from HBM once and serves all g query
+//    heads of its KV head.
 //  * 16 consumer warps (8 for g=8) each take 4 (8) keys of a tile, two at a
 //    time (one per half-warp; a lane holds 8 of the 128 dims, as fp32 pairs
-//    for the packed fma.rn.f32x2).  q.k partial sums of the g
-//    heads are reduced across the 16 lanes with a transposing butterfly
-//    (each shuffle step halves the number of heads still carried), and the
-//    softmax is kept online in fp32 (running max and sum per head, in base 2
-//    with scale*log2(e) folded into q).
-//  * When a CTA finishes its part of a segment it merges its warps.  If it
-//    covered the whole segment it writes the output; otherwise it stores a
-//    partial (max, sum, unnormalised o) and takes a ticket; the CTA that
-//    arrives last combines the partials of that segment and writes the output
-//    (the split-KV combine pass, fused, with no spin-wait).
+//    for the packed fma.rn.f32x2).  q.k partial sums of the g heads are
+//    reduced across the 16 lanes with a transposing butterfly (each shuffle
+//    step halves the number of heads still carried), and the softmax is kept
+//    online in fp32 (running max and sum per head, in base 2 with
+//    scale*log2(e) folded into q).
+//  * Two ways to split a segment over CTAs, both computed on the device from
+//    `positions` (one launch serves any positions; graph-capturable):
+//    - cluster mode (few segments, e.g. B=1): one thread-block cluster of C
+//      CTAs (16 or 8) per segment; CTA rank r takes tiles
+//      [r*n/C, (r+1)*n/C).  The partials (max, sum, unnormalised o) are
+//      merged through distributed shared memory between two cluster
+//      barriers -- no global scratch, no atomics.
+//    - stream-K mode (many segments): all tiles of all segments form one flat
+//      list; CTA c of a persistent grid (one per SM) takes
+//      [c*T/G, (c+1)*T/G), balanced to one tile however ragged the batch is.
+//      A segment split over CTAs is merged by the CTA that arrives last at
+//      the segment's arrival counter (fp32 partials in the workspace; no
+//      spin-wait).
 #include <cfloat>
+#include <cooperative_groups.h>
 
 #include "common.cuh"
 #include "internal.h"
 
 namespace gqa {
 namespace {
+
+namespace cg = cooperative_groups;
 
 constexpr int kD = 128;
 constexpr int kTile = 64;                          // keys per pipeline stage
@@ -65,14 +72,19 @@ struct Params {
   float qscale;  // scale * log2(e)
 };
 
-// Consumer warps per CTA: more warps hide the latency of the shuffle chains;
-// g=8 keeps 8 warps (its q and o registers would not fit 16).
+// Lanes per key (LPK): a key's 128 dims are spread over LPK lanes of a warp
+// (128/LPK dims each), so a warp takes 32/LPK keys per step.  Fewer lanes
+// per key means fewer shuffle-reduction steps but more q and o registers
+// (32*g/LPK*2 each): g <= 4 uses 8 lanes, g = 8 uses 16.  NW consumer warps
+// are as many as the registers allow.
 template <int G> struct Cfg {
-  static constexpr int NW = (G >= 8) ? 8 : 16;
+  static constexpr int LPK = (G >= 8) ? 16 : 8;
+  static constexpr int NW = (G == 1) ? 16 : 8;
   static constexpr int kThreads = (NW + 1) * 32;   // + one producer warp
   static constexpr int kConsumers = NW * 32;
   static constexpr int kKeysPerWarp = kTile / NW;  // 4 or 8
-  static constexpr int kIters = kKeysPerWarp / 2;  // two keys per warp step
+  static constexpr int kKeysPerStep = 32 / LPK;    // 4 or 2
+  static constexpr int kIters = kKeysPerWarp / kKeysPerStep;
   // registers per thread that still let one CTA of kThreads fit the SM
   // (the register file is handed out as if the block were a multiple of
   // 128 threads)
@@ -82,6 +94,11 @@ template <int G> struct Cfg {
 template <int NC>
 __device__ __forceinline__ void consumer_bar() {
   asm volatile("bar.sync 1, %0;" ::"n"(NC) : "memory");
+}
+
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
+               "barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
 // Position of flat tile t within (sequence, KV head, tile) order.
@@ -127,19 +144,20 @@ template <> struct Log2<1> { static constexpr int v = 0; };
 template <> struct Log2<2> { static constexpr int v = 1; };
 template <> struct Log2<4> { static constexpr int v = 2; };
 template <> struct Log2<8> { static constexpr int v = 3; };
+template <> struct Log2<16> { static constexpr int v = 4; };
 
-// Sum of acc[h] over the 16 lanes of a half-warp, for every head at once.
-// Step with offset `off` keeps half of the heads and ships the other half to
-// the partner lane, so after log2(G) steps each lane carries one head:
-// head = l16 >> (4 - log2 G).  The remaining steps are a plain butterfly.
-template <int G>
-__device__ __forceinline__ float reduce16(float (&acc)[G], int l16) {
+// Sum of acc[h] over the LPK lanes holding one key, for every head at once.
+// A step with offset `off` keeps half of the heads and ships the other half
+// to the partner lane, so after log2(G) steps each lane carries one head:
+// head = lk >> (log2 LPK - log2 G).  The remaining steps are a plain butterfly.
+template <int G, int LPK>
+__device__ __forceinline__ float reduce_key(float (&acc)[G], int lk) {
   constexpr int LG = Log2<G>::v;
 #pragma unroll
   for (int st = 0; st < LG; ++st) {
-    const int off = 8 >> st;
+    const int off = (LPK / 2) >> st;
     const int n = G >> (st + 1);
-    const bool upper = (l16 & off) != 0;
+    const bool upper = (lk & off) != 0;
 #pragma unroll
     for (int i = 0; i < n; ++i) {
       const float keep = upper ? acc[n + i] : acc[i];
@@ -149,7 +167,7 @@ __device__ __forceinline__ float reduce16(float (&acc)[G], int l16) {
   }
   float v = acc[0];
 #pragma unroll
-  for (int off = 8 >> LG; off >= 1; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+  for (int off = (LPK / 2) >> LG; off >= 1; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
   return v;
 }
 
@@ -161,6 +179,254 @@ __device__ __forceinline__ void unpack8x2(const uint4& u, f2 (&f)[4]) {
   f[3] = mk2(bf16lo(u.w), bf16hi(u.w));
 }
 
+// Per-warp consumer state and math: one KV head's g query heads.  Lane
+// `lane` works on key group grp = lane / LPK (32/LPK keys per step) and holds
+// 128/LPK dims of that key: VPL 16-byte vectors, vector v covering dims
+// 8*(lk + LPK*v) .. +8 (lk = lane % LPK), as fp32 pairs for fma.rn.f32x2.
+template <int G>
+struct Consumer {
+  static constexpr int LG = Log2<G>::v;
+  static constexpr int LPK = Cfg<G>::LPK;
+  static constexpr int LL = Log2<LPK>::v;
+  static constexpr int VPL = 16 / LPK;             // 16-byte vectors per lane per row
+  static constexpr int NP = 4 * VPL;               // fp32 pairs per lane per row
+  static constexpr int KPS = Cfg<G>::kKeysPerStep;
+  static constexpr int KPW = Cfg<G>::kKeysPerWarp;
+  static constexpr int IT = Cfg<G>::kIters;
+  static constexpr float kTau = 8.0f;  // a stale running max may lag by 2^8
+  f2 qf[G][NP];  // q[h][lane dims], pre-scaled by scale*log2(e)
+  f2 o[G][NP];   // unnormalised output accumulators, same layout
+  float m_run, l_run;  // for head hd (the same in every key group)
+  int grp, lk, hd;
+
+  __device__ __forceinline__ void init(int lane) {
+    grp = lane >> LL;
+    lk = lane & (LPK - 1);
+    hd = lk >> (LL - LG);  // head whose score this lane ends up with
+  }
+  __device__ __forceinline__ int dim_off(int v) const { return (lk + LPK * v) * 16; }  // bytes
+  // qb: q[b][kvh*G][0]
+  __device__ __forceinline__ void load_q(const uint16_t* qb, float qscale) {
+#pragma unroll
+    for (int h = 0; h < G; ++h)
+#pragma unroll
+      for (int v = 0; v < VPL; ++v) {
+        const uint4 u = *reinterpret_cast<const uint4*>(
+            reinterpret_cast<const uint8_t*>(qb + (size_t)h * kD) + dim_off(v));
+        const uint32_t wd[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          qf[h][4 * v + j] = mk2(bf16lo(wd[j]) * qscale, bf16hi(wd[j]) * qscale);
+      }
+  }
+  __device__ __forceinline__ void reset() {
+    m_run = -INFINITY;
+    l_run = 0.f;
+#pragma unroll
+    for (int h = 0; h < G; ++h)
+#pragma unroll
+      for (int j = 0; j < NP; ++j) o[h][j] = mk2(0.f, 0.f);
+  }
+  // Scores (log2 domain) of this warp's keys of a 64-key tile; keys >= rows
+  // are invalid (the rest of the stage may hold anything) and get -inf.
+  __device__ __forceinline__ void qk(const uint8_t* Ks, int rows, int warp, float (&sc)[IT]) {
+#pragma unroll
+    for (int it = 0; it < IT; ++it) {
+      const int key = warp * KPW + it * KPS + grp;
+      f2 a[G];
+#pragma unroll
+      for (int v = 0; v < VPL; ++v) {
+        const uint4 kv = *reinterpret_cast<const uint4*>(Ks + key * kRowBytes + dim_off(v));
+        f2 kf[4];
+        unpack8x2(kv, kf);
+#pragma unroll
+        for (int h = 0; h < G; ++h)
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            a[h] = (v == 0 && j == 0) ? mul2(qf[h][0], kf[0]) : fma2(qf[h][4 * v + j], kf[j], a[h]);
+      }
+      float acc[G];
+#pragma unroll
+      for (int h = 0; h < G; ++h) {
+        float lo, hi;
+        brk2(a[h], lo, hi);
+        acc[h] = lo + hi;
+      }
+      const float sv = reduce_key<G, LPK>(acc, lk);
+      sc[it] = (key < rows) ? sv : -INFINITY;
+    }
+  }
+  // Online softmax for head hd over the tile's scores -> probabilities pr.
+  __device__ __forceinline__ void softmax(const float (&sc)[IT], float (&pr)[IT]) {
+    float mx = sc[0];
+#pragma unroll
+    for (int it = 1; it < IT; ++it) mx = fmaxf(mx, sc[it]);
+#pragma unroll
+    for (int off = LPK; off < 32; off <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+    // Raise the running max only when it grows by more than 2^kTau (the
+    // first valid tile always does): p may then reach 2^kTau, harmless in
+    // fp32, and most tiles skip the rescale of o.
+    const bool grow = mx > m_run + kTau;
+    if (__any_sync(0xffffffffu, grow)) {
+      const float alpha = grow ? ex2(m_run - mx) : 1.f;  // m_run = -inf: 0
+      if (grow) m_run = mx;
+      l_run *= alpha;
+#pragma unroll
+      for (int h = 0; h < G; ++h) {
+        const float ah = __shfl_sync(0xffffffffu, alpha, h << (LL - LG));
+        const f2 a2 = mk2(ah, ah);
+#pragma unroll
+        for (int j = 0; j < NP; ++j) o[h][j] = mul2(o[h][j], a2);
+      }
+    }
+    const float m_use = (m_run == -INFINITY) ? 0.f : m_run;  // no valid key yet
+    float ps = 0.f;
+#pragma unroll
+    for (int it = 0; it < IT; ++it) {
+      pr[it] = ex2(sc[it] - m_use);
+      ps += pr[it];
+    }
+#pragma unroll
+    for (int off = LPK; off < 32; off <<= 1) ps += __shfl_xor_sync(0xffffffffu, ps, off);
+    l_run += ps;
+  }
+  // o += p * v over this warp's keys of a tile.
+  __device__ __forceinline__ void pv(const uint8_t* Vs, int rows, int warp, const float (&pr)[IT]) {
+#pragma unroll
+    for (int it = 0; it < IT; ++it) {
+      const int key = warp * KPW + it * KPS + grp;
+      float ph[G];
+#pragma unroll
+      for (int h = 0; h < G; ++h)
+        ph[h] = __shfl_sync(0xffffffffu, pr[it], (grp << LL) | (h << (LL - LG)));
+      const bool valid = key < rows;  // invalid: p = 0, and v forced to 0 (stale smem)
+#pragma unroll
+      for (int v = 0; v < VPL; ++v) {
+        uint4 vv = *reinterpret_cast<const uint4*>(Vs + key * kRowBytes + dim_off(v));
+        vv.x = valid ? vv.x : 0u;
+        vv.y = valid ? vv.y : 0u;
+        vv.z = valid ? vv.z : 0u;
+        vv.w = valid ? vv.w : 0u;
+        f2 vf[4];
+        unpack8x2(vv, vf);
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+          const f2 p2 = mk2(ph[h], ph[h]);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) o[h][4 * v + j] = fma2(p2, vf[j], o[h][4 * v + j]);
+        }
+      }
+    }
+  }
+  // One 64-key tile: scores, online softmax, P.V.
+  __device__ __forceinline__ void tile(const uint8_t* Ks, const uint8_t* Vs, int rows, int warp) {
+    float sc[IT], pr[IT];
+    qk(Ks, rows, warp, sc);
+    softmax(sc, pr);
+    pv(Vs, rows, warp, pr);
+  }
+  // This warp's (m, l, o) -> merge buffers [warp][G][...]: the key groups
+  // hold partial o for the same (m, l), so they are added first.
+  __device__ __forceinline__ void stash(float* merge_o, float* merge_ml, int warp) {
+#pragma unroll
+    for (int h = 0; h < G; ++h)
+#pragma unroll
+      for (int j = 0; j < NP; ++j) {
+        float lo, hi;
+        brk2(o[h][j], lo, hi);
+#pragma unroll
+        for (int off = LPK; off < 32; off <<= 1) {
+          lo += __shfl_xor_sync(0xffffffffu, lo, off);
+          hi += __shfl_xor_sync(0xffffffffu, hi, off);
+        }
+        o[h][j] = mk2(lo, hi);
+      }
+    if (grp == 0) {
+#pragma unroll
+      for (int h = 0; h < G; ++h)
+#pragma unroll
+        for (int v = 0; v < VPL; ++v) {
+          float f[8];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) brk2(o[h][4 * v + j], f[2 * j], f[2 * j + 1]);
+          float4* dst = reinterpret_cast<float4*>(
+              reinterpret_cast<uint8_t*>(merge_o + (warp * G + h) * kD) + dim_off(v) * 2);
+          dst[0] = make_float4(f[0], f[1], f[2], f[3]);
+          dst[1] = make_float4(f[4], f[5], f[6], f[7]);
+        }
+      if (lk == (hd << (LL - LG))) {
+        merge_ml[(warp * G + hd) * 2 + 0] = m_run;
+        merge_ml[(warp * G + hd) * 2 + 1] = l_run;
+      }
+    }
+  }
+};
+
+// Merge the NW warps' partials of (head h, dim d): returns max M, sum Ls and
+// unnormalised Os, all relative to M.
+template <int NW, int G>
+__device__ __forceinline__ void merge_warps(const float* merge_o, const float* merge_ml, int h,
+                                            int d, float& M, float& Ls, float& Os) {
+  M = -INFINITY;
+#pragma unroll
+  for (int ww = 0; ww < NW; ++ww) M = fmaxf(M, merge_ml[(ww * G + h) * 2]);
+  Ls = 0.f;
+  Os = 0.f;
+  const float Mu = (M == -INFINITY) ? 0.f : M;
+#pragma unroll
+  for (int ww = 0; ww < NW; ++ww) {
+    const float e = ex2(merge_ml[(ww * G + h) * 2] - Mu);
+    Ls = fmaf(merge_ml[(ww * G + h) * 2 + 1], e, Ls);
+    Os = fmaf(merge_o[(ww * G + h) * kD + d], e, Os);
+  }
+}
+
+// Producer: one tile's bulk copies.  With the fused append the segment's
+// last tile ends with row pos = n-1, taken from k_new/v_new (copied into the
+// tile and, by this thread, into the cache).  No other CTA reads that row.
+__device__ __forceinline__ void produce_tile(const Params& p, uint8_t* stages, uint64_t* bars,
+                                             int s, int b, int kvh, int k, int ntiles, int n) {
+  const int rows = min(kTile, n - k * kTile);
+  const size_t row0 = ((size_t)b * p.Hkv + kvh) * (size_t)p.L + (size_t)k * kTile;
+  const uint32_t full = smem_u32(&bars[s]);
+  const uint32_t sK = smem_u32(stages + (size_t)s * 2 * kTileBytes);
+  const uint32_t sV = sK + kTileBytes;
+  const bool fresh = p.k_new != nullptr && k == ntiles - 1;
+  const int cache_rows = fresh ? rows - 1 : rows;
+  mbar_arrive_expect_tx(full, 2u * (uint32_t)rows * kRowBytes);
+  if (cache_rows > 0) {
+    const uint32_t bytes = (uint32_t)cache_rows * kRowBytes;
+    bulk_g2s(sK, p.k_cache + row0 * kRowBytes, bytes, full);
+    bulk_g2s(sV, p.v_cache + row0 * kRowBytes, bytes, full);
+  }
+  if (fresh) {
+    const size_t src = ((size_t)b * p.Hkv + kvh) * kRowBytes;
+    const uint32_t off = (uint32_t)cache_rows * kRowBytes;
+    bulk_g2s(sK + off, p.k_new + src, kRowBytes, full);
+    bulk_g2s(sV + off, p.v_new + src, kRowBytes, full);
+    const uint4* kn = reinterpret_cast<const uint4*>(p.k_new + src);
+    const uint4* vn = reinterpret_cast<const uint4*>(p.v_new + src);
+    uint4* kd = reinterpret_cast<uint4*>(p.k_cache + (row0 + cache_rows) * kRowBytes);
+    uint4* vd = reinterpret_cast<uint4*>(p.v_cache + (row0 + cache_rows) * kRowBytes);
+#pragma unroll
+    for (int c = 0; c < kRowBytes / 16; ++c) {
+      kd[c] = kn[c];
+      vd[c] = vn[c];
+    }
+  }
+}
+
+__device__ __forceinline__ void write_nan_rows(const Params& p, int b) {
+  const uint4 nan4 = make_uint4(0x7fc07fc0u, 0x7fc07fc0u, 0x7fc07fc0u, 0x7fc07fc0u);
+  uint4* o4 = reinterpret_cast<uint4*>(p.out + (size_t)b * p.Hq * kD);
+  for (int i = 0; i < p.Hq * kD / 8; ++i) o4[i] = nan4;
+}
+
+__device__ __forceinline__ void store_bf16(uint16_t* dst, float v) {
+  __nv_bfloat16 r = __float2bfloat16_rn(v);
+  *dst = *reinterpret_cast<uint16_t*>(&r);
+}
+
 template <int G>
 size_t smem_bytes(int B) {
   constexpr int NW = Cfg<G>::NW;
@@ -169,13 +435,11 @@ size_t smem_bytes(int B) {
          (size_t)NW * G * kD * sizeof(float) + (size_t)(B + 1) * sizeof(int);
 }
 
+// ---------------------------------------------------------- stream-K mode --
 template <int G>
 __global__ void __maxnreg__(Cfg<G>::kMaxRegs) decode_splitkv_kernel(const Params p) {
-  constexpr int LG = Log2<G>::v;
   constexpr int NW = Cfg<G>::NW;
   constexpr int NC = Cfg<G>::kConsumers;
-  constexpr int KPW = Cfg<G>::kKeysPerWarp;
-  constexpr int IT = Cfg<G>::kIters;
   extern __shared__ __align__(1024) uint8_t smem[];
   uint8_t* stages = smem;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kStages * 2 * kTileBytes);
@@ -217,9 +481,7 @@ __global__ void __maxnreg__(Cfg<G>::kMaxRegs) decode_splitkv_kernel(const Params
       } else if (b % gridDim.x == blockIdx.x) {
         // out-of-range position: flag it and make the sequence's output NaN
         set_status(p.status, ATTN_DEV_BAD_POSITION);
-        uint4 nan4 = make_uint4(0x7fc07fc0u, 0x7fc07fc0u, 0x7fc07fc0u, 0x7fc07fc0u);
-        uint4* o4 = reinterpret_cast<uint4*>(p.out + (size_t)b * p.Hq * kD);
-        for (int i = 0; i < p.Hq * kD / 8; ++i) o4[i] = nan4;
+        write_nan_rows(p, b);
       }
     }
     int x = v;
@@ -272,37 +534,7 @@ __global__ void __maxnreg__(Cfg<G>::kMaxRegs) decode_splitkv_kernel(const Params
           set_status(p.status, ATTN_DEV_TIMEOUT);
           break;
         }
-        const int rows = min(kTile, w.n - w.k * kTile);
-        const size_t row0 = ((size_t)w.b * Hkv + w.kvh) * (size_t)L + (size_t)w.k * kTile;
-        const uint32_t full = smem_u32(&bars[s]);
-        const uint32_t sK = smem_u32(stages + (size_t)s * 2 * kTileBytes);
-        const uint32_t sV = sK + kTileBytes;
-        // Fused append: the segment's last tile ends with row pos = n-1,
-        // which comes from k_new/v_new (copied into the tile and, by this
-        // thread, into the cache).  No other CTA reads that row.
-        const bool fresh = p.k_new != nullptr && w.k == w.ntiles - 1;
-        const int cache_rows = fresh ? rows - 1 : rows;
-        mbar_arrive_expect_tx(full, 2u * (uint32_t)rows * kRowBytes);
-        if (cache_rows > 0) {
-          const uint32_t bytes = (uint32_t)cache_rows * kRowBytes;
-          bulk_g2s(sK, p.k_cache + row0 * kRowBytes, bytes, full);
-          bulk_g2s(sV, p.v_cache + row0 * kRowBytes, bytes, full);
-        }
-        if (fresh) {
-          const size_t src = ((size_t)w.b * Hkv + w.kvh) * kRowBytes;
-          const uint32_t off = (uint32_t)cache_rows * kRowBytes;
-          bulk_g2s(sK + off, p.k_new + src, kRowBytes, full);
-          bulk_g2s(sV + off, p.v_new + src, kRowBytes, full);
-          const uint4* kn = reinterpret_cast<const uint4*>(p.k_new + src);
-          const uint4* vn = reinterpret_cast<const uint4*>(p.v_new + src);
-          uint4* kd = reinterpret_cast<uint4*>(p.k_cache + (row0 + cache_rows) * kRowBytes);
-          uint4* vd = reinterpret_cast<uint4*>(p.v_cache + (row0 + cache_rows) * kRowBytes);
-#pragma unroll
-          for (int c = 0; c < kRowBytes / 16; ++c) {
-            kd[c] = kn[c];
-            vd[c] = vn[c];
-          }
-        }
+        produce_tile(p, stages, bars, s, w.b, w.kvh, w.k, w.ntiles, w.n);
         walk_next(w, prefix, p.positions, B, Hkv);
       }
     }
@@ -310,36 +542,12 @@ __global__ void __maxnreg__(Cfg<G>::kMaxRegs) decode_splitkv_kernel(const Params
   }
 
   // ------------------------------------------------------------ consumers --
-  const int half = lane >> 4, l16 = lane & 15;
-  const int hd = l16 >> (4 - LG);  // head whose score this lane ends up with
+  Consumer<G> cs;
+  cs.init(lane);
   Walk w;
   walk_init(w, t0, prefix, p.positions, B, Hkv);
-
-  f2 qf[G][4];   // q[h][8 lane dims] as 4 pairs, pre-scaled by scale*log2(e)
-  f2 o[G][4];    // unnormalised output accumulators, same layout
-  float m_run = -INFINITY, l_run = 0.f;
-
-  auto load_q = [&]() {
-    const uint16_t* qb = p.q + ((size_t)w.b * p.Hq + (size_t)w.kvh * G) * kD + l16 * 8;
-#pragma unroll
-    for (int h = 0; h < G; ++h) {
-      const uint4 u = *reinterpret_cast<const uint4*>(qb + (size_t)h * kD);
-      const uint32_t wd[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-      for (int j = 0; j < 4; ++j)
-        qf[h][j] = mk2(bf16lo(wd[j]) * p.qscale, bf16hi(wd[j]) * p.qscale);
-    }
-  };
-  auto reset_acc = [&]() {
-    m_run = -INFINITY;
-    l_run = 0.f;
-#pragma unroll
-    for (int h = 0; h < G; ++h)
-#pragma unroll
-      for (int j = 0; j < 4; ++j) o[h][j] = mk2(0.f, 0.f);
-  };
-  load_q();
-  reset_acc();
+  cs.load_q(p.q + ((size_t)w.b * p.Hq + (size_t)w.kvh * G) * kD, p.qscale);
+  cs.reset();
 
   long long i = 0;
   for (long long t = t0; t < t1; ++t, ++i) {
@@ -352,132 +560,29 @@ __global__ void __maxnreg__(Cfg<G>::kMaxRegs) decode_splitkv_kernel(const Params
     }
     const int rows = min(kTile, w.n - w.k * kTile);
     const uint8_t* Ks = stages + (size_t)s * 2 * kTileBytes;
-    const uint8_t* Vs = Ks + kTileBytes;
-
-    // scores of this warp's keys (two per step), log2 domain
-    float sc[IT];
-#pragma unroll
-    for (int it = 0; it < IT; ++it) {
-      const int key = warp * KPW + it * 2 + half;
-      const uint4 kv = *reinterpret_cast<const uint4*>(Ks + key * kRowBytes + l16 * 16);
-      f2 kf[4];
-      unpack8x2(kv, kf);
-      float acc[G];
-#pragma unroll
-      for (int h = 0; h < G; ++h) {
-        f2 a = mul2(qf[h][0], kf[0]);
-#pragma unroll
-        for (int j = 1; j < 4; ++j) a = fma2(qf[h][j], kf[j], a);
-        float lo, hi;
-        brk2(a, lo, hi);
-        acc[h] = lo + hi;
-      }
-      const float sv = reduce16<G>(acc, l16);
-      sc[it] = (key < rows) ? sv : -INFINITY;
-    }
-
-    // online softmax update for head hd
-    float mx = sc[0];
-#pragma unroll
-    for (int it = 1; it < IT; ++it) mx = fmaxf(mx, sc[it]);
-    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-    const float m_new = fmaxf(m_run, mx);
-    const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
-    const float alpha = ex2(m_run - m_use);
-    float pr[IT], ps = 0.f;
-#pragma unroll
-    for (int it = 0; it < IT; ++it) {
-      pr[it] = ex2(sc[it] - m_use);
-      ps += pr[it];
-    }
-    ps += __shfl_xor_sync(0xffffffffu, ps, 16);
-    l_run = l_run * alpha + ps;
-    m_run = m_new;
-
-#pragma unroll
-    for (int h = 0; h < G; ++h) {
-      const float a = __shfl_sync(0xffffffffu, alpha, h << (4 - LG));
-      const f2 a2 = mk2(a, a);
-#pragma unroll
-      for (int j = 0; j < 4; ++j) o[h][j] = mul2(o[h][j], a2);
-    }
-
-    // o += p * v
-#pragma unroll
-    for (int it = 0; it < IT; ++it) {
-      const int key = warp * KPW + it * 2 + half;
-      const uint4 vv = *reinterpret_cast<const uint4*>(Vs + key * kRowBytes + l16 * 16);
-      float ph[G];
-#pragma unroll
-      for (int h = 0; h < G; ++h)
-        ph[h] = __shfl_sync(0xffffffffu, pr[it], (half << 4) | (h << (4 - LG)));
-      if (key < rows) {
-        f2 vf[4];
-        unpack8x2(vv, vf);
-#pragma unroll
-        for (int h = 0; h < G; ++h) {
-          const f2 p2 = mk2(ph[h], ph[h]);
-#pragma unroll
-          for (int j = 0; j < 4; ++j) o[h][j] = fma2(p2, vf[j], o[h][j]);
-        }
-      }
-    }
+    cs.tile(Ks, Ks + kTileBytes, rows, warp);
     __syncwarp();
     if (lane == 0) mbar_arrive(smem_u32(&bars[kStages + s]));
+    const bool seg_end = (w.k == w.ntiles - 1) || (t == t1 - 1);
 
     // ---- end of this CTA's part of the segment: merge and emit ------------
-    if (w.k == w.ntiles - 1 || t == t1 - 1) {
+    if (seg_end) {
       const int seg = w.b * Hkv + w.kvh;
       const long long seg_t0 = (long long)Hkv * prefix[w.b] + (long long)w.kvh * w.ntiles;
       const long long seg_t1 = seg_t0 + w.ntiles;
       const bool whole = seg_t0 >= t0 && seg_t1 <= t1;
       const int ct = tid;
-
-      // both half-warps hold partial o for the same (m, l): add them
-#pragma unroll
-      for (int h = 0; h < G; ++h)
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          float lo, hi;
-          brk2(o[h][j], lo, hi);
-          lo += __shfl_xor_sync(0xffffffffu, lo, 16);
-          hi += __shfl_xor_sync(0xffffffffu, hi, 16);
-          o[h][j] = mk2(lo, hi);
-        }
-      if (half == 0) {
-#pragma unroll
-        for (int h = 0; h < G; ++h) {
-          float f[8];
-#pragma unroll
-          for (int j = 0; j < 4; ++j) brk2(o[h][j], f[2 * j], f[2 * j + 1]);
-          float4* dst = reinterpret_cast<float4*>(merge_o + ((warp * G + h) * kD + l16 * 8));
-          dst[0] = make_float4(f[0], f[1], f[2], f[3]);
-          dst[1] = make_float4(f[4], f[5], f[6], f[7]);
-        }
-        if (l16 == (hd << (4 - LG))) {
-          merge_ml[(warp * G + hd) * 2 + 0] = m_run;
-          merge_ml[(warp * G + hd) * 2 + 1] = l_run;
-        }
-      }
+      cs.stash(merge_o, merge_ml, warp);
       consumer_bar<NC>();
 
       const int slot = blockIdx.x + seg;
       uint16_t* out_seg = p.out + ((size_t)w.b * p.Hq + (size_t)w.kvh * G) * kD;
       for (int idx = ct; idx < G * kD; idx += NC) {
         const int h = idx / kD, d = idx % kD;
-        float M = -INFINITY;
-#pragma unroll
-        for (int ww = 0; ww < NW; ++ww) M = fmaxf(M, merge_ml[(ww * G + h) * 2]);
-        float Ls = 0.f, Os = 0.f;
-#pragma unroll
-        for (int ww = 0; ww < NW; ++ww) {
-          const float e = ex2(merge_ml[(ww * G + h) * 2] - M);
-          Ls = fmaf(merge_ml[(ww * G + h) * 2 + 1], e, Ls);
-          Os = fmaf(merge_o[(ww * G + h) * kD + d], e, Os);
-        }
+        float M, Ls, Os;
+        merge_warps<NW, G>(merge_o, merge_ml, h, d, M, Ls, Os);
         if (whole) {
-          __nv_bfloat16 r = __float2bfloat16_rn(Os / Ls);
-          out_seg[h * kD + d] = *reinterpret_cast<uint16_t*>(&r);
+          store_bf16(out_seg + h * kD + d, Os / Ls);
         } else {
           p.part_o[((size_t)slot * G + h) * kD + d] = Os;
           if (d == 0) {
@@ -538,17 +643,17 @@ __global__ void __maxnreg__(Cfg<G>::kMaxRegs) decode_splitkv_kernel(const Params
               }
               M = Mb;
             }
-            __nv_bfloat16 r = __float2bfloat16_rn(Os / Ls);
-            out_seg[h * kD + d] = *reinterpret_cast<uint16_t*>(&r);
+            store_bf16(out_seg + h * kD + d, Os / Ls);
           }
           if (ct == 0) p.counters[seg] = 0u;  // ready for the next launch
         }
       }
       consumer_bar<NC>();  // merge buffers are free again
-      reset_acc();
+      cs.reset();
     }
     walk_next(w, prefix, p.positions, B, Hkv);
-    if (w.k == 0 && t + 1 < t1) load_q();
+    if (w.k == 0 && t + 1 < t1)
+      cs.load_q(p.q + ((size_t)w.b * p.Hq + (size_t)w.kvh * G) * kD, p.qscale);
   }
 
   if (*abort_flag) {
@@ -559,34 +664,239 @@ __global__ void __maxnreg__(Cfg<G>::kMaxRegs) decode_splitkv_kernel(const Params
   }
 }
 
-int g_num_sms[64];
+// ------------------------------------------------------------ cluster mode --
+template <int G>
+size_t cluster_smem_bytes() {
+  constexpr int NW = Cfg<G>::NW;
+  return (size_t)kStages * 2 * kTileBytes + 2 * kStages * sizeof(uint64_t) +
+         kMiscInts * sizeof(int) + (size_t)NW * G * 2 * sizeof(float) +
+         (size_t)NW * G * kD * sizeof(float) + (size_t)G * (kD + 2) * sizeof(float);
+}
 
-int num_sms() {
+// Grid = B*Hkv clusters of C CTAs; cluster s handles segment s (sequence
+// s / Hkv, KV head s % Hkv).
+template <int G>
+__global__ void __maxnreg__(Cfg<G>::kMaxRegs) decode_cluster_kernel(const Params p) {
+  constexpr int NW = Cfg<G>::NW;
+  constexpr int NC = Cfg<G>::kConsumers;
+  extern __shared__ __align__(1024) uint8_t smem[];
+  uint8_t* stages = smem;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kStages * 2 * kTileBytes);
+  int* misc = reinterpret_cast<int*>(bars + 2 * kStages);
+  float* merge_ml = reinterpret_cast<float*>(misc + kMiscInts);  // [NW][G][2]
+  float* merge_o = merge_ml + NW * G * 2;                         // [NW][G][kD]
+  float* part_o = merge_o + NW * G * kD;                          // [G][kD]
+  float* part_ml = part_o + G * kD;                               // [G][2]
+
+  cg::cluster_group cluster = cg::this_cluster();
+  const int C = (int)cluster.num_blocks();
+  const int rank = (int)cluster.block_rank();
+  const int seg = blockIdx.x / C;
+  const int b = seg / p.Hkv, kvh = seg % p.Hkv;
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5, lane = tid & 31;
+  volatile int* abort_flag = misc;
+
+  if (tid == 0) {
+#pragma unroll
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(smem_u32(&bars[s]), 1);
+      mbar_init(smem_u32(&bars[kStages + s]), NW);
+    }
+    misc[0] = 0;
+    fence_mbar_init();
+  }
+  grid_dependency_wait();
+  grid_dependents_launch();
+  const int pos = p.positions[b];
+  if (pos < 0 || pos >= p.L) {
+    // the same for every CTA of the cluster: all leave, no cluster barrier
+    if (rank == 0 && kvh == 0 && tid == 0) {
+      set_status(p.status, ATTN_DEV_BAD_POSITION);
+      write_nan_rows(p, b);
+    }
+    return;
+  }
+  const int n = pos + 1;
+  const int ntiles = pos / kTile + 1;
+  const int k0 = (int)((long long)rank * ntiles / C);
+  const int k1 = (int)((long long)(rank + 1) * ntiles / C);
+  __syncthreads();  // barriers initialised
+
+  if (warp == NW) {
+    // ------------------------------------------------------------ producer --
+    if (lane == 0) {
+      for (int k = k0; k < k1; ++k) {
+        const int i = k - k0;
+        const int s = i % kStages;
+        const uint32_t u = (uint32_t)(i / kStages);
+        if (i >= kStages && !mbar_wait(smem_u32(&bars[kStages + s]), (u & 1u) ^ 1u, abort_flag)) {
+          *abort_flag = 1;
+          set_status(p.status, ATTN_DEV_TIMEOUT);
+          break;
+        }
+        produce_tile(p, stages, bars, s, b, kvh, k, ntiles, n);
+      }
+    }
+    __syncwarp();
+  } else {
+    // ----------------------------------------------------------- consumers --
+    Consumer<G> cs;
+    cs.init(lane);
+    cs.load_q(p.q + ((size_t)b * p.Hq + (size_t)kvh * G) * kD, p.qscale);
+    cs.reset();
+    for (int k = k0; k < k1; ++k) {
+      const int i = k - k0;
+      const int s = i % kStages;
+      if (!mbar_wait(smem_u32(&bars[s]), (uint32_t)(i / kStages) & 1u, abort_flag)) {
+        *abort_flag = 1;
+        set_status(p.status, ATTN_DEV_TIMEOUT);
+        break;
+      }
+      const int rows = min(kTile, n - k * kTile);
+      const uint8_t* Ks = stages + (size_t)s * 2 * kTileBytes;
+      cs.tile(Ks, Ks + kTileBytes, rows, warp);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&bars[kStages + s]));
+    }
+    // this CTA's partial (max, sum, unnormalised o); no tiles: (-inf, 0, 0)
+    cs.stash(merge_o, merge_ml, warp);
+    consumer_bar<NC>();
+    for (int idx = tid; idx < G * kD; idx += NC) {
+      const int h = idx / kD, d = idx % kD;
+      float M, Ls, Os;
+      merge_warps<NW, G>(merge_o, merge_ml, h, d, M, Ls, Os);
+      part_o[h * kD + d] = Os;
+      if (d == 0) {
+        part_ml[h * 2 + 0] = M;
+        part_ml[h * 2 + 1] = Ls;
+      }
+    }
+  }
+
+  // every CTA's partial is in its shared memory; rank 0 merges them
+  cluster.sync();
+  if (rank == 0) {
+    uint16_t* out_seg = p.out + ((size_t)b * p.Hq + (size_t)kvh * G) * kD;
+    for (int idx = tid; idx < G * kD; idx += blockDim.x) {
+      const int h = idx / kD, d = idx % kD;
+      float M = -INFINITY;
+      for (int r = 0; r < C; ++r) M = fmaxf(M, cluster.map_shared_rank(part_ml, r)[h * 2]);
+      float Ls = 0.f, Os = 0.f;
+      for (int r = 0; r < C; ++r) {
+        const float* pml = cluster.map_shared_rank(part_ml, r);
+        const float e = ex2(pml[h * 2] - M);  // empty partial: 2^-inf = 0
+        Ls = fmaf(pml[h * 2 + 1], e, Ls);
+        Os = fmaf(cluster.map_shared_rank(part_o, r)[h * kD + d], e, Os);
+      }
+      store_bf16(out_seg + h * kD + d, Os / Ls);
+    }
+  }
+  cluster.sync();  // keep every CTA's shared memory until rank 0 has read it
+
+  if (*abort_flag) {
+    const uint64_t t_start = globaltimer_ns();
+    while (globaltimer_ns() - t_start < 2000000ull) {
+    }
+  }
+}
+
+// ------------------------------------------------------------------ host --
+
+struct DevInfo {
+  int num_sms = 0;
+  bool configured[9] = {};  // per g
+  int clusters16[9] = {};   // co-resident clusters of 16 (per g); 0 = unusable
+  int clusters8[9] = {};
+};
+DevInfo g_dev[64];
+
+DevInfo& dev_info(int* dev_out) {
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 0 || dev >= 64) dev = 0;
-  if (g_num_sms[dev] == 0) {
+  *dev_out = dev;
+  DevInfo& d = g_dev[dev];
+  if (d.num_sms == 0) {
     int n = 0;
     if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
       n = 148;
-    g_num_sms[dev] = n;
+    d.num_sms = n;
   }
-  return g_num_sms[dev];
+  return d;
+}
+
+template <int G>
+int max_clusters(int C) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(C * 64);
+  cfg.blockDim = dim3(Cfg<G>::kThreads);
+  cfg.dynamicSmemBytes = cluster_smem_bytes<G>();
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = C;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, decode_cluster_kernel<G>, &cfg) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  return n;
+}
+
+template <int G>
+cudaError_t configure(DevInfo& d) {
+  if (d.configured[G]) return cudaSuccess;
+  cudaError_t e = cudaFuncSetAttribute(decode_splitkv_kernel<G>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)smem_bytes<G>(kMaxB));
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(decode_cluster_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)cluster_smem_bytes<G>());
+  if (e != cudaSuccess) return e;
+  if (cudaFuncSetAttribute(decode_cluster_kernel<G>,
+                           cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess)
+    d.clusters16[G] = max_clusters<G>(16);
+  else
+    cudaGetLastError();
+  d.clusters8[G] = max_clusters<G>(8);
+  d.configured[G] = true;
+  return cudaSuccess;
 }
 
 template <int G>
 cudaError_t launch_g(const Params& p, cudaStream_t stream) {
-  const size_t smem = smem_bytes<G>(kMaxB);
-  static bool configured[64] = {};
   int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev >= 0 && dev < 64 && !configured[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(decode_splitkv_kernel<G>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    configured[dev] = true;
+  DevInfo& d = dev_info(&dev);
+  cudaError_t e = configure<G>(d);
+  if (e != cudaSuccess) return e;
+  const long long nseg = (long long)p.B * p.Hkv;
+  // cluster mode when every segment gets its own co-resident cluster
+  int C = 0;
+  if (nseg <= d.clusters16[G]) C = 16;
+  else if (nseg <= d.clusters8[G]) C = 8;
+  if (C > 0) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(nseg * C));
+    cfg.blockDim = dim3(Cfg<G>::kThreads);
+    cfg.dynamicSmemBytes = cluster_smem_bytes<G>();
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = C;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    e = cudaLaunchKernelEx(&cfg, decode_cluster_kernel<G>, p);
+    return e != cudaSuccess ? e : cudaGetLastError();
   }
-  return launch_pdl(decode_splitkv_kernel<G>, dim3(min(kMaxGrid, num_sms())),
+  return launch_pdl(decode_splitkv_kernel<G>, dim3(min(kMaxGrid, d.num_sms)),
                     dim3(Cfg<G>::kThreads), smem_bytes<G>(p.B), stream, p);
 }
 

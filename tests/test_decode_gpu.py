@@ -271,3 +271,19 @@ def test_fused_streaming_loop_matches_two_call_loop():
         vc_o = vv[: s + 1].transpose(1, 0, 2)[None]
         want = oracle.decode(f64(q[s]), kc_o, vc_o, [s], scale)
         assert_attn_close(f64(outs[0][s]), want, f"fused streaming step {s}")
+
+
+@pytest.mark.parametrize("g,Hkv,positions", [
+    (2, 8, [8191]), (2, 8, [0]), (2, 8, [65]), (8, 1, [5000]), (1, 4, [1023, 64]),
+    (4, 2, [63, 3000]), (2, 8, [130, 7000]),
+])
+def test_small_batches_one_cluster_per_segment(g, Hkv, positions):
+    """Few (sequence, KV head) segments: each gets a cluster of CTAs that
+    merge through distributed shared memory.  Plain and fused calls."""
+    B = len(positions)
+    for fused in (False, True):
+        case = synth.decode_case(B=B, Hq=g * Hkv, Hkv=Hkv, D=128, L=8192, positions=positions,
+                                 fill="all", poison=True, seed=50 + g + int(fused), device="cuda")
+        want = _oracle_rows(case, range(B))
+        out = _fused_step(case) if fused else _run_step(case)
+        _check(case, want, out, f"small batch g={g} fused={fused}")
