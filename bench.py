@@ -48,7 +48,8 @@ def _args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--only", type=str, default=None,
                     help="run one workload a few times and exit (for ncu captures): "
-                         "streaming_sample, single_step, ragged, stress, prefill, prefill_prefix")
+                         "streaming_sample, position:N, single_step, ragged, stress, prefill, "
+                         "prefill_prefix")
     ap.add_argument("--reps", type=int, default=3, help="launches per --only run")
     ap.add_argument("--cpu-worker", type=str, default=None, help=argparse.SUPPRESS)
     return ap.parse_args()
@@ -183,13 +184,22 @@ def _barrier(ws):
 
 
 def _max_over_ranks(ws, x: float) -> float:
+    """Slowest rank's value (the step time every replica must wait for)."""
     if ws == 1:
         return x
     import torch
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def replica_throughput(ws: int, units_per_rank: float, local_ms: float) -> float:
+    """Whole-job throughput of ws independent replicas (weak scaling): all
+    ranks' units over the slowest rank's time, in units per second."""
+    ms = _max_over_ranks(ws, local_ms)
+    return ws * units_per_rank / (ms * 1e-3)
 
 
 class Stream:
@@ -426,7 +436,7 @@ def run_ours(args):
     dec_ms = statistics.mean(_time_graph(torch, dec.replay, flush, max(3, args.steps), 3))
     del dec
 
-    value = ws * nbytes / (ms * 1e-3) / 1e9
+    value = replica_throughput(ws, nbytes, statistics.mean(step_ms)) / 1e9
     line = {
         "metric": METRIC,
         "value": round(value, 2),
@@ -529,22 +539,24 @@ def run_only(args):
     torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
     ga.load_library()
     name = args.only
-    if name == "streaming_sample":
-        # the streaming loop at every 64th position: cache filled by a plain
-        # copy, then attn_kv_append + attn_decode_step at each sampled position
+    if name == "streaming_sample" or name.startswith("position:"):
+        # streaming_sample: the streaming step at every 64th position (cache
+        # filled by a plain copy, then attn_decode_step_append, as the timed
+        # step does); position:N: that one position, repeated
         q, k, v, pos = synth.streaming_inputs(steps=STEPS_STREAM, Hq=HQ, Hkv=HKV, D=D, seed=0,
                                               device="cuda")
         kc = k[:, 0].transpose(0, 1).contiguous().unsqueeze(0)
         vc = v[:, 0].transpose(0, 1).contiguous().unsqueeze(0)
         ws = ga.decode_workspace(1, HQ, HKV, L, D)
         out = torch.empty((1, HQ, D), dtype=torch.bfloat16, device="cuda")
+        sample = (range(0, STEPS_STREAM, 64) if name == "streaming_sample"
+                  else [int(name.split(":")[1])])
         for _ in range(args.reps):
-            for p in range(0, STEPS_STREAM, 64):
-                ga.attn_kv_append(k[p], v[p], pos[p], kc, vc)
-                ga.attn_decode_step(q[p], pos[p], kc, vc, 1.0 / math.sqrt(D), out=out,
-                                    workspace=ws)
+            for p in sample:
+                ga.attn_decode_step_append(q[p], k[p], v[p], pos[p], kc, vc, 1.0 / math.sqrt(D),
+                                           out=out, workspace=ws)
         torch.cuda.synchronize()
-        print(json.dumps({"only": name, "launches_per_rep": 2 * STEPS_STREAM // 64}))
+        print(json.dumps({"only": name, "launches_per_rep": len(sample)}))
         return
     w = synth.generators.WORKLOADS[name]
     case = synth.generators.workload_case(name, seed=0, device="cuda")
