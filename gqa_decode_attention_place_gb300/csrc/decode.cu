@@ -24,7 +24,8 @@
 //  * Two ways to split a segment over CTAs, both computed on the device from
 //    `positions` (one launch serves any positions; graph-capturable):
 //    - cluster mode (few segments, e.g. B=1): one thread-block cluster of C
-//      CTAs (16 or 8) per segment; CTA rank r takes tiles
+//      CTAs (8..16, the largest size that lets every segment's cluster be
+//      resident at once) per segment; CTA rank r takes tiles
 //      [r*n/C, (r+1)*n/C).  The partials (max, sum, unnormalised o) are
 //      merged through distributed shared memory between two cluster
 //      barriers -- no global scratch, no atomics.
@@ -803,11 +804,12 @@ __global__ void __maxnreg__(Cfg<G>::kMaxRegs) decode_cluster_kernel(const Params
 
 // ------------------------------------------------------------------ host --
 
+constexpr int kMaxCluster = 16;
+
 struct DevInfo {
   int num_sms = 0;
-  bool configured[9] = {};  // per g
-  int clusters16[9] = {};   // co-resident clusters of 16 (per g); 0 = unusable
-  int clusters8[9] = {};
+  bool configured[9] = {};               // per g
+  int clusters[9][kMaxCluster + 1] = {};  // [g][C]: co-resident clusters of C CTAs
 };
 DevInfo g_dev[64];
 
@@ -857,12 +859,13 @@ cudaError_t configure(DevInfo& d) {
   e = cudaFuncSetAttribute(decode_cluster_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)cluster_smem_bytes<G>());
   if (e != cudaSuccess) return e;
-  if (cudaFuncSetAttribute(decode_cluster_kernel<G>,
-                           cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess)
-    d.clusters16[G] = max_clusters<G>(16);
-  else
-    cudaGetLastError();
-  d.clusters8[G] = max_clusters<G>(8);
+  const bool big = cudaFuncSetAttribute(decode_cluster_kernel<G>,
+                                        cudaFuncAttributeNonPortableClusterSizeAllowed,
+                                        1) == cudaSuccess;
+  if (!big) cudaGetLastError();
+  // How many clusters of each size can run at once (a cluster stays within
+  // one GPC, so this is set by the SMs per GPC, not by the SM count).
+  for (int c = 2; c <= kMaxCluster; ++c) d.clusters[G][c] = (c <= 8 || big) ? max_clusters<G>(c) : 0;
   d.configured[G] = true;
   return cudaSuccess;
 }
@@ -874,10 +877,11 @@ cudaError_t launch_g(const Params& p, cudaStream_t stream) {
   cudaError_t e = configure<G>(d);
   if (e != cudaSuccess) return e;
   const long long nseg = (long long)p.B * p.Hkv;
-  // cluster mode when every segment gets its own co-resident cluster
+  // Cluster mode when every segment can have its own co-resident cluster of
+  // at least 8 CTAs: the largest such cluster size.  Otherwise stream-K.
   int C = 0;
-  if (nseg <= d.clusters16[G]) C = 16;
-  else if (nseg <= d.clusters8[G]) C = 8;
+  for (int c = kMaxCluster; c >= 8 && C == 0; --c)
+    if (nseg <= d.clusters[G][c]) C = c;
   if (C > 0) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(nseg * C));
