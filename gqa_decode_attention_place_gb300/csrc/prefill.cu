@@ -8,8 +8,10 @@
 // 0..start_pos+i (causal mask aligned to the bottom-right corner), query head
 // h reads KV head h/g.  out [S,Hq,d] bf16.
 //
-// How: one CTA per (pair of 128-token query tiles, query head), longest pairs
-// first.  Each K/V tile loaded serves both query tiles.
+// How: work items are (pair of 128-token query tiles, query head), sorted
+// longest first; a persistent grid (one CTA per SM) walks them in snake
+// order (CTA c takes items c, 2G-1-c, 2G+c, ...) so the causal work per CTA
+// evens out.  Each K/V tile loaded serves both query tiles of an item.
 //  * warp 0, one thread: TMA (cp.async.bulk.tensor, 128-byte swizzle) loads
 //    the two Q tiles once and streams 128-key K and V tiles through a 3-stage
 //    ring (4 stages).
@@ -28,6 +30,8 @@
 //    fp32 sums and bf16 P.
 //  Scores never leave the SM (no S or P in HBM).
 #include <cuda.h>
+
+#include <algorithm>
 
 #include "common.cuh"
 #include "internal.h"
@@ -61,7 +65,9 @@ constexpr int kBarSFull = kBarKVEmpty + kKVStages;  // + tile
 constexpr int kBarSFree = kBarSFull + kQT;
 constexpr int kBarPFull = kBarSFree + kQT;    // + tile
 constexpr int kBarPVDone = kBarPFull + kQT;   // + tile
-constexpr int kNumBars = kBarPVDone + kQT;
+constexpr int kBarOFree = kBarPVDone + kQT;   // + tile: epilogue has read O
+constexpr int kBarQFree = kBarOFree + kQT;    // QK^T of the item has read Q
+constexpr int kNumBars = kBarQFree + 1;
 
 __device__ unsigned int g_prefill_timeouts;   // diagnostic: waits that gave up
 
@@ -232,19 +238,35 @@ __global__ void __launch_bounds__(kPThreads, 1)
   auto bar = [&](int i) { return smem_u32(&bars[i]); };
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int h = blockIdx.x % p.Hq;
-  const int pair = p.n_pairs - 1 - (int)(blockIdx.x / p.Hq);  // longest pairs first
-  const int q0 = pair * kQT * kBM;
-  const int kvh = h / p.g;
-  // key tiles each query tile needs (0 if the tile holds no query row)
-  auto ntile = [&](int x) -> int {
-    const int r0 = q0 + x * kBM;
-    return r0 < p.S ? (p.start_pos + min(r0 + kBM, p.S) + kBN - 1) / kBN : 0;
+  const int n_items = p.n_pairs * p.Hq;
+  const int G = gridDim.x;
+  // Work item w (longest first): query-tile pair n_pairs-1-w/Hq of head w%Hq.
+  // CTA c takes items c, 2G-1-c, 2G+c, 4G-1-c, ... (a snake over the sorted
+  // list), which evens out the causal work per CTA.
+  auto item_of = [&](int r) -> int {
+    return r * G + ((r & 1) ? (G - 1 - (int)blockIdx.x) : (int)blockIdx.x);
   };
-  const int n_tiles = max(ntile(0), ntile(1));
+  struct Item {
+    int h, kvh, q0, nt[kQT], n;
+  };
+  auto item = [&](int w) -> Item {
+    Item it;
+    it.h = w % p.Hq;
+    it.kvh = it.h / p.g;
+    it.q0 = (p.n_pairs - 1 - w / p.Hq) * kQT * kBM;
+    it.n = 0;
+#pragma unroll
+    for (int x = 0; x < kQT; ++x) {  // key tiles query tile x needs (0: no query rows)
+      const int r0 = it.q0 + x * kBM;
+      it.nt[x] = r0 < p.S ? (p.start_pos + min(r0 + kBM, p.S) + kBN - 1) / kBN : 0;
+      it.n = max(it.n, it.nt[x]);
+    }
+    return it;
+  };
 
   if (tid == 0) {
     mbar_init(bar(kBarQ), 1);
+    mbar_init(bar(kBarQFree), 1);
     for (int s = 0; s < kKVStages; ++s) {
       mbar_init(bar(kBarKVFull + s), 1);
       mbar_init(bar(kBarKVEmpty + s), 1);
@@ -254,6 +276,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
       mbar_init(bar(kBarSFree + x), 128);
       mbar_init(bar(kBarPFull + x), 128);
       mbar_init(bar(kBarPVDone + x), 1);
+      mbar_init(bar(kBarOFree + x), 128);
     }
     *abort_flag = 0;
     fence_mbar_init();
@@ -273,20 +296,33 @@ __global__ void __launch_bounds__(kPThreads, 1)
   // O of tile x [384+64x, +64)
   const uint32_t sQ = base + kOffQ;
 
+  // Every mbarrier completes one phase per use; parities below come from
+  // running counts kept across this CTA's items.
   if (warp == 0) {
     // ------------------------------------------------------ TMA producer --
     if (lane == 0) {
-      mbar_arrive_expect_tx(bar(kBarQ), kQT * kTileBytes);
-      for (int x = 0; x < kQT; ++x)
-        tma_load_3d(sQ + x * kTileBytes, &tm_q, 0, h, q0 + x * kBM, bar(kBarQ));
-      for (int i = 0; i < n_tiles; ++i) {
-        const int s = i % kKVStages;
-        const uint32_t u = (uint32_t)(i / kKVStages);
-        if (i >= kKVStages && !wait_or_abort(bar(kBarKVEmpty + s), (u - 1) & 1u, abort_flag)) break;
-        const uint32_t sK = base + kOffKV + s * 2 * kTileBytes;
-        mbar_arrive_expect_tx(bar(kBarKVFull + s), 2 * kTileBytes);
-        tma_load_3d(sK, &tm_k, 0, kvh, i * kBN, bar(kBarKVFull + s));
-        tma_load_3d(sK + kTileBytes, &tm_v, 0, kvh, i * kBN, bar(kBarKVFull + s));
+      uint32_t gk = 0;  // K/V tiles issued so far
+      for (int r = 0; item_of(r) < n_items; ++r) {
+        const Item it = item(item_of(r));
+        // the previous item's QK^T MMAs have finished reading Q
+        if (r > 0 && !wait_or_abort(bar(kBarQFree), (uint32_t)(r - 1) & 1u, abort_flag)) break;
+        mbar_arrive_expect_tx(bar(kBarQ), kQT * kTileBytes);
+        for (int x = 0; x < kQT; ++x)
+          tma_load_3d(sQ + x * kTileBytes, &tm_q, 0, it.h, it.q0 + x * kBM, bar(kBarQ));
+        bool ok = true;
+        for (int i = 0; i < it.n; ++i, ++gk) {
+          const int s = gk % kKVStages;
+          const uint32_t u = gk / kKVStages;
+          if (gk >= kKVStages && !wait_or_abort(bar(kBarKVEmpty + s), (u - 1) & 1u, abort_flag)) {
+            ok = false;
+            break;
+          }
+          const uint32_t sK = base + kOffKV + s * 2 * kTileBytes;
+          mbar_arrive_expect_tx(bar(kBarKVFull + s), 2 * kTileBytes);
+          tma_load_3d(sK, &tm_k, 0, it.kvh, i * kBN, bar(kBarKVFull + s));
+          tma_load_3d(sK + kTileBytes, &tm_v, 0, it.kvh, i * kBN, bar(kBarKVFull + s));
+        }
+        if (!ok) break;
       }
     }
   } else if (warp == 1) {
@@ -294,46 +330,69 @@ __global__ void __launch_bounds__(kPThreads, 1)
     if (lane == 0) {
       constexpr uint32_t idesc_qk = make_idesc(kBM, kBN, false);
       constexpr uint32_t idesc_pv = make_idesc(kBM, kHD, true);
-      auto issue_pv = [&](int x, int j) -> bool {  // O_x (+)= P_x V_j
-        if (!wait_or_abort(bar(kBarPFull + x), (uint32_t)j & 1u, abort_flag)) return false;
-        tc_fence_after();
-        const uint32_t sV = base + kOffKV + (j % kKVStages) * 2 * kTileBytes + kTileBytes;
-        // A = P from TMEM (16 keys = 8 columns of bf16 pairs per MMA)
+      uint32_t gk = 0;             // K/V tiles consumed so far
+      uint32_t cs[kQT] = {0, 0};   // S_x issued so far
+      uint32_t cp[kQT] = {0, 0};   // P_x consumed (PV_x issued) so far
+      bool ok = true;
+      for (int r = 0; ok && item_of(r) < n_items; ++r) {
+        const Item it = item(item_of(r));
+        // O_x (+)= P_x V_j; gk0 is the item's first K/V tile in the ring order
+        auto issue_pv = [&](int x, int j, uint32_t gk0) -> bool {
+          if (j == 0 && r > 0 &&  // the previous item's epilogue has read O_x
+              !wait_or_abort(bar(kBarOFree + x), (uint32_t)(r - 1) & 1u, abort_flag))
+            return false;
+          if (!wait_or_abort(bar(kBarPFull + x), cp[x] & 1u, abort_flag)) return false;
+          tc_fence_after();
+          const uint32_t sV =
+              base + kOffKV + ((gk0 + j) % kKVStages) * 2 * kTileBytes + kTileBytes;
 #pragma unroll
-        for (int k = 0; k < kBN / 16; ++k)
-          tc_mma_ts(tmem + kTmemO + 64 * x, tmem + kTmemP + 64 * x + 8 * k,
-                    sw128_desc(sV + k * 16 * 128), idesc_pv, (j > 0 || k > 0) ? 1u : 0u);
-        tc_commit(bar(kBarPVDone + x));
-        return true;
-      };
-      bool ok = wait_or_abort(bar(kBarQ), 0, abort_flag);
-      for (int i = 0; ok && i < n_tiles; ++i) {
-        const int s = i % kKVStages;
-        if (!wait_or_abort(bar(kBarKVFull + s), (uint32_t)(i / kKVStages) & 1u, abort_flag)) break;
-        const uint32_t sK = base + kOffKV + s * 2 * kTileBytes;
-        for (int x = 0; ok && x < kQT; ++x) {
-          if (i >= ntile(x)) continue;
-          // the softmax has read S_x of tile i-1
-          if (i > 0 && !wait_or_abort(bar(kBarSFree + x), (uint32_t)(i - 1) & 1u, abort_flag)) {
+          for (int k = 0; k < kBN / 16; ++k)
+            tc_mma_ts(tmem + kTmemO + 64 * x, tmem + kTmemP + 64 * x + 8 * k,
+                      sw128_desc(sV + k * 16 * 128), idesc_pv, (j > 0 || k > 0) ? 1u : 0u);
+          tc_commit(bar(kBarPVDone + x));
+          ++cp[x];
+          return true;
+        };
+        if (!wait_or_abort(bar(kBarQ), (uint32_t)r & 1u, abort_flag)) { ok = false; break; }
+        const uint32_t gk0 = gk;
+        for (int i = 0; ok && i < it.n; ++i) {
+          const uint32_t g = gk0 + i;
+          const int s = g % kKVStages;
+          if (!wait_or_abort(bar(kBarKVFull + s), (g / kKVStages) & 1u, abort_flag)) {
             ok = false;
             break;
           }
-          tc_fence_after();
+          const uint32_t sK = base + kOffKV + s * 2 * kTileBytes;
+          for (int x = 0; ok && x < kQT; ++x) {
+            if (i >= it.nt[x]) continue;
+            // the softmax has read the previous S_x
+            if (cs[x] > 0 &&
+                !wait_or_abort(bar(kBarSFree + x), (cs[x] - 1) & 1u, abort_flag)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
 #pragma unroll
-          for (int k = 0; k < kHD / 16; ++k)
-            tc_mma(tmem + 128 * x, sw128_desc(sQ + x * kTileBytes + k * 32),
-                   sw128_desc(sK + k * 32), idesc_qk, k > 0);
-          tc_commit(bar(kBarSFull + x));
+            for (int k = 0; k < kHD / 16; ++k)
+              tc_mma(tmem + 128 * x, sw128_desc(sQ + x * kTileBytes + k * 32),
+                     sw128_desc(sK + k * 32), idesc_qk, k > 0);
+            tc_commit(bar(kBarSFull + x));
+            ++cs[x];
+          }
+          if (!ok) break;
+          if (i + 1 == it.n) tc_commit(bar(kBarQFree));  // last QK^T of this item
+          if (i > 0) {
+            for (int x = 0; ok && x < kQT; ++x)
+              if (i - 1 < it.nt[x]) ok = issue_pv(x, i - 1, gk0);
+            tc_commit(bar(kBarKVEmpty + (g - 1) % kKVStages));  // tile i-1 released
+          }
         }
         if (!ok) break;
-        if (i > 0) {
-          for (int x = 0; ok && x < kQT; ++x)
-            if (i - 1 < ntile(x)) ok = issue_pv(x, i - 1);
-          tc_commit(bar(kBarKVEmpty + (i - 1) % kKVStages));
-        }
+        for (int x = 0; ok && x < kQT; ++x)
+          if (it.n - 1 < it.nt[x]) ok = issue_pv(x, it.n - 1, gk0);
+        tc_commit(bar(kBarKVEmpty + (gk0 + it.n - 1) % kKVStages));  // last tile released
+        gk = gk0 + it.n;
       }
-      for (int x = 0; ok && x < kQT; ++x)
-        if (n_tiles - 1 < ntile(x)) ok = issue_pv(x, n_tiles - 1);
     }
   } else {
     // ------------------------------------------- softmax / epilogue (r) --
@@ -344,128 +403,136 @@ __global__ void __launch_bounds__(kPThreads, 1)
     const uint32_t tm_S = tmem + 128 * x + lane_off;
     const uint32_t tm_O = tmem + kTmemO + 64 * x + lane_off;
     const uint32_t tm_P = tmem + kTmemP + 64 * x + lane_off;
-    const int row = q0 + x * kBM + r;                   // query token index
-    const int qpos = p.start_pos + row;                 // its absolute position
     const float c = p.scale_log2;
-    float m_run = -INFINITY, l_run = 0.f;
-    const int nt = ntile(x);
+    uint32_t cs = 0;   // S_x consumed so far
+    uint32_t cpv = 0;  // PV_x issued before this item
     bool ok = true;
-    auto wait_pv = [&](int j) -> bool {  // PV_x of tile j done
-      if (!wait_or_abort(bar(kBarPVDone + x), (uint32_t)j & 1u, abort_flag)) return false;
-      tc_fence_after();
-      return true;
-    };
 
-    for (int i = 0; i < nt; ++i) {
-      if (!wait_or_abort(bar(kBarSFull + x), (uint32_t)i & 1u, abort_flag)) { ok = false; break; }
-      tc_fence_after();
-      const int kbase = i * kBN;
-      const bool diag = kbase + kBN - 1 > qpos;
+    for (int rr = 0; ok && item_of(rr) < n_items; ++rr) {
+      const Item it = item(item_of(rr));
+      const int row = it.q0 + x * kBM + r;             // query token index
+      const int qpos = p.start_pos + row;              // its absolute position
+      const int nt = it.nt[x];
+      float m_run = -INFINITY, l_run = 0.f;
+      auto wait_pv = [&](int j) -> bool {  // PV_x of tile j of this item done
+        if (!wait_or_abort(bar(kBarPVDone + x), (cpv + j) & 1u, abort_flag)) return false;
+        tc_fence_after();
+        return true;
+      };
 
-      // the whole S row in one round trip
-      float sv[kBN];
-#pragma unroll
-      for (int cc = 0; cc < kBN / 32; ++cc) {
-        float* dst = sv + cc * 32;
-        tmem_ld32(tm_S + cc * 32, *reinterpret_cast<float(*)[32]>(dst));
-      }
-      tmem_ld_wait();
-      tc_fence_before();
-      mbar_arrive(bar(kBarSFree + x));       // S_x may be overwritten
+      for (int i = 0; i < nt; ++i, ++cs) {
+        if (!wait_or_abort(bar(kBarSFull + x), cs & 1u, abort_flag)) { ok = false; break; }
+        tc_fence_after();
+        const int kbase = i * kBN;
+        const bool diag = kbase + kBN - 1 > qpos;
 
-      // scale (packed pairs) and mask; 8 independent running maxima
-      const f2 c2 = mk2(c, c);
+        // the whole S row in one round trip
+        float sv[kBN];
 #pragma unroll
-      for (int j = 0; j < kBN; j += 2) {
-        const f2 t = mul2(mk2(sv[j], sv[j + 1]), c2);
-        brk2(t, sv[j], sv[j + 1]);
-      }
-      if (diag) {
-#pragma unroll
-        for (int j = 0; j < kBN; ++j) sv[j] = (kbase + j > qpos) ? -INFINITY : sv[j];
-      }
-      float mx8[8];
-#pragma unroll
-      for (int a = 0; a < 8; ++a) mx8[a] = sv[a];
-#pragma unroll
-      for (int j = 8; j < kBN; ++j) mx8[j & 7] = fmaxf(mx8[j & 7], sv[j]);
-      const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                             fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
-
-      // PV of tile i-1 done: O is stable and P_x may be overwritten
-      if (i > 0 && !wait_pv(i - 1)) { ok = false; break; }
-      if (mx > m_run + kLazyTau) {  // first tile, or the max grew by > 2^8
-        const float alpha = ex2(m_run - mx);
-        m_run = mx;
-        l_run *= alpha;
-        if (i > 0) {
-#pragma unroll 1
-          for (int cc = 0; cc < kHD / 16; ++cc) {
-            float o[16];
-            tmem_ld16(tm_O + cc * 16, o);
-            tmem_ld_wait();
-#pragma unroll
-            for (int j = 0; j < 16; ++j) o[j] *= alpha;
-            tmem_st16(tm_O + cc * 16, o);
-          }
+        for (int cc = 0; cc < kBN / 32; ++cc) {
+          float* dst = sv + cc * 32;
+          tmem_ld32(tm_S + cc * 32, *reinterpret_cast<float(*)[32]>(dst));
         }
-      }
-
-      // P = 2^(s*c - m) (exactly 0 where masked: 2^-inf) as bf16 pairs into
-      // TMEM: column q of P holds keys 2q (low half) and 2q+1 (high half)
-      const f2 m2 = mk2(-m_run, -m_run);
-      f2 rs2[4];
-#pragma unroll
-      for (int a = 0; a < 4; ++a) rs2[a] = mk2(0.f, 0.f);
-#pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        float pw[32];
-#pragma unroll
-        for (int q = 0; q < 32; ++q) {
-          const int j = half * 64 + 2 * q;
-          float lo, hi;
-          brk2(add2(mk2(sv[j], sv[j + 1]), m2), lo, hi);
-          lo = ex2(lo);
-          hi = ex2(hi);
-          rs2[q & 3] = add2(rs2[q & 3], mk2(lo, hi));
-          pw[q] = __uint_as_float(pack_bf16x2(lo, hi));
-        }
-        tmem_st32(tm_P + half * 32, pw);
-      }
-      {
-        f2 t = add2(add2(rs2[0], rs2[1]), add2(rs2[2], rs2[3]));
-        float lo, hi;
-        brk2(t, lo, hi);
-        l_run += lo + hi;
-      }
-      tmem_st_wait();
-      tc_fence_before();
-      mbar_arrive(bar(kBarPFull + x));       // P_x (and any O rescale) ready
-    }
-
-    // epilogue: O / l for row r (128 contiguous bytes)
-    if (nt > 0) {
-      if (ok) ok = wait_pv(nt - 1);
-      tc_fence_after();
-      const float inv = ok ? 1.f / l_run : __int_as_float(0x7fc00000);
-      uint4* dst = reinterpret_cast<uint4*>(p.out + ((size_t)row * p.Hq + h) * kHD);
-#pragma unroll
-      for (int cc = 0; cc < kHD / 32; ++cc) {
-        float o[32];
-        tmem_ld32(tm_O + cc * 32, o);
         tmem_ld_wait();
-        if (row < p.S) {
+        tc_fence_before();
+        mbar_arrive(bar(kBarSFree + x));       // S_x may be overwritten
+
+        // scale (packed pairs) and mask; 8 independent running maxima
+        const f2 c2 = mk2(c, c);
 #pragma unroll
-          for (int q8 = 0; q8 < 4; ++q8) {
-            uint4 w;
-            w.x = pack_bf16x2(o[q8 * 8 + 0] * inv, o[q8 * 8 + 1] * inv);
-            w.y = pack_bf16x2(o[q8 * 8 + 2] * inv, o[q8 * 8 + 3] * inv);
-            w.z = pack_bf16x2(o[q8 * 8 + 4] * inv, o[q8 * 8 + 5] * inv);
-            w.w = pack_bf16x2(o[q8 * 8 + 6] * inv, o[q8 * 8 + 7] * inv);
-            dst[cc * 4 + q8] = w;
+        for (int j = 0; j < kBN; j += 2) {
+          const f2 t = mul2(mk2(sv[j], sv[j + 1]), c2);
+          brk2(t, sv[j], sv[j + 1]);
+        }
+        if (diag) {
+#pragma unroll
+          for (int j = 0; j < kBN; ++j) sv[j] = (kbase + j > qpos) ? -INFINITY : sv[j];
+        }
+        float mx8[8];
+#pragma unroll
+        for (int a = 0; a < 8; ++a) mx8[a] = sv[a];
+#pragma unroll
+        for (int j = 8; j < kBN; ++j) mx8[j & 7] = fmaxf(mx8[j & 7], sv[j]);
+        const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                               fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+
+        // PV of tile i-1 done: O is stable and P_x may be overwritten
+        if (i > 0 && !wait_pv(i - 1)) { ok = false; break; }
+        if (mx > m_run + kLazyTau) {  // first tile, or the max grew by > 2^8
+          const float alpha = ex2(m_run - mx);
+          m_run = mx;
+          l_run *= alpha;
+          if (i > 0) {
+#pragma unroll 1
+            for (int cc = 0; cc < kHD / 16; ++cc) {
+              float o[16];
+              tmem_ld16(tm_O + cc * 16, o);
+              tmem_ld_wait();
+#pragma unroll
+              for (int j = 0; j < 16; ++j) o[j] *= alpha;
+              tmem_st16(tm_O + cc * 16, o);
+            }
+          }
+        }
+
+        // P = 2^(s*c - m) (exactly 0 where masked: 2^-inf) as bf16 pairs into
+        // TMEM: column q of P holds keys 2q (low half) and 2q+1 (high half)
+        const f2 m2 = mk2(-m_run, -m_run);
+        f2 rs2[4];
+#pragma unroll
+        for (int a = 0; a < 4; ++a) rs2[a] = mk2(0.f, 0.f);
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          float pw[32];
+#pragma unroll
+          for (int q = 0; q < 32; ++q) {
+            const int j = half * 64 + 2 * q;
+            float lo, hi;
+            brk2(add2(mk2(sv[j], sv[j + 1]), m2), lo, hi);
+            lo = ex2(lo);
+            hi = ex2(hi);
+            rs2[q & 3] = add2(rs2[q & 3], mk2(lo, hi));
+            pw[q] = __uint_as_float(pack_bf16x2(lo, hi));
+          }
+          tmem_st32(tm_P + half * 32, pw);
+        }
+        {
+          f2 t = add2(add2(rs2[0], rs2[1]), add2(rs2[2], rs2[3]));
+          float lo, hi;
+          brk2(t, lo, hi);
+          l_run += lo + hi;
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(bar(kBarPFull + x));       // P_x (and any O rescale) ready
+      }
+
+      // epilogue: O / l for row r (128 contiguous bytes)
+      if (ok && nt > 0) {
+        ok = wait_pv(nt - 1);
+        const float inv = ok ? 1.f / l_run : __int_as_float(0x7fc00000);
+        uint4* dst = reinterpret_cast<uint4*>(p.out + ((size_t)row * p.Hq + it.h) * kHD);
+#pragma unroll
+        for (int cc = 0; cc < kHD / 32; ++cc) {
+          float o[32];
+          tmem_ld32(tm_O + cc * 32, o);
+          tmem_ld_wait();
+          if (row < p.S) {
+#pragma unroll
+            for (int q8 = 0; q8 < 4; ++q8) {
+              uint4 w;
+              w.x = pack_bf16x2(o[q8 * 8 + 0] * inv, o[q8 * 8 + 1] * inv);
+              w.y = pack_bf16x2(o[q8 * 8 + 2] * inv, o[q8 * 8 + 3] * inv);
+              w.z = pack_bf16x2(o[q8 * 8 + 4] * inv, o[q8 * 8 + 5] * inv);
+              w.w = pack_bf16x2(o[q8 * 8 + 6] * inv, o[q8 * 8 + 7] * inv);
+              dst[cc * 4 + q8] = w;
+            }
           }
         }
       }
+      cpv += nt;
+      tc_fence_before();
+      mbar_arrive(bar(kBarOFree + x));  // O_x may be overwritten by the next item
     }
   }
 
@@ -551,9 +618,13 @@ cudaError_t launch_prefill(const void* q, const void* k, const void* v, int S, i
   p.g = Hq / Hkv;
   p.n_pairs = (S + kQT * kBM - 1) / (kQT * kBM);
   p.scale_log2 = scale * 1.4426950408889634f;
-  const long long blocks = (long long)p.n_pairs * Hq;
-  if (blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
-  prefill_tcgen05_kernel<<<(unsigned)blocks, kPThreads, kSmemBytes, stream>>>(mq, mk, mv, p);
+  const long long items = (long long)p.n_pairs * Hq;
+  if (items > 0x7fffffffLL) return cudaErrorInvalidValue;
+  int sms = 0;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
+    sms = 148;
+  const unsigned blocks = (unsigned)std::min<long long>(items, sms);  // one CTA per SM
+  prefill_tcgen05_kernel<<<blocks, kPThreads, kSmemBytes, stream>>>(mq, mk, mv, p);
   return cudaGetLastError();
 }
 
