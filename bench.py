@@ -33,6 +33,11 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 STEPS_STREAM = 8192
+# DRAM bytes per launch of the streaming step's decode kernel, from the ncu
+# launch list summarised in profiles/decode_streaming_launches.md
+# (dram__bytes_read.sum + dram__bytes_write.sum, cold cache, mean over the
+# sampled positions).  None when the kernel has changed since that capture.
+TRAFFIC_BYTES_PER_LAUNCH = 16.699e6
 HQ, HKV, D, L = 16, 8, 128, 8192
 METRIC = "decode-attn HBM GB/s (% of peak) & steps/s; causal prefill TFLOP/s"
 FLUSH_BYTES = 512 << 20
@@ -469,7 +474,8 @@ def run_ours(args):
                 "d2h_bytes_per_step": d2h},
         "roofline": {"kernel": "decode_splitkv_kernel<2> (append fused)", "bound": "hbm",
                      "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
-                     "frac": round(achieved / hbm, 3), "traffic": None,
+                     "frac": round(achieved / hbm, 3), "traffic": TRAFFIC_BYTES_PER_LAUNCH,
+                     "traffic_unit": "bytes per launch (ncu, cold cache)",
                      "peak_source": f"{peak_src} hbm_gbs",
                      "avg_launch_us": round(dec_avg_us, 3),
                      "bytes_per_launch_avg": (nbytes + app_bytes) // STEPS_STREAM,
