@@ -33,10 +33,10 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 STEPS_STREAM = 8192
-# DRAM bytes per launch of the streaming step's decode kernel, from the ncu
-# launch list summarised in profiles/decode_streaming_launches.md
-# (dram__bytes_read.sum + dram__bytes_write.sum, cold cache, mean over the
-# sampled positions).  None when the kernel has changed since that capture.
+# DRAM bytes per launch of the streaming step's decode kernel, from an ncu
+# launch list of `bench.py --only streaming_sample` (dram__bytes_read.sum +
+# dram__bytes_write.sum, cold cache, mean over the sampled positions).  Set
+# to None when the kernel changes until it is measured again.
 TRAFFIC_BYTES_PER_LAUNCH = 16.699e6
 HQ, HKV, D, L = 16, 8, 128, 8192
 METRIC = "decode-attn HBM GB/s (% of peak) & steps/s; causal prefill TFLOP/s"
