@@ -10,13 +10,13 @@
 //
 // How (GB300 design, not the page's: the page calls PyTorch SDPA):
 //  * The attended rows of every (sequence, KV head) pair -- a "segment" -- are
-//    cut into 64-row tiles.  One producer thread streams K and V tiles with
-//    1-D bulk copies (TMA) into a 4-stage shared-memory ring guarded by
-//    mbarriers.  Each tile is read from HBM once and serves all g query
+//    cut into 128-row tiles.  One producer thread streams K and V tiles with
+//    1-D bulk copies (TMA) into a 2-stage shared-memory ring guarded by
+//    mbarriers (128 KB in flight per SM).  Each tile is read from HBM once and serves all g query
 //    heads of its KV head.
-//  * 16 consumer warps (8 for g=8) each take 4 (8) keys of a tile, two at a
-//    time (one per half-warp; a lane holds 8 of the 128 dims, as fp32 pairs
-//    for the packed fma.rn.f32x2).  q.k partial sums of the g heads are
+//  * 8 consumer warps (16 for g=1) each take 16 (8) keys of a tile; a key's
+//    128 dims are spread over 8 lanes (16 for g=8), as fp32 pairs for the
+//    packed fma.rn.f32x2.  q.k partial sums of the g heads are
 //    reduced across the 16 lanes with a transposing butterfly (each shuffle
 //    step halves the number of heads still carried), and the softmax is kept
 //    online in fp32 (running max and sum per head, in base 2 with
@@ -47,14 +47,14 @@ namespace {
 namespace cg = cooperative_groups;
 
 constexpr int kD = 128;
-constexpr int kTile = 64;                          // keys per pipeline stage
-constexpr int kStages = 4;
+constexpr int kTile = 128;                         // keys per pipeline stage
+constexpr int kStages = 2;
 constexpr int kRowBytes = kD * 2;
-constexpr int kTileBytes = kTile * kRowBytes;      // 16 KB
+constexpr int kTileBytes = kTile * kRowBytes;      // 32 KB per operand
 constexpr int kMaxB = 8192;
 constexpr int kMaxGrid = 1024;
 constexpr int kMiscInts = 32;                      // [0] abort [1] last [8..8+NW) scan
-constexpr int kWholeTiles = 8;                     // segments this short are not split
+constexpr int kWholeTiles = 4;                     // segments this short are not split
 constexpr float kLog2e = 1.4426950408889634f;
 
 struct Params {
@@ -83,7 +83,7 @@ template <int G> struct Cfg {
   static constexpr int NW = (G == 1) ? 16 : 8;
   static constexpr int kThreads = (NW + 1) * 32;   // + one producer warp
   static constexpr int kConsumers = NW * 32;
-  static constexpr int kKeysPerWarp = kTile / NW;  // 4 or 8
+  static constexpr int kKeysPerWarp = kTile / NW;  // 16 or 8
   static constexpr int kKeysPerStep = 32 / LPK;    // 4 or 2
   static constexpr int kIters = kKeysPerWarp / kKeysPerStep;
   // registers per thread that still let one CTA of kThreads fit the SM
@@ -228,7 +228,7 @@ struct Consumer {
 #pragma unroll
       for (int j = 0; j < NP; ++j) o[h][j] = mk2(0.f, 0.f);
   }
-  // Scores (log2 domain) of this warp's keys of a 64-key tile; keys >= rows
+  // Scores (log2 domain) of this warp's keys of a tile; keys >= rows
   // are invalid (the rest of the stage may hold anything) and get -inf.
   __device__ __forceinline__ void qk(const uint8_t* Ks, int rows, int warp, float (&sc)[IT]) {
 #pragma unroll
@@ -319,7 +319,7 @@ struct Consumer {
       }
     }
   }
-  // One 64-key tile: scores, online softmax, P.V.
+  // One tile: scores, online softmax, P.V.
   __device__ __forceinline__ void tile(const uint8_t* Ks, const uint8_t* Vs, int rows, int warp) {
     float sc[IT], pr[IT];
     qk(Ks, rows, warp, sc);

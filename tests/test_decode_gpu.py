@@ -67,7 +67,7 @@ def test_single_step_workload():
 @pytest.mark.parametrize("g", [1, 2, 4, 8])
 def test_tile_and_split_boundaries_poisoned(g):
     Hkv = 2
-    positions = [0, 1, 62, 63, 64, 65, 127, 128, 129, 1000, 4095, 4096, 8191]
+    positions = [0, 1, 62, 63, 64, 65, 127, 128, 129, 255, 256, 257, 1000, 4095, 4096, 8191]
     case = synth.decode_case(B=len(positions), Hq=g * Hkv, Hkv=Hkv, D=128, L=8192,
                              positions=positions, fill="all", poison=True, seed=g,
                              device="cuda")
@@ -215,7 +215,7 @@ def _fused_step(case, workspace=None):
 @pytest.mark.parametrize("g", [1, 2, 4, 8])
 def test_fused_append_decode_boundaries_poisoned(g):
     Hkv = 2
-    positions = [0, 1, 62, 63, 64, 65, 127, 128, 129, 1000, 4095, 4096, 8191]
+    positions = [0, 1, 62, 63, 64, 65, 127, 128, 129, 255, 256, 257, 1000, 4095, 4096, 8191]
     case = synth.decode_case(B=len(positions), Hq=g * Hkv, Hkv=Hkv, D=128, L=8192,
                              positions=positions, fill="all", poison=True, seed=20 + g,
                              device="cuda")
