@@ -8,8 +8,8 @@
 // 0..start_pos+i (causal mask aligned to the bottom-right corner), query head
 // h reads KV head h/g.  out [S,Hq,d] bf16.
 //
-// How: work items are (pair of 128-token query tiles, query head), sorted
-// longest first; a persistent grid (one CTA per SM) walks them in snake
+// How: work items are (pair of 128-token query tiles, query head) -- or a
+// single tile when pairs would leave SMs idle -- sorted longest first; a persistent grid (one CTA per SM) walks them in snake
 // order (CTA c takes items c, 2G-1-c, 2G+c, ...) so the causal work per CTA
 // evens out.  Each K/V tile loaded serves both query tiles of an item.
 //  * warp 0, one thread: TMA (cp.async.bulk.tensor, 128-byte swizzle) loads
@@ -73,7 +73,9 @@ __device__ unsigned int g_prefill_timeouts;   // diagnostic: waits that gave up
 
 struct PrefillParams {
   uint16_t* out;
-  int S, start_pos, Hq, Hkv, g, n_pairs;
+  int S, start_pos, Hq, Hkv, g;
+  int tpi;      // query tiles per work item: 2, or 1 when pairs would not fill the SMs
+  int n_units;  // work units per head: ceil(query tiles / tpi)
   float scale_log2;  // scale * log2(e)
 };
 
@@ -238,9 +240,10 @@ __global__ void __launch_bounds__(kPThreads, 1)
   auto bar = [&](int i) { return smem_u32(&bars[i]); };
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int n_items = p.n_pairs * p.Hq;
+  const int n_items = p.n_units * p.Hq;
   const int G = gridDim.x;
-  // Work item w (longest first): query-tile pair n_pairs-1-w/Hq of head w%Hq.
+  // Work item w (longest first): query-tile unit n_units-1-w/Hq of head w%Hq
+  // (a unit is tpi consecutive 128-token query tiles).
   // CTA c takes items c, 2G-1-c, 2G+c, 4G-1-c, ... (a snake over the sorted
   // list), which evens out the causal work per CTA.
   auto item_of = [&](int r) -> int {
@@ -253,12 +256,12 @@ __global__ void __launch_bounds__(kPThreads, 1)
     Item it;
     it.h = w % p.Hq;
     it.kvh = it.h / p.g;
-    it.q0 = (p.n_pairs - 1 - w / p.Hq) * kQT * kBM;
+    it.q0 = (p.n_units - 1 - w / p.Hq) * p.tpi * kBM;
     it.n = 0;
 #pragma unroll
     for (int x = 0; x < kQT; ++x) {  // key tiles query tile x needs (0: no query rows)
       const int r0 = it.q0 + x * kBM;
-      it.nt[x] = r0 < p.S ? (p.start_pos + min(r0 + kBM, p.S) + kBN - 1) / kBN : 0;
+      it.nt[x] = (x < p.tpi && r0 < p.S) ? (p.start_pos + min(r0 + kBM, p.S) + kBN - 1) / kBN : 0;
       it.n = max(it.n, it.nt[x]);
     }
     return it;
@@ -306,8 +309,8 @@ __global__ void __launch_bounds__(kPThreads, 1)
         const Item it = item(item_of(r));
         // the previous item's QK^T MMAs have finished reading Q
         if (r > 0 && !wait_or_abort(bar(kBarQFree), (uint32_t)(r - 1) & 1u, abort_flag)) break;
-        mbar_arrive_expect_tx(bar(kBarQ), kQT * kTileBytes);
-        for (int x = 0; x < kQT; ++x)
+        mbar_arrive_expect_tx(bar(kBarQ), p.tpi * kTileBytes);
+        for (int x = 0; x < p.tpi; ++x)
           tma_load_3d(sQ + x * kTileBytes, &tm_q, 0, it.h, it.q0 + x * kBM, bar(kBarQ));
         bool ok = true;
         for (int i = 0; i < it.n; ++i, ++gk) {
@@ -616,13 +619,17 @@ cudaError_t launch_prefill(const void* q, const void* k, const void* v, int S, i
   p.Hq = Hq;
   p.Hkv = Hkv;
   p.g = Hq / Hkv;
-  p.n_pairs = (S + kQT * kBM - 1) / (kQT * kBM);
   p.scale_log2 = scale * 1.4426950408889634f;
-  const long long items = (long long)p.n_pairs * Hq;
-  if (items > 0x7fffffffLL) return cudaErrorInvalidValue;
   int sms = 0;
   if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
     sms = 148;
+  // Two query tiles per item share each K/V tile and keep both softmax
+  // warpgroups busy; when that leaves SMs idle, one tile per item instead.
+  const long long n_qt = (S + kBM - 1) / kBM;
+  p.tpi = ((n_qt + 1) / 2 * (long long)Hq < sms) ? 1 : kQT;
+  p.n_units = (int)((n_qt + p.tpi - 1) / p.tpi);
+  const long long items = (long long)p.n_units * Hq;
+  if (items > 0x7fffffffLL) return cudaErrorInvalidValue;
   const unsigned blocks = (unsigned)std::min<long long>(items, sms);  // one CTA per SM
   prefill_tcgen05_kernel<<<blocks, kPThreads, kSmemBytes, stream>>>(mq, mk, mv, p);
   return cudaGetLastError();
