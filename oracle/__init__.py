@@ -12,7 +12,10 @@ than itself: a pure-Python brute force (``oracle.brute``), PyTorch's library
 and without its full-length boolean mask), closed forms (position 0 returns
 V[0]; identical keys or a zero query return the mean of V), and invariances
 (key-row permutation, GQA equal to repeat-KV MHA, prefill of one token equal to
-a decode step, prefix prefill equal to the tail of a full causal prefill).
+a decode step, prefix prefill equal to the tail of a full causal prefill),
+and for the rotary embedding: a hand-worked rotation, the identity at angle
+0, norm preservation, and dot products that depend only on the position
+difference.
 """
 
 from .attention import (  # noqa: F401
@@ -25,4 +28,7 @@ from .attention import (  # noqa: F401
     decode_bytes,
     decode_flops,
     prefill_flops,
+    rope_f32,
+    round_bf16,
+    decode_rope_step,
 )

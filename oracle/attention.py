@@ -161,6 +161,50 @@ def prefill(q, k, v, start_pos, scale):
     return prefill_rows(q, k, v, start_pos, scale, rows).reshape(S, Hq, d)
 
 
+# --- rotary position embedding (decode page, section 4.1) --------------------
+#
+# The decode page rotates q and the new k with apply_rotary_pos_emb(q, k,
+# cos, sin) before the cache write, without defining it.  The reading taken
+# is the rotate-half form: x' = x * cos + rotate_half(x) * sin with
+# rotate_half(x) = [-x[D/2:], x[:D/2]], computed in fp32 one IEEE operation
+# at a time (product, product, sum; no fused multiply-add), with the rotated
+# key rounded to bf16 (round to nearest even) for the bf16 cache and the
+# rotated query kept in fp32.
+
+def rope_f32(x, cos, sin):
+    """x [..., D] (bf16 values), cos/sin [..., D] fp32 -> fp32 rotated x."""
+    x = np.asarray(x, dtype=np.float32)
+    c = np.asarray(cos, dtype=np.float32)
+    s = np.asarray(sin, dtype=np.float32)
+    half = x.shape[-1] // 2
+    rot = np.concatenate([-x[..., half:], x[..., :half]], axis=-1)
+    return (x * c) + (rot * s)          # float32 ops, each rounded
+
+
+def round_bf16(x):
+    """fp32 -> nearest bf16 value (ties to even), returned as float64."""
+    u = np.asarray(x, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    lsb = (u >> 16) & 1
+    r = ((u + 0x7FFF + lsb) >> 16) << 16
+    return r.astype(np.uint32).view(np.float32).astype(np.float64)
+
+
+def decode_rope_step(q, k_new, v_new, cos, sin, k_cache, v_cache, positions, scale):
+    """One decode step with rotary embedding: rotate q and the new k at each
+    sequence's position, append (rotated k as bf16, v as is), attend.
+
+    q [B,Hq,D]; k_new, v_new [B,Hkv,D]; cos, sin [B,D] (the rotation at
+    positions[b], shared by all heads); caches [B,Hkv,L,D].  Returns
+    (out [B,Hq,D] float64, k_cache, v_cache after the append)."""
+    B = q.shape[0]
+    q_rot = rope_f32(q, np.asarray(cos)[:, None, :], np.asarray(sin)[:, None, :])
+    k_rot = round_bf16(rope_f32(k_new, np.asarray(cos)[:, None, :], np.asarray(sin)[:, None, :]))
+    kc, vc = kv_append(k_cache, v_cache, k_rot, v_new, positions)
+    out = decode(q_rot.astype(np.float64), kc, vc, positions, scale)
+    assert out.shape[0] == B
+    return out, kc, vc
+
+
 # --- algorithmic work (the counts the roofline divides by) -------------------
 
 def decode_bytes(positions, Hq, Hkv, D, elem=2):

@@ -348,3 +348,62 @@ def test_planted_mistakes_are_caught(monkeypatch, mutant):
     elif mutant == "no_normalise":
         monkeypatch.setattr(oatt, "_softmax", lambda s: np.exp(s - np.max(s)))
     assert not _pins_pass(), f"mutant {mutant} slipped past every pin"
+
+
+# ------------------------------------------------------ rotary embedding ---
+
+def test_rope_hand_example():
+    """D=4: rotate_half([1,2,3,4]) = [-3,-4,1,2]; x' = x*cos + rot*sin."""
+    x = np.array([1.0, 2.0, 3.0, 4.0])
+    cos = np.array([0.5, 0.25, 0.5, 0.25], dtype=np.float32)
+    sin = np.array([0.75, -1.0, 0.75, -1.0], dtype=np.float32)
+    want = [1 * 0.5 - 3 * 0.75, 2 * 0.25 - 4 * -1.0, 3 * 0.5 + 1 * 0.75, 4 * 0.25 + 2 * -1.0]
+    np.testing.assert_array_equal(oracle.rope_f32(x, cos, sin), np.array(want, dtype=np.float32))
+
+
+def _angles(pos, D, base=10000.0):
+    inv = base ** (-np.arange(0, D, 2) / D)
+    ang = np.outer(np.atleast_1d(pos), inv)
+    ang = np.concatenate([ang, ang], axis=-1)
+    return np.cos(ang).astype(np.float32), np.sin(ang).astype(np.float32)
+
+
+def test_rope_identity_norm_and_relative_position():
+    rng = np.random.default_rng(21)
+    D = 128
+    x = _rand(rng, (3, D))
+    c0, s0 = np.ones((3, D), np.float32), np.zeros((3, D), np.float32)
+    np.testing.assert_array_equal(oracle.rope_f32(x, c0, s0), x.astype(np.float32))
+    c, s = _angles([5, 900, 7000], D)
+    xr = oracle.rope_f32(x, c, s).astype(np.float64)
+    np.testing.assert_allclose(np.linalg.norm(xr, axis=-1), np.linalg.norm(x, axis=-1), rtol=1e-5)
+    # q at position m and k at position n: q'.k' depends only on m - n
+    q, k = _rand(rng, (D,)), _rand(rng, (D,))
+    dots = []
+    for m, n in [(10, 3), (107, 100), (5007, 5000)]:
+        cq, sq = _angles(m, D)
+        ck, sk = _angles(n, D)
+        dots.append(float(oracle.rope_f32(q, cq[0], sq[0]).astype(np.float64)
+                          @ oracle.rope_f32(k, ck[0], sk[0]).astype(np.float64)))
+    np.testing.assert_allclose(dots, dots[0], rtol=1e-4, atol=1e-4)
+
+
+def test_round_bf16_matches_torch():
+    rng = np.random.default_rng(3)
+    x = (rng.standard_normal(10000) * 10).astype(np.float32)
+    x[:4] = [1.0 + 2 ** -8, 1.0 + 3 * 2 ** -8, -2.5, 0.0]  # ties go to even
+    want = torch.from_numpy(x).to(torch.bfloat16).to(torch.float64).numpy()
+    np.testing.assert_array_equal(oracle.round_bf16(x), want)
+
+
+def test_rope_step_without_rotation_is_plain_decode():
+    rng = np.random.default_rng(8)
+    B, Hq, Hkv, D, L = 2, 8, 2, 16, 12
+    q, kn, vn = _rand(rng, (B, Hq, D)), _rand(rng, (B, Hkv, D)), _rand(rng, (B, Hkv, D))
+    kc, vc = _rand(rng, (B, Hkv, L, D)), _rand(rng, (B, Hkv, L, D))
+    pos = [11, 4]
+    ones, zeros = np.ones((B, D), np.float32), np.zeros((B, D), np.float32)
+    out, kc2, vc2 = oracle.decode_rope_step(q, kn, vn, ones, zeros, kc, vc, pos, 0.25)
+    k3, v3 = oracle.kv_append(kc, vc, kn, vn, pos)
+    np.testing.assert_array_equal(kc2, k3)
+    np.testing.assert_allclose(out, oracle.decode(q, k3, v3, pos, 0.25), rtol=1e-12, atol=1e-13)
