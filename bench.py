@@ -11,8 +11,11 @@ L2 is flushed (a 512 MB write) between timed steps, outside the timed events.
 value = algorithmic decode bytes (K and V rows 0..pos of every KV head, plus
 q and out) / device time of the step, in GB/s; `steps_per_s` is decode steps
 per second.  Extra legs: per-position decode time (warm and cold L2), the
-ragged B=64 batch, the B=256 g=8 stress batch, and the causal prefill
-workloads (TFLOP/s), each against its roofline.
+ragged B=64 batch, the B=256 g=8 stress batch, the ragged batch as a fused
+append step with and without the rotary embedding, and the causal prefill
+workloads (TFLOP/s), each against its roofline.  The cross-checks time the
+same 8192 positions as separate append/decode launches, as decode launches
+alone, and as fused steps with the rotary embedding.
 
 ``--impl reference`` times the fp64 CPU oracle (the only reference this
 method has) on the host cores, on a bounded sample of the same workload.
@@ -213,7 +216,10 @@ class Stream:
     mode "fused": attn_decode_step_append per position (append fused into
     the decode launch) -- the product's streaming path and the timed step.
     mode "pair": attn_kv_append then attn_decode_step per position.
-    mode "decode_only": attn_decode_step alone over a pre-filled cache."""
+    mode "decode_only": attn_decode_step alone over a pre-filled cache.
+    mode "rope": attn_decode_step_rope_append per position (the rotary
+    embedding of q and the new key fused in as well; cos/sin rows of the
+    usual base-10000 table at each position)."""
 
     def __init__(self, torch, ga, synth, mode="fused", seed=0):
         self.torch = torch
@@ -227,6 +233,8 @@ class Stream:
         self.scale = 1.0 / math.sqrt(D)
         self.ga = ga
         self.mode = mode
+        if mode == "rope":
+            self.cos, self.sin = synth.rope_tables(torch.arange(STEPS_STREAM), D, device=dev)
         if mode == "decode_only":  # fill the cache once so every position has its rows
             self._launch("append")
             torch.cuda.synchronize()
@@ -249,6 +257,12 @@ class Stream:
                 ga.attn_decode_step_append(self.q[s], self.k[s], self.v[s], self.pos[s], self.kc,
                                            self.vc, self.scale, out=self.outs[s],
                                            workspace=self.ws)
+                continue
+            if mode == "rope":
+                ga.attn_decode_step_rope_append(self.q[s], self.k[s], self.v[s],
+                                                self.cos[s:s + 1], self.sin[s:s + 1], self.pos[s],
+                                                self.kc, self.vc, self.scale, out=self.outs[s],
+                                                workspace=self.ws)
                 continue
             if mode in ("pair", "append"):
                 ga.attn_kv_append(self.k[s], self.v[s], self.pos[s], self.kc, self.vc)
@@ -337,6 +351,38 @@ def _decode_leg(torch, ga, synth, name, flush, hbm):
     r = {"us": round(ms * 1e3, 2), "GBs": round(nb / (ms * 1e-3) / 1e9, 1),
          "frac_hbm": round(nb / (ms * 1e-3) / 1e9 / hbm, 3),
          "TFLOPs_fp32_cuda_core": round(fl / (ms * 1e-3) / 1e12, 2), "bytes": nb,
+         "shape": {"B": B, "Hq": Hq, "Hkv": Hkv, "D": Dd, "L": Ll}}
+    del case, ws, out
+    torch.cuda.empty_cache()
+    return r
+
+
+def _append_leg(torch, ga, synth, name, flush, hbm, rope):
+    """The fused step (append + decode, with or without the rotary embedding)
+    on a decode workload.  Every launch rewrites the same rows with the same
+    values, so repeated launches do identical work."""
+    import oracle
+    case = synth.generators.workload_case(name, seed=0, device="cuda")
+    B, Hq, Dd = case.q.shape
+    Hkv, Ll = case.k_cache.shape[1], case.k_cache.shape[2]
+    ws = ga.decode_workspace(B, Hq, Hkv, Ll, Dd)
+    out = torch.empty_like(case.q)
+    cos, sin = synth.rope_tables(case.positions, Dd, device="cuda")
+
+    def one():
+        if rope:
+            ga.attn_decode_step_rope_append(case.q, case.k_new, case.v_new, cos, sin,
+                                            case.positions, case.k_cache, case.v_cache,
+                                            case.scale, out=out, workspace=ws)
+        else:
+            ga.attn_decode_step_append(case.q, case.k_new, case.v_new, case.positions,
+                                       case.k_cache, case.v_cache, case.scale, out=out,
+                                       workspace=ws)
+    ms = statistics.median(_time_graph(torch, one, flush, 10, 3))
+    pos = case.positions.cpu().tolist()
+    nb = oracle.decode_bytes(pos, Hq, Hkv, Dd) + 2 * 2 * B * Hkv * Dd * 2
+    r = {"us": round(ms * 1e3, 2), "GBs": round(nb / (ms * 1e-3) / 1e9, 1),
+         "frac_hbm": round(nb / (ms * 1e-3) / 1e9 / hbm, 3), "bytes": nb,
          "shape": {"B": B, "Hq": Hq, "Hkv": Hkv, "D": Dd, "L": Ll}}
     del case, ws, out
     torch.cuda.empty_cache()
@@ -440,6 +486,9 @@ def run_ours(args):
     dec = Stream(torch, ga, synth, mode="decode_only", seed=1)
     dec_ms = statistics.mean(_time_graph(torch, dec.replay, flush, max(3, args.steps), 3))
     del dec
+    rope = Stream(torch, ga, synth, mode="rope", seed=1)
+    rope_ms = statistics.mean(_time_graph(torch, rope.replay, flush, max(3, args.steps), 3))
+    del rope
 
     value = replica_throughput(ws, nbytes, statistics.mean(step_ms)) / 1e9
     line = {
@@ -483,7 +532,9 @@ def run_ours(args):
                              "33.5 MB cache is L2-resident within the loop"},
         "cross_checks": {"pair_append_then_decode_ms": round(pair_ms, 3),
                          "decode_only_ms": round(dec_ms, 3),
-                         "decode_only_GBs": round(nbytes / (dec_ms * 1e-3) / 1e9, 1)},
+                         "decode_only_GBs": round(nbytes / (dec_ms * 1e-3) / 1e9, 1),
+                         "rope_fused_ms": round(rope_ms, 3),
+                         "rope_fused_GBs": round(nbytes / (rope_ms * 1e-3) / 1e9, 1)},
     }
     if clk:
         line["clocks"] = clk
@@ -493,6 +544,9 @@ def run_ours(args):
         torch.cuda.empty_cache()
         for name in ("ragged", "stress"):
             legs[name] = _decode_leg(torch, ga, synth, name, flush, hbm)
+        legs["ragged_append"] = _append_leg(torch, ga, synth, "ragged", flush, hbm, rope=False)
+        legs["ragged_rope_append"] = _append_leg(torch, ga, synth, "ragged", flush, hbm,
+                                                 rope=True)
         for name in ("prefill_prefix", "prefill"):
             legs[name] = _prefill_leg(torch, ga, synth, name, flush, tf_burst)
         line["legs"] = legs

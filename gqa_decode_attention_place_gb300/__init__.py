@@ -22,7 +22,7 @@ __all__ = [
     "attn_kv_append", "attn_decode_workspace_size", "attn_decode_step",
     "attn_prefill_causal", "attn_read_device_status", "attn_status_string",
     "attn_last_cuda_error", "decode_workspace", "attn_decode_step_noalloc",
-    "attn_decode_step_append",
+    "attn_decode_step_append", "attn_decode_step_rope_append",
 ]
 
 ATTN_OK = 0
@@ -65,6 +65,9 @@ def load_library(build_if_missing: bool = True) -> ctypes.CDLL:
     lib.attn_decode_step_append.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, f32,
                                             vp, vp, sz, vp]
     lib.attn_decode_step_append.restype = i32
+    lib.attn_decode_step_rope_append.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32,
+                                                 i32, i32, f32, vp, vp, sz, vp]
+    lib.attn_decode_step_rope_append.restype = i32
     lib.attn_decode_step_noalloc.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, i32, f32, vp, vp]
     lib.attn_decode_step_noalloc.restype = i32
     lib.attn_prefill_causal.argtypes = [vp, vp, vp, i32, i32, i32, i32, i32, f32, vp, vp]
@@ -171,9 +174,8 @@ def attn_decode_step(q, positions, k_cache, v_cache, scale: float, out=None, wor
     return out
 
 
-def attn_decode_step_append(q, k_new, v_new, positions, k_cache, v_cache, scale: float,
-                            out=None, workspace=None, stream=None) -> torch.Tensor:
-    """attn_kv_append followed by attn_decode_step, in one launch."""
+def _decode_append(name, q, k_new, v_new, rope, positions, k_cache, v_cache, scale, out,
+                   workspace, stream) -> torch.Tensor:
     _check(q, "q", torch.bfloat16, 3)
     for t, n in ((k_new, "k_new"), (v_new, "v_new")):
         _check(t, n, torch.bfloat16, 3)
@@ -185,21 +187,48 @@ def attn_decode_step_append(q, k_new, v_new, positions, k_cache, v_cache, scale:
     if tuple(k_cache.shape) != (B, Hkv, L, D) or tuple(v_cache.shape) != (B, Hkv, L, D) \
             or tuple(k_new.shape) != (B, Hkv, D) or tuple(v_new.shape) != (B, Hkv, D) \
             or positions.shape[0] != B:
-        raise ValueError("attn_decode_step_append: inconsistent shapes")
+        raise ValueError(f"{name}: inconsistent shapes")
     if out is None:
         out = torch.empty_like(q)
     else:
         _check(out, "out", torch.bfloat16, 3)
         if tuple(out.shape) != (B, Hq, D):
-            raise ValueError("attn_decode_step_append: out has the wrong shape")
+            raise ValueError(f"{name}: out has the wrong shape")
     if workspace is None:
         workspace = decode_workspace(B, Hq, Hkv, L, D, device=q.device)
-    code = load_library().attn_decode_step_append(
-        q.data_ptr(), k_new.data_ptr(), v_new.data_ptr(), positions.data_ptr(),
-        k_cache.data_ptr(), v_cache.data_ptr(), B, Hq, Hkv, L, D, float(scale), out.data_ptr(),
-        workspace.data_ptr(), workspace.numel() * workspace.element_size(), _stream(stream))
-    _raise(code, "attn_decode_step_append")
+    lib = load_library()
+    head = (q.data_ptr(), k_new.data_ptr(), v_new.data_ptr())
+    if rope is not None:
+        head += (rope[0].data_ptr(), rope[1].data_ptr())
+    code = getattr(lib, name)(
+        *head, positions.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), B, Hq, Hkv, L, D,
+        float(scale), out.data_ptr(), workspace.data_ptr(),
+        workspace.numel() * workspace.element_size(), _stream(stream))
+    _raise(code, name)
     return out
+
+
+def attn_decode_step_append(q, k_new, v_new, positions, k_cache, v_cache, scale: float,
+                            out=None, workspace=None, stream=None) -> torch.Tensor:
+    """attn_kv_append followed by attn_decode_step, in one launch."""
+    return _decode_append("attn_decode_step_append", q, k_new, v_new, None, positions, k_cache,
+                          v_cache, scale, out, workspace, stream)
+
+
+def attn_decode_step_rope_append(q, k_new, v_new, cos, sin, positions, k_cache, v_cache,
+                                 scale: float, out=None, workspace=None,
+                                 stream=None) -> torch.Tensor:
+    """attn_decode_step_append with the rotary embedding applied first: q and
+    k_new are rotated by row b of ``cos``/``sin`` ([B, D] float32, the
+    rotation at positions[b]); the cache receives the rotated key."""
+    _check(q, "q", torch.bfloat16, 3)
+    for t, n in ((cos, "cos"), (sin, "sin")):
+        _check(t, n, torch.float32, 2)
+    B, _, D = q.shape
+    if tuple(cos.shape) != (B, D) or tuple(sin.shape) != (B, D):
+        raise ValueError("attn_decode_step_rope_append: cos and sin must be [B, D]")
+    return _decode_append("attn_decode_step_rope_append", q, k_new, v_new, (cos, sin), positions,
+                          k_cache, v_cache, scale, out, workspace, stream)
 
 
 def attn_decode_step_noalloc(q, positions, k_cache, v_cache, scale: float, out=None,

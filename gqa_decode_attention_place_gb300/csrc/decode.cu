@@ -6,7 +6,10 @@
 // over cache rows j = 0..positions[b] only (the slice replaces the
 // full-length boolean mask of section 2.1, so the work follows position+1 and
 // not max_len, sections 2.4 and 6.4).  Optionally the step's new K/V row is
-// appended in the same launch (the page writes the row, then attends).
+// appended in the same launch (the page writes the row, then attends), and
+// optionally q and the new key row are first rotated by the rotary embedding
+// at each sequence's position (the page's apply_rotary_pos_emb, run before
+// the cache write; rotate-half form, fp32, one rounding per operation).
 //
 // How (GB300 design, not the page's: the page calls PyTorch SDPA):
 //  * The attended rows of every (sequence, KV head) pair -- a "segment" -- are
@@ -69,6 +72,8 @@ struct Params {
   uint32_t* counters;
   float* part_ml;
   float* part_o;
+  const float* rope_cos;  // [B, D] rotation at positions[b] (with k_new), or null
+  const float* rope_sin;
   int B, Hq, Hkv, L;
   float qscale;  // scale * log2(e)
 };
@@ -95,11 +100,6 @@ template <int G> struct Cfg {
 template <int NC>
 __device__ __forceinline__ void consumer_bar() {
   asm volatile("bar.sync 1, %0;" ::"n"(NC) : "memory");
-}
-
-__device__ __forceinline__ void cluster_sync_all() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
-               "barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
 // Position of flat tile t within (sequence, KV head, tile) order.
@@ -180,6 +180,17 @@ __device__ __forceinline__ void unpack8x2(const uint4& u, f2 (&f)[4]) {
   f[3] = mk2(bf16lo(u.w), bf16hi(u.w));
 }
 
+// Rotary embedding, rotate-half form, on N consecutive dims x of a row whose
+// partner dims (64 away) are y: x' = x*cos + r*sin with r = -y in the first
+// half of the row and r = y in the second.  Each product and the sum are
+// rounded separately (no contraction into a fused multiply-add), so the
+// result is the same fp32 value however the caller splits the row.
+__device__ __forceinline__ float rope1(float x, float partner, float c, float sn,
+                                       bool first_half) {
+  const float r = first_half ? -partner : partner;
+  return __fadd_rn(__fmul_rn(x, c), __fmul_rn(r, sn));
+}
+
 // Per-warp consumer state and math: one KV head's g query heads.  Lane
 // `lane` works on key group grp = lane / LPK (32/LPK keys per step) and holds
 // 128/LPK dims of that key: VPL 16-byte vectors, vector v covering dims
@@ -218,6 +229,21 @@ struct Consumer {
 #pragma unroll
         for (int j = 0; j < 4; ++j)
           qf[h][4 * v + j] = mk2(bf16lo(wd[j]) * qscale, bf16hi(wd[j]) * qscale);
+      }
+  }
+  // The same from the rotated query, q_rot [G][kD] fp32 in shared memory.
+  __device__ __forceinline__ void load_q_rot(const float* q_rot, float qscale) {
+#pragma unroll
+    for (int h = 0; h < G; ++h)
+#pragma unroll
+      for (int v = 0; v < VPL; ++v) {
+        const float* src = q_rot + h * kD + dim_off(v) / 2;
+        const float4 a = *reinterpret_cast<const float4*>(src);
+        const float4 c = *reinterpret_cast<const float4*>(src + 4);
+        qf[h][4 * v + 0] = mk2(a.x * qscale, a.y * qscale);
+        qf[h][4 * v + 1] = mk2(a.z * qscale, a.w * qscale);
+        qf[h][4 * v + 2] = mk2(c.x * qscale, c.y * qscale);
+        qf[h][4 * v + 3] = mk2(c.z * qscale, c.w * qscale);
       }
   }
   __device__ __forceinline__ void reset() {
@@ -382,18 +408,19 @@ __device__ __forceinline__ void merge_warps(const float* merge_o, const float* m
   }
 }
 
-// Producer: one tile's bulk copies.  With the fused append the segment's
-// last tile ends with row pos = n-1, taken from k_new/v_new (copied into the
-// tile and, by this thread, into the cache).  No other CTA reads that row.
+// Producer (one thread): one tile's bulk copies.  With the fused append the
+// segment's last tile ends with row pos = n-1, taken from k_new/v_new instead
+// of the cache; the consumers rotate it if asked (rope_fresh_key) and write
+// it to the cache (write_fresh_rows).  No other CTA reads that row.
 __device__ __forceinline__ void produce_tile(const Params& p, uint8_t* stages, uint64_t* bars,
                                              int s, int b, int kvh, int k, int ntiles, int n) {
   const int rows = min(kTile, n - k * kTile);
   const size_t row0 = ((size_t)b * p.Hkv + kvh) * (size_t)p.L + (size_t)k * kTile;
+  const bool fresh = p.k_new != nullptr && k == ntiles - 1;
+  const int cache_rows = fresh ? rows - 1 : rows;
   const uint32_t full = smem_u32(&bars[s]);
   const uint32_t sK = smem_u32(stages + (size_t)s * 2 * kTileBytes);
   const uint32_t sV = sK + kTileBytes;
-  const bool fresh = p.k_new != nullptr && k == ntiles - 1;
-  const int cache_rows = fresh ? rows - 1 : rows;
   mbar_arrive_expect_tx(full, 2u * (uint32_t)rows * kRowBytes);
   if (cache_rows > 0) {
     const uint32_t bytes = (uint32_t)cache_rows * kRowBytes;
@@ -405,16 +432,67 @@ __device__ __forceinline__ void produce_tile(const Params& p, uint8_t* stages, u
     const uint32_t off = (uint32_t)cache_rows * kRowBytes;
     bulk_g2s(sK + off, p.k_new + src, kRowBytes, full);
     bulk_g2s(sV + off, p.v_new + src, kRowBytes, full);
-    const uint4* kn = reinterpret_cast<const uint4*>(p.k_new + src);
-    const uint4* vn = reinterpret_cast<const uint4*>(p.v_new + src);
-    uint4* kd = reinterpret_cast<uint4*>(p.k_cache + (row0 + cache_rows) * kRowBytes);
-    uint4* vd = reinterpret_cast<uint4*>(p.v_cache + (row0 + cache_rows) * kRowBytes);
-#pragma unroll
-    for (int c = 0; c < kRowBytes / 16; ++c) {
-      kd[c] = kn[c];
-      vd[c] = vn[c];
-    }
   }
+}
+
+// Rotary embedding of one segment, by the consumers.  rope_segment (all NC
+// consumer threads, at the start of a segment, followed by a consumer
+// barrier): the G query rows of the segment, rotated, into q_rot [G][kD] fp32,
+// and the sequence's cos/sin row into rope_cs [2][kD].  rope_fresh_key (one
+// warp, once the segment's last tile has landed): the appended key row of
+// the tile rotated in place, lane l taking dims 4l..4l+3 and reading its
+// partner dims 64 away before any lane writes.
+template <int G, int NC>
+__device__ __forceinline__ void rope_segment(const uint16_t* qb, const float* rc, const float* rs,
+                                             float* q_rot, float* rope_cs, int ct) {
+  constexpr int kH = kD / 2;
+  for (int i = ct; i < G * kH; i += NC) {
+    const int h = i / kH, d = i % kH;
+    const uint16_t* qh = qb + (size_t)h * kD;
+    const float x0 = __uint_as_float((uint32_t)qh[d] << 16);
+    const float x1 = __uint_as_float((uint32_t)qh[d + kH] << 16);
+    q_rot[h * kD + d] = rope1(x0, x1, rc[d], rs[d], true);
+    q_rot[h * kD + d + kH] = rope1(x1, x0, rc[d + kH], rs[d + kH], false);
+  }
+  for (int i = ct; i < 2 * kD; i += NC) rope_cs[i] = i < kD ? rc[i] : rs[i - kD];
+}
+
+__device__ __forceinline__ void rope_fresh_key(uint8_t* row, const float* rope_cs, int lane) {
+  const int d0 = 4 * lane;
+  const uint2 a = *reinterpret_cast<const uint2*>(row + d0 * 2);
+  const uint2 y2 = *reinterpret_cast<const uint2*>(row + (d0 ^ 64) * 2);
+  __syncwarp();
+  const float4 c4 = *reinterpret_cast<const float4*>(rope_cs + d0);
+  const float4 s4 = *reinterpret_cast<const float4*>(rope_cs + kD + d0);
+  float x[4] = {bf16lo(a.x), bf16hi(a.x), bf16lo(a.y), bf16hi(a.y)};
+  const float y[4] = {bf16lo(y2.x), bf16hi(y2.x), bf16lo(y2.y), bf16hi(y2.y)};
+  const float c[4] = {c4.x, c4.y, c4.z, c4.w};
+  const float sn[4] = {s4.x, s4.y, s4.z, s4.w};
+#pragma unroll
+  for (int j = 0; j < 4; ++j) x[j] = rope1(x[j], y[j], c[j], sn[j], d0 < kD / 2);
+  *reinterpret_cast<uint2*>(row + d0 * 2) =
+      make_uint2(pack_bf16x2(x[0], x[1]), pack_bf16x2(x[2], x[3]));
+}
+
+// The fused append's cache write: once a segment's last tile has landed, the
+// appended K and V rows (its last row, rotated key included) go from shared
+// memory to cache row pos = n-1, one 16-byte store per lane of one consumer
+// warp (lanes 0-15 the K row, 16-31 the V row).
+__device__ __forceinline__ void write_fresh_rows(const Params& p, const uint8_t* Ks, int rows,
+                                                 int b, int kvh, int n, int lane) {
+  const int c = lane & 15;
+  const bool is_v = lane >= 16;
+  const uint8_t* src = Ks + (is_v ? kTileBytes : 0) + (size_t)(rows - 1) * kRowBytes + c * 16;
+  uint8_t* dst = (is_v ? p.v_cache : p.k_cache) +
+                 (((size_t)b * p.Hkv + kvh) * (size_t)p.L + (size_t)(n - 1)) * kRowBytes + c * 16;
+  *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<const uint4*>(src);
+}
+
+// Row b of a [B, D] rotation table, or null in kernels built without the
+// rotary embedding (the compiler then drops the rotation code).
+template <bool R>
+__device__ __forceinline__ const float* rope_row(const float* t, int b) {
+  return R ? t + (size_t)b * kD : nullptr;
 }
 
 __device__ __forceinline__ void write_nan_rows(const Params& p, int b) {
@@ -433,11 +511,12 @@ size_t smem_bytes(int B) {
   constexpr int NW = Cfg<G>::NW;
   return (size_t)kStages * 2 * kTileBytes + 2 * kStages * sizeof(uint64_t) +
          kMiscInts * sizeof(int) + (size_t)NW * G * 2 * sizeof(float) +
-         (size_t)NW * G * kD * sizeof(float) + (size_t)(B + 1) * sizeof(int);
+         (size_t)NW * G * kD * sizeof(float) + (2 + G) * kD * sizeof(float) +
+         (size_t)(B + 1) * sizeof(int);
 }
 
 // ---------------------------------------------------------- stream-K mode --
-template <int G>
+template <int G, bool R>
 __global__ void __maxnreg__(Cfg<G>::kMaxRegs) decode_splitkv_kernel(const Params p) {
   constexpr int NW = Cfg<G>::NW;
   constexpr int NC = Cfg<G>::kConsumers;
@@ -447,7 +526,9 @@ __global__ void __maxnreg__(Cfg<G>::kMaxRegs) decode_splitkv_kernel(const Params
   int* misc = reinterpret_cast<int*>(bars + 2 * kStages);
   float* merge_ml = reinterpret_cast<float*>(misc + kMiscInts);  // [NW][G][2]
   float* merge_o = merge_ml + NW * G * 2;                         // [NW][G][kD]
-  int* prefix = reinterpret_cast<int*>(merge_o + NW * G * kD);    // [B+1]
+  float* rope_cs = merge_o + NW * G * kD;                         // [2][kD] cos, sin
+  float* q_rot = rope_cs + 2 * kD;                                 // [G][kD]
+  int* prefix = reinterpret_cast<int*>(q_rot + G * kD);            // [B+1]
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
@@ -547,7 +628,15 @@ __global__ void __maxnreg__(Cfg<G>::kMaxRegs) decode_splitkv_kernel(const Params
   cs.init(lane);
   Walk w;
   walk_init(w, t0, prefix, p.positions, B, Hkv);
-  cs.load_q(p.q + ((size_t)w.b * p.Hq + (size_t)w.kvh * G) * kD, p.qscale);
+  const uint16_t* qb = p.q + ((size_t)w.b * p.Hq + (size_t)w.kvh * G) * kD;
+  if (R) {
+    rope_segment<G, NC>(qb, rope_row<R>(p.rope_cos, w.b), rope_row<R>(p.rope_sin, w.b), q_rot,
+                        rope_cs, tid);
+    consumer_bar<NC>();
+    cs.load_q_rot(q_rot, p.qscale);
+  } else {
+    cs.load_q(qb, p.qscale);
+  }
   cs.reset();
 
   long long i = 0;
@@ -560,7 +649,14 @@ __global__ void __maxnreg__(Cfg<G>::kMaxRegs) decode_splitkv_kernel(const Params
       break;
     }
     const int rows = min(kTile, w.n - w.k * kTile);
-    const uint8_t* Ks = stages + (size_t)s * 2 * kTileBytes;
+    uint8_t* Ks = stages + (size_t)s * 2 * kTileBytes;
+    if (p.k_new != nullptr && w.k == w.ntiles - 1) {
+      if (R) {
+        if (warp == 0) rope_fresh_key(Ks + (size_t)(rows - 1) * kRowBytes, rope_cs, lane);
+        consumer_bar<NC>();
+      }
+      if (warp == 0) write_fresh_rows(p, Ks, rows, w.b, w.kvh, w.n, lane);
+    }
     cs.tile(Ks, Ks + kTileBytes, rows, warp);
     __syncwarp();
     if (lane == 0) mbar_arrive(smem_u32(&bars[kStages + s]));
@@ -653,8 +749,19 @@ __global__ void __maxnreg__(Cfg<G>::kMaxRegs) decode_splitkv_kernel(const Params
       cs.reset();
     }
     walk_next(w, prefix, p.positions, B, Hkv);
-    if (w.k == 0 && t + 1 < t1)
-      cs.load_q(p.q + ((size_t)w.b * p.Hq + (size_t)w.kvh * G) * kD, p.qscale);
+    if (w.k == 0 && t + 1 < t1) {
+      // a new segment; every consumer has read q_rot and rope_cs of the last
+      // one (seg_end's barriers came after), so they may be overwritten
+      const uint16_t* qn = p.q + ((size_t)w.b * p.Hq + (size_t)w.kvh * G) * kD;
+      if (R) {
+        rope_segment<G, NC>(qn, rope_row<R>(p.rope_cos, w.b), rope_row<R>(p.rope_sin, w.b),
+                            q_rot, rope_cs, tid);
+        consumer_bar<NC>();
+        cs.load_q_rot(q_rot, p.qscale);
+      } else {
+        cs.load_q(qn, p.qscale);
+      }
+    }
   }
 
   if (*abort_flag) {
@@ -671,12 +778,13 @@ size_t cluster_smem_bytes() {
   constexpr int NW = Cfg<G>::NW;
   return (size_t)kStages * 2 * kTileBytes + 2 * kStages * sizeof(uint64_t) +
          kMiscInts * sizeof(int) + (size_t)NW * G * 2 * sizeof(float) +
-         (size_t)NW * G * kD * sizeof(float) + (size_t)G * (kD + 2) * sizeof(float);
+         (size_t)NW * G * kD * sizeof(float) + (2 + G) * kD * sizeof(float) +
+         (size_t)G * (kD + 2) * sizeof(float);
 }
 
 // Grid = B*Hkv clusters of C CTAs; cluster s handles segment s (sequence
 // s / Hkv, KV head s % Hkv).
-template <int G>
+template <int G, bool R>
 __global__ void __maxnreg__(Cfg<G>::kMaxRegs) decode_cluster_kernel(const Params p) {
   constexpr int NW = Cfg<G>::NW;
   constexpr int NC = Cfg<G>::kConsumers;
@@ -686,7 +794,9 @@ __global__ void __maxnreg__(Cfg<G>::kMaxRegs) decode_cluster_kernel(const Params
   int* misc = reinterpret_cast<int*>(bars + 2 * kStages);
   float* merge_ml = reinterpret_cast<float*>(misc + kMiscInts);  // [NW][G][2]
   float* merge_o = merge_ml + NW * G * 2;                         // [NW][G][kD]
-  float* part_o = merge_o + NW * G * kD;                          // [G][kD]
+  float* rope_cs = merge_o + NW * G * kD;                         // [2][kD] cos, sin
+  float* q_rot = rope_cs + 2 * kD;                                 // [G][kD]
+  float* part_o = q_rot + G * kD;                                 // [G][kD]
   float* part_ml = part_o + G * kD;                               // [G][2]
 
   cg::cluster_group cluster = cg::this_cluster();
@@ -744,7 +854,15 @@ __global__ void __maxnreg__(Cfg<G>::kMaxRegs) decode_cluster_kernel(const Params
     // ----------------------------------------------------------- consumers --
     Consumer<G> cs;
     cs.init(lane);
-    cs.load_q(p.q + ((size_t)b * p.Hq + (size_t)kvh * G) * kD, p.qscale);
+    const uint16_t* qb = p.q + ((size_t)b * p.Hq + (size_t)kvh * G) * kD;
+    if (R) {
+      rope_segment<G, NC>(qb, rope_row<R>(p.rope_cos, b), rope_row<R>(p.rope_sin, b), q_rot,
+                          rope_cs, tid);
+      consumer_bar<NC>();
+      cs.load_q_rot(q_rot, p.qscale);
+    } else {
+      cs.load_q(qb, p.qscale);
+    }
     cs.reset();
     for (int k = k0; k < k1; ++k) {
       const int i = k - k0;
@@ -755,7 +873,14 @@ __global__ void __maxnreg__(Cfg<G>::kMaxRegs) decode_cluster_kernel(const Params
         break;
       }
       const int rows = min(kTile, n - k * kTile);
-      const uint8_t* Ks = stages + (size_t)s * 2 * kTileBytes;
+      uint8_t* Ks = stages + (size_t)s * 2 * kTileBytes;
+      if (p.k_new != nullptr && k == ntiles - 1) {
+        if (R) {
+          if (warp == 0) rope_fresh_key(Ks + (size_t)(rows - 1) * kRowBytes, rope_cs, lane);
+          consumer_bar<NC>();
+        }
+        if (warp == 0) write_fresh_rows(p, Ks, rows, b, kvh, n, lane);
+      }
       cs.tile(Ks, Ks + kTileBytes, rows, warp);
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&bars[kStages + s]));
@@ -842,35 +967,48 @@ int max_clusters(int C) {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, decode_cluster_kernel<G>, &cfg) != cudaSuccess) {
+  if (cudaOccupancyMaxActiveClusters(&n, decode_cluster_kernel<G, false>, &cfg) != cudaSuccess) {
     cudaGetLastError();
     return 0;
   }
   return n;
 }
 
-template <int G>
-cudaError_t configure(DevInfo& d) {
-  if (d.configured[G]) return cudaSuccess;
-  cudaError_t e = cudaFuncSetAttribute(decode_splitkv_kernel<G>,
+template <int G, bool R>
+cudaError_t set_attributes(bool* big) {
+  cudaError_t e = cudaFuncSetAttribute(decode_splitkv_kernel<G, R>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)smem_bytes<G>(kMaxB));
   if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(decode_cluster_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  e = cudaFuncSetAttribute(decode_cluster_kernel<G, R>,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)cluster_smem_bytes<G>());
   if (e != cudaSuccess) return e;
-  const bool big = cudaFuncSetAttribute(decode_cluster_kernel<G>,
-                                        cudaFuncAttributeNonPortableClusterSizeAllowed,
-                                        1) == cudaSuccess;
-  if (!big) cudaGetLastError();
-  // How many clusters of each size can run at once (a cluster stays within
-  // one GPC, so this is set by the SMs per GPC, not by the SM count).
-  for (int c = 2; c <= kMaxCluster; ++c) d.clusters[G][c] = (c <= 8 || big) ? max_clusters<G>(c) : 0;
-  d.configured[G] = true;
+  *big = cudaFuncSetAttribute(decode_cluster_kernel<G, R>,
+                              cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess;
+  if (!*big) cudaGetLastError();
   return cudaSuccess;
 }
 
 template <int G>
+cudaError_t configure(DevInfo& d) {
+  if (d.configured[G]) return cudaSuccess;
+  bool big = false, big_rope = false;
+  cudaError_t e = set_attributes<G, false>(&big);
+  if (e == cudaSuccess) e = set_attributes<G, true>(&big_rope);
+  if (e != cudaSuccess) return e;
+  big = big && big_rope;
+  // How many clusters of each size can run at once (a cluster stays within
+  // one GPC, so this is set by the SMs per GPC, not by the SM count).  Both
+  // variants have the same block, shared memory and register cap, so the
+  // plain one stands for both.
+  for (int c = 2; c <= kMaxCluster; ++c)
+    d.clusters[G][c] = (c <= 8 || big) ? max_clusters<G>(c) : 0;
+  d.configured[G] = true;
+  return cudaSuccess;
+}
+
+template <int G, bool R>
 cudaError_t launch_g(const Params& p, cudaStream_t stream) {
   int dev = 0;
   DevInfo& d = dev_info(&dev);
@@ -897,10 +1035,10 @@ cudaError_t launch_g(const Params& p, cudaStream_t stream) {
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    e = cudaLaunchKernelEx(&cfg, decode_cluster_kernel<G>, p);
+    e = cudaLaunchKernelEx(&cfg, decode_cluster_kernel<G, R>, p);
     return e != cudaSuccess ? e : cudaGetLastError();
   }
-  return launch_pdl(decode_splitkv_kernel<G>, dim3(min(kMaxGrid, d.num_sms)),
+  return launch_pdl(decode_splitkv_kernel<G, R>, dim3(min(kMaxGrid, d.num_sms)),
                     dim3(Cfg<G>::kThreads), smem_bytes<G>(p.B), stream, p);
 }
 
@@ -927,9 +1065,9 @@ bool decode_supported(int B, int Hq, int Hkv, int L, int D) {
 }
 
 cudaError_t launch_decode(const void* q, const void* k_new, const void* v_new,
-                          const int32_t* positions, const void* k_cache, const void* v_cache,
-                          int B, int Hq, int Hkv, int L, int D, float scale, void* out,
-                          void* workspace, cudaStream_t stream) {
+                          const float* rope_cos, const float* rope_sin, const int32_t* positions,
+                          const void* k_cache, const void* v_cache, int B, int Hq, int Hkv, int L,
+                          int D, float scale, void* out, void* workspace, cudaStream_t stream) {
   const DecodeWorkspace ws = decode_workspace_layout(B, Hq, Hkv, D);
   uint8_t* base = static_cast<uint8_t*>(workspace);
   Params p;
@@ -944,16 +1082,19 @@ cudaError_t launch_decode(const void* q, const void* k_new, const void* v_new,
   p.counters = reinterpret_cast<uint32_t*>(base + ws.counters_off);
   p.part_ml = reinterpret_cast<float*>(base + ws.ml_off);
   p.part_o = reinterpret_cast<float*>(base + ws.o_off);
+  p.rope_cos = rope_cos;
+  p.rope_sin = rope_sin;
   p.B = B;
   p.Hq = Hq;
   p.Hkv = Hkv;
   p.L = L;
   p.qscale = scale * kLog2e;
+  const bool rope = rope_cos != nullptr;
   switch (Hq / Hkv) {
-    case 1: return launch_g<1>(p, stream);
-    case 2: return launch_g<2>(p, stream);
-    case 4: return launch_g<4>(p, stream);
-    case 8: return launch_g<8>(p, stream);
+    case 1: return rope ? launch_g<1, true>(p, stream) : launch_g<1, false>(p, stream);
+    case 2: return rope ? launch_g<2, true>(p, stream) : launch_g<2, false>(p, stream);
+    case 4: return rope ? launch_g<4, true>(p, stream) : launch_g<4, false>(p, stream);
+    case 8: return rope ? launch_g<8, true>(p, stream) : launch_g<8, false>(p, stream);
   }
   return cudaErrorInvalidValue;
 }
@@ -1007,8 +1148,8 @@ cudaError_t launch_decode_noalloc(const void* q, const int32_t* positions, const
   const DecodeWorkspace ws = decode_workspace_layout(B, Hq, Hkv, D);
   e = cudaMemsetAsync(scratch, 0, ws.ml_off, stream);
   if (e != cudaSuccess) return e;
-  return launch_decode(q, nullptr, nullptr, positions, k_cache, v_cache, B, Hq, Hkv, L, D, scale,
-                       out, scratch, stream);
+  return launch_decode(q, nullptr, nullptr, nullptr, nullptr, positions, k_cache, v_cache, B, Hq,
+                       Hkv, L, D, scale, out, scratch, stream);
 }
 
 }  // namespace gqa

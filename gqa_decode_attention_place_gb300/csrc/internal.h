@@ -21,10 +21,12 @@ DecodeWorkspace decode_workspace_layout(int B, int Hq, int Hkv, int D);
 
 // k_new/v_new null: attention only.  Non-null: the rows are appended at
 // positions[b] inside the same launch (kv append fused into decode).
+// rope_cos/rope_sin ([B, D] fp32, only with k_new) non-null: q and the new
+// key row are first rotated by the rotary embedding given by those rows.
 cudaError_t launch_decode(const void* q, const void* k_new, const void* v_new,
-                          const int32_t* positions, const void* k_cache, const void* v_cache,
-                          int B, int Hq, int Hkv, int L, int D, float scale, void* out,
-                          void* workspace, cudaStream_t stream);
+                          const float* rope_cos, const float* rope_sin, const int32_t* positions,
+                          const void* k_cache, const void* v_cache, int B, int Hq, int Hkv, int L,
+                          int D, float scale, void* out, void* workspace, cudaStream_t stream);
 
 // Allocation-free decode: scratch in a fixed device array (decode.cu).
 size_t noalloc_scratch_bytes();

@@ -145,6 +145,33 @@ int attn_decode_step_append(const void* q, const void* k_new, const void* v_new,
                             cudaStream_t stream);
 
 /*
+ * attn_decode_step_rope_append -- attn_decode_step_append with the rotary
+ * position embedding applied first, as the decode page's forward_step does
+ * (section 4.1: apply_rotary_pos_emb(q, k, cos, sin) runs before the cache
+ * write).  The page does not define the rotation; this library takes the
+ * rotate-half form, for every dim d of a row x:
+ *     x'[d] = x[d]*cos[d] - x[d+D/2]*sin[d]          for d <  D/2
+ *     x'[d] = x[d]*cos[d] + x[d-D/2]*sin[d]          for d >= D/2
+ * in fp32, each product and the sum rounded separately (no fused
+ * multiply-add).  The rotated key is rounded to bf16 (nearest even) and that
+ * is what the cache row holds; the rotated query is kept in fp32 for the
+ * attention.  v_new is appended unrotated.
+ *
+ *   cos, sin : [B, D] fp32, device memory, 16-byte aligned; row b is the
+ *              rotation for sequence b at positions[b] (the caller computes
+ *              it, so any frequency base or scaling works).  Read only.
+ *   all other arguments, sizes and errors: as attn_decode_step_append.
+ *
+ * Errors: ATTN_ERR_INVALID_ARG also for a null or misaligned cos or sin.
+ */
+int attn_decode_step_rope_append(const void* q, const void* k_new, const void* v_new,
+                                 const float* cos, const float* sin,
+                                 const int32_t* positions, void* k_cache, void* v_cache,
+                                 int B, int Hq, int Hkv, int L, int D, float scale,
+                                 void* out, void* workspace, size_t workspace_bytes,
+                                 cudaStream_t stream);
+
+/*
  * attn_decode_step_noalloc -- attn_decode_step without a workspace argument.
  * The decode page has no counterpart: this entry point exists for callers
  * that cannot call cudaMalloc, for example code running while a CUDA graph is

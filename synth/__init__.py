@@ -1,8 +1,9 @@
 """Seeded synthetic inputs shared by the CUDA path's tests/bench and the oracle.
 
 This module only *draws* inputs (random numbers, shapes, positions, poison
-rows).  It holds none of the attention arithmetic, so both the CUDA path and the
-CPU oracle can consume its outputs without sharing any of the method's code.
+rows, the rotary embedding's cos/sin tables).  It holds none of the attention
+or rotation arithmetic, so both the CUDA path and the CPU oracle can consume
+its outputs without sharing any of the method's code.
 """
 
 from .generators import (  # noqa: F401
@@ -11,6 +12,7 @@ from .generators import (  # noqa: F401
     decode_case,
     prefill_case,
     streaming_inputs,
+    rope_tables,
     bf16_from_f32,
     WORKLOADS,
 )

@@ -186,6 +186,20 @@ def streaming_inputs(steps=8192, B=1, Hq=16, Hkv=8, D=128, seed: int = 0,
     return q, k, v, pos
 
 
+def rope_tables(positions, D: int = 128, base: float = 10000.0, device="cpu"):
+    """cos/sin tables [B, D] float32 for the rotary embedding at each
+    sequence's position: the usual frequencies base**(-2i/D), i < D/2, each
+    repeated for both halves of the row.  Angles and their cos/sin are taken in
+    float64 and rounded once to float32; they are inputs to the rotation (the
+    model's table), not part of it."""
+    pos = torch.as_tensor(positions).to(device="cpu", dtype=torch.float64).view(-1, 1)
+    inv = base ** (-torch.arange(0, D, 2, dtype=torch.float64) / D)
+    ang = pos * inv.view(1, -1)
+    ang = torch.cat([ang, ang], dim=1)
+    return (torch.cos(ang).to(torch.float32).to(device).contiguous(),
+            torch.sin(ang).to(torch.float32).to(device).contiguous())
+
+
 def workload_case(name: str, seed: int = 0, device="cpu", poison=False):
     """The named workload's inputs (decode or prefill)."""
     w = dict(WORKLOADS[name])

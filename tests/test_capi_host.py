@@ -37,7 +37,8 @@ def test_header_declares_the_boundary():
     names = _declared_functions()
     for want in ["attn_kv_append", "attn_decode_workspace_size", "attn_decode_step",
                  "attn_prefill_causal", "attn_read_device_status", "attn_status_string",
-                 "attn_last_cuda_error"]:
+                 "attn_last_cuda_error", "attn_decode_step_append",
+                 "attn_decode_step_rope_append", "attn_decode_step_noalloc"]:
         assert want in names
 
 
@@ -92,6 +93,13 @@ def test_host_validation_happens_before_any_launch(lib):
     assert lib.attn_prefill_causal(P, P, P, 4, 0, 32, 7, 64, 0.125, P, None) == 1
     assert lib.attn_prefill_causal(P, P, P, 4, 0, 32, 32, 80, 0.125, P, None) == 2
     assert lib.attn_read_device_status(None, None, None) == 1
+    # rotary step: null or misaligned cos/sin, then the append step's own checks
+    rope = lib.attn_decode_step_rope_append
+    assert rope(P, P, P, None, P, P, P, P, 1, 16, 8, 16, 128, 1.0, P, P, 1 << 20, None) == 1
+    assert rope(P, P, P, P, P + 4, P, P, P, 1, 16, 8, 16, 128, 1.0, P, P, 1 << 20, None) == 1
+    assert rope(P, None, P, P, P, P, P, P, 1, 16, 8, 16, 128, 1.0, P, P, 1 << 20, None) == 1
+    assert rope(P, P, P, P, P, P, P, P, 1, 32, 2, 16, 128, 1.0, P, P, 1 << 20, None) == 2
+    assert rope(P, P, P, P, P, P, P, P, 1, 16, 8, 16, 128, 1.0, P, P, need - 1, None) == 3
 
 
 def test_binding_rejects_cpu_tensors():
