@@ -97,10 +97,34 @@ template <int G> struct Cfg {
   static constexpr int kMaxRegs = (65536 / ((kThreads + 127) / 128 * 128)) & ~7;
 };
 
+// A named barrier among the consumers, only for the one place every consumer
+// warp reaches unconditionally: before the first tile wait.
 template <int NC>
 __device__ __forceinline__ void consumer_bar() {
   asm volatile("bar.sync 1, %0;" ::"n"(NC) : "memory");
 }
+
+// Barrier among the NW consumer warps everywhere else.  It sits on an
+// mbarrier (count NW, one arrival per warp from lane 0 once the warp's lanes
+// have synced) so that its wait is bounded like every other: a named barrier
+// has no time limit, and a warp that gave up on a tile after a timeout would
+// leave the others waiting at one for ever.
+struct ConsumerSync {
+  uint32_t bar;
+  volatile int* abort_flag;
+  uint32_t* status;
+  uint32_t n;  // completed phases
+  __device__ __forceinline__ void operator()(int lane) {
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bar);
+    if (!mbar_wait(bar, n & 1u, abort_flag) && lane == 0) {
+      *abort_flag = 1;
+      set_status(status, ATTN_DEV_TIMEOUT);
+    }
+    ++n;
+    __syncwarp();
+  }
+};
 
 // Position of flat tile t within (sequence, KV head, tile) order.
 struct Walk {
@@ -410,8 +434,8 @@ __device__ __forceinline__ void merge_warps(const float* merge_o, const float* m
 
 // Producer (one thread): one tile's bulk copies.  With the fused append the
 // segment's last tile ends with row pos = n-1, taken from k_new/v_new instead
-// of the cache; the consumers rotate it if asked (rope_fresh_key) and write
-// it to the cache (write_fresh_rows).  No other CTA reads that row.
+// of the cache; a consumer warp rotates it if asked and writes it to the
+// cache (fresh_row).  No other CTA reads that row.
 __device__ __forceinline__ void produce_tile(const Params& p, uint8_t* stages, uint64_t* bars,
                                              int s, int b, int kvh, int k, int ntiles, int n) {
   const int rows = min(kTile, n - k * kTile);
@@ -474,10 +498,24 @@ __device__ __forceinline__ void rope_fresh_key(uint8_t* row, const float* rope_c
       make_uint2(pack_bf16x2(x[0], x[1]), pack_bf16x2(x[2], x[3]));
 }
 
+// A consumer warp's wait for a tile, with the outcome made warp-uniform (the
+// tile math uses full-warp shuffles, so either every lane goes on or every
+// lane leaves the loop).
+__device__ __forceinline__ bool consumer_wait(uint32_t bar, uint32_t parity,
+                                              volatile int* abort_flag, uint32_t* status,
+                                              int lane) {
+  if (__all_sync(0xffffffffu, mbar_wait(bar, parity, abort_flag))) return true;
+  if (lane == 0) {
+    *abort_flag = 1;
+    set_status(status, ATTN_DEV_TIMEOUT);
+  }
+  return false;
+}
+
 // The fused append's cache write: once a segment's last tile has landed, the
 // appended K and V rows (its last row, rotated key included) go from shared
-// memory to cache row pos = n-1, one 16-byte store per lane of one consumer
-// warp (lanes 0-15 the K row, 16-31 the V row).
+// memory to cache row pos = n-1, one 16-byte store per lane of one warp
+// (lanes 0-15 the K row, 16-31 the V row).
 __device__ __forceinline__ void write_fresh_rows(const Params& p, const uint8_t* Ks, int rows,
                                                  int b, int kvh, int n, int lane) {
   const int c = lane & 15;
@@ -486,6 +524,19 @@ __device__ __forceinline__ void write_fresh_rows(const Params& p, const uint8_t*
   uint8_t* dst = (is_v ? p.v_cache : p.k_cache) +
                  (((size_t)b * p.Hkv + kvh) * (size_t)p.L + (size_t)(n - 1)) * kRowBytes + c * 16;
   *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<const uint4*>(src);
+}
+
+// The appended row of a segment's last tile, by the one consumer warp whose
+// keys include it (row rows-1): rotated in place first with the rotary
+// embedding, then written to the cache.  No other warp reads the K row.
+template <bool R>
+__device__ __forceinline__ void fresh_row(const Params& p, uint8_t* Ks, int rows, int b, int kvh,
+                                          int n, const float* rope_cs, int lane) {
+  if (R) {
+    rope_fresh_key(Ks + (size_t)(rows - 1) * kRowBytes, rope_cs, lane);
+    __syncwarp();
+  }
+  write_fresh_rows(p, Ks, rows, b, kvh, n, lane);
 }
 
 // Row b of a [B, D] rotation table, or null in kernels built without the
@@ -509,7 +560,7 @@ __device__ __forceinline__ void store_bf16(uint16_t* dst, float v) {
 template <int G>
 size_t smem_bytes(int B) {
   constexpr int NW = Cfg<G>::NW;
-  return (size_t)kStages * 2 * kTileBytes + 2 * kStages * sizeof(uint64_t) +
+  return (size_t)kStages * 2 * kTileBytes + (2 * kStages + 2) * sizeof(uint64_t) +
          kMiscInts * sizeof(int) + (size_t)NW * G * 2 * sizeof(float) +
          (size_t)NW * G * kD * sizeof(float) + (2 + G) * kD * sizeof(float) +
          (size_t)(B + 1) * sizeof(int);
@@ -519,11 +570,12 @@ size_t smem_bytes(int B) {
 template <int G, bool R>
 __global__ void __maxnreg__(Cfg<G>::kMaxRegs) decode_splitkv_kernel(const Params p) {
   constexpr int NW = Cfg<G>::NW;
+  constexpr int KPW = Cfg<G>::kKeysPerWarp;
   constexpr int NC = Cfg<G>::kConsumers;
   extern __shared__ __align__(1024) uint8_t smem[];
   uint8_t* stages = smem;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kStages * 2 * kTileBytes);
-  int* misc = reinterpret_cast<int*>(bars + 2 * kStages);
+  int* misc = reinterpret_cast<int*>(bars + 2 * kStages + 2);  // after full, empty, csync, pad
   float* merge_ml = reinterpret_cast<float*>(misc + kMiscInts);  // [NW][G][2]
   float* merge_o = merge_ml + NW * G * 2;                         // [NW][G][kD]
   float* rope_cs = merge_o + NW * G * kD;                         // [2][kD] cos, sin
@@ -541,6 +593,7 @@ __global__ void __maxnreg__(Cfg<G>::kMaxRegs) decode_splitkv_kernel(const Params
       mbar_init(smem_u32(&bars[s]), 1);             // full: producer arrival + bytes
       mbar_init(smem_u32(&bars[kStages + s]), NW);  // empty: one arrival per consumer warp
     }
+    mbar_init(smem_u32(&bars[2 * kStages]), NW);    // consumer barrier
     misc[0] = 0;
     misc[1] = 0;
     fence_mbar_init();
@@ -626,13 +679,14 @@ __global__ void __maxnreg__(Cfg<G>::kMaxRegs) decode_splitkv_kernel(const Params
   // ------------------------------------------------------------ consumers --
   Consumer<G> cs;
   cs.init(lane);
+  ConsumerSync csync{smem_u32(&bars[2 * kStages]), abort_flag, p.status, 0u};
   Walk w;
   walk_init(w, t0, prefix, p.positions, B, Hkv);
   const uint16_t* qb = p.q + ((size_t)w.b * p.Hq + (size_t)w.kvh * G) * kD;
   if (R) {
     rope_segment<G, NC>(qb, rope_row<R>(p.rope_cos, w.b), rope_row<R>(p.rope_sin, w.b), q_rot,
                         rope_cs, tid);
-    consumer_bar<NC>();
+    consumer_bar<NC>();  // before any tile wait: every consumer warp gets here
     cs.load_q_rot(q_rot, p.qscale);
   } else {
     cs.load_q(qb, p.qscale);
@@ -643,20 +697,11 @@ __global__ void __maxnreg__(Cfg<G>::kMaxRegs) decode_splitkv_kernel(const Params
   for (long long t = t0; t < t1; ++t, ++i) {
     const int s = (int)(i % kStages);
     const uint32_t u = (uint32_t)(i / kStages);
-    if (!mbar_wait(smem_u32(&bars[s]), u & 1u, abort_flag)) {
-      *abort_flag = 1;
-      set_status(p.status, ATTN_DEV_TIMEOUT);
-      break;
-    }
+    if (!consumer_wait(smem_u32(&bars[s]), u & 1u, abort_flag, p.status, lane)) break;
     const int rows = min(kTile, w.n - w.k * kTile);
     uint8_t* Ks = stages + (size_t)s * 2 * kTileBytes;
-    if (p.k_new != nullptr && w.k == w.ntiles - 1) {
-      if (R) {
-        if (warp == 0) rope_fresh_key(Ks + (size_t)(rows - 1) * kRowBytes, rope_cs, lane);
-        consumer_bar<NC>();
-      }
-      if (warp == 0) write_fresh_rows(p, Ks, rows, w.b, w.kvh, w.n, lane);
-    }
+    if (p.k_new != nullptr && w.k == w.ntiles - 1 && warp == (rows - 1) / KPW)
+      fresh_row<R>(p, Ks, rows, w.b, w.kvh, w.n, rope_cs, lane);
     cs.tile(Ks, Ks + kTileBytes, rows, warp);
     __syncwarp();
     if (lane == 0) mbar_arrive(smem_u32(&bars[kStages + s]));
@@ -670,7 +715,7 @@ __global__ void __maxnreg__(Cfg<G>::kMaxRegs) decode_splitkv_kernel(const Params
       const bool whole = seg_t0 >= t0 && seg_t1 <= t1;
       const int ct = tid;
       cs.stash(merge_o, merge_ml, warp);
-      consumer_bar<NC>();
+      csync(lane);
 
       const int slot = blockIdx.x + seg;
       uint16_t* out_seg = p.out + ((size_t)w.b * p.Hq + (size_t)w.kvh * G) * kD;
@@ -691,7 +736,7 @@ __global__ void __maxnreg__(Cfg<G>::kMaxRegs) decode_splitkv_kernel(const Params
       if (!whole) {
         const int c_first = cta_of(seg_t0, T, Gd);
         const int c_last = cta_of(seg_t1 - 1, T, Gd);
-        consumer_bar<NC>();
+        csync(lane);
         if (ct == 0) {
           // release: this CTA's partial (ordered before by the barrier) is
           // visible to whoever acquires the counter; acquire: the last
@@ -703,7 +748,7 @@ __global__ void __maxnreg__(Cfg<G>::kMaxRegs) decode_splitkv_kernel(const Params
                        : "memory");
           misc[1] = (old == (unsigned)(c_last - c_first)) ? 1 : 0;
         }
-        consumer_bar<NC>();
+        csync(lane);
         if (misc[1]) {
           // last to arrive: merge the segment's partials.  Batches of 8
           // independent loads keep several L2 round trips in flight.
@@ -745,7 +790,7 @@ __global__ void __maxnreg__(Cfg<G>::kMaxRegs) decode_splitkv_kernel(const Params
           if (ct == 0) p.counters[seg] = 0u;  // ready for the next launch
         }
       }
-      consumer_bar<NC>();  // merge buffers are free again
+      csync(lane);  // merge buffers are free again
       cs.reset();
     }
     walk_next(w, prefix, p.positions, B, Hkv);
@@ -756,7 +801,7 @@ __global__ void __maxnreg__(Cfg<G>::kMaxRegs) decode_splitkv_kernel(const Params
       if (R) {
         rope_segment<G, NC>(qn, rope_row<R>(p.rope_cos, w.b), rope_row<R>(p.rope_sin, w.b),
                             q_rot, rope_cs, tid);
-        consumer_bar<NC>();
+        csync(lane);
         cs.load_q_rot(q_rot, p.qscale);
       } else {
         cs.load_q(qn, p.qscale);
@@ -776,7 +821,7 @@ __global__ void __maxnreg__(Cfg<G>::kMaxRegs) decode_splitkv_kernel(const Params
 template <int G>
 size_t cluster_smem_bytes() {
   constexpr int NW = Cfg<G>::NW;
-  return (size_t)kStages * 2 * kTileBytes + 2 * kStages * sizeof(uint64_t) +
+  return (size_t)kStages * 2 * kTileBytes + (2 * kStages + 2) * sizeof(uint64_t) +
          kMiscInts * sizeof(int) + (size_t)NW * G * 2 * sizeof(float) +
          (size_t)NW * G * kD * sizeof(float) + (2 + G) * kD * sizeof(float) +
          (size_t)G * (kD + 2) * sizeof(float);
@@ -787,11 +832,12 @@ size_t cluster_smem_bytes() {
 template <int G, bool R>
 __global__ void __maxnreg__(Cfg<G>::kMaxRegs) decode_cluster_kernel(const Params p) {
   constexpr int NW = Cfg<G>::NW;
+  constexpr int KPW = Cfg<G>::kKeysPerWarp;
   constexpr int NC = Cfg<G>::kConsumers;
   extern __shared__ __align__(1024) uint8_t smem[];
   uint8_t* stages = smem;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kStages * 2 * kTileBytes);
-  int* misc = reinterpret_cast<int*>(bars + 2 * kStages);
+  int* misc = reinterpret_cast<int*>(bars + 2 * kStages + 2);  // after full, empty, csync, pad
   float* merge_ml = reinterpret_cast<float*>(misc + kMiscInts);  // [NW][G][2]
   float* merge_o = merge_ml + NW * G * 2;                         // [NW][G][kD]
   float* rope_cs = merge_o + NW * G * kD;                         // [2][kD] cos, sin
@@ -814,6 +860,7 @@ __global__ void __maxnreg__(Cfg<G>::kMaxRegs) decode_cluster_kernel(const Params
       mbar_init(smem_u32(&bars[s]), 1);
       mbar_init(smem_u32(&bars[kStages + s]), NW);
     }
+    mbar_init(smem_u32(&bars[2 * kStages]), NW);
     misc[0] = 0;
     fence_mbar_init();
   }
@@ -854,11 +901,12 @@ __global__ void __maxnreg__(Cfg<G>::kMaxRegs) decode_cluster_kernel(const Params
     // ----------------------------------------------------------- consumers --
     Consumer<G> cs;
     cs.init(lane);
+    ConsumerSync csync{smem_u32(&bars[2 * kStages]), abort_flag, p.status, 0u};
     const uint16_t* qb = p.q + ((size_t)b * p.Hq + (size_t)kvh * G) * kD;
     if (R) {
       rope_segment<G, NC>(qb, rope_row<R>(p.rope_cos, b), rope_row<R>(p.rope_sin, b), q_rot,
                           rope_cs, tid);
-      consumer_bar<NC>();
+      consumer_bar<NC>();  // before any tile wait: every consumer warp gets here
       cs.load_q_rot(q_rot, p.qscale);
     } else {
       cs.load_q(qb, p.qscale);
@@ -867,27 +915,20 @@ __global__ void __maxnreg__(Cfg<G>::kMaxRegs) decode_cluster_kernel(const Params
     for (int k = k0; k < k1; ++k) {
       const int i = k - k0;
       const int s = i % kStages;
-      if (!mbar_wait(smem_u32(&bars[s]), (uint32_t)(i / kStages) & 1u, abort_flag)) {
-        *abort_flag = 1;
-        set_status(p.status, ATTN_DEV_TIMEOUT);
+      if (!consumer_wait(smem_u32(&bars[s]), (uint32_t)(i / kStages) & 1u, abort_flag, p.status,
+                         lane))
         break;
-      }
       const int rows = min(kTile, n - k * kTile);
       uint8_t* Ks = stages + (size_t)s * 2 * kTileBytes;
-      if (p.k_new != nullptr && k == ntiles - 1) {
-        if (R) {
-          if (warp == 0) rope_fresh_key(Ks + (size_t)(rows - 1) * kRowBytes, rope_cs, lane);
-          consumer_bar<NC>();
-        }
-        if (warp == 0) write_fresh_rows(p, Ks, rows, b, kvh, n, lane);
-      }
+      if (p.k_new != nullptr && k == ntiles - 1 && warp == (rows - 1) / KPW)
+        fresh_row<R>(p, Ks, rows, b, kvh, n, rope_cs, lane);
       cs.tile(Ks, Ks + kTileBytes, rows, warp);
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&bars[kStages + s]));
     }
     // this CTA's partial (max, sum, unnormalised o); no tiles: (-inf, 0, 0)
     cs.stash(merge_o, merge_ml, warp);
-    consumer_bar<NC>();
+    csync(lane);
     for (int idx = tid; idx < G * kD; idx += NC) {
       const int h = idx / kD, d = idx % kD;
       float M, Ls, Os;

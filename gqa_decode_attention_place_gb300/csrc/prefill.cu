@@ -226,6 +226,14 @@ __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, vol
   return false;
 }
 
+// The same for a whole warp that goes on to warp-collective TMEM loads and
+// stores (.sync.aligned): the outcome is made uniform over the warp, so
+// either every lane carries on or every lane stops.
+__device__ __forceinline__ bool warp_wait_or_abort(uint32_t bar, uint32_t parity,
+                                                   volatile int* abort_flag) {
+  return __all_sync(0xffffffffu, wait_or_abort(bar, parity, abort_flag));
+}
+
 __global__ void __launch_bounds__(kPThreads, 1)
     prefill_tcgen05_kernel(const __grid_constant__ CUtensorMap tm_q,
                            const __grid_constant__ CUtensorMap tm_k,
@@ -418,13 +426,13 @@ __global__ void __launch_bounds__(kPThreads, 1)
       const int nt = it.nt[x];
       float m_run = -INFINITY, l_run = 0.f;
       auto wait_pv = [&](int j) -> bool {  // PV_x of tile j of this item done
-        if (!wait_or_abort(bar(kBarPVDone + x), (cpv + j) & 1u, abort_flag)) return false;
+        if (!warp_wait_or_abort(bar(kBarPVDone + x), (cpv + j) & 1u, abort_flag)) return false;
         tc_fence_after();
         return true;
       };
 
       for (int i = 0; i < nt; ++i, ++cs) {
-        if (!wait_or_abort(bar(kBarSFull + x), cs & 1u, abort_flag)) { ok = false; break; }
+        if (!warp_wait_or_abort(bar(kBarSFull + x), cs & 1u, abort_flag)) { ok = false; break; }
         tc_fence_after();
         const int kbase = i * kBN;
         const bool diag = kbase + kBN - 1 > qpos;
@@ -461,9 +469,14 @@ __global__ void __launch_bounds__(kPThreads, 1)
 
         // PV of tile i-1 done: O is stable and P_x may be overwritten
         if (i > 0 && !wait_pv(i - 1)) { ok = false; break; }
-        if (mx > m_run + kLazyTau) {  // first tile, or the max grew by > 2^8
-          const float alpha = ex2(m_run - mx);
-          m_run = mx;
+        // Raise the running max on the first tile, or when it grew by more
+        // than 2^8.  The O rescale below uses warp-collective TMEM loads and
+        // stores, so the decision is taken for the whole warp: rows whose
+        // max did not grow keep it and scale by 1.
+        const bool grow = mx > m_run + kLazyTau;
+        if (__any_sync(0xffffffffu, grow)) {
+          const float alpha = grow ? ex2(m_run - mx) : 1.f;
+          m_run = grow ? mx : m_run;
           l_run *= alpha;
           if (i > 0) {
 #pragma unroll 1
