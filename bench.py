@@ -105,6 +105,155 @@ def cpu_worker(kind: str):
         raise ValueError(kind)
 
 
+# Per-config oracle timing: a bounded sample of every workload, on one thread
+# and on all host cores.  A sample is a list of "units" (decode: one
+# (sequence, query head) row; prefill: one (token, head) row), each with its
+# algorithmic bytes or flops; the full config's time is extrapolated from the
+# sample's rate.  Inputs are drawn with numpy (exact bf16 values are not
+# needed to time the oracle).
+
+CPU_CONFIGS = {
+    # name: (kind, shape, sample description)
+    "single_step": ("decode", dict(B=1, Hq=16, Hkv=8, pos=[100]), "the whole step, 20 times"),
+    "streaming_pos100": ("decode", dict(B=1, Hq=16, Hkv=8, pos=[100]), "one step at position 100, 20 times"),
+    "streaming_pos1000": ("decode", dict(B=1, Hq=16, Hkv=8, pos=[1000]), "one step at position 1000, 4 times"),
+    "streaming_pos4000": ("decode", dict(B=1, Hq=16, Hkv=8, pos=[4000]), "one step at position 4000"),
+    "streaming_pos8000": ("decode", dict(B=1, Hq=16, Hkv=8, pos=[8000]), "one step at position 8000"),
+    "ragged": ("decode", dict(B=64, Hq=32, Hkv=8, pos="ragged", sample_b=8),
+               "8 of the 64 sequences, all heads"),
+    "stress": ("decode", dict(B=256, Hq=64, Hkv=8, pos=[8191] * 256, sample_b=1),
+               "1 of the 256 sequences, all 64 heads"),
+    "prefill_prefix": ("prefill", dict(S=512, start_pos=2048, H=32, sample_rows=256),
+                       "256 (token, head) rows spread over the 512 x 32"),
+    "prefill": ("prefill", dict(S=2048, start_pos=0, H=32, sample_rows=256),
+                "256 (token, head) rows spread over the 2048 x 32"),
+}
+_CPU_REPEAT = {"single_step": 20, "streaming_pos100": 20, "streaming_pos1000": 4}
+
+
+def _cpu_units(name):
+    """(unit list, units of the full config, unit name) for a config: each
+    unit is (key, work) with key = (b, h) or (i, h)."""
+    import numpy as np
+    import oracle
+    kind, sh, _ = CPU_CONFIGS[name]
+    if kind == "decode":
+        B, Hq, Hkv = sh["B"], sh["Hq"], sh["Hkv"]
+        if sh["pos"] == "ragged":
+            pos = np.random.default_rng(1).integers(0, L, B).tolist()
+        else:
+            pos = list(sh["pos"])
+        bs = list(range(min(B, sh.get("sample_b", B))))
+        per_row = lambda b: oracle.decode_bytes([pos[b]], Hq, Hkv, D) / Hq
+        units = [((b, h), per_row(b)) for b in bs for h in range(Hq)]
+        return units, float(oracle.decode_bytes(pos, Hq, Hkv, D)), pos
+    S, sp, H = sh["S"], sh["start_pos"], sh["H"]
+    rows = np.random.default_rng(2).choice(S * H, sh["sample_rows"], replace=False)
+    units = [((int(r) // H, int(r) % H), 4.0 * 64 * (sp + int(r) // H + 1)) for r in sorted(rows)]
+    return units, float(oracle.prefill_flops(S, sp, H, 64)), None
+
+
+def _cpu_inputs(name, keys, pos):
+    """Inputs for the given unit keys only (float32 storage of bf16-like values)."""
+    import numpy as np
+    kind, sh, _ = CPU_CONFIGS[name]
+    rng = np.random.default_rng(sorted(CPU_CONFIGS).index(name) * 1000 + len(keys))
+    if kind == "decode":
+        Hq, Hkv = sh["Hq"], sh["Hkv"]
+        bs = sorted({b for b, _ in keys})
+        data = {}
+        for b in bs:
+            n = pos[b] + 1
+            data[b] = (rng.standard_normal((1, Hq, D)).astype(np.float32),
+                       rng.standard_normal((1, Hkv, n, D)).astype(np.float32),
+                       rng.standard_normal((1, Hkv, n, D)).astype(np.float32))
+        return data
+    S, sp, H = sh["S"], sh["start_pos"], sh["H"]
+    return (rng.standard_normal((S, H, 64)).astype(np.float32),
+            rng.standard_normal((sp + S, H, 64)).astype(np.float32),
+            rng.standard_normal((sp + S, H, 64)).astype(np.float32))
+
+
+def _cpu_run(name, keys, pos, data):
+    """The oracle on the given units; returns nothing (timed by the caller)."""
+    import oracle
+    kind, sh, _ = CPU_CONFIGS[name]
+    if kind == "decode":
+        by_b = {}
+        for b, h in keys:
+            by_b.setdefault(b, []).append(h)
+        for b, hs in by_b.items():
+            q, kc, vc = data[b]
+            oracle.decode_rows(q, kc, vc, [pos[b]], 1.0 / math.sqrt(D), [(0, h) for h in hs])
+    else:
+        q, k, v = data
+        oracle.prefill_rows(q, k, v, sh["start_pos"], 1.0 / 8.0, list(keys))
+
+
+_POOL_BARRIER = None
+
+
+def _pool_init(barrier):
+    global _POOL_BARRIER
+    _POOL_BARRIER = barrier
+
+
+def _pool_job(name, keys, pos, reps):
+    """One worker's share: build inputs, meet the others, time the oracle."""
+    data = _cpu_inputs(name, keys, pos)
+    _POOL_BARRIER.wait(timeout=300)
+    t0 = time.time()
+    for _ in range(reps):
+        _cpu_run(name, keys, pos, data)
+    return t0, time.time()
+
+
+def cpu_configs_worker():
+    """Every config's sample on 1 thread, then on all cores (spawn pool)."""
+    import multiprocessing as mp
+    ncpu = os.cpu_count() or 1
+    out = {"cores_available": ncpu, "configs": {}}
+    ctx = mp.get_context("spawn")
+    barrier = ctx.Barrier(ncpu)
+    with ctx.Pool(ncpu, initializer=_pool_init, initargs=(barrier,)) as pool:
+        for name in CPU_CONFIGS:
+            units, full, pos = _cpu_units(name)
+            keys = [k for k, _ in units]
+            work = sum(w for _, w in units)
+            reps = _CPU_REPEAT.get(name, 1)
+            data = _cpu_inputs(name, keys, pos)
+            t0 = time.perf_counter()
+            for _ in range(reps):
+                _cpu_run(name, keys, pos, data)
+            t1 = (time.perf_counter() - t0) / reps
+            del data
+            chunks = [keys[i::ncpu] for i in range(ncpu)]
+            spans = pool.starmap(_pool_job, [(name, c, pos, reps) for c in chunks])
+            tn = (max(e for _, e in spans) - min(s0 for s0, _ in spans)) / reps
+            kind = CPU_CONFIGS[name][0]
+            unit, scale = ("GB/s", 1e9) if kind == "decode" else ("GFLOP/s", 1e9)
+            out["configs"][name] = {
+                "sample": CPU_CONFIGS[name][2], "unit": unit,
+                "threads_1": {"value": round(work / t1 / scale, 4),
+                              "full_config_s": round(full / (work / t1), 4)},
+                f"threads_{ncpu}": {"value": round(work / tn / scale, 4),
+                                    "full_config_s": round(full / (work / tn), 4)},
+            }
+    print(json.dumps(out))
+
+
+def run_cpu_configs():
+    env = dict(os.environ)
+    for var in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+        env[var] = "1"
+    env["CUDA_VISIBLE_DEVICES"] = ""
+    r = subprocess.run([sys.executable, os.path.abspath(__file__), "--cpu-worker", "configs"],
+                       capture_output=True, text=True, env=env, timeout=900)
+    if r.returncode != 0:
+        return {"error": r.stderr[-400:]}
+    return json.loads(r.stdout.strip().splitlines()[-1])
+
+
 def run_cpu_baseline(kind="streaming"):
     env = dict(os.environ)
     for var in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
@@ -521,7 +670,7 @@ def run_ours(args):
         "e2e": {"value": round(ws * nbytes / (e2e * 1e-3) / 1e9, 2), "unit": "GB/s",
                 "ms_per_step": round(e2e, 3), "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
-        "roofline": {"kernel": "decode_splitkv_kernel<2> (append fused)", "bound": "hbm",
+        "roofline": {"kernel": "decode_cluster_kernel<2, false> (append fused; clusters of 12)", "bound": "hbm",
                      "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
                      "frac": round(achieved / hbm, 3), "traffic": TRAFFIC_BYTES_PER_LAUNCH,
                      "traffic_unit": "bytes per launch (ncu, cold cache)",
@@ -552,6 +701,7 @@ def run_ours(args):
         line["legs"] = legs
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = run_cpu_baseline("streaming")
+        line["cpu_baseline"]["per_config"] = run_cpu_configs()
     if rank == 0:
         print(json.dumps(line), flush=True)
     if ws > 1:
@@ -640,6 +790,9 @@ def main():
     args = _args()
     if args.only:
         run_only(args)
+        return
+    if args.cpu_worker == "configs":
+        cpu_configs_worker()
         return
     if args.cpu_worker:
         cpu_worker(args.cpu_worker)
