@@ -13,7 +13,8 @@ q and out) / device time of the step, in GB/s; `steps_per_s` is decode steps
 per second.  Extra legs: per-position decode time (warm and cold L2), the
 ragged B=64 batch, the B=256 g=8 stress batch, the ragged batch as a fused
 append step with and without the rotary embedding, and the causal prefill
-workloads (TFLOP/s), each against its roofline.  The cross-checks time the
+workloads (TFLOP/s; also GQA prompt chunks at d_head=128), each against its
+roofline.  The cross-checks time the
 same 8192 positions as separate append/decode launches, as decode launches
 alone, and as fused steps with the rotary embedding.
 
@@ -57,7 +58,7 @@ def _args():
     ap.add_argument("--only", type=str, default=None,
                     help="run one workload a few times and exit (for ncu captures): "
                          "streaming_sample, position:N, single_step, ragged, stress, prefill, "
-                         "prefill_prefix")
+                         "prefill_prefix, prefill_d128_chunk, prefill_d128")
     ap.add_argument("--reps", type=int, default=3, help="launches per --only run")
     ap.add_argument("--cpu-worker", type=str, default=None, help=argparse.SUPPRESS)
     return ap.parse_args()
@@ -554,7 +555,8 @@ def _prefill_leg(torch, ga, synth, name, flush, tflops_peak):
     fl = oracle.prefill_flops(S, case.start_pos, Hq, d)
     return {"us": round(ms * 1e3, 2), "TFLOPs": round(fl / (ms * 1e-3) / 1e12, 1),
             "frac_tensor": round(fl / (ms * 1e-3) / 1e12 / tflops_peak, 3), "flops": fl,
-            "shape": {"S": S, "start_pos": case.start_pos, "H": Hq, "d": d}}
+            "shape": {"S": S, "start_pos": case.start_pos, "Hq": Hq, "Hkv": case.k.shape[1],
+                      "d": d}}
 
 
 def run_ours(args):
@@ -696,7 +698,7 @@ def run_ours(args):
         legs["ragged_append"] = _append_leg(torch, ga, synth, "ragged", flush, hbm, rope=False)
         legs["ragged_rope_append"] = _append_leg(torch, ga, synth, "ragged", flush, hbm,
                                                  rope=True)
-        for name in ("prefill_prefix", "prefill"):
+        for name in ("prefill_prefix", "prefill", "prefill_d128_chunk", "prefill_d128"):
             legs[name] = _prefill_leg(torch, ga, synth, name, flush, tf_burst)
         line["legs"] = legs
     if rank == 0 and not args.no_cpu_baseline:

@@ -41,27 +41,40 @@ namespace {
 
 constexpr int kBM = 128;   // query rows per tile (MMA M)
 constexpr int kBN = 128;   // keys per tile (MMA N of QK^T, K of PV)
-constexpr int kHD = 64;    // head dim (MMA K of QK^T, N of PV)
-constexpr int kQT = 2;     // query tiles per CTA
-constexpr int kKVStages = 4;
+constexpr int kQT = 2;     // query-tile slots per CTA (softmax warpgroups)
+constexpr int kMaxKVStages = 4;
 constexpr int kPThreads = 320;             // 10 warps
-constexpr int kTileBytes = kBM * kHD * 2;  // 16 KB: a 128 x 64 bf16 tile
-constexpr uint32_t kTmemCols = 512;        // S: 2 x 128, P: 2 x 64, O: 2 x 64
+constexpr int kChunkBytes = kBM * 64 * 2;  // 16 KB: 128 rows x 128 bytes, one swizzle column block
+constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemP = 256;           // P of tile x at 256 + 64x (bf16 pairs)
-constexpr uint32_t kTmemO = 384;           // O of tile x at 384 + 64x
+constexpr uint32_t kTmemO = 384;           // O of tile x at 384 + HD*x
 constexpr float kLazyTau = 8.0f;           // keep a stale max up to 2^8 below
 
-// shared memory map (offsets from a 1024-byte aligned base)
-constexpr int kOffQ = 0;                                        // tile X at X * 16 KB
-constexpr int kOffKV = kOffQ + kQT * kTileBytes;                // stage s: K, then V
-constexpr int kOffBar = kOffKV + kKVStages * 2 * kTileBytes;
-constexpr int kSmemBytes = kOffBar + 256 + 1024;                // + alignment slack
+// Per head dim HD (64 or 128): a 128-row tile of HD bf16 is HD/64 column
+// blocks of 128 bytes (the 128-byte swizzle span), each 16 KB, one after the
+// other.  TMEM holds S (128 columns), P (64) and O (HD) per query tile: two
+// tiles for HD=64 (S 0..255, P 256..383, O 384..511), one for HD=128
+// (S 0..127, P 256..319, O 384..511).
+template <int HD>
+struct PL {
+  static constexpr int kChunks = HD / 64;
+  static constexpr int kTileBytes = kBM * HD * 2;
+  static constexpr int kQTiles = HD == 64 ? 2 : 1;  // query tiles an item may hold
+  static constexpr int kStages = HD == 64 ? 4 : 3;  // K/V ring depth
+  // shared memory map (offsets from a 1024-byte aligned base)
+  static constexpr int kOffQ = 0;                                   // query tile x
+  static constexpr int kOffKV = kOffQ + kQTiles * kTileBytes;       // stage s: K, then V
+  static constexpr int kOffBar = kOffKV + kStages * 2 * kTileBytes;
+  static constexpr int kSmemBytes = kOffBar + 256 + 1024;           // + alignment slack
+  static_assert(kSmemBytes <= 232448, "shared memory per CTA");
+  static_assert(kTmemO + kQTiles * HD <= kTmemCols, "tensor memory columns");
+};
 
 // barrier slots
 constexpr int kBarQ = 0;
 constexpr int kBarKVFull = 1;                     // + stage
-constexpr int kBarKVEmpty = kBarKVFull + kKVStages;
-constexpr int kBarSFull = kBarKVEmpty + kKVStages;  // + tile
+constexpr int kBarKVEmpty = kBarKVFull + kMaxKVStages;
+constexpr int kBarSFull = kBarKVEmpty + kMaxKVStages;  // + tile
 constexpr int kBarSFree = kBarSFull + kQT;
 constexpr int kBarPFull = kBarSFree + kQT;    // + tile
 constexpr int kBarPVDone = kBarPFull + kQT;   // + tile
@@ -234,6 +247,7 @@ __device__ __forceinline__ bool warp_wait_or_abort(uint32_t bar, uint32_t parity
   return __all_sync(0xffffffffu, wait_or_abort(bar, parity, abort_flag));
 }
 
+template <int HD>
 __global__ void __launch_bounds__(kPThreads, 1)
     prefill_tcgen05_kernel(const __grid_constant__ CUtensorMap tm_q,
                            const __grid_constant__ CUtensorMap tm_k,
@@ -242,7 +256,10 @@ __global__ void __launch_bounds__(kPThreads, 1)
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* smem = smem_raw + (base - raw);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
+  using L = PL<HD>;
+  constexpr int kKVStages = L::kStages;
+  constexpr int kTileBytes = L::kTileBytes;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kOffBar);
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + kNumBars);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
   auto bar = [&](int i) { return smem_u32(&bars[i]); };
@@ -305,7 +322,12 @@ __global__ void __launch_bounds__(kPThreads, 1)
   const uint32_t tmem = *tmem_holder;
   // TMEM columns: S of tile x [128x, +128); P of tile x [256+64x, +64);
   // O of tile x [384+64x, +64)
-  const uint32_t sQ = base + kOffQ;
+  const uint32_t sQ = base + L::kOffQ;
+  // one 128-row tile: its HD/64 column blocks, each at +16 KB
+  auto tma_tile = [&](uint32_t dst, const CUtensorMap* map, int head, int row, uint32_t b) {
+#pragma unroll
+    for (int c = 0; c < L::kChunks; ++c) tma_load_3d(dst + c * kChunkBytes, map, 64 * c, head, row, b);
+  };
 
   // Every mbarrier completes one phase per use; parities below come from
   // running counts kept across this CTA's items.
@@ -319,7 +341,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
         if (r > 0 && !wait_or_abort(bar(kBarQFree), (uint32_t)(r - 1) & 1u, abort_flag)) break;
         mbar_arrive_expect_tx(bar(kBarQ), p.tpi * kTileBytes);
         for (int x = 0; x < p.tpi; ++x)
-          tma_load_3d(sQ + x * kTileBytes, &tm_q, 0, it.h, it.q0 + x * kBM, bar(kBarQ));
+          tma_tile(sQ + x * kTileBytes, &tm_q, it.h, it.q0 + x * kBM, bar(kBarQ));
         bool ok = true;
         for (int i = 0; i < it.n; ++i, ++gk) {
           const int s = gk % kKVStages;
@@ -328,10 +350,10 @@ __global__ void __launch_bounds__(kPThreads, 1)
             ok = false;
             break;
           }
-          const uint32_t sK = base + kOffKV + s * 2 * kTileBytes;
+          const uint32_t sK = base + L::kOffKV + s * 2 * kTileBytes;
           mbar_arrive_expect_tx(bar(kBarKVFull + s), 2 * kTileBytes);
-          tma_load_3d(sK, &tm_k, 0, it.kvh, i * kBN, bar(kBarKVFull + s));
-          tma_load_3d(sK + kTileBytes, &tm_v, 0, it.kvh, i * kBN, bar(kBarKVFull + s));
+          tma_tile(sK, &tm_k, it.kvh, i * kBN, bar(kBarKVFull + s));
+          tma_tile(sK + kTileBytes, &tm_v, it.kvh, i * kBN, bar(kBarKVFull + s));
         }
         if (!ok) break;
       }
@@ -340,7 +362,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
     // ------------------------------------------------------- MMA issuer --
     if (lane == 0) {
       constexpr uint32_t idesc_qk = make_idesc(kBM, kBN, false);
-      constexpr uint32_t idesc_pv = make_idesc(kBM, kHD, true);
+      constexpr uint32_t idesc_pv = make_idesc(kBM, 64, true);  // one 64-column block of O
       uint32_t gk = 0;             // K/V tiles consumed so far
       uint32_t cs[kQT] = {0, 0};   // S_x issued so far
       uint32_t cp[kQT] = {0, 0};   // P_x consumed (PV_x issued) so far
@@ -355,11 +377,15 @@ __global__ void __launch_bounds__(kPThreads, 1)
           if (!wait_or_abort(bar(kBarPFull + x), cp[x] & 1u, abort_flag)) return false;
           tc_fence_after();
           const uint32_t sV =
-              base + kOffKV + ((gk0 + j) % kKVStages) * 2 * kTileBytes + kTileBytes;
+              base + L::kOffKV + ((gk0 + j) % kKVStages) * 2 * kTileBytes + kTileBytes;
+          // O columns [64c, 64c+64) from V's column block c
 #pragma unroll
-          for (int k = 0; k < kBN / 16; ++k)
-            tc_mma_ts(tmem + kTmemO + 64 * x, tmem + kTmemP + 64 * x + 8 * k,
-                      sw128_desc(sV + k * 16 * 128), idesc_pv, (j > 0 || k > 0) ? 1u : 0u);
+          for (int c = 0; c < L::kChunks; ++c)
+#pragma unroll
+            for (int k = 0; k < kBN / 16; ++k)
+              tc_mma_ts(tmem + kTmemO + HD * x + 64 * c, tmem + kTmemP + 64 * x + 8 * k,
+                        sw128_desc(sV + c * kChunkBytes + k * 16 * 128), idesc_pv,
+                        (j > 0 || k > 0) ? 1u : 0u);
           tc_commit(bar(kBarPVDone + x));
           ++cp[x];
           return true;
@@ -373,7 +399,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
             ok = false;
             break;
           }
-          const uint32_t sK = base + kOffKV + s * 2 * kTileBytes;
+          const uint32_t sK = base + L::kOffKV + s * 2 * kTileBytes;
           for (int x = 0; ok && x < kQT; ++x) {
             if (i >= it.nt[x]) continue;
             // the softmax has read the previous S_x
@@ -384,9 +410,11 @@ __global__ void __launch_bounds__(kPThreads, 1)
             }
             tc_fence_after();
 #pragma unroll
-            for (int k = 0; k < kHD / 16; ++k)
-              tc_mma(tmem + 128 * x, sw128_desc(sQ + x * kTileBytes + k * 32),
-                     sw128_desc(sK + k * 32), idesc_qk, k > 0);
+            for (int k = 0; k < HD / 16; ++k) {  // 4 K-steps per 128-byte column block
+              const uint32_t off = (k >> 2) * kChunkBytes + (k & 3) * 32;
+              tc_mma(tmem + 128 * x, sw128_desc(sQ + x * kTileBytes + off), sw128_desc(sK + off),
+                     idesc_qk, k > 0);
+            }
             tc_commit(bar(kBarSFull + x));
             ++cs[x];
           }
@@ -412,7 +440,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
     const int r = sub * 32 + lane;                      // row within the tile
     const uint32_t lane_off = (uint32_t)(sub * 32) << 16;
     const uint32_t tm_S = tmem + 128 * x + lane_off;
-    const uint32_t tm_O = tmem + kTmemO + 64 * x + lane_off;
+    const uint32_t tm_O = tmem + kTmemO + HD * x + lane_off;
     const uint32_t tm_P = tmem + kTmemP + 64 * x + lane_off;
     const float c = p.scale_log2;
     uint32_t cs = 0;   // S_x consumed so far
@@ -480,7 +508,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
           l_run *= alpha;
           if (i > 0) {
 #pragma unroll 1
-            for (int cc = 0; cc < kHD / 16; ++cc) {
+            for (int cc = 0; cc < HD / 16; ++cc) {
               float o[16];
               tmem_ld16(tm_O + cc * 16, o);
               tmem_ld_wait();
@@ -527,9 +555,9 @@ __global__ void __launch_bounds__(kPThreads, 1)
       if (ok && nt > 0) {
         ok = wait_pv(nt - 1);
         const float inv = ok ? 1.f / l_run : __int_as_float(0x7fc00000);
-        uint4* dst = reinterpret_cast<uint4*>(p.out + ((size_t)row * p.Hq + it.h) * kHD);
+        uint4* dst = reinterpret_cast<uint4*>(p.out + ((size_t)row * p.Hq + it.h) * HD);
 #pragma unroll
-        for (int cc = 0; cc < kHD / 32; ++cc) {
+        for (int cc = 0; cc < HD / 32; ++cc) {
           float o[32];
           tmem_ld32(tm_O + cc * 32, o);
           tmem_ld_wait();
@@ -589,13 +617,14 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// [tokens, heads, 64] bf16 viewed as 3-D (64, heads, tokens); box 64 x 1 x 128.
-bool make_map(CUtensorMap* m, const void* ptr, int tokens, int heads) {
+// [tokens, heads, hd] bf16 viewed as 3-D (hd, heads, tokens); box 64 x 1 x 128
+// (one 128-byte column block of a tile; hd = 128 takes two boxes).
+bool make_map(CUtensorMap* m, const void* ptr, int tokens, int heads, int hd) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return false;
-  cuuint64_t dims[3] = {(cuuint64_t)kHD, (cuuint64_t)heads, (cuuint64_t)tokens};
-  cuuint64_t strides[2] = {(cuuint64_t)kHD * 2, (cuuint64_t)heads * kHD * 2};
-  cuuint32_t box[3] = {(cuuint32_t)kHD, 1, (cuuint32_t)kBM};
+  cuuint64_t dims[3] = {(cuuint64_t)hd, (cuuint64_t)heads, (cuuint64_t)tokens};
+  cuuint64_t strides[2] = {(cuuint64_t)hd * 2, (cuuint64_t)heads * hd * 2};
+  cuuint32_t box[3] = {64, 1, (cuuint32_t)kBM};
   cuuint32_t estr[3] = {1, 1, 1};
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box,
              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -605,26 +634,51 @@ bool make_map(CUtensorMap* m, const void* ptr, int tokens, int heads) {
 }  // namespace
 
 bool prefill_supported(int Hq, int Hkv, int d) {
-  return d == kHD && Hq >= 1 && Hkv >= 1 && Hq % Hkv == 0 && Hq <= 65535;
+  return (d == 64 || d == 128) && Hq >= 1 && Hkv >= 1 && Hq % Hkv == 0 && Hq <= 65535;
 }
 
-cudaError_t launch_prefill(const void* q, const void* k, const void* v, int S, int start_pos,
-                           int Hq, int Hkv, int d, float scale, void* out,
-                           cudaStream_t stream) {
-  (void)d;
-  const int T = start_pos + S;
-  CUtensorMap mq, mk, mv;
-  if (!make_map(&mq, q, S, Hq) || !make_map(&mk, k, T, Hkv) || !make_map(&mv, v, T, Hkv))
-    return cudaErrorInvalidValue;
+namespace {
+
+template <int HD>
+cudaError_t launch_prefill_hd(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
+                              PrefillParams p, cudaStream_t stream) {
+  using L = PL<HD>;
   static bool configured[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev >= 0 && dev < 64 && !configured[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(prefill_tcgen05_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    cudaError_t e = cudaFuncSetAttribute(prefill_tcgen05_kernel<HD>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         L::kSmemBytes);
     if (e != cudaSuccess) return e;
     configured[dev] = true;
   }
+  int sms = 0;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
+    sms = 148;
+  // Two query tiles per item share each K/V tile and keep both softmax
+  // warpgroups busy; when that leaves SMs idle, or tensor memory holds only
+  // one tile's O (HD = 128), one tile per item instead.
+  const long long n_qt = (p.S + kBM - 1) / kBM;
+  p.tpi = (L::kQTiles == 1 || (n_qt + 1) / 2 * (long long)p.Hq < sms) ? 1 : kQT;
+  p.n_units = (int)((n_qt + p.tpi - 1) / p.tpi);
+  const long long items = (long long)p.n_units * p.Hq;
+  if (items > 0x7fffffffLL) return cudaErrorInvalidValue;
+  const unsigned blocks = (unsigned)std::min<long long>(items, sms);  // one CTA per SM
+  prefill_tcgen05_kernel<HD><<<blocks, kPThreads, L::kSmemBytes, stream>>>(mq, mk, mv, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_prefill(const void* q, const void* k, const void* v, int S, int start_pos,
+                           int Hq, int Hkv, int d, float scale, void* out,
+                           cudaStream_t stream) {
+  const int T = start_pos + S;
+  CUtensorMap mq, mk, mv;
+  if (!make_map(&mq, q, S, Hq, d) || !make_map(&mk, k, T, Hkv, d) ||
+      !make_map(&mv, v, T, Hkv, d))
+    return cudaErrorInvalidValue;
   PrefillParams p;
   p.out = static_cast<uint16_t*>(out);
   p.S = S;
@@ -633,19 +687,10 @@ cudaError_t launch_prefill(const void* q, const void* k, const void* v, int S, i
   p.Hkv = Hkv;
   p.g = Hq / Hkv;
   p.scale_log2 = scale * 1.4426950408889634f;
-  int sms = 0;
-  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
-    sms = 148;
-  // Two query tiles per item share each K/V tile and keep both softmax
-  // warpgroups busy; when that leaves SMs idle, one tile per item instead.
-  const long long n_qt = (S + kBM - 1) / kBM;
-  p.tpi = ((n_qt + 1) / 2 * (long long)Hq < sms) ? 1 : kQT;
-  p.n_units = (int)((n_qt + p.tpi - 1) / p.tpi);
-  const long long items = (long long)p.n_units * Hq;
-  if (items > 0x7fffffffLL) return cudaErrorInvalidValue;
-  const unsigned blocks = (unsigned)std::min<long long>(items, sms);  // one CTA per SM
-  prefill_tcgen05_kernel<<<blocks, kPThreads, kSmemBytes, stream>>>(mq, mk, mv, p);
-  return cudaGetLastError();
+  p.tpi = 1;
+  p.n_units = 0;
+  return d == 128 ? launch_prefill_hd<128>(mq, mk, mv, p, stream)
+                  : launch_prefill_hd<64>(mq, mk, mv, p, stream);
 }
 
 }  // namespace gqa

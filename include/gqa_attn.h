@@ -209,7 +209,7 @@ int attn_decode_step_noalloc(const void* q, const int32_t* positions,
  *   k, v      : [start_pos + S, Hkv, d] bf16, cached prefix rows first.
  *   out       : [S, Hq, d] bf16 (= [S, Hq*d]).
  *
- * Supported: d == 64; g = Hq / Hkv >= 1; S >= 0 (S == 0 does nothing);
+ * Supported: d == 64 or d == 128; g = Hq / Hkv >= 1; S >= 0 (S == 0 does nothing);
  * start_pos >= 0; start_pos + S < 2^31.  QK^T and PV run on the tcgen05
  * tensor cores (bf16 operands, fp32 accumulation in tensor memory).
  */

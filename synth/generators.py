@@ -38,6 +38,11 @@ WORKLOADS = {
                            Hkv=32, d=64),
     # causal prefill from scratch, 2048 tokens
     "prefill": dict(kind="prefill", S=2048, start_pos=0, Hq=32, Hkv=32, d=64),
+    # prompt chunks at the decode shapes (GQA, D=128): 512 tokens over a
+    # 2048-token cache, and 2048 tokens from scratch
+    "prefill_d128_chunk": dict(kind="prefill", S=512, start_pos=2048, Hq=32,
+                               Hkv=8, d=128),
+    "prefill_d128": dict(kind="prefill", S=2048, start_pos=0, Hq=32, Hkv=8, d=128),
     # B=256, g=8, every sequence at the last position, 1% of key rows x8
     "stress": dict(kind="decode", B=256, Hq=64, Hkv=8, D=128, L=8192,
                    positions="fixed:8191", fill="all", peaky=0.01),

@@ -3,7 +3,9 @@
 Covers both prefill workloads (512 new tokens over a 2048-token prefix; 2048
 tokens from scratch; 32 heads of d=64), query tiles and prefixes that are not
 multiples of the 128-row tile, a single new token, GQA head sharing and the
-empty problem.
+empty problem; and the same kernel at d_head=128 (small cases against the
+full oracle, a 512-token GQA prompt chunk at the decode shapes, and one new
+token through both the prefill and the decode kernel).
 """
 
 import numpy as np
@@ -92,3 +94,52 @@ def test_prefill_matches_decode_path():
     out = _run(case)
     want = oracle.prefill(f64(case.q), f64(case.k), f64(case.v), start_pos, case.scale)
     assert_attn_close(f64(out), want, "S=1 prefill")
+
+
+# ------------------------------------------------------------- d_head = 128 ---
+# The decode model's head size: prompt chunks of a GQA model with D=128 go
+# through the same kernel, each 128-wide row as two 128-byte column blocks.
+
+@pytest.mark.parametrize("S,start_pos,Hq,Hkv", [
+    (128, 0, 1, 1),      # one tile, no prefix
+    (1, 0, 2, 2),        # a single token
+    (129, 0, 2, 1),      # tile + 1 row, GQA g=2
+    (300, 37, 4, 4),     # prefix not tile aligned
+    (1, 500, 4, 2),      # one new token over a prefix (== a decode step)
+    (200, 127, 16, 8),   # the decode shapes' g=2, prefix one short of a tile
+    (64, 129, 8, 1),     # g=8
+])
+def test_d128_small_cases_full_oracle(S, start_pos, Hq, Hkv):
+    case = synth.prefill_case(S=S, start_pos=start_pos, Hq=Hq, Hkv=Hkv, d=128,
+                              seed=1000 + S + start_pos, device="cuda")
+    _full_check(case, f"d=128 S={S} start_pos={start_pos} Hq={Hq} Hkv={Hkv}")
+
+
+def test_d128_gqa_prompt_chunk():
+    """A 512-token prompt chunk over a 2048-token cache at the decode shapes
+    (Hq=32, Hkv=8, D=128), sampled rows against the oracle."""
+    case = synth.prefill_case(S=512, start_pos=2048, Hq=32, Hkv=8, d=128, seed=77,
+                              device="cuda")
+    rng = np.random.default_rng(77)
+    rows = [(int(i), int(h)) for i, h in zip(rng.integers(0, 512, 400), rng.integers(0, 32, 400))]
+    rows += [(i, 9) for i in range(0, 512, 5)] + [(0, h) for h in range(32)]
+    rows += [(511, h) for h in range(32)] + [(127, 3), (128, 3)]
+    _sampled_check(case, rows, "d=128 prompt chunk")
+
+
+def test_d128_first_token_is_v0_and_one_token_equals_decode():
+    case = synth.prefill_case(S=3, start_pos=0, Hq=4, Hkv=2, d=128, seed=78, device="cuda")
+    out = _run(case)
+    assert torch.equal(out[0, 0].view(torch.int16), case.v[0, 0].view(torch.int16))
+    assert torch.equal(out[0, 3].view(torch.int16), case.v[0, 1].view(torch.int16))
+    # one new token over a 700-token prefix through prefill and through decode
+    pc = synth.prefill_case(S=1, start_pos=700, Hq=16, Hkv=8, d=128, seed=79, device="cuda")
+    pout = _run(pc)
+    kc = pc.k.permute(1, 0, 2).unsqueeze(0).contiguous()  # [1, Hkv, 701, D]
+    vc = pc.v.permute(1, 0, 2).unsqueeze(0).contiguous()
+    pos = torch.tensor([700], dtype=torch.int32, device="cuda")
+    dout = ga.attn_decode_step(pc.q, pos, kc, vc, pc.scale)
+    torch.cuda.synchronize()
+    want = oracle.prefill(f64(pc.q), f64(pc.k), f64(pc.v), 700, pc.scale)
+    assert_attn_close(f64(pout), want, "d=128 one token (prefill)")
+    assert_attn_close(f64(dout), want, "d=128 one token (decode)")
