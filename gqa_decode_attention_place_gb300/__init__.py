@@ -22,7 +22,7 @@ __all__ = [
     "attn_kv_append", "attn_decode_workspace_size", "attn_decode_step",
     "attn_prefill_causal", "attn_read_device_status", "attn_status_string",
     "attn_last_cuda_error", "decode_workspace", "attn_decode_step_noalloc",
-    "attn_decode_step_append", "attn_decode_step_rope_append",
+    "attn_decode_step_append", "attn_decode_step_rope_append", "attn_decode_stream_step",
 ]
 
 ATTN_OK = 0
@@ -68,6 +68,9 @@ def load_library(build_if_missing: bool = True) -> ctypes.CDLL:
     lib.attn_decode_step_rope_append.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32,
                                                  i32, i32, f32, vp, vp, sz, vp]
     lib.attn_decode_step_rope_append.restype = i32
+    lib.attn_decode_stream_step.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32,
+                                            i32, f32, vp, vp, sz, vp]
+    lib.attn_decode_stream_step.restype = i32
     lib.attn_decode_step_noalloc.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, i32, f32, vp, vp]
     lib.attn_decode_step_noalloc.restype = i32
     lib.attn_prefill_causal.argtypes = [vp, vp, vp, i32, i32, i32, i32, i32, f32, vp, vp]
@@ -199,7 +202,7 @@ def _decode_append(name, q, k_new, v_new, rope, positions, k_cache, v_cache, sca
     lib = load_library()
     head = (q.data_ptr(), k_new.data_ptr(), v_new.data_ptr())
     if rope is not None:
-        head += (rope[0].data_ptr(), rope[1].data_ptr())
+        head += tuple(t.data_ptr() if t is not None else None for t in rope)
     code = getattr(lib, name)(
         *head, positions.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), B, Hq, Hkv, L, D,
         float(scale), out.data_ptr(), workspace.data_ptr(),
@@ -229,6 +232,25 @@ def attn_decode_step_rope_append(q, k_new, v_new, cos, sin, positions, k_cache, 
         raise ValueError("attn_decode_step_rope_append: cos and sin must be [B, D]")
     return _decode_append("attn_decode_step_rope_append", q, k_new, v_new, (cos, sin), positions,
                           k_cache, v_cache, scale, out, workspace, stream)
+
+
+def attn_decode_stream_step(q, k_new, v_new, positions, k_cache, v_cache, scale: float,
+                            cos_table=None, sin_table=None, out=None, workspace=None,
+                            stream=None) -> torch.Tensor:
+    """One streaming step that a CUDA graph can replay unchanged: the fused
+    append + decode (after the rotary embedding when ``cos_table``/``sin_table``,
+    [L, D] float32 indexed by position, are given), then ``positions += 1`` on
+    the device."""
+    if (cos_table is None) != (sin_table is None):
+        raise ValueError("attn_decode_stream_step: give both cos_table and sin_table, or neither")
+    if cos_table is not None:
+        L, D = k_cache.shape[2], q.shape[2]
+        for t, n in ((cos_table, "cos_table"), (sin_table, "sin_table")):
+            _check(t, n, torch.float32, 2)
+            if tuple(t.shape) != (L, D):
+                raise ValueError(f"attn_decode_stream_step: {n} must be [L, D]")
+    return _decode_append("attn_decode_stream_step", q, k_new, v_new, (cos_table, sin_table),
+                          positions, k_cache, v_cache, scale, out, workspace, stream)
 
 
 def attn_decode_step_noalloc(q, positions, k_cache, v_cache, scale: float, out=None,

@@ -58,16 +58,18 @@ int attn_decode_step(const void* q, const int32_t* positions, const void* k_cach
   if (!workspace || !aligned16(workspace) ||
       workspace_bytes < gqa::decode_workspace_layout(B, Hq, Hkv, D).total)
     return ATTN_ERR_WORKSPACE;
-  return cuda_status(gqa::launch_decode(q, nullptr, nullptr, nullptr, nullptr, positions, k_cache,
-                                        v_cache, B, Hq, Hkv, L, D, scale, out, workspace, stream));
+  return cuda_status(gqa::launch_decode(q, nullptr, nullptr, nullptr, nullptr, false, positions,
+                                        nullptr, k_cache, v_cache, B, Hq, Hkv, L, D, scale, out,
+                                        workspace, stream));
 }
 
 namespace {
 
 int decode_append(const void* q, const void* k_new, const void* v_new, const float* rope_cos,
-                  const float* rope_sin, const int32_t* positions, void* k_cache, void* v_cache,
-                  int B, int Hq, int Hkv, int L, int D, float scale, void* out, void* workspace,
-                  size_t workspace_bytes, cudaStream_t stream) {
+                  const float* rope_sin, bool rope_by_pos, const int32_t* positions,
+                  int32_t* advance, void* k_cache, void* v_cache, int B, int Hq, int Hkv, int L,
+                  int D, float scale, void* out, void* workspace, size_t workspace_bytes,
+                  cudaStream_t stream) {
   if (!q || !k_new || !v_new || !positions || !k_cache || !v_cache || !out)
     return ATTN_ERR_INVALID_ARG;
   if (B <= 0 || Hq <= 0 || Hkv <= 0 || L <= 0 || D <= 0 || Hq % Hkv != 0)
@@ -79,8 +81,9 @@ int decode_append(const void* q, const void* k_new, const void* v_new, const flo
   if (!workspace || !aligned16(workspace) ||
       workspace_bytes < gqa::decode_workspace_layout(B, Hq, Hkv, D).total)
     return ATTN_ERR_WORKSPACE;
-  return cuda_status(gqa::launch_decode(q, k_new, v_new, rope_cos, rope_sin, positions, k_cache,
-                                        v_cache, B, Hq, Hkv, L, D, scale, out, workspace, stream));
+  return cuda_status(gqa::launch_decode(q, k_new, v_new, rope_cos, rope_sin, rope_by_pos,
+                                        positions, advance, k_cache, v_cache, B, Hq, Hkv, L, D,
+                                        scale, out, workspace, stream));
 }
 
 }  // namespace
@@ -89,8 +92,8 @@ int attn_decode_step_append(const void* q, const void* k_new, const void* v_new,
                             const int32_t* positions, void* k_cache, void* v_cache, int B,
                             int Hq, int Hkv, int L, int D, float scale, void* out,
                             void* workspace, size_t workspace_bytes, cudaStream_t stream) {
-  return decode_append(q, k_new, v_new, nullptr, nullptr, positions, k_cache, v_cache, B, Hq, Hkv,
-                       L, D, scale, out, workspace, workspace_bytes, stream);
+  return decode_append(q, k_new, v_new, nullptr, nullptr, false, positions, nullptr, k_cache,
+                       v_cache, B, Hq, Hkv, L, D, scale, out, workspace, workspace_bytes, stream);
 }
 
 int attn_decode_step_rope_append(const void* q, const void* k_new, const void* v_new,
@@ -99,8 +102,19 @@ int attn_decode_step_rope_append(const void* q, const void* k_new, const void* v
                                  int D, float scale, void* out, void* workspace,
                                  size_t workspace_bytes, cudaStream_t stream) {
   if (!cos || !sin || !aligned16(cos) || !aligned16(sin)) return ATTN_ERR_INVALID_ARG;
-  return decode_append(q, k_new, v_new, cos, sin, positions, k_cache, v_cache, B, Hq, Hkv, L, D,
-                       scale, out, workspace, workspace_bytes, stream);
+  return decode_append(q, k_new, v_new, cos, sin, false, positions, nullptr, k_cache, v_cache, B,
+                       Hq, Hkv, L, D, scale, out, workspace, workspace_bytes, stream);
+}
+
+int attn_decode_stream_step(const void* q, const void* k_new, const void* v_new,
+                            const float* cos_table, const float* sin_table, int32_t* positions,
+                            void* k_cache, void* v_cache, int B, int Hq, int Hkv, int L, int D,
+                            float scale, void* out, void* workspace, size_t workspace_bytes,
+                            cudaStream_t stream) {
+  if ((cos_table == nullptr) != (sin_table == nullptr)) return ATTN_ERR_INVALID_ARG;
+  if (cos_table && (!aligned16(cos_table) || !aligned16(sin_table))) return ATTN_ERR_INVALID_ARG;
+  return decode_append(q, k_new, v_new, cos_table, sin_table, true, positions, positions, k_cache,
+                       v_cache, B, Hq, Hkv, L, D, scale, out, workspace, workspace_bytes, stream);
 }
 
 int attn_decode_step_noalloc(const void* q, const int32_t* positions, const void* k_cache,

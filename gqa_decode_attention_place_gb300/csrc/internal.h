@@ -14,19 +14,23 @@ cudaError_t launch_kv_append(const void* k_new, const void* v_new, const int32_t
 
 // Decode workspace layout (bytes), shared by the size query and the launcher.
 struct DecodeWorkspace {
-  size_t status_off, counters_off, ml_off, o_off, total;
+  size_t status_off, ticket_off, counters_off, ml_off, o_off, total;
   int slots;
 };
 DecodeWorkspace decode_workspace_layout(int B, int Hq, int Hkv, int D);
 
 // k_new/v_new null: attention only.  Non-null: the rows are appended at
 // positions[b] inside the same launch (kv append fused into decode).
-// rope_cos/rope_sin ([B, D] fp32, only with k_new) non-null: q and the new
-// key row are first rotated by the rotary embedding given by those rows.
+// rope_cos/rope_sin (fp32, only with k_new) non-null: q and the new key row
+// are first rotated by the rotary embedding: row b of [B, D] tables, or
+// (rope_by_pos) row positions[b] of [L, D] tables.  advance non-null (the
+// positions array itself): every position is incremented once the step has
+// read them all.
 cudaError_t launch_decode(const void* q, const void* k_new, const void* v_new,
-                          const float* rope_cos, const float* rope_sin, const int32_t* positions,
-                          const void* k_cache, const void* v_cache, int B, int Hq, int Hkv, int L,
-                          int D, float scale, void* out, void* workspace, cudaStream_t stream);
+                          const float* rope_cos, const float* rope_sin, bool rope_by_pos,
+                          const int32_t* positions, int32_t* advance, const void* k_cache,
+                          const void* v_cache, int B, int Hq, int Hkv, int L, int D, float scale,
+                          void* out, void* workspace, cudaStream_t stream);
 
 // Allocation-free decode: scratch in a fixed device array (decode.cu).
 size_t noalloc_scratch_bytes();

@@ -172,6 +172,38 @@ int attn_decode_step_rope_append(const void* q, const void* k_new, const void* v
                                  cudaStream_t stream);
 
 /*
+ * attn_decode_stream_step -- one step of a streaming decode loop that a CUDA
+ * graph can capture once and replay unchanged.  It performs the fused step of
+ * attn_decode_step_append (preceded by the rotary embedding of
+ * attn_decode_step_rope_append when tables are given), then adds one to every
+ * positions[b] on the device.  The decode page calls forward_step once per
+ * new token at position_id, the next one at position_id + 1 (section 4.1);
+ * keeping that counter on the device lets one captured launch serve every
+ * step of the loop.
+ *
+ *   positions : [B] int32, device memory.  It is read as this step's positions,
+ *               then every entry is incremented by one, out-of-range ones
+ *               included.  The increment happens after every part of the
+ *               launch has read them, so the result is the same as a step at
+ *               the old positions followed by a host-side increment.
+ *   cos_table,
+ *   sin_table : [L, D] fp32, device memory, 16-byte aligned, or both null for
+ *               no rotation.  Row p is the rotation at position p; the step
+ *               uses row positions[b] for sequence b.  Read only.
+ *   all other arguments, sizes and errors: as attn_decode_step_append.  The
+ *   step uses a counter in the workspace and leaves it at zero again.
+ *
+ * Errors: ATTN_ERR_INVALID_ARG also when exactly one of cos_table and
+ * sin_table is null, or either is misaligned.
+ */
+int attn_decode_stream_step(const void* q, const void* k_new, const void* v_new,
+                            const float* cos_table, const float* sin_table,
+                            int32_t* positions, void* k_cache, void* v_cache,
+                            int B, int Hq, int Hkv, int L, int D, float scale,
+                            void* out, void* workspace, size_t workspace_bytes,
+                            cudaStream_t stream);
+
+/*
  * attn_decode_step_noalloc -- attn_decode_step without a workspace argument.
  * The decode page has no counterpart: this entry point exists for callers
  * that cannot call cudaMalloc, for example code running while a CUDA graph is

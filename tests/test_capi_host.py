@@ -38,7 +38,8 @@ def test_header_declares_the_boundary():
     for want in ["attn_kv_append", "attn_decode_workspace_size", "attn_decode_step",
                  "attn_prefill_causal", "attn_read_device_status", "attn_status_string",
                  "attn_last_cuda_error", "attn_decode_step_append",
-                 "attn_decode_step_rope_append", "attn_decode_step_noalloc"]:
+                 "attn_decode_step_rope_append", "attn_decode_step_noalloc",
+                 "attn_decode_stream_step"]:
         assert want in names
 
 
@@ -100,6 +101,15 @@ def test_host_validation_happens_before_any_launch(lib):
     assert rope(P, None, P, P, P, P, P, P, 1, 16, 8, 16, 128, 1.0, P, P, 1 << 20, None) == 1
     assert rope(P, P, P, P, P, P, P, P, 1, 32, 2, 16, 128, 1.0, P, P, 1 << 20, None) == 2
     assert rope(P, P, P, P, P, P, P, P, 1, 16, 8, 16, 128, 1.0, P, P, need - 1, None) == 3
+    # streaming step: tables both or neither, aligned; then the append step's checks
+    stream = lib.attn_decode_stream_step
+    assert stream(P, P, P, P, None, P, P, P, 1, 16, 8, 16, 128, 1.0, P, P, 1 << 20, None) == 1
+    assert stream(P, P, P, P + 8, P, P, P, P, 1, 16, 8, 16, 128, 1.0, P, P, 1 << 20, None) == 1
+    assert stream(P, P, P, None, None, None, P, P, 1, 16, 8, 16, 128, 1.0, P, P, 1 << 20,
+                  None) == 1
+    assert stream(P, P, P, None, None, P, P, P, 1, 16, 8, 16, 96, 1.0, P, P, 1 << 20, None) == 2
+    assert stream(P, P, P, None, None, P, P, P, 1, 16, 8, 16, 128, 1.0, P, None, need,
+                  None) == 3
 
 
 def test_binding_rejects_cpu_tensors():
