@@ -18,10 +18,13 @@
 //
 // How (GB300 design, not the page's: the page calls PyTorch SDPA):
 //  * The attended rows of every (sequence, KV head) pair -- a "segment" -- are
-//    cut into 128-row tiles.  One producer thread streams K and V tiles with
-//    1-D bulk copies (TMA) into a 2-stage shared-memory ring guarded by
-//    mbarriers (128 KB in flight per SM).  Each tile is read from HBM once
-//    and serves all g query heads of its KV head.
+//    cut into 128-row tiles, streamed with 1-D bulk copies (TMA) into a
+//    2-stage shared-memory ring guarded by mbarriers (128 KB in flight per
+//    SM) by a producer warp (one thread).  For g = 8 there is no producer
+//    warp: one thread issues the first two tiles and the last consumer warp
+//    to finish with a stage refills it, so a CTA is 256 threads that may use
+//    248 registers each.  Each tile is read from HBM once and serves all g
+//    query heads of its KV head.
 //  * 8 consumer warps (16 for g=1) each take 16 (8) keys of a tile; a key's
 //    128 dims are spread over 16 lanes, 8 each, as fp32 pairs for the packed
 //    fma.rn.f32x2.  q.k partial sums of the g heads are reduced across the
@@ -78,7 +81,12 @@ using Params = DecodeParams;
 template <int G> struct Cfg {
   static constexpr int LPK = 16;
   static constexpr int NW = (G == 1) ? 16 : 8;
-  static constexpr int kThreads = (NW + 1) * 32;   // + one producer warp
+  // A producer warp streams the tiles for g <= 4.  For g = 8 the registers
+  // are worth more: with it, a CTA of 288 threads may use 168 registers a
+  // thread and the key loop spilled; without it, 256 threads get 248, and the
+  // last consumer warp to finish with a stage refills it (last_to_release).
+  static constexpr bool kProducer = G < 8;
+  static constexpr int kThreads = (NW + (kProducer ? 1 : 0)) * 32;
   static constexpr int kConsumers = NW * 32;
   static constexpr int kKeysPerWarp = kTile / NW;  // 16 or 8
   static constexpr int kKeysPerStep = 32 / LPK;    // 2
@@ -86,7 +94,8 @@ template <int G> struct Cfg {
   // registers per thread that still let one CTA of kThreads fit the SM
   // (the register file is handed out as if the block were a multiple of
   // 128 threads)
-  static constexpr int kMaxRegs = (65536 / ((kThreads + 127) / 128 * 128)) & ~7;
+  static constexpr int kRegsFit = 65536 / ((kThreads + 127) / 128 * 128);
+  static constexpr int kMaxRegs = (kRegsFit > 255 ? 255 : kRegsFit) & ~7;
 };
 
 // A named barrier among the consumers, only for the one place every consumer
@@ -451,6 +460,24 @@ __device__ __forceinline__ void produce_tile(const Params& p, uint8_t* stages, u
   }
 }
 
+// A consumer warp's release of pipeline stage s once it is done with the
+// stage's tile (lane 0, after the warp synced).  The counter rel[s] picks
+// the last of the NW warps; that one rearms the counter and returns true, and
+// the caller refills the stage with the tile kStages ahead.  The acquire
+// orders every other warp's reads of the stage before the refill's bulk
+// copies, so no producer warp has to wait on the stage.
+__device__ __forceinline__ bool last_to_release(int* rel, int s, int nw) {
+  int old;
+  asm volatile("atom.acq_rel.cta.shared::cta.add.u32 %0, [%1], 1;"
+               : "=r"(old)
+               : "r"(smem_u32(&rel[s]))
+               : "memory");
+  if (old != nw - 1) return false;
+  rel[s] = 0;
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  return true;
+}
+
 // Rotary embedding of one segment, by the consumers.  rope_segment (all NC
 // consumer threads, at the start of a segment, followed by a consumer
 // barrier): the G query rows of the segment, rotated, into q_rot [G][kD] fp32,
@@ -581,12 +608,13 @@ size_t smem_bytes(int B) {
 template <int G, bool R, bool A>
 __global__ void __maxnreg__(Cfg<G>::kMaxRegs) decode_splitkv_kernel(const Params p) {
   constexpr int NW = Cfg<G>::NW;
+  constexpr bool kProducer = Cfg<G>::kProducer;
   constexpr int KPW = Cfg<G>::kKeysPerWarp;
   constexpr int NC = Cfg<G>::kConsumers;
   extern __shared__ __align__(1024) uint8_t smem[];
   uint8_t* stages = smem;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kStages * 2 * kTileBytes);
-  int* misc = reinterpret_cast<int*>(bars + 2 * kStages + 2);  // after full, empty, csync, pad
+  int* misc = reinterpret_cast<int*>(bars + 2 * kStages + 2);  // after full, empty, csync, done
   float* merge_ml = reinterpret_cast<float*>(misc + kMiscInts);  // [NW][G][2]
   float* merge_o = merge_ml + NW * G * 2;                         // [NW][G][kD]
   float* rope_cs = merge_o + NW * G * kD;                         // [2][kD] cos, sin
@@ -601,13 +629,15 @@ __global__ void __maxnreg__(Cfg<G>::kMaxRegs) decode_splitkv_kernel(const Params
   if (tid == 0) {
 #pragma unroll
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(smem_u32(&bars[s]), 1);             // full: producer arrival + bytes
-      mbar_init(smem_u32(&bars[kStages + s]), NW);  // empty: one arrival per consumer warp
+      mbar_init(smem_u32(&bars[s]), 1);             // full: issuing thread's arrival + bytes
+      if (kProducer) mbar_init(smem_u32(&bars[kStages + s]), NW);  // empty: per consumer warp
     }
     mbar_init(smem_u32(&bars[2 * kStages]), NW);    // consumer barrier
-    mbar_init(smem_u32(&bars[2 * kStages + 1]), NW + 1);  // every warp done with positions
+    mbar_init(smem_u32(&bars[2 * kStages + 1]), kProducer ? NW + 1 : NW);  // done with positions
     misc[0] = 0;
     misc[1] = 0;
+    misc[2] = 0;  // release counters of the stages
+    misc[3] = 0;
     fence_mbar_init();
   }
   // Launched with programmatic stream serialisation: everything above may run
@@ -670,26 +700,43 @@ __global__ void __maxnreg__(Cfg<G>::kMaxRegs) decode_splitkv_kernel(const Params
   const long long t0 = T * blockIdx.x / Gd;
   const long long t1 = T * (blockIdx.x + 1) / Gd;
 
-  // ------------------------------------------------------------- producer --
-  if (warp == NW) {
-    if (lane == 0) {
-      Walk w;
-      walk_init(w, t0, prefix, p.positions, B, Hkv);
-      long long i = 0;
-      for (long long t = t0; t < t1; ++t, ++i) {
-        const int s = (int)(i % kStages);
-        const uint32_t u = (uint32_t)(i / kStages);
-        if (i >= kStages && !mbar_wait(smem_u32(&bars[kStages + s]), (u & 1u) ^ 1u, abort_flag)) {
-          *abort_flag = 1;
-          set_status(p.status, ATTN_DEV_TIMEOUT);
-          break;
+  // -------------------------------------------------------------- pipeline --
+  int* rel = misc + 2;
+  Walk ahead;  // without a producer: the tile kStages after the current one
+  if constexpr (kProducer) {
+    if (warp == NW) {
+      if (lane == 0) {
+        Walk w;
+        walk_init(w, t0, prefix, p.positions, B, Hkv);
+        long long i = 0;
+        for (long long t = t0; t < t1; ++t, ++i) {
+          const int s = (int)(i % kStages);
+          const uint32_t u = (uint32_t)(i / kStages);
+          if (i >= kStages &&
+              !mbar_wait(smem_u32(&bars[kStages + s]), (u & 1u) ^ 1u, abort_flag)) {
+            *abort_flag = 1;
+            set_status(p.status, ATTN_DEV_TIMEOUT);
+            break;
+          }
+          produce_tile(p, stages, bars, s, w.b, w.kvh, w.k, w.ntiles, w.n);
+          walk_next(w, prefix, p.positions, B, Hkv);
         }
-        produce_tile(p, stages, bars, s, w.b, w.kvh, w.k, w.ntiles, w.n);
-        walk_next(w, prefix, p.positions, B, Hkv);
+        if (A) mbar_arrive(smem_u32(&bars[2 * kStages + 1]));  // no more reads of positions
       }
-      if (A) mbar_arrive(smem_u32(&bars[2 * kStages + 1]));  // no more reads of positions
+      return;
     }
-    return;
+  } else {
+    // the first kStages tiles now; after that the last warp to release a
+    // stage refills it, so every warp is a consumer
+    if (tid == 0) {
+      Walk pw;
+      walk_init(pw, t0, prefix, p.positions, B, Hkv);
+      for (long long t = t0; t < t1 && t < t0 + kStages; ++t) {
+        produce_tile(p, stages, bars, (int)(t - t0), pw.b, pw.kvh, pw.k, pw.ntiles, pw.n);
+        walk_next(pw, prefix, p.positions, B, Hkv);
+      }
+    }
+    if (t0 + kStages < t1) walk_init(ahead, t0 + kStages, prefix, p.positions, B, Hkv);
   }
 
   // ------------------------------------------------------------ consumers --
@@ -721,7 +768,13 @@ __global__ void __maxnreg__(Cfg<G>::kMaxRegs) decode_splitkv_kernel(const Params
       fresh_row<R>(p, Ks, rows, w.b, w.kvh, w.n, rope_cs, lane);
     cs.tile(Ks, Ks + kTileBytes, rows, warp);
     __syncwarp();
-    if (lane == 0) mbar_arrive(smem_u32(&bars[kStages + s]));
+    if constexpr (kProducer) {
+      if (lane == 0) mbar_arrive(smem_u32(&bars[kStages + s]));
+    } else {
+      if (lane == 0 && last_to_release(rel, s, NW) && t + kStages < t1)
+        produce_tile(p, stages, bars, s, ahead.b, ahead.kvh, ahead.k, ahead.ntiles, ahead.n);
+      if (t + kStages < t1) walk_next(ahead, prefix, p.positions, B, Hkv);
+    }
     const bool seg_end = (w.k == w.ntiles - 1) || (t == t1 - 1);
 
     // ---- end of this CTA's part of the segment: merge and emit ------------
@@ -860,12 +913,13 @@ size_t cluster_smem_bytes() {
 template <int G, bool R, bool A>
 __global__ void __maxnreg__(Cfg<G>::kMaxRegs) decode_cluster_kernel(const Params p) {
   constexpr int NW = Cfg<G>::NW;
+  constexpr bool kProducer = Cfg<G>::kProducer;
   constexpr int KPW = Cfg<G>::kKeysPerWarp;
   constexpr int NC = Cfg<G>::kConsumers;
   extern __shared__ __align__(1024) uint8_t smem[];
   uint8_t* stages = smem;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kStages * 2 * kTileBytes);
-  int* misc = reinterpret_cast<int*>(bars + 2 * kStages + 2);  // after full, empty, csync, pad
+  int* misc = reinterpret_cast<int*>(bars + 2 * kStages + 2);  // after full, empty, csync, done
   float* merge_ml = reinterpret_cast<float*>(misc + kMiscInts);  // [NW][G][2]
   float* merge_o = merge_ml + NW * G * 2;                         // [NW][G][kD]
   float* rope_cs = merge_o + NW * G * kD;                         // [2][kD] cos, sin
@@ -886,10 +940,12 @@ __global__ void __maxnreg__(Cfg<G>::kMaxRegs) decode_cluster_kernel(const Params
 #pragma unroll
     for (int s = 0; s < kStages; ++s) {
       mbar_init(smem_u32(&bars[s]), 1);
-      mbar_init(smem_u32(&bars[kStages + s]), NW);
+      if (kProducer) mbar_init(smem_u32(&bars[kStages + s]), NW);
     }
     mbar_init(smem_u32(&bars[2 * kStages]), NW);
     misc[0] = 0;
+    misc[2] = 0;  // release counters of the stages
+    misc[3] = 0;
     fence_mbar_init();
   }
   grid_dependency_wait();
@@ -913,7 +969,14 @@ __global__ void __maxnreg__(Cfg<G>::kMaxRegs) decode_cluster_kernel(const Params
   const int k1 = (int)((long long)(rank + 1) * ntiles / C);
   __syncthreads();  // barriers initialised
 
-  if (warp == NW) {
+  int* rel = misc + 2;
+  if constexpr (!kProducer) {
+    // the first kStages tiles now; the last warp to release a stage refills it
+    if (tid == 0)
+      for (int k = k0; k < k1 && k < k0 + kStages; ++k)
+        produce_tile(p, stages, bars, k - k0, b, kvh, k, ntiles, n);
+  }
+  if (kProducer && warp == NW) {
     // ------------------------------------------------------------ producer --
     if (lane == 0) {
       for (int k = k0; k < k1; ++k) {
@@ -957,7 +1020,12 @@ __global__ void __maxnreg__(Cfg<G>::kMaxRegs) decode_cluster_kernel(const Params
         fresh_row<R>(p, Ks, rows, b, kvh, n, rope_cs, lane);
       cs.tile(Ks, Ks + kTileBytes, rows, warp);
       __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&bars[kStages + s]));
+      if constexpr (kProducer) {
+        if (lane == 0) mbar_arrive(smem_u32(&bars[kStages + s]));
+      } else {
+        if (lane == 0 && last_to_release(rel, s, NW) && k + kStages < k1)
+          produce_tile(p, stages, bars, s, b, kvh, k + kStages, ntiles, n);
+      }
     }
     // this CTA's partial (max, sum, unnormalised o); no tiles: (-inf, 0, 0)
     cs.stash(merge_o, merge_ml, warp);
