@@ -41,7 +41,7 @@ STEPS_STREAM = 8192
 # launch list of `bench.py --only streaming_sample` (dram__bytes_read.sum +
 # dram__bytes_write.sum, cold cache, mean over the sampled positions).  Set
 # to None when the kernel changes until it is measured again.
-TRAFFIC_BYTES_PER_LAUNCH = 16.703e6
+TRAFFIC_BYTES_PER_LAUNCH = 16.694e6
 HQ, HKV, D, L = 16, 8, 128, 8192
 METRIC = "decode-attn HBM GB/s (% of peak) & steps/s; causal prefill TFLOP/s"
 FLUSH_BYTES = 512 << 20
@@ -60,6 +60,9 @@ def _args():
                          "streaming_sample, position:N, single_step, ragged, stress, prefill, "
                          "prefill_prefix, prefill_d128_chunk, prefill_d128")
     ap.add_argument("--reps", type=int, default=3, help="launches per --only run")
+    ap.add_argument("--batch", type=int, default=None,
+                    help="--only with a decode workload: use this batch size instead "
+                         "(a smaller capture of the same kernel)")
     ap.add_argument("--cpu-worker", type=str, default=None, help=argparse.SUPPRESS)
     return ap.parse_args()
 
@@ -770,8 +773,14 @@ def run_only(args):
         torch.cuda.synchronize()
         print(json.dumps({"only": name, "launches_per_rep": len(sample)}))
         return
-    w = synth.generators.WORKLOADS[name]
-    case = synth.generators.workload_case(name, seed=0, device="cuda")
+    w = dict(synth.generators.WORKLOADS[name])
+    if args.batch and w["kind"] == "decode":
+        w["B"] = args.batch
+        kind = w.pop("kind")
+        case = synth.generators.decode_case(seed=0, device="cuda", name=name, **w)
+        w["kind"] = kind
+    else:
+        case = synth.generators.workload_case(name, seed=0, device="cuda")
     if w["kind"] == "decode":
         B, Hq, Dd = case.q.shape
         ws = ga.decode_workspace(B, Hq, case.k_cache.shape[1], case.k_cache.shape[2], Dd)
