@@ -41,7 +41,7 @@ STEPS_STREAM = 8192
 # launch list of `bench.py --only streaming_sample` (dram__bytes_read.sum +
 # dram__bytes_write.sum, cold cache, mean over the sampled positions).  Set
 # to None when the kernel changes until it is measured again.
-TRAFFIC_BYTES_PER_LAUNCH = 16.694e6
+TRAFFIC_BYTES_PER_LAUNCH = 16.687e6
 HQ, HKV, D, L = 16, 8, 128, 8192
 METRIC = "decode-attn HBM GB/s (% of peak) & steps/s; causal prefill TFLOP/s"
 FLUSH_BYTES = 512 << 20

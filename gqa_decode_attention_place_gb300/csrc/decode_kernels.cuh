@@ -35,11 +35,12 @@
 //  * Two ways to split a segment over CTAs, both computed on the device from
 //    `positions` (one launch serves any positions; graph-capturable):
 //    - cluster mode (few segments, e.g. B=1): one thread-block cluster of C
-//      CTAs (8..16, the largest size that lets every segment's cluster be
-//      resident at once) per segment; CTA rank r takes tiles
-//      [r*n/C, (r+1)*n/C).  The partials (max, sum, unnormalised o) are
-//      merged through distributed shared memory between two cluster
-//      barriers -- no global scratch, no atomics.
+//      CTAs (8..16, 8..12 for g = 8; the largest size that lets every
+//      segment's cluster be resident at once) per segment; CTA rank r takes
+//      tiles [r*n/C, (r+1)*n/C).  Each CTA stores its partial (max, sum,
+//      unnormalised o) straight into rank 0's shared memory (distributed
+//      shared memory); after one cluster barrier rank 0 merges them locally
+//      -- no global scratch, no atomics.
 //    - stream-K mode (many segments): all tiles of all segments form one flat
 //      list; CTA c of a persistent grid (one per SM) takes
 //      [c*T/G, (c+1)*T/G), balanced to one tile however ragged the batch is.
@@ -69,6 +70,7 @@ constexpr int kMaxB = kDecodeMaxB;
 constexpr int kMaxGrid = kDecodeMaxGrid;
 constexpr int kMiscInts = 32;                      // [0] abort [1] last [8..8+NW) scan
 constexpr int kWholeTiles = 4;                     // segments this short are not split
+constexpr int kMaxCluster = 16;                    // CTAs per cluster in cluster mode
 
 using Params = DecodeParams;
 
@@ -86,6 +88,9 @@ template <int G> struct Cfg {
   // thread and the key loop spilled; without it, 256 threads get 248, and the
   // last consumer warp to finish with a stage refills it (last_to_release).
   static constexpr bool kProducer = G < 8;
+  // largest cluster: rank 0 keeps a landing slot for every rank's partial
+  // (G x (kD + 2) floats each), and at g = 8 sixteen would not fit
+  static constexpr int kMaxC = G == 8 ? 12 : 16;
   static constexpr int kThreads = (NW + (kProducer ? 1 : 0)) * 32;
   static constexpr int kConsumers = NW * 32;
   static constexpr int kKeysPerWarp = kTile / NW;  // 16 or 8
@@ -905,7 +910,7 @@ size_t cluster_smem_bytes() {
   return (size_t)kStages * 2 * kTileBytes + (2 * kStages + 2) * sizeof(uint64_t) +
          kMiscInts * sizeof(int) + (size_t)NW * G * 2 * sizeof(float) +
          (size_t)NW * G * kD * sizeof(float) + (2 + G) * kD * sizeof(float) +
-         (size_t)G * (kD + 2) * sizeof(float);
+         (size_t)Cfg<G>::kMaxC * G * (kD + 2) * sizeof(float);
 }
 
 // Grid = B*Hkv clusters of C CTAs; cluster s handles segment s (sequence
@@ -924,8 +929,8 @@ __global__ void __maxnreg__(Cfg<G>::kMaxRegs) decode_cluster_kernel(const Params
   float* merge_o = merge_ml + NW * G * 2;                         // [NW][G][kD]
   float* rope_cs = merge_o + NW * G * kD;                         // [2][kD] cos, sin
   float* q_rot = rope_cs + 2 * kD;                                 // [G][kD]
-  float* part_o = q_rot + G * kD;                                 // [G][kD]
-  float* part_ml = part_o + G * kD;                               // [G][2]
+  float* land_o = q_rot + G * kD;                    // [kMaxC][G][kD]: rank r's partial o
+  float* land_ml = land_o + Cfg<G>::kMaxC * G * kD;  // [kMaxC][G][2]: its (max, sum)
 
   cg::cluster_group cluster = cg::this_cluster();
   const int C = (int)cluster.num_blocks();
@@ -968,6 +973,9 @@ __global__ void __maxnreg__(Cfg<G>::kMaxRegs) decode_cluster_kernel(const Params
   const int k0 = (int)((long long)rank * ntiles / C);
   const int k1 = (int)((long long)(rank + 1) * ntiles / C);
   __syncthreads();  // barriers initialised
+  // this CTA runs: the matching wait comes before any write into rank 0's
+  // shared memory, so rank 0 is known to have started by then
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
 
   int* rel = misc + 2;
   if constexpr (!kProducer) {
@@ -1027,53 +1035,73 @@ __global__ void __maxnreg__(Cfg<G>::kMaxRegs) decode_cluster_kernel(const Params
           produce_tile(p, stages, bars, s, b, kvh, k + kStages, ntiles, n);
       }
     }
-    // this CTA's partial (max, sum, unnormalised o); no tiles: (-inf, 0, 0)
+    // this CTA's warps' partials (max, sum, unnormalised o) merged below;
+    // no tiles: (-inf, 0, 0)
     cs.stash(merge_o, merge_ml, warp);
     csync(lane);
+  }
+
+  // The CTA's partial goes straight into slot `rank` of rank 0's shared
+  // memory (remote stores; nobody waits for them but the barrier below), so
+  // rank 0 then merges from local memory and no CTA reads another's.
+  asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
+  if (tid < NC) {
+    float* to_o = cluster.map_shared_rank(land_o, 0) + rank * G * kD;
+    float* to_ml = cluster.map_shared_rank(land_ml, 0) + rank * G * 2;
     for (int idx = tid; idx < G * kD; idx += NC) {
       const int h = idx / kD, d = idx % kD;
       float M, Ls, Os;
       merge_warps<NW, G>(merge_o, merge_ml, h, d, M, Ls, Os);
-      part_o[h * kD + d] = Os;
+      to_o[h * kD + d] = Os;
       if (d == 0) {
-        part_ml[h * 2 + 0] = M;
-        part_ml[h * 2 + 1] = Ls;
+        to_ml[h * 2 + 0] = M;
+        to_ml[h * 2 + 1] = Ls;
       }
     }
   }
 
-  // every CTA's partial is in its shared memory; rank 0 merges them
-  cluster.sync();
+  cluster.sync();  // every rank's partial is in rank 0's shared memory
   if (rank == 0) {
+    // weights 2^(m_r - M) / L per (rank, head): warp h reduces over the
+    // ranks, lane r holding rank r's (max, sum); merge_ml is free by now
+    float* wr = merge_ml;  // [C][G]
+    if (warp < G) {
+      const int h = warp;
+      const bool in = lane < C;
+      const float m = in ? land_ml[(lane * G + h) * 2] : -INFINITY;
+      const float l = in ? land_ml[(lane * G + h) * 2 + 1] : 0.f;
+      float M = m;
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+      const float e = in ? ex2(m - M) : 0.f;  // a rank without tiles: 2^-inf = 0
+      float Ls = l * e;
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) Ls += __shfl_xor_sync(0xffffffffu, Ls, off);
+      if (in) wr[lane * G + h] = e / Ls;
+    }
+    __syncthreads();
     uint16_t* out_seg = p.out + ((size_t)b * p.Hq + (size_t)kvh * G) * kD;
     for (int idx = tid; idx < G * kD; idx += blockDim.x) {
       const int h = idx / kD, d = idx % kD;
-      float M = -INFINITY;
-      for (int r = 0; r < C; ++r) M = fmaxf(M, cluster.map_shared_rank(part_ml, r)[h * 2]);
-      float Ls = 0.f, Os = 0.f;
-      for (int r = 0; r < C; ++r) {
-        const float* pml = cluster.map_shared_rank(part_ml, r);
-        const float e = ex2(pml[h * 2] - M);  // empty partial: 2^-inf = 0
-        Ls = fmaf(pml[h * 2 + 1], e, Ls);
-        Os = fmaf(cluster.map_shared_rank(part_o, r)[h * kD + d], e, Os);
-      }
-      store_bf16(out_seg + h * kD + d, Os / Ls);
+      float Os = 0.f;
+#pragma unroll 4
+      for (int r = 0; r < C; ++r) Os = fmaf(land_o[(r * G + h) * kD + d], wr[r * G + h], Os);
+      store_bf16(out_seg + h * kD + d, Os);
     }
   }
-  cluster.sync();  // keep every CTA's shared memory until rank 0 has read it
+  // no second cluster barrier: no CTA reads another's shared memory any more
 
   if (*abort_flag) {
     const uint64_t t_start = globaltimer_ns();
     while (globaltimer_ns() - t_start < 2000000ull) {
     }
   }
-  // every thread read positions only before the cluster barriers above
+  // every thread read positions only before the cluster barrier above
   if (A && warp == 0) advance_ticket(p, lane);
 }
 
 // ------------------------------------------------------------------ host --
 
-constexpr int kMaxCluster = 16;
 
 struct DevInfo {
   int num_sms = 0;
@@ -1165,7 +1193,7 @@ cudaError_t launch_g(const Params& p, cudaStream_t stream) {
   // Cluster mode when every segment can have its own co-resident cluster of
   // at least 8 CTAs: the largest such cluster size.  Otherwise stream-K.
   int C = 0;
-  for (int c = kMaxCluster; c >= 8 && C == 0; --c)
+  for (int c = Cfg<G>::kMaxC; c >= 8 && C == 0; --c)
     if (nseg <= d.clusters[G][c]) C = c;
   if (C > 0) {
     cudaLaunchConfig_t cfg = {};
