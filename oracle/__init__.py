@@ -15,7 +15,9 @@ V[0]; identical keys or a zero query return the mean of V), and invariances
 a decode step, prefix prefill equal to the tail of a full causal prefill),
 and for the rotary embedding: a hand-worked rotation, the identity at angle
 0, norm preservation, and dot products that depend only on the position
-difference.
+difference; for the local window: a window of one returning V[pos], any
+window of pos + 1 or more equal to the full decode, and the windowed decode
+equal to the full decode of the shifted slice.
 """
 
 from .attention import (  # noqa: F401
@@ -31,4 +33,5 @@ from .attention import (  # noqa: F401
     rope_f32,
     round_bf16,
     decode_rope_step,
+    decode_window,
 )

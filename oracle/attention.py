@@ -161,6 +161,36 @@ def prefill(q, k, v, start_pos, scale):
     return prefill_rows(q, k, v, start_pos, scale, rows).reshape(S, Hq, d)
 
 
+# --- local-window decode -----------------------------------------------------
+#
+# Attend only the most recent W cache rows.  The reading taken: rows
+# max(0, pos - W + 1) .. pos inclusive (W keys, the current one included);
+# W >= pos + 1 is the full decode above.
+
+def _window_rows(position: int, window: int) -> range:
+    """Cache rows a windowed decode step at ``position`` attends."""
+    return range(max(0, position - window + 1), position + 1)
+
+
+def decode_window(q, k_cache, v_cache, positions, scale, window):
+    """Decode over the last ``window`` rows up to each sequence's position.
+
+    q [B, Hq, D]; caches [B, Hkv, L, D] (after this step's append).  Returns
+    out [B, Hq, D] float64."""
+    B, Hq, D = q.shape
+    Hkv = k_cache.shape[1]
+    g = Hq // Hkv
+    out = np.empty((B, Hq, D), dtype=np.float64)
+    for b in range(B):
+        idx = list(_window_rows(int(positions[b]), int(window)))
+        for h in range(Hq):
+            kvh = _kv_head(h, g, Hkv)
+            K = np.asarray(k_cache[b, kvh, idx, :], dtype=np.float64)
+            V = np.asarray(v_cache[b, kvh, idx, :], dtype=np.float64)
+            out[b, h] = _attend(np.asarray(q[b, h], dtype=np.float64), K, V, scale)
+    return out
+
+
 # --- rotary position embedding (decode page, section 4.1) --------------------
 #
 # The decode page rotates q and the new k with apply_rotary_pos_emb(q, k,

@@ -48,6 +48,24 @@ def decode(q, k_cache, v_cache, positions, scale):
     return out
 
 
+def decode_window(q, k_cache, v_cache, positions, scale, window):
+    """As decode, over the last ``window`` rows up to each position only."""
+    B, Hq, Hkv = len(q), len(q[0]), len(k_cache[0])
+    g = Hq // Hkv
+    out = []
+    for b in range(B):
+        P = int(positions[b])
+        first = P - window + 1 if P - window + 1 > 0 else 0
+        rows_b = []
+        for h in range(Hq):
+            kv = h // g
+            keys = [k_cache[b][kv][j] for j in range(first, P + 1)]
+            vals = [v_cache[b][kv][j] for j in range(first, P + 1)]
+            rows_b.append(attend_one(q[b][h], keys, vals, scale))
+        out.append(rows_b)
+    return out
+
+
 def prefill(q, k, v, start_pos, scale):
     """q[i][h][d] for new tokens; k, v [t][kvh][d] including the prefix."""
     S, Hq, Hkv = len(q), len(q[0]), len(k[0])

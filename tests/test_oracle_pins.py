@@ -407,3 +407,64 @@ def test_rope_step_without_rotation_is_plain_decode():
     k3, v3 = oracle.kv_append(kc, vc, kn, vn, pos)
     np.testing.assert_array_equal(kc2, k3)
     np.testing.assert_allclose(out, oracle.decode(q, k3, v3, pos, 0.25), rtol=1e-12, atol=1e-13)
+
+
+# ------------------------------------------------------------ local window ---
+
+def test_window_of_one_is_v_at_position():
+    rng = np.random.default_rng(31)
+    B, Hq, Hkv, D, L = 2, 4, 2, 16, 40
+    q = _rand(rng, (B, Hq, D))
+    kc, vc = _rand(rng, (B, Hkv, L, D)), _rand(rng, (B, Hkv, L, D))
+    pos = [0, 33]
+    out = oracle.decode_window(q, kc, vc, pos, 0.3, 1)
+    for b in range(B):
+        for h in range(Hq):
+            np.testing.assert_array_equal(out[b, h], vc[b, h // 2, pos[b]])
+
+
+def test_wide_window_is_full_decode_and_window_is_shifted_slice():
+    rng = np.random.default_rng(32)
+    B, Hq, Hkv, D, L = 3, 8, 2, 16, 300
+    q = _rand(rng, (B, Hq, D))
+    kc, vc = _rand(rng, (B, Hkv, L, D)), _rand(rng, (B, Hkv, L, D))
+    pos = [5, 130, 299]
+    full = oracle.decode(q, kc, vc, pos, 0.25)
+    for W in (300, 301, 10 ** 6):
+        np.testing.assert_allclose(oracle.decode_window(q, kc, vc, pos, 0.25, W), full,
+                                   rtol=1e-13, atol=1e-14)
+    for W in (1, 2, 6, 64, 131):
+        got = oracle.decode_window(q, kc, vc, pos, 0.25, W)
+        for b, p in enumerate(pos):
+            lo = max(0, p - W + 1)
+            want = oracle.decode(q[b:b + 1], kc[b:b + 1, :, lo:p + 1], vc[b:b + 1, :, lo:p + 1],
+                                 [p - lo], 0.25)
+            np.testing.assert_allclose(got[b:b + 1], want, rtol=1e-13, atol=1e-14)
+
+
+def test_window_matches_brute_force():
+    rng = np.random.default_rng(33)
+    B, Hq, Hkv, D, L = 2, 4, 2, 8, 20
+    q = _rand(rng, (B, Hq, D))
+    kc, vc = _rand(rng, (B, Hkv, L, D)), _rand(rng, (B, Hkv, L, D))
+    for pos in ([19, 3], [0, 12]):
+        for W in (1, 3, 7, 25):
+            want = np.array(brute.decode_window(q.tolist(), kc.tolist(), vc.tolist(), pos, 0.5, W))
+            np.testing.assert_allclose(oracle.decode_window(q, kc, vc, pos, 0.5, W), want,
+                                       rtol=1e-12, atol=1e-12)
+
+
+def test_window_pin_catches_an_off_by_one():
+    """A window one row too wide (a plausible mistake) fails the shifted-slice
+    pin: the pins are not vacuous."""
+    rng = np.random.default_rng(34)
+    q = _rand(rng, (1, 2, 8))
+    kc, vc = _rand(rng, (1, 1, 30, 8)), _rand(rng, (1, 1, 30, 8))
+    good = oracle.decode_window(q, kc, vc, [20], 0.5, 5)
+    saved = oatt._window_rows
+    try:
+        oatt._window_rows = lambda position, window: range(max(0, position - window), position + 1)
+        bad = oracle.decode_window(q, kc, vc, [20], 0.5, 5)
+    finally:
+        oatt._window_rows = saved
+    assert np.abs(good - bad).max() > 1e-3
