@@ -12,7 +12,8 @@ value = algorithmic decode bytes (K and V rows 0..pos of every KV head, plus
 q and out) / device time of the step, in GB/s; `steps_per_s` is decode steps
 per second.  Extra legs: per-position decode time (warm and cold L2), the
 ragged B=64 batch, the B=256 g=8 stress batch, the ragged batch as a fused
-append step with and without the rotary embedding, and the causal prefill
+append step with and without the rotary embedding, the ragged batch over a
+1024-row local window, and the causal prefill
 workloads (TFLOP/s; also GQA prompt chunks at d_head=128), each against its
 roofline.  The cross-checks time the
 same 8192 positions as separate append/decode launches, as decode launches
@@ -542,6 +543,30 @@ def _append_leg(torch, ga, synth, name, flush, hbm, rope):
     return r
 
 
+def _window_leg(torch, ga, synth, name, flush, hbm, window):
+    """Local-window decode on a decode workload: algorithmic bytes count the
+    window rows only (min(window, pos + 1) per sequence)."""
+    import oracle
+    case = synth.generators.workload_case(name, seed=0, device="cuda")
+    B, Hq, Dd = case.q.shape
+    Hkv, Ll = case.k_cache.shape[1], case.k_cache.shape[2]
+    ws = ga.decode_workspace(B, Hq, Hkv, Ll, Dd)
+    out = torch.empty_like(case.q)
+
+    def one():
+        ga.attn_decode_step_window(case.q, case.positions, case.k_cache, case.v_cache,
+                                   case.scale, window, out=out, workspace=ws)
+    ms = statistics.median(_time_graph(torch, one, flush, 10, 3))
+    rows_pos = [min(int(p), window - 1) for p in case.positions.cpu().tolist()]
+    nb = oracle.decode_bytes(rows_pos, Hq, Hkv, Dd)
+    r = {"us": round(ms * 1e3, 2), "GBs": round(nb / (ms * 1e-3) / 1e9, 1),
+         "frac_hbm": round(nb / (ms * 1e-3) / 1e9 / hbm, 3), "bytes": nb, "window": window,
+         "shape": {"B": B, "Hq": Hq, "Hkv": Hkv, "D": Dd, "L": Ll}}
+    del case, ws, out
+    torch.cuda.empty_cache()
+    return r
+
+
 def _prefill_leg(torch, ga, synth, name, flush, tflops_peak):
     import oracle
     case = synth.generators.workload_case(name, seed=0, device="cuda")
@@ -701,6 +726,7 @@ def run_ours(args):
         legs["ragged_append"] = _append_leg(torch, ga, synth, "ragged", flush, hbm, rope=False)
         legs["ragged_rope_append"] = _append_leg(torch, ga, synth, "ragged", flush, hbm,
                                                  rope=True)
+        legs["ragged_window1024"] = _window_leg(torch, ga, synth, "ragged", flush, hbm, 1024)
         for name in ("prefill_prefix", "prefill", "prefill_d128_chunk", "prefill_d128"):
             legs[name] = _prefill_leg(torch, ga, synth, name, flush, tf_burst)
         line["legs"] = legs

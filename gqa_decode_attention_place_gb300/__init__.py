@@ -23,6 +23,7 @@ __all__ = [
     "attn_prefill_causal", "attn_read_device_status", "attn_status_string",
     "attn_last_cuda_error", "decode_workspace", "attn_decode_step_noalloc",
     "attn_decode_step_append", "attn_decode_step_rope_append", "attn_decode_stream_step",
+    "attn_decode_step_window",
 ]
 
 ATTN_OK = 0
@@ -71,6 +72,9 @@ def load_library(build_if_missing: bool = True) -> ctypes.CDLL:
     lib.attn_decode_stream_step.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32,
                                             i32, f32, vp, vp, sz, vp]
     lib.attn_decode_stream_step.restype = i32
+    lib.attn_decode_step_window.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32,
+                                            f32, vp, vp, sz, vp]
+    lib.attn_decode_step_window.restype = i32
     lib.attn_decode_step_noalloc.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, i32, f32, vp, vp]
     lib.attn_decode_step_noalloc.restype = i32
     lib.attn_prefill_causal.argtypes = [vp, vp, vp, i32, i32, i32, i32, i32, f32, vp, vp]
@@ -251,6 +255,44 @@ def attn_decode_stream_step(q, k_new, v_new, positions, k_cache, v_cache, scale:
                 raise ValueError(f"attn_decode_stream_step: {n} must be [L, D]")
     return _decode_append("attn_decode_stream_step", q, k_new, v_new, (cos_table, sin_table),
                           positions, k_cache, v_cache, scale, out, workspace, stream)
+
+
+def attn_decode_step_window(q, positions, k_cache, v_cache, scale: float, window: int,
+                            k_new=None, v_new=None, out=None, workspace=None,
+                            stream=None) -> torch.Tensor:
+    """Decode over the last ``window`` rows up to each position (rows
+    max(0, pos - window + 1) .. pos), appending k_new/v_new first if given."""
+    _check(q, "q", torch.bfloat16, 3)
+    _check(positions, "positions", torch.int32, 1)
+    for t, n in ((k_cache, "k_cache"), (v_cache, "v_cache")):
+        _check(t, n, torch.bfloat16, 4)
+    if (k_new is None) != (v_new is None):
+        raise ValueError("attn_decode_step_window: give both k_new and v_new, or neither")
+    B, Hq, D = q.shape
+    Hkv, L = k_cache.shape[1], k_cache.shape[2]
+    if tuple(v_cache.shape) != tuple(k_cache.shape) or k_cache.shape[0] != B or \
+            k_cache.shape[3] != D or positions.shape[0] != B:
+        raise ValueError("attn_decode_step_window: inconsistent shapes")
+    if k_new is not None:
+        for t, n in ((k_new, "k_new"), (v_new, "v_new")):
+            _check(t, n, torch.bfloat16, 3)
+            if tuple(t.shape) != (B, Hkv, D):
+                raise ValueError(f"attn_decode_step_window: {n} must be [B, Hkv, D]")
+    if out is None:
+        out = torch.empty_like(q)
+    else:
+        _check(out, "out", torch.bfloat16, 3)
+        if tuple(out.shape) != (B, Hq, D):
+            raise ValueError("attn_decode_step_window: out has the wrong shape")
+    if workspace is None:
+        workspace = decode_workspace(B, Hq, Hkv, L, D, device=q.device)
+    ptr = lambda t: t.data_ptr() if t is not None else None
+    code = load_library().attn_decode_step_window(
+        q.data_ptr(), ptr(k_new), ptr(v_new), positions.data_ptr(), k_cache.data_ptr(),
+        v_cache.data_ptr(), B, Hq, Hkv, L, D, int(window), float(scale), out.data_ptr(),
+        workspace.data_ptr(), workspace.numel() * workspace.element_size(), _stream(stream))
+    _raise(code, "attn_decode_step_window")
+    return out
 
 
 def attn_decode_step_noalloc(q, positions, k_cache, v_cache, scale: float, out=None,

@@ -59,7 +59,7 @@ int attn_decode_step(const void* q, const int32_t* positions, const void* k_cach
       workspace_bytes < gqa::decode_workspace_layout(B, Hq, Hkv, D).total)
     return ATTN_ERR_WORKSPACE;
   return cuda_status(gqa::launch_decode(q, nullptr, nullptr, nullptr, nullptr, false, positions,
-                                        nullptr, k_cache, v_cache, B, Hq, Hkv, L, D, scale, out,
+                                        nullptr, k_cache, v_cache, B, Hq, Hkv, L, D, 0, scale, out,
                                         workspace, stream));
 }
 
@@ -69,13 +69,16 @@ int decode_append(const void* q, const void* k_new, const void* v_new, const flo
                   const float* rope_sin, bool rope_by_pos, const int32_t* positions,
                   int32_t* advance, void* k_cache, void* v_cache, int B, int Hq, int Hkv, int L,
                   int D, float scale, void* out, void* workspace, size_t workspace_bytes,
-                  cudaStream_t stream) {
-  if (!q || !k_new || !v_new || !positions || !k_cache || !v_cache || !out)
+                  cudaStream_t stream, int window = 0) {
+  if (!q || !positions || !k_cache || !v_cache || !out || !k_new != !v_new)
     return ATTN_ERR_INVALID_ARG;
+  if (!k_new && (rope_cos || advance)) return ATTN_ERR_INVALID_ARG;
+  if (window < 0) return ATTN_ERR_INVALID_ARG;
   if (B <= 0 || Hq <= 0 || Hkv <= 0 || L <= 0 || D <= 0 || Hq % Hkv != 0)
     return ATTN_ERR_INVALID_ARG;
-  if (!aligned16(q) || !aligned16(k_new) || !aligned16(v_new) || !aligned16(k_cache) ||
-      !aligned16(v_cache) || !aligned16(out) || (reinterpret_cast<uintptr_t>(positions) & 3u))
+  if (!aligned16(q) || (k_new && (!aligned16(k_new) || !aligned16(v_new))) ||
+      !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out) ||
+      (reinterpret_cast<uintptr_t>(positions) & 3u))
     return ATTN_ERR_INVALID_ARG;
   if (!gqa::decode_supported(B, Hq, Hkv, L, D)) return ATTN_ERR_UNSUPPORTED;
   if (!workspace || !aligned16(workspace) ||
@@ -83,7 +86,7 @@ int decode_append(const void* q, const void* k_new, const void* v_new, const flo
     return ATTN_ERR_WORKSPACE;
   return cuda_status(gqa::launch_decode(q, k_new, v_new, rope_cos, rope_sin, rope_by_pos,
                                         positions, advance, k_cache, v_cache, B, Hq, Hkv, L, D,
-                                        scale, out, workspace, stream));
+                                        window, scale, out, workspace, stream));
 }
 
 }  // namespace
@@ -92,6 +95,7 @@ int attn_decode_step_append(const void* q, const void* k_new, const void* v_new,
                             const int32_t* positions, void* k_cache, void* v_cache, int B,
                             int Hq, int Hkv, int L, int D, float scale, void* out,
                             void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  if (!k_new || !v_new) return ATTN_ERR_INVALID_ARG;
   return decode_append(q, k_new, v_new, nullptr, nullptr, false, positions, nullptr, k_cache,
                        v_cache, B, Hq, Hkv, L, D, scale, out, workspace, workspace_bytes, stream);
 }
@@ -101,9 +105,20 @@ int attn_decode_step_rope_append(const void* q, const void* k_new, const void* v
                                  void* k_cache, void* v_cache, int B, int Hq, int Hkv, int L,
                                  int D, float scale, void* out, void* workspace,
                                  size_t workspace_bytes, cudaStream_t stream) {
+  if (!k_new || !v_new) return ATTN_ERR_INVALID_ARG;
   if (!cos || !sin || !aligned16(cos) || !aligned16(sin)) return ATTN_ERR_INVALID_ARG;
   return decode_append(q, k_new, v_new, cos, sin, false, positions, nullptr, k_cache, v_cache, B,
                        Hq, Hkv, L, D, scale, out, workspace, workspace_bytes, stream);
+}
+
+int attn_decode_step_window(const void* q, const void* k_new, const void* v_new,
+                            const int32_t* positions, void* k_cache, void* v_cache, int B, int Hq,
+                            int Hkv, int L, int D, int window, float scale, void* out,
+                            void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  if (window <= 0) return ATTN_ERR_INVALID_ARG;
+  return decode_append(q, k_new, v_new, nullptr, nullptr, false, positions, nullptr, k_cache,
+                       v_cache, B, Hq, Hkv, L, D, scale, out, workspace, workspace_bytes, stream,
+                       window);
 }
 
 int attn_decode_stream_step(const void* q, const void* k_new, const void* v_new,
@@ -111,6 +126,7 @@ int attn_decode_stream_step(const void* q, const void* k_new, const void* v_new,
                             void* k_cache, void* v_cache, int B, int Hq, int Hkv, int L, int D,
                             float scale, void* out, void* workspace, size_t workspace_bytes,
                             cudaStream_t stream) {
+  if (!k_new || !v_new) return ATTN_ERR_INVALID_ARG;
   if ((cos_table == nullptr) != (sin_table == nullptr)) return ATTN_ERR_INVALID_ARG;
   if (cos_table && (!aligned16(cos_table) || !aligned16(sin_table))) return ATTN_ERR_INVALID_ARG;
   return decode_append(q, k_new, v_new, cos_table, sin_table, true, positions, positions, k_cache,

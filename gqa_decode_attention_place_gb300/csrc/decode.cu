@@ -34,8 +34,8 @@ bool decode_supported(int B, int Hq, int Hkv, int L, int D) {
 cudaError_t launch_decode(const void* q, const void* k_new, const void* v_new,
                           const float* rope_cos, const float* rope_sin, bool rope_by_pos,
                           const int32_t* positions, int32_t* advance, const void* k_cache,
-                          const void* v_cache, int B, int Hq, int Hkv, int L, int D, float scale,
-                          void* out, void* workspace, cudaStream_t stream) {
+                          const void* v_cache, int B, int Hq, int Hkv, int L, int D, int window,
+                          float scale, void* out, void* workspace, cudaStream_t stream) {
   const DecodeWorkspace ws = decode_workspace_layout(B, Hq, Hkv, D);
   uint8_t* base = static_cast<uint8_t*>(workspace);
   DecodeParams p;
@@ -53,6 +53,7 @@ cudaError_t launch_decode(const void* q, const void* k_new, const void* v_new,
   p.rope_cos = rope_cos;
   p.rope_sin = rope_sin;
   p.rope_by_pos = rope_by_pos ? 1 : 0;
+  p.window = window;
   p.advance = advance;
   p.ticket = reinterpret_cast<uint32_t*>(base + ws.ticket_off);
   p.B = B;
@@ -119,7 +120,7 @@ cudaError_t launch_decode_noalloc(const void* q, const int32_t* positions, const
   e = cudaMemsetAsync(scratch, 0, ws.ml_off, stream);
   if (e != cudaSuccess) return e;
   return launch_decode(q, nullptr, nullptr, nullptr, nullptr, false, positions, nullptr, k_cache,
-                       v_cache, B, Hq, Hkv, L, D, scale, out, scratch, stream);
+                       v_cache, B, Hq, Hkv, L, D, 0, scale, out, scratch, stream);
 }
 
 }  // namespace gqa

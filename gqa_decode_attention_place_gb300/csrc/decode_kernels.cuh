@@ -5,7 +5,8 @@
 // What it computes ("MiniCPM4 `forward_step` Attention Performance Fix",
 // sections 3 and 4.1): for every sequence b and query head h,
 //   out[b,h,:] = softmax_j(scale * q[b,h,:] . K[b,h/g,j,:]) V[b,h/g,j,:]
-// over cache rows j = 0..positions[b] only (the slice replaces the
+// over cache rows j = 0..positions[b] only, or the last W of them with a
+// local window (the slice replaces the
 // full-length boolean mask of section 2.1, so the work follows position+1 and
 // not max_len, sections 2.4 and 6.4).  Optionally the step's new K/V row is
 // appended in the same launch (the page writes the row, then attends), and
@@ -74,6 +75,13 @@ constexpr int kMaxCluster = 16;                    // CTAs per cluster in cluste
 
 using Params = DecodeParams;
 
+// Kernel variants: a mode M of compile-time flags, so that a plain step's
+// kernel carries none of the optional work (even unused code moved register
+// allocation and cost a few percent).
+constexpr int kModeRope = 1;     // rotary embedding of q and the new key
+constexpr int kModeAdvance = 2;  // positions += 1 after the step
+constexpr int kModeWindow = 4;   // attend only the last p.window rows
+
 // Lanes per key (LPK): a key's 128 dims are spread over LPK lanes of a warp
 // (128/LPK dims each), so a warp takes 32/LPK keys per step.  Fewer lanes
 // per key means fewer shuffle-reduction steps but more q and o registers
@@ -133,12 +141,19 @@ struct ConsumerSync {
 };
 
 // Position of flat tile t within (sequence, KV head, tile) order.
+// Rows a step at position pos attends: n rows from lo (lo = 0 without a
+// local window; with window W the last W rows, the current one included).
+__device__ __forceinline__ void attended_rows(int pos, int window, int& lo, int& n) {
+  lo = (window > 0 && pos >= window) ? pos - window + 1 : 0;
+  n = pos - lo + 1;
+}
+
 struct Walk {
-  int b, kvh, k, ntiles, n;  // n = attended rows of sequence b
+  int b, kvh, k, ntiles, n, lo;  // n attended rows of sequence b, from row lo
 };
 
 __device__ __forceinline__ void walk_init(Walk& w, long long t, const int* prefix,
-                                          const int32_t* positions, int B, int Hkv) {
+                                          const int32_t* positions, int B, int Hkv, int window) {
   int lo = 0, hi = B - 1;  // largest b with Hkv*prefix[b] <= t
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
@@ -149,11 +164,11 @@ __device__ __forceinline__ void walk_init(Walk& w, long long t, const int* prefi
   const long long off = t - (long long)Hkv * prefix[lo];
   w.kvh = (int)(off / w.ntiles);
   w.k = (int)(off % w.ntiles);
-  w.n = positions[lo] + 1;
+  attended_rows(positions[lo], window, w.lo, w.n);
 }
 
 __device__ __forceinline__ void walk_next(Walk& w, const int* prefix, const int32_t* positions,
-                                          int B, int Hkv) {
+                                          int B, int Hkv, int window) {
   if (++w.k < w.ntiles) return;
   w.k = 0;
   if (++w.kvh < Hkv) return;
@@ -161,7 +176,7 @@ __device__ __forceinline__ void walk_next(Walk& w, const int* prefix, const int3
   do { ++w.b; } while (w.b < B && prefix[w.b + 1] == prefix[w.b]);
   if (w.b < B) {
     w.ntiles = prefix[w.b + 1] - prefix[w.b];
-    w.n = positions[w.b] + 1;
+    attended_rows(positions[w.b], window, w.lo, w.n);
   }
 }
 
@@ -443,9 +458,10 @@ __device__ __forceinline__ void merge_warps(const float* merge_o, const float* m
 // of the cache; a consumer warp rotates it if asked and writes it to the
 // cache (fresh_row).  No other CTA reads that row.
 __device__ __forceinline__ void produce_tile(const Params& p, uint8_t* stages, uint64_t* bars,
-                                             int s, int b, int kvh, int k, int ntiles, int n) {
+                                             int s, int b, int kvh, int k, int ntiles, int n,
+                                             int lo) {
   const int rows = min(kTile, n - k * kTile);
-  const size_t row0 = ((size_t)b * p.Hkv + kvh) * (size_t)p.L + (size_t)k * kTile;
+  const size_t row0 = ((size_t)b * p.Hkv + kvh) * (size_t)p.L + (size_t)lo + (size_t)k * kTile;
   const bool fresh = p.k_new != nullptr && k == ntiles - 1;
   const int cache_rows = fresh ? rows - 1 : rows;
   const uint32_t full = smem_u32(&bars[s]);
@@ -541,12 +557,12 @@ __device__ __forceinline__ bool consumer_wait(uint32_t bar, uint32_t parity,
 // memory to cache row pos = n-1, one 16-byte store per lane of one warp
 // (lanes 0-15 the K row, 16-31 the V row).
 __device__ __forceinline__ void write_fresh_rows(const Params& p, const uint8_t* Ks, int rows,
-                                                 int b, int kvh, int n, int lane) {
+                                                 int b, int kvh, int pos, int lane) {
   const int c = lane & 15;
   const bool is_v = lane >= 16;
   const uint8_t* src = Ks + (is_v ? kTileBytes : 0) + (size_t)(rows - 1) * kRowBytes + c * 16;
   uint8_t* dst = (is_v ? p.v_cache : p.k_cache) +
-                 (((size_t)b * p.Hkv + kvh) * (size_t)p.L + (size_t)(n - 1)) * kRowBytes + c * 16;
+                 (((size_t)b * p.Hkv + kvh) * (size_t)p.L + (size_t)pos) * kRowBytes + c * 16;
   *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<const uint4*>(src);
 }
 
@@ -555,12 +571,12 @@ __device__ __forceinline__ void write_fresh_rows(const Params& p, const uint8_t*
 // embedding, then written to the cache.  No other warp reads the K row.
 template <bool R>
 __device__ __forceinline__ void fresh_row(const Params& p, uint8_t* Ks, int rows, int b, int kvh,
-                                          int n, const float* rope_cs, int lane) {
+                                          int pos, const float* rope_cs, int lane) {
   if (R) {
     rope_fresh_key(Ks + (size_t)(rows - 1) * kRowBytes, rope_cs, lane);
     __syncwarp();
   }
-  write_fresh_rows(p, Ks, rows, b, kvh, n, lane);
+  write_fresh_rows(p, Ks, rows, b, kvh, pos, lane);
 }
 
 // The rotation row of sequence b at position pos: row b of a [B, D] table,
@@ -610,8 +626,9 @@ size_t smem_bytes(int B) {
 }
 
 // ---------------------------------------------------------- stream-K mode --
-template <int G, bool R, bool A>
+template <int G, int M>
 __global__ void __maxnreg__(Cfg<G>::kMaxRegs) decode_splitkv_kernel(const Params p) {
+  constexpr bool R = (M & kModeRope) != 0, A = (M & kModeAdvance) != 0;
   constexpr int NW = Cfg<G>::NW;
   constexpr bool kProducer = Cfg<G>::kProducer;
   constexpr int KPW = Cfg<G>::kKeysPerWarp;
@@ -629,6 +646,7 @@ __global__ void __maxnreg__(Cfg<G>::kMaxRegs) decode_splitkv_kernel(const Params
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
   const int B = p.B, Hkv = p.Hkv, L = p.L;
+  const int win = (M & kModeWindow) ? p.window : 0;
   volatile int* abort_flag = misc;
 
   if (tid == 0) {
@@ -659,7 +677,9 @@ __global__ void __maxnreg__(Cfg<G>::kMaxRegs) decode_splitkv_kernel(const Params
     if (tid < NC && b < B) {
       const int pos = p.positions[b];
       if (pos >= 0 && pos < L) {
-        v = pos / kTile + 1;  // ceil((pos + 1) / kTile)
+        int lo, n;
+        attended_rows(pos, win, lo, n);
+        v = (n - 1) / kTile + 1;  // ceil(n / kTile)
       } else if (b % gridDim.x == blockIdx.x) {
         // out-of-range position: flag it and make the sequence's output NaN
         set_status(p.status, ATTN_DEV_BAD_POSITION);
@@ -712,7 +732,7 @@ __global__ void __maxnreg__(Cfg<G>::kMaxRegs) decode_splitkv_kernel(const Params
     if (warp == NW) {
       if (lane == 0) {
         Walk w;
-        walk_init(w, t0, prefix, p.positions, B, Hkv);
+        walk_init(w, t0, prefix, p.positions, B, Hkv, win);
         long long i = 0;
         for (long long t = t0; t < t1; ++t, ++i) {
           const int s = (int)(i % kStages);
@@ -723,8 +743,8 @@ __global__ void __maxnreg__(Cfg<G>::kMaxRegs) decode_splitkv_kernel(const Params
             set_status(p.status, ATTN_DEV_TIMEOUT);
             break;
           }
-          produce_tile(p, stages, bars, s, w.b, w.kvh, w.k, w.ntiles, w.n);
-          walk_next(w, prefix, p.positions, B, Hkv);
+          produce_tile(p, stages, bars, s, w.b, w.kvh, w.k, w.ntiles, w.n, w.lo);
+          walk_next(w, prefix, p.positions, B, Hkv, win);
         }
         if (A) mbar_arrive(smem_u32(&bars[2 * kStages + 1]));  // no more reads of positions
       }
@@ -735,13 +755,13 @@ __global__ void __maxnreg__(Cfg<G>::kMaxRegs) decode_splitkv_kernel(const Params
     // stage refills it, so every warp is a consumer
     if (tid == 0) {
       Walk pw;
-      walk_init(pw, t0, prefix, p.positions, B, Hkv);
+      walk_init(pw, t0, prefix, p.positions, B, Hkv, win);
       for (long long t = t0; t < t1 && t < t0 + kStages; ++t) {
-        produce_tile(p, stages, bars, (int)(t - t0), pw.b, pw.kvh, pw.k, pw.ntiles, pw.n);
-        walk_next(pw, prefix, p.positions, B, Hkv);
+        produce_tile(p, stages, bars, (int)(t - t0), pw.b, pw.kvh, pw.k, pw.ntiles, pw.n, pw.lo);
+        walk_next(pw, prefix, p.positions, B, Hkv, win);
       }
     }
-    if (t0 + kStages < t1) walk_init(ahead, t0 + kStages, prefix, p.positions, B, Hkv);
+    if (t0 + kStages < t1) walk_init(ahead, t0 + kStages, prefix, p.positions, B, Hkv, win);
   }
 
   // ------------------------------------------------------------ consumers --
@@ -749,11 +769,11 @@ __global__ void __maxnreg__(Cfg<G>::kMaxRegs) decode_splitkv_kernel(const Params
   cs.init(lane);
   ConsumerSync csync{smem_u32(&bars[2 * kStages]), abort_flag, p.status, 0u};
   Walk w;
-  walk_init(w, t0, prefix, p.positions, B, Hkv);
+  walk_init(w, t0, prefix, p.positions, B, Hkv, win);
   const uint16_t* qb = p.q + ((size_t)w.b * p.Hq + (size_t)w.kvh * G) * kD;
   if (R) {
-    rope_segment<G, NC>(qb, rope_row<R>(p, p.rope_cos, w.b, w.n - 1),
-                        rope_row<R>(p, p.rope_sin, w.b, w.n - 1), q_rot,
+    rope_segment<G, NC>(qb, rope_row<R>(p, p.rope_cos, w.b, w.lo + w.n - 1),
+                        rope_row<R>(p, p.rope_sin, w.b, w.lo + w.n - 1), q_rot,
                         rope_cs, tid);
     consumer_bar<NC>();  // before any tile wait: every consumer warp gets here
     cs.load_q_rot(q_rot, p.qscale);
@@ -770,15 +790,16 @@ __global__ void __maxnreg__(Cfg<G>::kMaxRegs) decode_splitkv_kernel(const Params
     const int rows = min(kTile, w.n - w.k * kTile);
     uint8_t* Ks = stages + (size_t)s * 2 * kTileBytes;
     if (p.k_new != nullptr && w.k == w.ntiles - 1 && warp == (rows - 1) / KPW)
-      fresh_row<R>(p, Ks, rows, w.b, w.kvh, w.n, rope_cs, lane);
+      fresh_row<R>(p, Ks, rows, w.b, w.kvh, w.lo + w.n - 1, rope_cs, lane);
     cs.tile(Ks, Ks + kTileBytes, rows, warp);
     __syncwarp();
     if constexpr (kProducer) {
       if (lane == 0) mbar_arrive(smem_u32(&bars[kStages + s]));
     } else {
       if (lane == 0 && last_to_release(rel, s, NW) && t + kStages < t1)
-        produce_tile(p, stages, bars, s, ahead.b, ahead.kvh, ahead.k, ahead.ntiles, ahead.n);
-      if (t + kStages < t1) walk_next(ahead, prefix, p.positions, B, Hkv);
+        produce_tile(p, stages, bars, s, ahead.b, ahead.kvh, ahead.k, ahead.ntiles, ahead.n,
+                   ahead.lo);
+      if (t + kStages < t1) walk_next(ahead, prefix, p.positions, B, Hkv, win);
     }
     const bool seg_end = (w.k == w.ntiles - 1) || (t == t1 - 1);
 
@@ -868,14 +889,14 @@ __global__ void __maxnreg__(Cfg<G>::kMaxRegs) decode_splitkv_kernel(const Params
       csync(lane);  // merge buffers are free again
       cs.reset();
     }
-    walk_next(w, prefix, p.positions, B, Hkv);
+    walk_next(w, prefix, p.positions, B, Hkv, win);
     if (w.k == 0 && t + 1 < t1) {
       // a new segment; every consumer has read q_rot and rope_cs of the last
       // one (seg_end's barriers came after), so they may be overwritten
       const uint16_t* qn = p.q + ((size_t)w.b * p.Hq + (size_t)w.kvh * G) * kD;
       if (R) {
-        rope_segment<G, NC>(qn, rope_row<R>(p, p.rope_cos, w.b, w.n - 1),
-                            rope_row<R>(p, p.rope_sin, w.b, w.n - 1),
+        rope_segment<G, NC>(qn, rope_row<R>(p, p.rope_cos, w.b, w.lo + w.n - 1),
+                            rope_row<R>(p, p.rope_sin, w.b, w.lo + w.n - 1),
                             q_rot, rope_cs, tid);
         csync(lane);
         cs.load_q_rot(q_rot, p.qscale);
@@ -915,8 +936,9 @@ size_t cluster_smem_bytes() {
 
 // Grid = B*Hkv clusters of C CTAs; cluster s handles segment s (sequence
 // s / Hkv, KV head s % Hkv).
-template <int G, bool R, bool A>
+template <int G, int M>
 __global__ void __maxnreg__(Cfg<G>::kMaxRegs) decode_cluster_kernel(const Params p) {
+  constexpr bool R = (M & kModeRope) != 0, A = (M & kModeAdvance) != 0;
   constexpr int NW = Cfg<G>::NW;
   constexpr bool kProducer = Cfg<G>::kProducer;
   constexpr int KPW = Cfg<G>::kKeysPerWarp;
@@ -937,6 +959,7 @@ __global__ void __maxnreg__(Cfg<G>::kMaxRegs) decode_cluster_kernel(const Params
   const int rank = (int)cluster.block_rank();
   const int seg = blockIdx.x / C;
   const int b = seg / p.Hkv, kvh = seg % p.Hkv;
+  const int win = (M & kModeWindow) ? p.window : 0;
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
   volatile int* abort_flag = misc;
@@ -968,8 +991,9 @@ __global__ void __maxnreg__(Cfg<G>::kMaxRegs) decode_cluster_kernel(const Params
     }
     return;
   }
-  const int n = pos + 1;
-  const int ntiles = pos / kTile + 1;
+  int lo, n;
+  attended_rows(pos, win, lo, n);
+  const int ntiles = (n - 1) / kTile + 1;
   const int k0 = (int)((long long)rank * ntiles / C);
   const int k1 = (int)((long long)(rank + 1) * ntiles / C);
   __syncthreads();  // barriers initialised
@@ -982,7 +1006,7 @@ __global__ void __maxnreg__(Cfg<G>::kMaxRegs) decode_cluster_kernel(const Params
     // the first kStages tiles now; the last warp to release a stage refills it
     if (tid == 0)
       for (int k = k0; k < k1 && k < k0 + kStages; ++k)
-        produce_tile(p, stages, bars, k - k0, b, kvh, k, ntiles, n);
+        produce_tile(p, stages, bars, k - k0, b, kvh, k, ntiles, n, lo);
   }
   if (kProducer && warp == NW) {
     // ------------------------------------------------------------ producer --
@@ -996,7 +1020,7 @@ __global__ void __maxnreg__(Cfg<G>::kMaxRegs) decode_cluster_kernel(const Params
           set_status(p.status, ATTN_DEV_TIMEOUT);
           break;
         }
-        produce_tile(p, stages, bars, s, b, kvh, k, ntiles, n);
+        produce_tile(p, stages, bars, s, b, kvh, k, ntiles, n, lo);
       }
     }
     __syncwarp();
@@ -1025,14 +1049,14 @@ __global__ void __maxnreg__(Cfg<G>::kMaxRegs) decode_cluster_kernel(const Params
       const int rows = min(kTile, n - k * kTile);
       uint8_t* Ks = stages + (size_t)s * 2 * kTileBytes;
       if (p.k_new != nullptr && k == ntiles - 1 && warp == (rows - 1) / KPW)
-        fresh_row<R>(p, Ks, rows, b, kvh, n, rope_cs, lane);
+        fresh_row<R>(p, Ks, rows, b, kvh, pos, rope_cs, lane);
       cs.tile(Ks, Ks + kTileBytes, rows, warp);
       __syncwarp();
       if constexpr (kProducer) {
         if (lane == 0) mbar_arrive(smem_u32(&bars[kStages + s]));
       } else {
         if (lane == 0 && last_to_release(rel, s, NW) && k + kStages < k1)
-          produce_tile(p, stages, bars, s, b, kvh, k + kStages, ntiles, n);
+          produce_tile(p, stages, bars, s, b, kvh, k + kStages, ntiles, n, lo);
       }
     }
     // this CTA's warps' partials (max, sum, unnormalised o) merged below;
@@ -1139,7 +1163,7 @@ int max_clusters(int C) {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, decode_cluster_kernel<G, false, false>, &cfg) !=
+  if (cudaOccupancyMaxActiveClusters(&n, decode_cluster_kernel<G, 0>, &cfg) !=
       cudaSuccess) {
     cudaGetLastError();
     return 0;
@@ -1147,17 +1171,17 @@ int max_clusters(int C) {
   return n;
 }
 
-template <int G, bool R, bool A>
+template <int G, int M>
 cudaError_t set_attributes(bool* big) {
-  cudaError_t e = cudaFuncSetAttribute(decode_splitkv_kernel<G, R, A>,
+  cudaError_t e = cudaFuncSetAttribute(decode_splitkv_kernel<G, M>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)smem_bytes<G>(kMaxB));
   if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(decode_cluster_kernel<G, R, A>,
+  e = cudaFuncSetAttribute(decode_cluster_kernel<G, M>,
                            cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)cluster_smem_bytes<G>());
   if (e != cudaSuccess) return e;
-  *big = cudaFuncSetAttribute(decode_cluster_kernel<G, R, A>,
+  *big = cudaFuncSetAttribute(decode_cluster_kernel<G, M>,
                               cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess;
   if (!*big) cudaGetLastError();
   return cudaSuccess;
@@ -1166,24 +1190,25 @@ cudaError_t set_attributes(bool* big) {
 template <int G>
 cudaError_t configure(DevInfo& d) {
   if (d.configured[G]) return cudaSuccess;
-  bool big[4] = {};
-  cudaError_t e = set_attributes<G, false, false>(&big[0]);
-  if (e == cudaSuccess) e = set_attributes<G, true, false>(&big[1]);
-  if (e == cudaSuccess) e = set_attributes<G, false, true>(&big[2]);
-  if (e == cudaSuccess) e = set_attributes<G, true, true>(&big[3]);
+  bool big[5] = {};
+  cudaError_t e = set_attributes<G, 0>(&big[0]);
+  if (e == cudaSuccess) e = set_attributes<G, kModeRope>(&big[1]);
+  if (e == cudaSuccess) e = set_attributes<G, kModeAdvance>(&big[2]);
+  if (e == cudaSuccess) e = set_attributes<G, kModeRope | kModeAdvance>(&big[3]);
+  if (e == cudaSuccess) e = set_attributes<G, kModeWindow>(&big[4]);
   if (e != cudaSuccess) return e;
-  const bool big_all = big[0] && big[1] && big[2] && big[3];
+  const bool big_all = big[0] && big[1] && big[2] && big[3] && big[4];
   // How many clusters of each size can run at once (a cluster stays within
-  // one GPC, so this is set by the SMs per GPC, not by the SM count).  Both
+  // one GPC, so this is set by the SMs per GPC, not by the SM count).  All
   // variants have the same block, shared memory and register cap, so the
-  // plain one stands for both.
+  // plain one stands for all.
   for (int c = 2; c <= kMaxCluster; ++c)
     d.clusters[G][c] = (c <= 8 || big_all) ? max_clusters<G>(c) : 0;
   d.configured[G] = true;
   return cudaSuccess;
 }
 
-template <int G, bool R, bool A>
+template <int G, int M>
 cudaError_t launch_g(const Params& p, cudaStream_t stream) {
   int dev = 0;
   DevInfo& d = dev_info(&dev);
@@ -1210,20 +1235,27 @@ cudaError_t launch_g(const Params& p, cudaStream_t stream) {
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    e = cudaLaunchKernelEx(&cfg, decode_cluster_kernel<G, R, A>, p);
+    e = cudaLaunchKernelEx(&cfg, decode_cluster_kernel<G, M>, p);
     return e != cudaSuccess ? e : cudaGetLastError();
   }
-  return launch_pdl(decode_splitkv_kernel<G, R, A>, dim3(min(kMaxGrid, d.num_sms)),
+  return launch_pdl(decode_splitkv_kernel<G, M>, dim3(min(kMaxGrid, d.num_sms)),
                     dim3(Cfg<G>::kThreads), smem_bytes<G>(p.B), stream, p);
 }
 
-// The variant for this launch: rotary embedding (R) and position advance (A)
-// are compile-time, so the plain kernels carry neither.
+// The variant for this launch.  The entry points use five combinations:
+// plain, rotation, advance, rotation + advance, and the local window alone.
 template <int G>
 cudaError_t launch_group(const Params& p, cudaStream_t stream) {
-  const bool rope = p.rope_cos != nullptr, adv = p.advance != nullptr;
-  if (rope) return adv ? launch_g<G, true, true>(p, stream) : launch_g<G, true, false>(p, stream);
-  return adv ? launch_g<G, false, true>(p, stream) : launch_g<G, false, false>(p, stream);
+  const int mode = (p.rope_cos != nullptr ? kModeRope : 0) |
+                   (p.advance != nullptr ? kModeAdvance : 0) | (p.window > 0 ? kModeWindow : 0);
+  switch (mode) {
+    case 0: return launch_g<G, 0>(p, stream);
+    case kModeRope: return launch_g<G, kModeRope>(p, stream);
+    case kModeAdvance: return launch_g<G, kModeAdvance>(p, stream);
+    case kModeRope | kModeAdvance: return launch_g<G, kModeRope | kModeAdvance>(p, stream);
+    case kModeWindow: return launch_g<G, kModeWindow>(p, stream);
+  }
+  return cudaErrorInvalidValue;  // a combination no entry point makes
 }
 
 }  // namespace

@@ -28,6 +28,7 @@ struct DecodeParams {
   int32_t* advance;       // the positions array, to add 1 to after the step, or null
   uint32_t* ticket;       // grid-wide arrival counter for the advance
   int rope_by_pos;
+  int window;             // 0: rows 0..pos; W > 0: rows max(0, pos-W+1)..pos
   int B, Hq, Hkv, L;
   float qscale;  // scale * log2(e)
 };

@@ -25,12 +25,12 @@ DecodeWorkspace decode_workspace_layout(int B, int Hq, int Hkv, int D);
 // are first rotated by the rotary embedding: row b of [B, D] tables, or
 // (rope_by_pos) row positions[b] of [L, D] tables.  advance non-null (the
 // positions array itself): every position is incremented once the step has
-// read them all.
+// read them all.  window > 0: attend only rows max(0, pos-window+1)..pos.
 cudaError_t launch_decode(const void* q, const void* k_new, const void* v_new,
                           const float* rope_cos, const float* rope_sin, bool rope_by_pos,
                           const int32_t* positions, int32_t* advance, const void* k_cache,
-                          const void* v_cache, int B, int Hq, int Hkv, int L, int D, float scale,
-                          void* out, void* workspace, cudaStream_t stream);
+                          const void* v_cache, int B, int Hq, int Hkv, int L, int D, int window,
+                          float scale, void* out, void* workspace, cudaStream_t stream);
 
 // Allocation-free decode: scratch in a fixed device array (decode.cu).
 size_t noalloc_scratch_bytes();

@@ -172,6 +172,30 @@ int attn_decode_step_rope_append(const void* q, const void* k_new, const void* v
                                  cudaStream_t stream);
 
 /*
+ * attn_decode_step_window -- decode attention over a local window: each
+ * sequence attends only its last `window` cache rows up to its position,
+ *     rows max(0, positions[b] - window + 1) .. positions[b] inclusive,
+ * so the current token is always included.  The decode pages name the
+ * variant without defining it; this reading takes the W most recent rows.
+ * Rows outside the window are never read.  The cost of a step follows
+ * min(window, positions[b] + 1), not the position.
+ *
+ *   k_new, v_new : [B, Hkv, D] bf16 rows to append at positions[b] first
+ *                  (as attn_decode_step_append), or both null to attend only
+ *                  (as attn_decode_step).
+ *   window       : > 0; window >= positions[b] + 1 is the full decode.
+ *   all other arguments, sizes and errors: as attn_decode_step_append.
+ *
+ * Errors: ATTN_ERR_INVALID_ARG also for window <= 0, or for exactly one of
+ * k_new and v_new null.
+ */
+int attn_decode_step_window(const void* q, const void* k_new, const void* v_new,
+                            const int32_t* positions, void* k_cache, void* v_cache,
+                            int B, int Hq, int Hkv, int L, int D, int window, float scale,
+                            void* out, void* workspace, size_t workspace_bytes,
+                            cudaStream_t stream);
+
+/*
  * attn_decode_stream_step -- one step of a streaming decode loop that a CUDA
  * graph can capture once and replay unchanged.  It performs the fused step of
  * attn_decode_step_append (preceded by the rotary embedding of

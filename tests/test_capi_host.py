@@ -39,7 +39,7 @@ def test_header_declares_the_boundary():
                  "attn_prefill_causal", "attn_read_device_status", "attn_status_string",
                  "attn_last_cuda_error", "attn_decode_step_append",
                  "attn_decode_step_rope_append", "attn_decode_step_noalloc",
-                 "attn_decode_stream_step"]:
+                 "attn_decode_stream_step", "attn_decode_step_window"]:
         assert want in names
 
 
@@ -110,6 +110,17 @@ def test_host_validation_happens_before_any_launch(lib):
     assert stream(P, P, P, None, None, P, P, P, 1, 16, 8, 16, 96, 1.0, P, P, 1 << 20, None) == 2
     assert stream(P, P, P, None, None, P, P, P, 1, 16, 8, 16, 128, 1.0, P, None, need,
                   None) == 3
+    assert stream(P, None, None, None, None, P, P, P, 1, 16, 8, 16, 128, 1.0, P, P, need,
+                  None) == 1
+    # local window: window > 0, new rows both or neither
+    win = lib.attn_decode_step_window
+    assert win(P, None, None, P, P, P, 1, 16, 8, 16, 128, 0, 1.0, P, P, need, None) == 1
+    assert win(P, P, None, P, P, P, 1, 16, 8, 16, 128, 4, 1.0, P, P, need, None) == 1
+    assert win(P, None, None, P, P, P, 1, 32, 2, 16, 128, 4, 1.0, P, P, need, None) == 2
+    assert win(P, None, None, P, P, P, 1, 16, 8, 16, 128, 4, 1.0, P, P, need - 1, None) == 3
+    # the append entry points still refuse missing new rows
+    assert lib.attn_decode_step_append(P, None, None, P, P, P, 1, 16, 8, 16, 128, 1.0, P, P,
+                                       need, None) == 1
 
 
 def test_binding_rejects_cpu_tensors():
