@@ -17,7 +17,9 @@ and for the rotary embedding: a hand-worked rotation, the identity at angle
 0, norm preservation, and dot products that depend only on the position
 difference; for the local window: a window of one returning V[pos], any
 window of pos + 1 or more equal to the full decode, and the windowed decode
-equal to the full decode of the shifted slice.
+equal to the full decode of the shifted slice; for multi-token decode: one
+token equal to the decode, and a sequence's tokens equal to a prefill over
+its cache rows from their first position.
 """
 
 from .attention import (  # noqa: F401
@@ -34,4 +36,5 @@ from .attention import (  # noqa: F401
     round_bf16,
     decode_rope_step,
     decode_window,
+    decode_multi,
 )

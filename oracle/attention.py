@@ -191,6 +191,31 @@ def decode_window(q, k_cache, v_cache, positions, scale, window):
     return out
 
 
+# --- multi-token decode --------------------------------------------------------
+#
+# S new tokens per sequence (e.g. draft tokens to verify): token t of
+# sequence b sits at position positions[b] + t and attends cache rows
+# 0 .. positions[b] + t (its own row included, later new tokens not).  The
+# cache already holds the S new rows.
+
+def decode_multi(q, k_cache, v_cache, positions, scale):
+    """q [B, S, Hq, D]; caches [B, Hkv, L, D] holding rows up to
+    positions[b] + S - 1.  Returns out [B, S, Hq, D] float64."""
+    B, S, Hq, D = q.shape
+    Hkv = k_cache.shape[1]
+    g = Hq // Hkv
+    out = np.empty((B, S, Hq, D), dtype=np.float64)
+    for b in range(B):
+        for t in range(S):
+            idx = list(_attended_rows(int(positions[b]) + t))
+            for h in range(Hq):
+                kvh = _kv_head(h, g, Hkv)
+                K = np.asarray(k_cache[b, kvh, idx, :], dtype=np.float64)
+                V = np.asarray(v_cache[b, kvh, idx, :], dtype=np.float64)
+                out[b, t, h] = _attend(np.asarray(q[b, t, h], dtype=np.float64), K, V, scale)
+    return out
+
+
 # --- rotary position embedding (decode page, section 4.1) --------------------
 #
 # The decode page rotates q and the new k with apply_rotary_pos_emb(q, k,

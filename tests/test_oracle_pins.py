@@ -468,3 +468,44 @@ def test_window_pin_catches_an_off_by_one():
     finally:
         oatt._window_rows = saved
     assert np.abs(good - bad).max() > 1e-3
+
+
+# ------------------------------------------------------- multi-token decode ---
+
+def test_multi_token_one_token_is_decode():
+    rng = np.random.default_rng(41)
+    B, Hq, Hkv, D, L = 2, 8, 2, 16, 50
+    q = _rand(rng, (B, 1, Hq, D))
+    kc, vc = _rand(rng, (B, Hkv, L, D)), _rand(rng, (B, Hkv, L, D))
+    pos = [0, 37]
+    np.testing.assert_allclose(oracle.decode_multi(q, kc, vc, pos, 0.3)[:, 0],
+                               oracle.decode(q[:, 0], kc, vc, pos, 0.3), rtol=1e-13, atol=1e-14)
+
+
+def test_multi_token_equals_prefill_over_the_cache():
+    """Sequence b's S tokens at positions p..p+S-1 are a causal prefill of S
+    tokens with start_pos = p over the cache rows 0..p+S-1 (token-major)."""
+    rng = np.random.default_rng(42)
+    B, S, Hq, Hkv, D, L = 3, 4, 8, 2, 16, 60
+    q = _rand(rng, (B, S, Hq, D))
+    kc, vc = _rand(rng, (B, Hkv, L, D)), _rand(rng, (B, Hkv, L, D))
+    pos = [0, 9, 56]
+    got = oracle.decode_multi(q, kc, vc, pos, 0.25)
+    for b, p in enumerate(pos):
+        k_tok = kc[b, :, : p + S].transpose(1, 0, 2)  # [T, Hkv, D]
+        v_tok = vc[b, :, : p + S].transpose(1, 0, 2)
+        want = oracle.prefill(q[b], k_tok, v_tok, p, 0.25)
+        np.testing.assert_allclose(got[b], want, rtol=1e-13, atol=1e-14)
+
+
+def test_multi_token_matches_brute_force():
+    rng = np.random.default_rng(43)
+    B, S, Hq, Hkv, D, L = 2, 3, 4, 2, 8, 12
+    q = _rand(rng, (B, S, Hq, D))
+    kc, vc = _rand(rng, (B, Hkv, L, D)), _rand(rng, (B, Hkv, L, D))
+    pos = [0, 8]
+    got = oracle.decode_multi(q, kc, vc, pos, 0.5)
+    for t in range(S):
+        want = np.array(brute.decode(q[:, t].tolist(), kc.tolist(), vc.tolist(),
+                                     [p + t for p in pos], 0.5))
+        np.testing.assert_allclose(got[:, t], want, rtol=1e-12, atol=1e-12)
