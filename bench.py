@@ -13,7 +13,8 @@ q and out) / device time of the step, in GB/s; `steps_per_s` is decode steps
 per second.  Extra legs: per-position decode time (warm and cold L2), the
 ragged B=64 batch, the B=256 g=8 stress batch, the ragged batch as a fused
 append step with and without the rotary embedding, the ragged batch over a
-1024-row local window, and the causal prefill
+1024-row local window and with two new tokens per sequence, and the causal
+prefill
 workloads (TFLOP/s; also GQA prompt chunks at d_head=128), each against its
 roofline.  The cross-checks time the
 same 8192 positions as separate append/decode launches, as decode launches
@@ -567,6 +568,33 @@ def _window_leg(torch, ga, synth, name, flush, hbm, window):
     return r
 
 
+def _multi_leg(torch, ga, synth, name, flush, hbm, S):
+    """Multi-token decode on a decode workload: S new tokens per sequence
+    (q and out [B, S, Hq, D], the tokens' rows already in the cache).
+    Algorithmic bytes: K and V rows 0 .. pos + S - 1, plus q and out."""
+    import oracle
+    case = synth.generators.workload_case(name, seed=0, device="cuda")
+    B, Hq, Dd = case.q.shape
+    Hkv, Ll = case.k_cache.shape[1], case.k_cache.shape[2]
+    pos = torch.clamp(case.positions, max=Ll - S).contiguous()
+    q = torch.randn(B, S, Hq, Dd, device="cuda").to(torch.bfloat16)
+    ws = ga.decode_workspace(B, S * Hq, Hkv, Ll, Dd)
+    out = torch.empty_like(q)
+
+    def one():
+        ga.attn_decode_multi(q, pos, case.k_cache, case.v_cache, case.scale, out=out,
+                             workspace=ws)
+    ms = statistics.median(_time_graph(torch, one, flush, 10, 3))
+    last = [int(p) + S - 1 for p in pos.cpu().tolist()]
+    nb = oracle.decode_bytes(last, Hq, Hkv, Dd) + 2 * (S - 1) * B * Hq * Dd * 2
+    r = {"us": round(ms * 1e3, 2), "GBs": round(nb / (ms * 1e-3) / 1e9, 1),
+         "frac_hbm": round(nb / (ms * 1e-3) / 1e9 / hbm, 3), "bytes": nb, "S": S,
+         "shape": {"B": B, "Hq": Hq, "Hkv": Hkv, "D": Dd, "L": Ll}}
+    del case, ws, out, q
+    torch.cuda.empty_cache()
+    return r
+
+
 def _prefill_leg(torch, ga, synth, name, flush, tflops_peak):
     import oracle
     case = synth.generators.workload_case(name, seed=0, device="cuda")
@@ -727,6 +755,7 @@ def run_ours(args):
         legs["ragged_rope_append"] = _append_leg(torch, ga, synth, "ragged", flush, hbm,
                                                  rope=True)
         legs["ragged_window1024"] = _window_leg(torch, ga, synth, "ragged", flush, hbm, 1024)
+        legs["ragged_multi_s2"] = _multi_leg(torch, ga, synth, "ragged", flush, hbm, 2)
         for name in ("prefill_prefix", "prefill", "prefill_d128_chunk", "prefill_d128"):
             legs[name] = _prefill_leg(torch, ga, synth, name, flush, tf_burst)
         line["legs"] = legs

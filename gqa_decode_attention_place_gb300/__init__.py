@@ -23,7 +23,7 @@ __all__ = [
     "attn_prefill_causal", "attn_read_device_status", "attn_status_string",
     "attn_last_cuda_error", "decode_workspace", "attn_decode_step_noalloc",
     "attn_decode_step_append", "attn_decode_step_rope_append", "attn_decode_stream_step",
-    "attn_decode_step_window",
+    "attn_decode_step_window", "attn_decode_multi",
 ]
 
 ATTN_OK = 0
@@ -75,6 +75,9 @@ def load_library(build_if_missing: bool = True) -> ctypes.CDLL:
     lib.attn_decode_step_window.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32,
                                             f32, vp, vp, sz, vp]
     lib.attn_decode_step_window.restype = i32
+    lib.attn_decode_multi.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, f32,
+                                      vp, vp, sz, vp]
+    lib.attn_decode_multi.restype = i32
     lib.attn_decode_step_noalloc.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, i32, f32, vp, vp]
     lib.attn_decode_step_noalloc.restype = i32
     lib.attn_prefill_causal.argtypes = [vp, vp, vp, i32, i32, i32, i32, i32, f32, vp, vp]
@@ -292,6 +295,44 @@ def attn_decode_step_window(q, positions, k_cache, v_cache, scale: float, window
         v_cache.data_ptr(), B, Hq, Hkv, L, D, int(window), float(scale), out.data_ptr(),
         workspace.data_ptr(), workspace.numel() * workspace.element_size(), _stream(stream))
     _raise(code, "attn_decode_step_window")
+    return out
+
+
+def attn_decode_multi(q, positions, k_cache, v_cache, scale: float, k_new=None, v_new=None,
+                      out=None, workspace=None, stream=None) -> torch.Tensor:
+    """S new tokens per sequence: q [B, S, Hq, D]; token t at positions[b] + t
+    attends rows 0 .. positions[b] + t.  k_new/v_new [B, S, Hkv, D], if given,
+    are appended first.  Returns out [B, S, Hq, D]."""
+    _check(q, "q", torch.bfloat16, 4)
+    _check(positions, "positions", torch.int32, 1)
+    for t, n in ((k_cache, "k_cache"), (v_cache, "v_cache")):
+        _check(t, n, torch.bfloat16, 4)
+    if (k_new is None) != (v_new is None):
+        raise ValueError("attn_decode_multi: give both k_new and v_new, or neither")
+    B, S, Hq, D = q.shape
+    Hkv, L = k_cache.shape[1], k_cache.shape[2]
+    if tuple(v_cache.shape) != tuple(k_cache.shape) or k_cache.shape[0] != B or \
+            k_cache.shape[3] != D or positions.shape[0] != B:
+        raise ValueError("attn_decode_multi: inconsistent shapes")
+    if k_new is not None:
+        for t, n in ((k_new, "k_new"), (v_new, "v_new")):
+            _check(t, n, torch.bfloat16, 4)
+            if tuple(t.shape) != (B, S, Hkv, D):
+                raise ValueError(f"attn_decode_multi: {n} must be [B, S, Hkv, D]")
+    if out is None:
+        out = torch.empty_like(q)
+    else:
+        _check(out, "out", torch.bfloat16, 4)
+        if tuple(out.shape) != (B, S, Hq, D):
+            raise ValueError("attn_decode_multi: out has the wrong shape")
+    if workspace is None:
+        workspace = decode_workspace(B, S * Hq, Hkv, L, D, device=q.device)
+    ptr = lambda t: t.data_ptr() if t is not None else None
+    code = load_library().attn_decode_multi(
+        q.data_ptr(), ptr(k_new), ptr(v_new), positions.data_ptr(), k_cache.data_ptr(),
+        v_cache.data_ptr(), B, S, Hq, Hkv, L, D, float(scale), out.data_ptr(),
+        workspace.data_ptr(), workspace.numel() * workspace.element_size(), _stream(stream))
+    _raise(code, "attn_decode_multi")
     return out
 
 

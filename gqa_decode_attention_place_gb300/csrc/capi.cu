@@ -121,6 +121,33 @@ int attn_decode_step_window(const void* q, const void* k_new, const void* v_new,
                        window);
 }
 
+int attn_decode_multi(const void* q, const void* k_new, const void* v_new,
+                      const int32_t* positions, void* k_cache, void* v_cache, int B, int S,
+                      int Hq, int Hkv, int L, int D, float scale, void* out, void* workspace,
+                      size_t workspace_bytes, cudaStream_t stream) {
+  if (!q || !positions || !k_cache || !v_cache || !out || !k_new != !v_new)
+    return ATTN_ERR_INVALID_ARG;
+  if (B <= 0 || S <= 0 || Hq <= 0 || Hkv <= 0 || L <= 0 || D <= 0 || Hq % Hkv != 0)
+    return ATTN_ERR_INVALID_ARG;
+  if (!aligned16(q) || (k_new && (!aligned16(k_new) || !aligned16(v_new))) ||
+      !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out) ||
+      (reinterpret_cast<uintptr_t>(positions) & 3u))
+    return ATTN_ERR_INVALID_ARG;
+  if ((long long)S * Hq > 65536 || !gqa::decode_supported(B, S * Hq, Hkv, L, D))
+    return ATTN_ERR_UNSUPPORTED;  // S * g must be 1, 2, 4 or 8
+  if (!workspace || !aligned16(workspace) ||
+      workspace_bytes < gqa::decode_workspace_layout(B, S * Hq, Hkv, D).total)
+    return ATTN_ERR_WORKSPACE;
+  if (k_new) {
+    const int st = cuda_status(gqa::launch_kv_append(k_new, v_new, positions, k_cache, v_cache, B,
+                                                     Hkv, L, D, stream, S));
+    if (st != ATTN_OK) return st;
+  }
+  return cuda_status(gqa::launch_decode(q, nullptr, nullptr, nullptr, nullptr, false, positions,
+                                        nullptr, k_cache, v_cache, B, Hq, Hkv, L, D, 0, scale,
+                                        out, workspace, stream, S));
+}
+
 int attn_decode_stream_step(const void* q, const void* k_new, const void* v_new,
                             const float* cos_table, const float* sin_table, int32_t* positions,
                             void* k_cache, void* v_cache, int B, int Hq, int Hkv, int L, int D,

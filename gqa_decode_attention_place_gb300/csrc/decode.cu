@@ -35,8 +35,8 @@ cudaError_t launch_decode(const void* q, const void* k_new, const void* v_new,
                           const float* rope_cos, const float* rope_sin, bool rope_by_pos,
                           const int32_t* positions, int32_t* advance, const void* k_cache,
                           const void* v_cache, int B, int Hq, int Hkv, int L, int D, int window,
-                          float scale, void* out, void* workspace, cudaStream_t stream) {
-  const DecodeWorkspace ws = decode_workspace_layout(B, Hq, Hkv, D);
+                          float scale, void* out, void* workspace, cudaStream_t stream, int S) {
+  const DecodeWorkspace ws = decode_workspace_layout(B, S * Hq, Hkv, D);
   uint8_t* base = static_cast<uint8_t*>(workspace);
   DecodeParams p;
   p.q = static_cast<const uint16_t*>(q);
@@ -54,6 +54,7 @@ cudaError_t launch_decode(const void* q, const void* k_new, const void* v_new,
   p.rope_sin = rope_sin;
   p.rope_by_pos = rope_by_pos ? 1 : 0;
   p.window = window;
+  p.S = S;
   p.advance = advance;
   p.ticket = reinterpret_cast<uint32_t*>(base + ws.ticket_off);
   p.B = B;
@@ -61,7 +62,7 @@ cudaError_t launch_decode(const void* q, const void* k_new, const void* v_new,
   p.Hkv = Hkv;
   p.L = L;
   p.qscale = scale * 1.4426950408889634f;  // scale * log2(e)
-  switch (Hq / Hkv) {
+  switch (S * Hq / Hkv) {  // the kernel's heads per KV head: S tokens x g
     case 1: return launch_decode_group1(p, stream);
     case 2: return launch_decode_group2(p, stream);
     case 4: return launch_decode_group4(p, stream);

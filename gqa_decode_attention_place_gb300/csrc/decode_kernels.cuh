@@ -81,6 +81,17 @@ using Params = DecodeParams;
 constexpr int kModeRope = 1;     // rotary embedding of q and the new key
 constexpr int kModeAdvance = 2;  // positions += 1 after the step
 constexpr int kModeWindow = 4;   // attend only the last p.window rows
+constexpr int kModeMulti = 8;    // p.S new tokens per sequence (see head_row)
+
+// Multi-token decode: the kernel's G "heads" of a KV head are p.S new tokens
+// x g query heads (h = t*g + j), q and out are [B, S, Hq, D], token t sits at
+// positions[b] + t and attends rows up to there.  Row of q/out for head h:
+template <int G, bool MT>
+__device__ __forceinline__ size_t head_row(const DecodeParams& p, int b, int kvh, int h) {
+  if (!MT) return (size_t)b * p.Hq + (size_t)kvh * G + h;
+  const int gr = G / p.S;
+  return ((size_t)b * p.S + h / gr) * p.Hq + (size_t)kvh * gr + h % gr;
+}
 
 // Lanes per key (LPK): a key's 128 dims are spread over LPK lanes of a warp
 // (128/LPK dims each), so a warp takes 32/LPK keys per step.  Fewer lanes
@@ -153,7 +164,8 @@ struct Walk {
 };
 
 __device__ __forceinline__ void walk_init(Walk& w, long long t, const int* prefix,
-                                          const int32_t* positions, int B, int Hkv, int window) {
+                                          const int32_t* positions, int B, int Hkv, int window,
+                                          int shift) {
   int lo = 0, hi = B - 1;  // largest b with Hkv*prefix[b] <= t
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
@@ -164,11 +176,11 @@ __device__ __forceinline__ void walk_init(Walk& w, long long t, const int* prefi
   const long long off = t - (long long)Hkv * prefix[lo];
   w.kvh = (int)(off / w.ntiles);
   w.k = (int)(off % w.ntiles);
-  attended_rows(positions[lo], window, w.lo, w.n);
+  attended_rows(positions[lo] + shift, window, w.lo, w.n);
 }
 
 __device__ __forceinline__ void walk_next(Walk& w, const int* prefix, const int32_t* positions,
-                                          int B, int Hkv, int window) {
+                                          int B, int Hkv, int window, int shift) {
   if (++w.k < w.ntiles) return;
   w.k = 0;
   if (++w.kvh < Hkv) return;
@@ -176,7 +188,7 @@ __device__ __forceinline__ void walk_next(Walk& w, const int* prefix, const int3
   do { ++w.b; } while (w.b < B && prefix[w.b + 1] == prefix[w.b]);
   if (w.b < B) {
     w.ntiles = prefix[w.b + 1] - prefix[w.b];
-    attended_rows(positions[w.b], window, w.lo, w.n);
+    attended_rows(positions[w.b] + shift, window, w.lo, w.n);
   }
 }
 
@@ -255,6 +267,7 @@ struct Consumer {
   f2 o[G][NP];   // unnormalised output accumulators, same layout
   float m_run, l_run;  // for head hd (the same in every key group)
   int grp, lk, hd;
+  int head_last;       // multi-token decode: last row head hd's token may see
 
   __device__ __forceinline__ void init(int lane) {
     grp = lane >> LL;
@@ -262,14 +275,16 @@ struct Consumer {
     hd = lk >> (LL - LG);  // head whose score this lane ends up with
   }
   __device__ __forceinline__ int dim_off(int v) const { return (lk + LPK * v) * 16; }  // bytes
-  // qb: q[b][kvh*G][0]
-  __device__ __forceinline__ void load_q(const uint16_t* qb, float qscale) {
+  // the G query rows of KV head kvh of sequence b (head_row)
+  template <bool MT>
+  __device__ __forceinline__ void load_q(const DecodeParams& p, int b, int kvh, float qscale) {
 #pragma unroll
     for (int h = 0; h < G; ++h)
 #pragma unroll
       for (int v = 0; v < VPL; ++v) {
         const uint4 u = *reinterpret_cast<const uint4*>(
-            reinterpret_cast<const uint8_t*>(qb + (size_t)h * kD) + dim_off(v));
+            reinterpret_cast<const uint8_t*>(p.q + head_row<G, MT>(p, b, kvh, h) * kD) +
+            dim_off(v));
         const uint32_t wd[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
         for (int j = 0; j < 4; ++j)
@@ -301,6 +316,8 @@ struct Consumer {
   }
   // Scores (log2 domain) of this warp's keys of a tile; keys >= rows
   // are invalid (the rest of the stage may hold anything) and get -inf.
+  // rows: keys of the tile this lane's head may see (all valid rows, or fewer
+  // for an early token of a multi-token step)
   __device__ __forceinline__ void qk(const uint8_t* Ks, int rows, int warp, float (&sc)[IT]) {
 #pragma unroll
     for (int it = 0; it < IT; ++it) {
@@ -391,9 +408,10 @@ struct Consumer {
     }
   }
   // One tile: scores, online softmax, P.V.
-  __device__ __forceinline__ void tile(const uint8_t* Ks, const uint8_t* Vs, int rows, int warp) {
+  __device__ __forceinline__ void tile(const uint8_t* Ks, const uint8_t* Vs, int rows, int rows_h,
+                                       int warp) {
     float sc[IT], pr[IT];
-    qk(Ks, rows, warp, sc);
+    qk(Ks, rows_h, warp, sc);
     softmax(sc, pr);
     pv(Vs, rows, warp, pr);
   }
@@ -605,10 +623,12 @@ __device__ __forceinline__ void advance_ticket(const Params& p, int lane) {
   if (lane == 0) *p.ticket = 0u;
 }
 
-__device__ __forceinline__ void write_nan_rows(const Params& p, int b) {
+// NaN into every output row of sequence b (its S tokens' rows in
+// multi-token decode).
+__device__ __forceinline__ void write_nan_rows(const Params& p, int b, int S) {
   const uint4 nan4 = make_uint4(0x7fc07fc0u, 0x7fc07fc0u, 0x7fc07fc0u, 0x7fc07fc0u);
-  uint4* o4 = reinterpret_cast<uint4*>(p.out + (size_t)b * p.Hq * kD);
-  for (int i = 0; i < p.Hq * kD / 8; ++i) o4[i] = nan4;
+  uint4* o4 = reinterpret_cast<uint4*>(p.out + (size_t)b * S * p.Hq * kD);
+  for (int i = 0; i < S * p.Hq * kD / 8; ++i) o4[i] = nan4;
 }
 
 __device__ __forceinline__ void store_bf16(uint16_t* dst, float v) {
@@ -629,6 +649,7 @@ size_t smem_bytes(int B) {
 template <int G, int M>
 __global__ void __maxnreg__(Cfg<G>::kMaxRegs) decode_splitkv_kernel(const Params p) {
   constexpr bool R = (M & kModeRope) != 0, A = (M & kModeAdvance) != 0;
+  constexpr bool MT = (M & kModeMulti) != 0;
   constexpr int NW = Cfg<G>::NW;
   constexpr bool kProducer = Cfg<G>::kProducer;
   constexpr int KPW = Cfg<G>::kKeysPerWarp;
@@ -647,6 +668,7 @@ __global__ void __maxnreg__(Cfg<G>::kMaxRegs) decode_splitkv_kernel(const Params
   const int warp = tid >> 5, lane = tid & 31;
   const int B = p.B, Hkv = p.Hkv, L = p.L;
   const int win = (M & kModeWindow) ? p.window : 0;
+  const int shift = MT ? p.S - 1 : 0;  // positions[b] + shift: the last new token's row
   volatile int* abort_flag = misc;
 
   if (tid == 0) {
@@ -675,15 +697,15 @@ __global__ void __maxnreg__(Cfg<G>::kMaxRegs) decode_splitkv_kernel(const Params
     const int b = base + tid;
     int v = 0;
     if (tid < NC && b < B) {
-      const int pos = p.positions[b];
-      if (pos >= 0 && pos < L) {
+      const int pos = p.positions[b] + shift;
+      if (pos - shift >= 0 && pos < L) {
         int lo, n;
         attended_rows(pos, win, lo, n);
         v = (n - 1) / kTile + 1;  // ceil(n / kTile)
       } else if (b % gridDim.x == blockIdx.x) {
         // out-of-range position: flag it and make the sequence's output NaN
         set_status(p.status, ATTN_DEV_BAD_POSITION);
-        write_nan_rows(p, b);
+        write_nan_rows(p, b, MT ? p.S : 1);
       }
     }
     int x = v;
@@ -732,7 +754,7 @@ __global__ void __maxnreg__(Cfg<G>::kMaxRegs) decode_splitkv_kernel(const Params
     if (warp == NW) {
       if (lane == 0) {
         Walk w;
-        walk_init(w, t0, prefix, p.positions, B, Hkv, win);
+        walk_init(w, t0, prefix, p.positions, B, Hkv, win, shift);
         long long i = 0;
         for (long long t = t0; t < t1; ++t, ++i) {
           const int s = (int)(i % kStages);
@@ -744,7 +766,7 @@ __global__ void __maxnreg__(Cfg<G>::kMaxRegs) decode_splitkv_kernel(const Params
             break;
           }
           produce_tile(p, stages, bars, s, w.b, w.kvh, w.k, w.ntiles, w.n, w.lo);
-          walk_next(w, prefix, p.positions, B, Hkv, win);
+          walk_next(w, prefix, p.positions, B, Hkv, win, shift);
         }
         if (A) mbar_arrive(smem_u32(&bars[2 * kStages + 1]));  // no more reads of positions
       }
@@ -755,13 +777,13 @@ __global__ void __maxnreg__(Cfg<G>::kMaxRegs) decode_splitkv_kernel(const Params
     // stage refills it, so every warp is a consumer
     if (tid == 0) {
       Walk pw;
-      walk_init(pw, t0, prefix, p.positions, B, Hkv, win);
+      walk_init(pw, t0, prefix, p.positions, B, Hkv, win, shift);
       for (long long t = t0; t < t1 && t < t0 + kStages; ++t) {
         produce_tile(p, stages, bars, (int)(t - t0), pw.b, pw.kvh, pw.k, pw.ntiles, pw.n, pw.lo);
-        walk_next(pw, prefix, p.positions, B, Hkv, win);
+        walk_next(pw, prefix, p.positions, B, Hkv, win, shift);
       }
     }
-    if (t0 + kStages < t1) walk_init(ahead, t0 + kStages, prefix, p.positions, B, Hkv, win);
+    if (t0 + kStages < t1) walk_init(ahead, t0 + kStages, prefix, p.positions, B, Hkv, win, shift);
   }
 
   // ------------------------------------------------------------ consumers --
@@ -769,8 +791,9 @@ __global__ void __maxnreg__(Cfg<G>::kMaxRegs) decode_splitkv_kernel(const Params
   cs.init(lane);
   ConsumerSync csync{smem_u32(&bars[2 * kStages]), abort_flag, p.status, 0u};
   Walk w;
-  walk_init(w, t0, prefix, p.positions, B, Hkv, win);
+  walk_init(w, t0, prefix, p.positions, B, Hkv, win, shift);
   const uint16_t* qb = p.q + ((size_t)w.b * p.Hq + (size_t)w.kvh * G) * kD;
+  if (MT) cs.head_last = w.lo + w.n - 1 - shift + cs.hd / (G / p.S);
   if (R) {
     rope_segment<G, NC>(qb, rope_row<R>(p, p.rope_cos, w.b, w.lo + w.n - 1),
                         rope_row<R>(p, p.rope_sin, w.b, w.lo + w.n - 1), q_rot,
@@ -778,7 +801,7 @@ __global__ void __maxnreg__(Cfg<G>::kMaxRegs) decode_splitkv_kernel(const Params
     consumer_bar<NC>();  // before any tile wait: every consumer warp gets here
     cs.load_q_rot(q_rot, p.qscale);
   } else {
-    cs.load_q(qb, p.qscale);
+    cs.load_q<MT>(p, w.b, w.kvh, p.qscale);
   }
   cs.reset();
 
@@ -791,7 +814,8 @@ __global__ void __maxnreg__(Cfg<G>::kMaxRegs) decode_splitkv_kernel(const Params
     uint8_t* Ks = stages + (size_t)s * 2 * kTileBytes;
     if (p.k_new != nullptr && w.k == w.ntiles - 1 && warp == (rows - 1) / KPW)
       fresh_row<R>(p, Ks, rows, w.b, w.kvh, w.lo + w.n - 1, rope_cs, lane);
-    cs.tile(Ks, Ks + kTileBytes, rows, warp);
+    cs.tile(Ks, Ks + kTileBytes, rows,
+            MT ? min(rows, cs.head_last + 1 - (w.lo + w.k * kTile)) : rows, warp);
     __syncwarp();
     if constexpr (kProducer) {
       if (lane == 0) mbar_arrive(smem_u32(&bars[kStages + s]));
@@ -799,7 +823,7 @@ __global__ void __maxnreg__(Cfg<G>::kMaxRegs) decode_splitkv_kernel(const Params
       if (lane == 0 && last_to_release(rel, s, NW) && t + kStages < t1)
         produce_tile(p, stages, bars, s, ahead.b, ahead.kvh, ahead.k, ahead.ntiles, ahead.n,
                    ahead.lo);
-      if (t + kStages < t1) walk_next(ahead, prefix, p.positions, B, Hkv, win);
+      if (t + kStages < t1) walk_next(ahead, prefix, p.positions, B, Hkv, win, shift);
     }
     const bool seg_end = (w.k == w.ntiles - 1) || (t == t1 - 1);
 
@@ -814,13 +838,13 @@ __global__ void __maxnreg__(Cfg<G>::kMaxRegs) decode_splitkv_kernel(const Params
       csync(lane);
 
       const int slot = blockIdx.x + seg;
-      uint16_t* out_seg = p.out + ((size_t)w.b * p.Hq + (size_t)w.kvh * G) * kD;
+      const int ob = w.b, okvh = w.kvh;  // the segment whose output this is
       for (int idx = ct; idx < G * kD; idx += NC) {
         const int h = idx / kD, d = idx % kD;
         float M, Ls, Os;
         merge_warps<NW, G>(merge_o, merge_ml, h, d, M, Ls, Os);
         if (whole) {
-          store_bf16(out_seg + h * kD + d, Os / Ls);
+          store_bf16(p.out + head_row<G, MT>(p, ob, okvh, h) * kD + d, Os / Ls);
         } else {
           p.part_o[((size_t)slot * G + h) * kD + d] = Os;
           if (d == 0) {
@@ -881,7 +905,7 @@ __global__ void __maxnreg__(Cfg<G>::kMaxRegs) decode_splitkv_kernel(const Params
               }
               M = Mb;
             }
-            store_bf16(out_seg + h * kD + d, Os / Ls);
+            store_bf16(p.out + head_row<G, MT>(p, ob, okvh, h) * kD + d, Os / Ls);
           }
           if (ct == 0) p.counters[seg] = 0u;  // ready for the next launch
         }
@@ -889,7 +913,7 @@ __global__ void __maxnreg__(Cfg<G>::kMaxRegs) decode_splitkv_kernel(const Params
       csync(lane);  // merge buffers are free again
       cs.reset();
     }
-    walk_next(w, prefix, p.positions, B, Hkv, win);
+    walk_next(w, prefix, p.positions, B, Hkv, win, shift);
     if (w.k == 0 && t + 1 < t1) {
       // a new segment; every consumer has read q_rot and rope_cs of the last
       // one (seg_end's barriers came after), so they may be overwritten
@@ -901,8 +925,9 @@ __global__ void __maxnreg__(Cfg<G>::kMaxRegs) decode_splitkv_kernel(const Params
         csync(lane);
         cs.load_q_rot(q_rot, p.qscale);
       } else {
-        cs.load_q(qn, p.qscale);
+        cs.load_q<MT>(p, w.b, w.kvh, p.qscale);
       }
+      if (MT) cs.head_last = w.lo + w.n - 1 - shift + cs.hd / (G / p.S);
     }
   }
 
@@ -939,6 +964,7 @@ size_t cluster_smem_bytes() {
 template <int G, int M>
 __global__ void __maxnreg__(Cfg<G>::kMaxRegs) decode_cluster_kernel(const Params p) {
   constexpr bool R = (M & kModeRope) != 0, A = (M & kModeAdvance) != 0;
+  constexpr bool MT = (M & kModeMulti) != 0;
   constexpr int NW = Cfg<G>::NW;
   constexpr bool kProducer = Cfg<G>::kProducer;
   constexpr int KPW = Cfg<G>::kKeysPerWarp;
@@ -960,6 +986,7 @@ __global__ void __maxnreg__(Cfg<G>::kMaxRegs) decode_cluster_kernel(const Params
   const int seg = blockIdx.x / C;
   const int b = seg / p.Hkv, kvh = seg % p.Hkv;
   const int win = (M & kModeWindow) ? p.window : 0;
+  const int shift = MT ? p.S - 1 : 0;  // positions[b] + shift: the last new token's row
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
   volatile int* abort_flag = misc;
@@ -978,12 +1005,12 @@ __global__ void __maxnreg__(Cfg<G>::kMaxRegs) decode_cluster_kernel(const Params
   }
   grid_dependency_wait();
   grid_dependents_launch();
-  const int pos = p.positions[b];
-  if (pos < 0 || pos >= p.L) {
+  const int pos = p.positions[b] + shift;
+  if (pos - shift < 0 || pos >= p.L) {
     // the same for every CTA of the cluster: all leave, no cluster barrier
     if (rank == 0 && kvh == 0 && tid == 0) {
       set_status(p.status, ATTN_DEV_BAD_POSITION);
-      write_nan_rows(p, b);
+      write_nan_rows(p, b, MT ? p.S : 1);
     }
     if (A) {
       __syncthreads();  // every thread's read of positions is done
@@ -1037,8 +1064,9 @@ __global__ void __maxnreg__(Cfg<G>::kMaxRegs) decode_cluster_kernel(const Params
       consumer_bar<NC>();  // before any tile wait: every consumer warp gets here
       cs.load_q_rot(q_rot, p.qscale);
     } else {
-      cs.load_q(qb, p.qscale);
+      cs.load_q<MT>(p, b, kvh, p.qscale);
     }
+    if (MT) cs.head_last = pos - shift + cs.hd / (G / p.S);
     cs.reset();
     for (int k = k0; k < k1; ++k) {
       const int i = k - k0;
@@ -1050,7 +1078,8 @@ __global__ void __maxnreg__(Cfg<G>::kMaxRegs) decode_cluster_kernel(const Params
       uint8_t* Ks = stages + (size_t)s * 2 * kTileBytes;
       if (p.k_new != nullptr && k == ntiles - 1 && warp == (rows - 1) / KPW)
         fresh_row<R>(p, Ks, rows, b, kvh, pos, rope_cs, lane);
-      cs.tile(Ks, Ks + kTileBytes, rows, warp);
+      cs.tile(Ks, Ks + kTileBytes, rows,
+              MT ? min(rows, cs.head_last + 1 - (lo + k * kTile)) : rows, warp);
       __syncwarp();
       if constexpr (kProducer) {
         if (lane == 0) mbar_arrive(smem_u32(&bars[kStages + s]));
@@ -1104,13 +1133,12 @@ __global__ void __maxnreg__(Cfg<G>::kMaxRegs) decode_cluster_kernel(const Params
       if (in) wr[lane * G + h] = e / Ls;
     }
     __syncthreads();
-    uint16_t* out_seg = p.out + ((size_t)b * p.Hq + (size_t)kvh * G) * kD;
     for (int idx = tid; idx < G * kD; idx += blockDim.x) {
       const int h = idx / kD, d = idx % kD;
       float Os = 0.f;
 #pragma unroll 4
       for (int r = 0; r < C; ++r) Os = fmaf(land_o[(r * G + h) * kD + d], wr[r * G + h], Os);
-      store_bf16(out_seg + h * kD + d, Os);
+      store_bf16(p.out + head_row<G, MT>(p, b, kvh, h) * kD + d, Os);
     }
   }
   // no second cluster barrier: no CTA reads another's shared memory any more
@@ -1190,14 +1218,15 @@ cudaError_t set_attributes(bool* big) {
 template <int G>
 cudaError_t configure(DevInfo& d) {
   if (d.configured[G]) return cudaSuccess;
-  bool big[5] = {};
+  bool big[6] = {};
   cudaError_t e = set_attributes<G, 0>(&big[0]);
   if (e == cudaSuccess) e = set_attributes<G, kModeRope>(&big[1]);
   if (e == cudaSuccess) e = set_attributes<G, kModeAdvance>(&big[2]);
   if (e == cudaSuccess) e = set_attributes<G, kModeRope | kModeAdvance>(&big[3]);
   if (e == cudaSuccess) e = set_attributes<G, kModeWindow>(&big[4]);
+  if (e == cudaSuccess) e = set_attributes<G, kModeMulti>(&big[5]);
   if (e != cudaSuccess) return e;
-  const bool big_all = big[0] && big[1] && big[2] && big[3] && big[4];
+  const bool big_all = big[0] && big[1] && big[2] && big[3] && big[4] && big[5];
   // How many clusters of each size can run at once (a cluster stays within
   // one GPC, so this is set by the SMs per GPC, not by the SM count).  All
   // variants have the same block, shared memory and register cap, so the
@@ -1242,18 +1271,21 @@ cudaError_t launch_g(const Params& p, cudaStream_t stream) {
                     dim3(Cfg<G>::kThreads), smem_bytes<G>(p.B), stream, p);
 }
 
-// The variant for this launch.  The entry points use five combinations:
-// plain, rotation, advance, rotation + advance, and the local window alone.
+// The variant for this launch.  The entry points use six combinations:
+// plain, rotation, advance, rotation + advance, and the local window and the
+// multi-token step alone.
 template <int G>
 cudaError_t launch_group(const Params& p, cudaStream_t stream) {
   const int mode = (p.rope_cos != nullptr ? kModeRope : 0) |
-                   (p.advance != nullptr ? kModeAdvance : 0) | (p.window > 0 ? kModeWindow : 0);
+                   (p.advance != nullptr ? kModeAdvance : 0) | (p.window > 0 ? kModeWindow : 0) |
+                   (p.S > 1 ? kModeMulti : 0);
   switch (mode) {
     case 0: return launch_g<G, 0>(p, stream);
     case kModeRope: return launch_g<G, kModeRope>(p, stream);
     case kModeAdvance: return launch_g<G, kModeAdvance>(p, stream);
     case kModeRope | kModeAdvance: return launch_g<G, kModeRope | kModeAdvance>(p, stream);
     case kModeWindow: return launch_g<G, kModeWindow>(p, stream);
+    case kModeMulti: return launch_g<G, kModeMulti>(p, stream);
   }
   return cudaErrorInvalidValue;  // a combination no entry point makes
 }

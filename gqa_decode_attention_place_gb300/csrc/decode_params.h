@@ -29,6 +29,7 @@ struct DecodeParams {
   uint32_t* ticket;       // grid-wide arrival counter for the advance
   int rope_by_pos;
   int window;             // 0: rows 0..pos; W > 0: rows max(0, pos-W+1)..pos
+  int S;                  // new tokens per sequence (1; > 1: multi-token decode)
   int B, Hq, Hkv, L;
   float qscale;  // scale * log2(e)
 };

@@ -8,9 +8,10 @@
 
 namespace gqa {
 
+// S rows per sequence (k_new [B, S, Hkv, D]) at positions[b] .. + S - 1.
 cudaError_t launch_kv_append(const void* k_new, const void* v_new, const int32_t* positions,
                              void* k_cache, void* v_cache, int B, int Hkv, int L, int D,
-                             cudaStream_t stream);
+                             cudaStream_t stream, int S = 1);
 
 // Decode workspace layout (bytes), shared by the size query and the launcher.
 struct DecodeWorkspace {
@@ -26,11 +27,14 @@ DecodeWorkspace decode_workspace_layout(int B, int Hq, int Hkv, int D);
 // (rope_by_pos) row positions[b] of [L, D] tables.  advance non-null (the
 // positions array itself): every position is incremented once the step has
 // read them all.  window > 0: attend only rows max(0, pos-window+1)..pos.
+// S > 1: multi-token decode (q and out [B, S, Hq, D], token t at
+// positions[b] + t; the workspace is laid out for S * Hq heads).
 cudaError_t launch_decode(const void* q, const void* k_new, const void* v_new,
                           const float* rope_cos, const float* rope_sin, bool rope_by_pos,
                           const int32_t* positions, int32_t* advance, const void* k_cache,
                           const void* v_cache, int B, int Hq, int Hkv, int L, int D, int window,
-                          float scale, void* out, void* workspace, cudaStream_t stream);
+                          float scale, void* out, void* workspace, cudaStream_t stream,
+                          int S = 1);
 
 // Allocation-free decode: scratch in a fixed device array (decode.cu).
 size_t noalloc_scratch_bytes();

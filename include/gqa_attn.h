@@ -196,6 +196,40 @@ int attn_decode_step_window(const void* q, const void* k_new, const void* v_new,
                             cudaStream_t stream);
 
 /*
+ * attn_decode_multi -- multi-token decode: S new tokens per sequence (for
+ * example draft tokens to verify) in one launch.  Token t of sequence b sits
+ * at position positions[b] + t and attends cache rows
+ * 0 .. positions[b] + t: the earlier new tokens and itself, not the later
+ * ones.  Each KV byte is read once for all S tokens and g query heads of its
+ * KV head.  This is the decode page's step for several tokens at once.  The
+ * causal rule for the new block is the prefill page's, aligned to the
+ * bottom-right corner.
+ *
+ *   q            : [B, S, Hq, D] bf16.
+ *   k_new, v_new : [B, S, Hkv, D] bf16, appended first at rows
+ *                  positions[b] .. positions[b] + S - 1 (a separate launch
+ *                  ahead of the attention); or both null when the cache
+ *                  already holds them.
+ *   positions    : [B] int32, device memory: the first new token's position.
+ *   out          : [B, S, Hq, D] bf16.
+ *   workspace    : at least attn_decode_workspace_size(B, S * Hq, Hkv, L, D)
+ *                  bytes, zero-filled before first use.
+ *   Supported: D == 128; S * g in {1, 2, 4, 8}; other limits as
+ *   attn_decode_step.  S == 1 is attn_decode_step (after the append).
+ *
+ * A sequence whose positions[b] + S - 1 falls outside [0, L) gets NaN in all
+ * of its output rows, no cache write, and ATTN_DEV_BAD_POSITION.
+ * Errors: ATTN_ERR_INVALID_ARG for null or misaligned pointers, exactly one
+ * of k_new and v_new null, or non-positive sizes; ATTN_ERR_UNSUPPORTED when
+ * S * g is not 1, 2, 4 or 8; ATTN_ERR_WORKSPACE as above.
+ */
+int attn_decode_multi(const void* q, const void* k_new, const void* v_new,
+                      const int32_t* positions, void* k_cache, void* v_cache,
+                      int B, int S, int Hq, int Hkv, int L, int D, float scale,
+                      void* out, void* workspace, size_t workspace_bytes,
+                      cudaStream_t stream);
+
+/*
  * attn_decode_stream_step -- one step of a streaming decode loop that a CUDA
  * graph can capture once and replay unchanged.  It performs the fused step of
  * attn_decode_step_append (preceded by the rotary embedding of

@@ -39,7 +39,7 @@ def test_header_declares_the_boundary():
                  "attn_prefill_causal", "attn_read_device_status", "attn_status_string",
                  "attn_last_cuda_error", "attn_decode_step_append",
                  "attn_decode_step_rope_append", "attn_decode_step_noalloc",
-                 "attn_decode_stream_step", "attn_decode_step_window"]:
+                 "attn_decode_stream_step", "attn_decode_step_window", "attn_decode_multi"]:
         assert want in names
 
 
@@ -118,6 +118,14 @@ def test_host_validation_happens_before_any_launch(lib):
     assert win(P, P, None, P, P, P, 1, 16, 8, 16, 128, 4, 1.0, P, P, need, None) == 1
     assert win(P, None, None, P, P, P, 1, 32, 2, 16, 128, 4, 1.0, P, P, need, None) == 2
     assert win(P, None, None, P, P, P, 1, 16, 8, 16, 128, 4, 1.0, P, P, need - 1, None) == 3
+    # multi-token decode: S * g must be 1, 2, 4 or 8; workspace for S * Hq heads
+    multi = lib.attn_decode_multi
+    need2 = ga.attn_decode_workspace_size(1, 32, 8, 16, 128)
+    assert need2 > need
+    assert multi(P, None, None, P, P, P, 1, 3, 16, 8, 16, 128, 1.0, P, P, 1 << 24, None) == 2
+    assert multi(P, None, None, P, P, P, 1, 0, 16, 8, 16, 128, 1.0, P, P, 1 << 24, None) == 1
+    assert multi(P, P, None, P, P, P, 1, 2, 16, 8, 16, 128, 1.0, P, P, 1 << 24, None) == 1
+    assert multi(P, None, None, P, P, P, 1, 2, 16, 8, 16, 128, 1.0, P, P, need2 - 1, None) == 3
     # the append entry points still refuse missing new rows
     assert lib.attn_decode_step_append(P, None, None, P, P, P, 1, 16, 8, 16, 128, 1.0, P, P,
                                        need, None) == 1
