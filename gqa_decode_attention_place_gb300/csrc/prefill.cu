@@ -212,10 +212,13 @@ __device__ __forceinline__ void tmem_st_wait() {
 // Shared-memory matrix descriptor of a tcgen05 operand in the 128-byte
 // swizzled canonical layout (8-row x 128-byte swizzle atoms, atoms 1024 bytes
 // apart along the strided dimension).
-__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+// lbo: for an MN-major operand wider than one 64-element swizzle span, the
+// byte distance between its successive 64-wide column blocks (unused, 16,
+// otherwise).
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr, uint32_t lbo = 16) {
   uint64_t d = 0;
   d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);        // start address
-  d |= (uint64_t)1 << 16;                          // leading byte offset (unused here)
+  d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;      // leading byte offset
   d |= (uint64_t)(1024 >> 4) << 32;                // stride byte offset: next 8 rows
   d |= (uint64_t)1 << 46;                          // descriptor version
   d |= (uint64_t)2 << 61;                          // 128-byte swizzle
@@ -362,7 +365,8 @@ __global__ void __launch_bounds__(kPThreads, 1)
     // ------------------------------------------------------- MMA issuer --
     if (lane == 0) {
       constexpr uint32_t idesc_qk = make_idesc(kBM, kBN, false);
-      constexpr uint32_t idesc_pv = make_idesc(kBM, 64, true);  // one 64-column block of O
+      // O (+)= P V at N = HD: V's HD/64 column blocks, kChunkBytes apart
+      constexpr uint32_t idesc_pv = make_idesc(kBM, HD, true);
       uint32_t gk = 0;             // K/V tiles consumed so far
       uint32_t cs[kQT] = {0, 0};   // S_x issued so far
       uint32_t cp[kQT] = {0, 0};   // P_x consumed (PV_x issued) so far
@@ -378,14 +382,11 @@ __global__ void __launch_bounds__(kPThreads, 1)
           tc_fence_after();
           const uint32_t sV =
               base + L::kOffKV + ((gk0 + j) % kKVStages) * 2 * kTileBytes + kTileBytes;
-          // O columns [64c, 64c+64) from V's column block c
 #pragma unroll
-          for (int c = 0; c < L::kChunks; ++c)
-#pragma unroll
-            for (int k = 0; k < kBN / 16; ++k)
-              tc_mma_ts(tmem + kTmemO + HD * x + 64 * c, tmem + kTmemP + 64 * x + 8 * k,
-                        sw128_desc(sV + c * kChunkBytes + k * 16 * 128), idesc_pv,
-                        (j > 0 || k > 0) ? 1u : 0u);
+          for (int k = 0; k < kBN / 16; ++k)
+            tc_mma_ts(tmem + kTmemO + HD * x, tmem + kTmemP + 64 * x + 8 * k,
+                      sw128_desc(sV + k * 16 * 128, HD > 64 ? kChunkBytes : 16), idesc_pv,
+                      (j > 0 || k > 0) ? 1u : 0u);
           tc_commit(bar(kBarPVDone + x));
           ++cp[x];
           return true;
