@@ -89,8 +89,10 @@ constexpr int kModeMulti = 8;    // p.S new tokens per sequence (see head_row)
 template <int G, bool MT>
 __device__ __forceinline__ size_t head_row(const DecodeParams& p, int b, int kvh, int h) {
   if (!MT) return (size_t)b * p.Hq + (size_t)kvh * G + h;
-  const int gr = G / p.S;
-  return ((size_t)b * p.S + h / gr) * p.Hq + (size_t)kvh * gr + h % gr;
+  // g = G / S query heads per token, a power of two: token h >> log2(g)
+  const int lg = 31 - __clz(G / p.S);
+  const int gr = 1 << lg;
+  return ((size_t)b * p.S + (h >> lg)) * p.Hq + (size_t)(kvh << lg) + (h & (gr - 1));
 }
 
 // Lanes per key (LPK): a key's 128 dims are spread over LPK lanes of a warp
