@@ -23,7 +23,7 @@ __all__ = [
     "attn_prefill_causal", "attn_read_device_status", "attn_status_string",
     "attn_last_cuda_error", "decode_workspace", "attn_decode_step_noalloc",
     "attn_decode_step_append", "attn_decode_step_rope_append", "attn_decode_stream_step",
-    "attn_decode_step_window", "attn_decode_multi",
+    "attn_decode_step_window", "attn_decode_multi", "attn_test_skip_tile",
 ]
 
 ATTN_OK = 0
@@ -78,6 +78,8 @@ def load_library(build_if_missing: bool = True) -> ctypes.CDLL:
     lib.attn_decode_multi.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, f32,
                                       vp, vp, sz, vp]
     lib.attn_decode_multi.restype = i32
+    lib.attn_test_skip_tile.argtypes = [i32]
+    lib.attn_test_skip_tile.restype = i32
     lib.attn_decode_step_noalloc.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, i32, f32, vp, vp]
     lib.attn_decode_step_noalloc.restype = i32
     lib.attn_prefill_causal.argtypes = [vp, vp, vp, i32, i32, i32, i32, i32, f32, vp, vp]
@@ -381,6 +383,12 @@ def attn_prefill_causal(q, k, v, start_pos: int, scale: float, out=None,
         out.data_ptr(), _stream(stream))
     _raise(code, "attn_prefill_causal")
     return out
+
+
+def attn_test_skip_tile(tile: int) -> None:
+    """Failure-path tests only: the next decode launches never issue tile
+    ``tile`` of the first segment, so the waits for it run out (-1: off)."""
+    _raise(load_library().attn_test_skip_tile(int(tile)), "attn_test_skip_tile")
 
 
 def attn_read_device_status(workspace, stream=None) -> int:

@@ -3,6 +3,7 @@
 #include <cstdint>
 
 #include "gqa_attn.h"
+#include "decode_params.h"
 #include "internal.h"
 
 namespace gqa {
@@ -199,6 +200,12 @@ int attn_read_device_status(void* workspace, uint32_t* bits, cudaStream_t stream
   if (e != cudaSuccess) return cuda_status(e);
   if (bits) *bits = word;
   return word ? ATTN_ERR_DEVICE : ATTN_OK;
+}
+
+int attn_test_skip_tile(int tile) {
+  if (tile < -1) return ATTN_ERR_INVALID_ARG;
+  gqa::g_decode_test_skip = tile;
+  return ATTN_OK;
 }
 
 const char* attn_status_string(int status) {

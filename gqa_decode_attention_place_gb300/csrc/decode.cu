@@ -6,6 +6,9 @@
 #include "internal.h"
 
 namespace gqa {
+
+int g_decode_test_skip = -1;
+
 namespace {
 
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
@@ -55,6 +58,7 @@ cudaError_t launch_decode(const void* q, const void* k_new, const void* v_new,
   p.rope_by_pos = rope_by_pos ? 1 : 0;
   p.window = window;
   p.S = S;
+  p.test_skip = g_decode_test_skip;
   p.advance = advance;
   p.ticket = reinterpret_cast<uint32_t*>(base + ws.ticket_off);
   p.B = B;

@@ -30,9 +30,14 @@ struct DecodeParams {
   int rope_by_pos;
   int window;             // 0: rows 0..pos; W > 0: rows max(0, pos-W+1)..pos
   int S;                  // new tokens per sequence (1; > 1: multi-token decode)
+  int test_skip;          // failure-path tests: a tile never issued, or -1
   int B, Hq, Hkv, L;
   float qscale;  // scale * log2(e)
 };
+
+// Failure-path tests: a tile of the first segment the next decode launches
+// will not issue (-1: none).  Process-wide; set through attn_test_skip_tile.
+extern int g_decode_test_skip;
 
 // One launcher per group size g = Hq / Hkv (decode_g<g>.cu).
 cudaError_t launch_decode_group1(const DecodeParams& p, cudaStream_t stream);

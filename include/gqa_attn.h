@@ -322,6 +322,20 @@ const char* attn_status_string(int status);
  * thread, 0 if none. */
 int attn_last_cuda_error(void);
 
+/*
+ * attn_test_skip_tile -- for tests of the failure path only.  From the next
+ * decode launch on, the bulk copy of tile `tile` (128 rows) of the first
+ * (sequence, KV head) segment is never issued.  The waits for that tile
+ * therefore run out: every wait in the kernels gives up
+ * after 500 ms.  The kernel then sets ATTN_DEV_TIMEOUT in the workspace's
+ * status word and returns, and the CUDA context stays usable; the outputs of
+ * that launch are undefined, and its workspace must be zero-filled again
+ * before reuse.  -1 (the default) turns this off.  Process-wide and not
+ * thread-safe.
+ * Errors: ATTN_ERR_INVALID_ARG for tile < -1.
+ */
+int attn_test_skip_tile(int tile);
+
 #ifdef __cplusplus
 }
 #endif

@@ -39,7 +39,8 @@ def test_header_declares_the_boundary():
                  "attn_prefill_causal", "attn_read_device_status", "attn_status_string",
                  "attn_last_cuda_error", "attn_decode_step_append",
                  "attn_decode_step_rope_append", "attn_decode_step_noalloc",
-                 "attn_decode_stream_step", "attn_decode_step_window", "attn_decode_multi"]:
+                 "attn_decode_stream_step", "attn_decode_step_window", "attn_decode_multi",
+                 "attn_test_skip_tile"]:
         assert want in names
 
 
@@ -126,6 +127,8 @@ def test_host_validation_happens_before_any_launch(lib):
     assert multi(P, None, None, P, P, P, 1, 0, 16, 8, 16, 128, 1.0, P, P, 1 << 24, None) == 1
     assert multi(P, P, None, P, P, P, 1, 2, 16, 8, 16, 128, 1.0, P, P, 1 << 24, None) == 1
     assert multi(P, None, None, P, P, P, 1, 2, 16, 8, 16, 128, 1.0, P, P, need2 - 1, None) == 3
+    assert lib.attn_test_skip_tile(-2) == 1
+    assert lib.attn_test_skip_tile(-1) == 0
     # the append entry points still refuse missing new rows
     assert lib.attn_decode_step_append(P, None, None, P, P, P, 1, 16, 8, 16, 128, 1.0, P, P,
                                        need, None) == 1
