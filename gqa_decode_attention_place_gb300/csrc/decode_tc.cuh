@@ -60,8 +60,9 @@ constexpr int kTcN = 16;                       // MMA N: the g heads, padded
 constexpr int kTcSW = 4;                       // softmax warps (TMEM lane quarters)
 constexpr int kTcNC = kTcSW * 32;              // softmax threads
 constexpr int kTcProdWarp = kTcSW;             // TMA
-constexpr int kTcMmaWarp = kTcSW + 1;          // MMA issue, TMEM allocation
-constexpr int kTcThreads = (kTcSW + 2) * 32;
+constexpr int kTcMmaWarp = kTcSW + 1;          // S^T MMAs, TMEM allocation
+constexpr int kTcPvWarp = kTcSW + 2;           // O^T MMAs
+constexpr int kTcThreads = (kTcSW + 3) * 32;
 constexpr int kTcMaxStages = 3;                // K/V ring: 3 stages where shared memory allows, else 2
 constexpr int kTcHalf = kTile * 128;           // 16 KB: 128 rows x 64 dims (one swizzle block)
 constexpr int kTcOpBlock = kTcN * 128;         // 2 KB: 16 rows x 64 columns of Q or P
@@ -229,7 +230,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const int shift = MT ? p.S - 1 : 0;  // positions[b] + shift: the last new token's row
   volatile int* abort_flag = misc;
 
-  if (tid == 0) {
+  // The TMA thread initialises the mbarriers itself, so it may start loading
+  // as soon as it knows its tiles; everyone else sees them after the setup
+  // barrier below.
+  const bool tma_thread = warp == kTcProdWarp && lane == 0;
+  if (tma_thread) {
 #pragma unroll
     for (int s = 0; s < kTcMaxStages; ++s) {
       mbar_init(bar(kTbFull + s), 1);   // the TMA thread's arrival + bytes
@@ -344,6 +349,37 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     walk_init(w0, t0, prefix, p.positions, B, Hkv, win, shift);
   }
 
+  // ---- the first loads, before the rest of the setup -------------------------
+  Walk pw = w0;         // TMA thread: next tile to load,
+  int pi = 0, ps = 0;   //   its index and stage,
+  uint32_t pu = 0;      //   and index / ns
+  auto produce_until = [&](int i_end) {
+    for (; pi < i_end; ++pi) {
+      if (pi >= ns && !lane_wait(bar(kTbEmpty + ps), (pu & 1u) ^ 1u, abort_flag, p.status)) {
+        pi = count;
+        break;
+      }
+      // failure-path tests only: tile test_skip of the first segment is
+      // never issued, so the bounded waits for it run out
+      if (!(p.test_skip >= 0 && pw.b == 0 && pw.kvh == 0 && pw.k == p.test_skip)) {
+        const uint32_t full = bar(kTbFull + ps);
+        const uint32_t sK = base + (uint32_t)(ps * 2 * kTileBytes);
+        const int row = pw.lo + pw.k * kTile, z = pw.b * Hkv + pw.kvh;
+        mbar_arrive_expect_tx(full, 2u * kTileBytes);
+        tma_load_3d(sK, &tm_k, 0, row, z, full);
+        tma_load_3d(sK + kTcHalf, &tm_k, 64, row, z, full);
+        tma_load_3d(sK + kTileBytes, &tm_v, 0, row, z, full);
+        tma_load_3d(sK + kTileBytes + kTcHalf, &tm_v, 64, row, z, full);
+      }
+      tiles_next<CL>(pw, p, prefix, win, shift);
+      if (++ps == ns) {
+        ps = 0;
+        ++pu;
+      }
+    }
+  };
+  if (tma_thread) produce_until(min(ns, count));  // no stage to wait for yet
+
   // ---- tensor memory, operand buffers -------------------------------------
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(misc + 4);
   if (warp == kTcMmaWarp) {
@@ -371,25 +407,39 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
   if (warp == kTcProdWarp) {
     // ------------------------------------------------------ TMA producer --
+    if (lane == 0) produce_until(count);
+    __syncwarp();
+  } else if (warp == kTcMmaWarp) {
+    // ------------------------------------------------------- S^T = K Q^T --
+    // One thread per MMA stream, each blocking on its own barriers (a thread
+    // polling several would steal issue slots from the softmax warp that
+    // shares its scheduler).  Tile nq needs its K/V landed, its segment's Q
+    // written, and S buffer nq&1 free: the softmax is past tile nq-2.
     if (lane == 0) {
+      constexpr uint32_t idesc_s = make_idesc(128, kTcN, false);
       Walk w = w0;
-      int s = 0;
-      uint32_t u = 0;  // stage of tile i, and i / ns
-      for (int i = 0; i < count; ++i) {
-        if (i >= ns && !lane_wait(bar(kTbEmpty + s), (u & 1u) ^ 1u, abort_flag, p.status))
+      int j = -1, s = 0;
+      uint32_t u = 0;
+      for (int nq = 0; nq < count; ++nq) {
+        const bool first = (nq == 0) || w.k == 0;
+        if (first) ++j;
+        if (first &&
+            !lane_wait(bar(kTbQFull + (j & 1)), (uint32_t)(j >> 1) & 1u, abort_flag, p.status))
           break;
-        // failure-path tests only: tile test_skip of the first segment is
-        // never issued, so the bounded waits for it run out
-        if (!(p.test_skip >= 0 && w.b == 0 && w.kvh == 0 && w.k == p.test_skip)) {
-          const uint32_t full = bar(kTbFull + s);
-          const uint32_t sK = base + (uint32_t)(s * 2 * kTileBytes);
-          const int row = w.lo + w.k * kTile, z = w.b * Hkv + w.kvh;
-          mbar_arrive_expect_tx(full, 2u * kTileBytes);
-          tma_load_3d(sK, &tm_k, 0, row, z, full);
-          tma_load_3d(sK + kTcHalf, &tm_k, 64, row, z, full);
-          tma_load_3d(sK + kTileBytes, &tm_v, 0, row, z, full);
-          tma_load_3d(sK + kTileBytes + kTcHalf, &tm_v, 64, row, z, full);
-        }
+        if (!lane_wait(bar(kTbFull + s), u & 1u, abort_flag, p.status)) break;
+        if (nq >= 2 && !lane_wait(bar(kTbPFull + (nq & 1)), (uint32_t)((nq - 2) >> 1) & 1u,
+                                  abort_flag, p.status))
+          break;
+        tc_fence_after();
+        const uint32_t sK = base + (uint32_t)(s * 2 * kTileBytes);
+        const uint32_t sQ = base + (uint32_t)(fix + kToQ + (j & 1) * kTcOpBytes);
+#pragma unroll
+        for (int kk = 0; kk < kD / 16; ++kk)  // 4 K-steps per 64-dim column block
+          tc_mma(tmem + kTcTmemS + (uint32_t)((nq & 1) * kTcN),
+                 sw128_desc(sK + (kk >> 2) * kTcHalf + (kk & 3) * 32),
+                 sw128_desc(sQ + (kk >> 2) * kTcOpBlock + (kk & 3) * 32), idesc_s,
+                 kk > 0 ? 1u : 0u);
+        tc_commit(bar(kTbSFull + (nq & 1)));
         tiles_next<CL>(w, p, prefix, win, shift);
         if (++s == ns) {
           s = 0;
@@ -398,88 +448,35 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       }
     }
     __syncwarp();
-  } else if (warp == kTcMmaWarp) {
-    // -------------------------------------------------------- MMA issue --
-    // One thread serves two cursors and issues whichever work is ready:
-    //   nq: S^T_nq = K_nq Q^T, once the tile landed (and, for a segment's
-    //       first tile, its Q operand is written); S buffer nq&1 is free once
-    //       the softmax has passed tile nq-2, i.e. nq < np + 2.
-    //   np: O^T += V^T_np P^T_np, once the softmax wrote P_np (and, for a
-    //       segment's first tile, the previous segment's epilogue read O^T).
-    // The P.V of a tile -- which frees its stage for the next load -- thus
-    // never waits for a later tile's data.
+  } else if (warp == kTcPvWarp) {
+    // ---------------------------------------------------- O^T += V^T P^T --
+    // Tile np needs its P written (so its S^T, and the K half of its stage,
+    // are done with) and, first in a segment, the previous segment's
+    // epilogue done reading O^T.  Its completion frees the stage.
     if (lane == 0) {
-      constexpr uint32_t idesc_s = make_idesc(128, kTcN, false);
       constexpr uint32_t idesc_o = make_idesc(128, kTcN, false, true);  // V^T: MN-major
       Walk w = w0;
-      int nq = 0, np = 0;
-      int sq = 0, sp = 0;  // stages of tiles nq and np
-      uint32_t uq = 0;     // nq / ns
-      int jq = -1;                      // segment of tile nq-1 (within this CTA)
-      // per issued S^T, by tile parity: segment (within this CTA) * 2 + 1 if
-      // the tile is its segment's first (registers, no indexed array)
-      int meta0 = 0, meta1 = 0;
-      uint64_t t_last = globaltimer_ns();
-      while (np < count) {
-        bool progress = false;
-        if (nq < count && nq < np + 2) {
-          const bool first = (nq == 0) || w.k == 0;
-          const int j = first ? jq + 1 : jq;
-          if ((!first || mbar_test(bar(kTbQFull + (j & 1)), (uint32_t)(j >> 1) & 1u)) &&
-              mbar_test(bar(kTbFull + sq), uq & 1u)) {
-            tc_fence_after();
-            const uint32_t sK = base + (uint32_t)(sq * 2 * kTileBytes);
-            const uint32_t sQ = base + (uint32_t)(fix + kToQ + (j & 1) * kTcOpBytes);
-#pragma unroll
-            for (int kk = 0; kk < kD / 16; ++kk)  // 4 K-steps per 64-dim column block
-              tc_mma(tmem + kTcTmemS + (uint32_t)((nq & 1) * kTcN),
-                     sw128_desc(sK + (kk >> 2) * kTcHalf + (kk & 3) * 32),
-                     sw128_desc(sQ + (kk >> 2) * kTcOpBlock + (kk & 3) * 32), idesc_s,
-                     kk > 0 ? 1u : 0u);
-            tc_commit(bar(kTbSFull + (nq & 1)));
-            const int meta = j * 2 + (first ? 1 : 0);
-            meta0 = (nq & 1) ? meta0 : meta;
-            meta1 = (nq & 1) ? meta : meta1;
-            jq = j;
-            ++nq;
-            if (++sq == ns) {
-              sq = 0;
-              ++uq;
-            }
-            tiles_next<CL>(w, p, prefix, win, shift);
-            progress = true;
-          }
-        }
-        if (np < nq) {
-          const int meta = (np & 1) ? meta1 : meta0;
-          const bool first = (meta & 1) != 0;
-          const int jx = meta >> 1;
-          if (mbar_test(bar(kTbPFull + (np & 1)), (uint32_t)(np >> 1) & 1u) &&
-              (!first || jx == 0 || mbar_test(bar(kTbOFree), (uint32_t)(jx - 1) & 1u))) {
-            tc_fence_after();
-            const uint32_t sV = base + (uint32_t)(sp * 2 * kTileBytes + kTileBytes);
-            const uint32_t sP = base + (uint32_t)(fix + kToP + (np & 1) * kTcOpBytes);
-#pragma unroll
-            for (int kk = 0; kk < kTile / 16; ++kk)
-              tc_mma(tmem + kTcTmemO, sw128_desc(sV + kk * 16 * 128, kTcHalf),
-                     sw128_desc(sP + (kk >> 2) * kTcOpBlock + (kk & 3) * 32), idesc_o,
-                     (first && kk == 0) ? 0u : 1u);
-            tc_commit(bar(kTbPVDone + (np & 1)));
-            tc_commit(bar(kTbEmpty + sp));  // the stage may be refilled
-            ++np;
-            if (++sp == ns) sp = 0;
-            progress = true;
-          }
-        }
-        if (progress) {
-          t_last = globaltimer_ns();
-        } else if (*abort_flag) {
+      int j = -1, s = 0;
+      for (int np = 0; np < count; ++np) {
+        const bool first = (np == 0) || w.k == 0;
+        if (first) ++j;
+        if (!lane_wait(bar(kTbPFull + (np & 1)), (uint32_t)(np >> 1) & 1u, abort_flag, p.status))
           break;
-        } else if (globaltimer_ns() - t_last > kWaitLimitNs) {
-          *abort_flag = 1;
-          set_status(p.status, ATTN_DEV_TIMEOUT);
+        if (first && j > 0 &&
+            !lane_wait(bar(kTbOFree), (uint32_t)(j - 1) & 1u, abort_flag, p.status))
           break;
-        }
+        tc_fence_after();
+        const uint32_t sV = base + (uint32_t)(s * 2 * kTileBytes + kTileBytes);
+        const uint32_t sP = base + (uint32_t)(fix + kToP + (np & 1) * kTcOpBytes);
+#pragma unroll
+        for (int kk = 0; kk < kTile / 16; ++kk)
+          tc_mma(tmem + kTcTmemO, sw128_desc(sV + kk * 16 * 128, kTcHalf),
+                 sw128_desc(sP + (kk >> 2) * kTcOpBlock + (kk & 3) * 32), idesc_o,
+                 (first && kk == 0) ? 0u : 1u);
+        tc_commit(bar(kTbPVDone + (np & 1)));
+        tc_commit(bar(kTbEmpty + s));  // the stage may be refilled
+        tiles_next<CL>(w, p, prefix, win, shift);
+        if (++s == ns) s = 0;
       }
     }
     __syncwarp();
