@@ -276,6 +276,9 @@ def test_fused_streaming_loop_matches_two_call_loop():
 @pytest.mark.parametrize("g,Hkv,positions", [
     (2, 8, [8191]), (2, 8, [0]), (2, 8, [65]), (8, 1, [5000]), (1, 4, [1023, 64]),
     (4, 2, [63, 3000]), (2, 8, [130, 7000]),
+    # tensor-core kernels: position 0 (with the fused append the tile holds
+    # only the appended row) and the first tile boundaries
+    (4, 8, [0]), (8, 8, [0]), (8, 2, [127, 128]), (4, 4, [1, 8191]),
 ])
 def test_small_batches_one_cluster_per_segment(g, Hkv, positions):
     """Few (sequence, KV head) segments: each gets a cluster of CTAs that
