@@ -806,7 +806,7 @@ __global__ void __maxnreg__(Cfg<G>::kMaxRegs) decode_splitkv_kernel(const Params
     consumer_bar<NC>();  // before any tile wait: every consumer warp gets here
     cs.load_q_rot(q_rot, p.qscale);
   } else {
-    cs.load_q<MT>(p, w.b, w.kvh, p.qscale);
+    cs.template load_q<MT>(p, w.b, w.kvh, p.qscale);
   }
   cs.reset();
 
@@ -846,14 +846,14 @@ __global__ void __maxnreg__(Cfg<G>::kMaxRegs) decode_splitkv_kernel(const Params
       const int ob = w.b, okvh = w.kvh;  // the segment whose output this is
       for (int idx = ct; idx < G * kD; idx += NC) {
         const int h = idx / kD, d = idx % kD;
-        float M, Ls, Os;
-        merge_warps<NW, G>(merge_o, merge_ml, h, d, M, Ls, Os);
+        float Mx, Ls, Os;
+        merge_warps<NW, G>(merge_o, merge_ml, h, d, Mx, Ls, Os);
         if (whole) {
           store_bf16(p.out + head_row<G, MT>(p, ob, okvh, h) * kD + d, Os / Ls);
         } else {
           p.part_o[((size_t)slot * G + h) * kD + d] = Os;
           if (d == 0) {
-            p.part_ml[((size_t)slot * G + h) * 2 + 0] = M;
+            p.part_ml[((size_t)slot * G + h) * 2 + 0] = Mx;
             p.part_ml[((size_t)slot * G + h) * 2 + 1] = Ls;
           }
         }
@@ -879,7 +879,7 @@ __global__ void __maxnreg__(Cfg<G>::kMaxRegs) decode_splitkv_kernel(const Params
           // independent loads keep several L2 round trips in flight.
           for (int idx = ct; idx < G * kD; idx += NC) {
             const int h = idx / kD, d = idx % kD;
-            float M = -INFINITY, Ls = 0.f, Os = 0.f;
+            float Mm = -INFINITY, Ls = 0.f, Os = 0.f;
             for (int c0 = c_first; c0 <= c_last; c0 += 8) {
               float mm[8], ll[8], oo[8];
 #pragma unroll
@@ -896,10 +896,10 @@ __global__ void __maxnreg__(Cfg<G>::kMaxRegs) decode_splitkv_kernel(const Params
                   oo[uu] = 0.f;
                 }
               }
-              float Mb = M;
+              float Mb = Mm;
 #pragma unroll
               for (int uu = 0; uu < 8; ++uu) Mb = fmaxf(Mb, mm[uu]);
-              const float sc0 = ex2(M - Mb);  // M = -inf on the first batch: 0
+              const float sc0 = ex2(Mm - Mb);  // Mm = -inf on the first batch: 0
               Ls *= sc0;
               Os *= sc0;
 #pragma unroll
@@ -908,7 +908,7 @@ __global__ void __maxnreg__(Cfg<G>::kMaxRegs) decode_splitkv_kernel(const Params
                 Ls = fmaf(ll[uu], e, Ls);
                 Os = fmaf(oo[uu], e, Os);
               }
-              M = Mb;
+              Mm = Mb;
             }
             store_bf16(p.out + head_row<G, MT>(p, ob, okvh, h) * kD + d, Os / Ls);
           }
@@ -930,7 +930,7 @@ __global__ void __maxnreg__(Cfg<G>::kMaxRegs) decode_splitkv_kernel(const Params
         csync(lane);
         cs.load_q_rot(q_rot, p.qscale);
       } else {
-        cs.load_q<MT>(p, w.b, w.kvh, p.qscale);
+        cs.template load_q<MT>(p, w.b, w.kvh, p.qscale);
       }
       if (MT) cs.head_last = w.lo + w.n - 1 - shift + cs.hd / (G / p.S);
     }
@@ -1069,7 +1069,7 @@ __global__ void __maxnreg__(Cfg<G>::kMaxRegs) decode_cluster_kernel(const Params
       consumer_bar<NC>();  // before any tile wait: every consumer warp gets here
       cs.load_q_rot(q_rot, p.qscale);
     } else {
-      cs.load_q<MT>(p, b, kvh, p.qscale);
+      cs.template load_q<MT>(p, b, kvh, p.qscale);
     }
     if (MT) cs.head_last = pos - shift + cs.hd / (G / p.S);
     cs.reset();
@@ -1108,11 +1108,11 @@ __global__ void __maxnreg__(Cfg<G>::kMaxRegs) decode_cluster_kernel(const Params
     float* to_ml = cluster.map_shared_rank(land_ml, 0) + rank * G * 2;
     for (int idx = tid; idx < G * kD; idx += NC) {
       const int h = idx / kD, d = idx % kD;
-      float M, Ls, Os;
-      merge_warps<NW, G>(merge_o, merge_ml, h, d, M, Ls, Os);
+      float Mx, Ls, Os;
+      merge_warps<NW, G>(merge_o, merge_ml, h, d, Mx, Ls, Os);
       to_o[h * kD + d] = Os;
       if (d == 0) {
-        to_ml[h * 2 + 0] = M;
+        to_ml[h * 2 + 0] = Mx;
         to_ml[h * 2 + 1] = Ls;
       }
     }
@@ -1128,10 +1128,10 @@ __global__ void __maxnreg__(Cfg<G>::kMaxRegs) decode_cluster_kernel(const Params
       const bool in = lane < C;
       const float m = in ? land_ml[(lane * G + h) * 2] : -INFINITY;
       const float l = in ? land_ml[(lane * G + h) * 2 + 1] : 0.f;
-      float M = m;
+      float Mx = m;
 #pragma unroll
-      for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-      const float e = in ? ex2(m - M) : 0.f;  // a rank without tiles: 2^-inf = 0
+      for (int off = 16; off > 0; off >>= 1) Mx = fmaxf(Mx, __shfl_xor_sync(0xffffffffu, Mx, off));
+      const float e = in ? ex2(m - Mx) : 0.f;  // a rank without tiles: 2^-inf = 0
       float Ls = l * e;
 #pragma unroll
       for (int off = 16; off > 0; off >>= 1) Ls += __shfl_xor_sync(0xffffffffu, Ls, off);
