@@ -1242,18 +1242,29 @@ cudaError_t configure(DevInfo& d) {
   return cudaSuccess;
 }
 
-template <int G, int M>
-cudaError_t launch_g(const Params& p, cudaStream_t stream) {
+// Cluster size for this launch: the largest in 8..kMaxC that lets every
+// segment have its own co-resident cluster, or 0 (stream-K).
+template <int G>
+cudaError_t cluster_size(const Params& p, int* C) {
   int dev = 0;
   DevInfo& d = dev_info(&dev);
   cudaError_t e = configure<G>(d);
   if (e != cudaSuccess) return e;
   const long long nseg = (long long)p.B * p.Hkv;
-  // Cluster mode when every segment can have its own co-resident cluster of
-  // at least 8 CTAs: the largest such cluster size.  Otherwise stream-K.
+  *C = 0;
+  for (int c = Cfg<G>::kMaxC; c >= 8 && *C == 0; --c)
+    if (nseg <= d.clusters[G][c]) *C = c;
+  return cudaSuccess;
+}
+
+template <int G, int M>
+cudaError_t launch_g(const Params& p, cudaStream_t stream) {
+  int dev = 0;
+  DevInfo& d = dev_info(&dev);
   int C = 0;
-  for (int c = Cfg<G>::kMaxC; c >= 8 && C == 0; --c)
-    if (nseg <= d.clusters[G][c]) C = c;
+  cudaError_t e = cluster_size<G>(p, &C);
+  if (e != cudaSuccess) return e;
+  const long long nseg = (long long)p.B * p.Hkv;
   if (C > 0) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(nseg * C));

@@ -105,11 +105,13 @@ size_t attn_decode_workspace_size(int B, int Hq, int Hkv, int L, int D);
  *   v_cache   : [B, Hkv, L, D] bf16.
  *   scale     : fp32 score scale (the page's default is 1/sqrt(D)).
  *   out       : [B, Hq, D] bf16 (= [B, Hq*D]), fp32 softmax and accumulation,
- *               rounded to nearest even.  For g <= 2 the products run on
- *               CUDA cores in fp32; for g >= 4 both contractions of a tile
- *               run on the tcgen05 tensor cores (bf16 operands, fp32
- *               accumulation), with the probabilities rounded to bf16 before
- *               P.V.
+ *               rounded to nearest even.  For g <= 2, and for g = 4 when
+ *               B * Hkv is small (one thread-block cluster per segment), the
+ *               products run on CUDA cores in fp32; otherwise (g = 8, and
+ *               g = 4 with many segments) both contractions of a tile run
+ *               on the tcgen05 tensor cores (bf16 operands, fp32
+ *               accumulation), with the probabilities rounded to bf16
+ *               before P.V.
  *   workspace : device buffer of at least attn_decode_workspace_size(...)
  *               bytes, zero-filled before first use (see above).
  *
@@ -130,10 +132,10 @@ int attn_decode_step(const void* q, const int32_t* positions,
  * row positions[b] of every KV head of sequence b becomes k_new/v_new
  * (bit-exact) and out is attention over rows 0..positions[b], the new row
  * included.  The new rows are fed to the attention straight from k_new/v_new
- * and written to the cache in the same launch.  For g <= 2 out is
- * bit-identical to the two calls; for g >= 4 the new row's score and value
- * are folded in fp32 beside the tensor-core tile, so out agrees with the two
- * calls to rounding.
+ * and written to the cache in the same launch.  On the CUDA-core kernels out
+ * is bit-identical to the two calls; on the tensor-core ones (see
+ * attn_decode_step) the new row's score and value are folded in fp32 beside
+ * the tile, so out agrees with the two calls to rounding.
  *
  *   q            : [B, Hq, D] bf16.
  *   k_new, v_new : [B, Hkv, D] bf16.
