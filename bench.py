@@ -520,7 +520,7 @@ def _decode_leg(torch, ga, synth, name, flush, hbm):
     pos = case.positions.cpu().tolist()
     nb = oracle.decode_bytes(pos, Hq, Hkv, Dd)
     fl = oracle.decode_flops(pos, Hq, Dd)
-    tc = Hq // Hkv >= 4  # g >= 4 runs on the tcgen05 kernel, g <= 2 on CUDA cores
+    tc = Hq // Hkv == 8  # g = 8 runs on the tcgen05 kernel, g <= 4 on CUDA cores
     r = {"us": round(ms * 1e3, 2), "GBs": round(nb / (ms * 1e-3) / 1e9, 1),
          "frac_hbm": round(nb / (ms * 1e-3) / 1e9 / hbm, 3),
          ("TFLOPs_tensor" if tc else "TFLOPs_fp32_cuda_core"): round(fl / (ms * 1e-3) / 1e12, 2),

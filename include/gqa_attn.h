@@ -105,11 +105,9 @@ size_t attn_decode_workspace_size(int B, int Hq, int Hkv, int L, int D);
  *   v_cache   : [B, Hkv, L, D] bf16.
  *   scale     : fp32 score scale (the page's default is 1/sqrt(D)).
  *   out       : [B, Hq, D] bf16 (= [B, Hq*D]), fp32 softmax and accumulation,
- *               rounded to nearest even.  For g <= 2, and for g = 4 when
- *               B * Hkv is small (one thread-block cluster per segment), the
- *               products run on CUDA cores in fp32; otherwise (g = 8, and
- *               g = 4 with many segments) both contractions of a tile run
- *               on the tcgen05 tensor cores (bf16 operands, fp32
+ *               rounded to nearest even.  For g <= 4 the products run on
+ *               CUDA cores in fp32; for g = 8 both contractions of a tile
+ *               run on the tcgen05 tensor cores (bf16 operands, fp32
  *               accumulation), with the probabilities rounded to bf16
  *               before P.V.
  *   workspace : device buffer of at least attn_decode_workspace_size(...)

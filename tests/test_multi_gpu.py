@@ -73,13 +73,13 @@ def test_multi_clusters(S, Hq, Hkv):
     _run_and_check(2, S, Hq, Hkv, [126, 8190 - S], 311 + S, f"multi S={S} Hq={Hq} B=2")
 
 
-@pytest.mark.parametrize("Hq,Hkv", [(16, 8), (32, 8)])
+@pytest.mark.parametrize("Hq,Hkv", [(16, 8), (64, 8)])
 def test_one_token_is_the_plain_decode(Hq, Hkv):
     """S = 1 writes the same cache bits as the fused append step.  At g = 2
-    (CUDA-core kernels) the outputs are the same bits too.  At g = 4 with 24
-    segments (tensor-core kernels) the fused step folds its new row in fp32
-    on the side, while the multi-token path reads it back through the tile,
-    so there the two agree to rounding, within the attention tolerance."""
+    (CUDA-core kernels) the outputs are the same bits too.  At g = 8
+    (tensor-core kernels) the fused step folds its new row in fp32 on the
+    side, while the multi-token path reads it back through the tile, so
+    there the two agree to rounding, within the attention tolerance."""
     q, kn, vn, pos, kc, vc = _case(3, 1, Hq, Hkv, [5, 700, 8191], 320)
     kc2, vc2 = kc.clone(), vc.clone()
     out = ga.attn_decode_multi(q, pos, kc, vc, 0.088, k_new=kn, v_new=vn)
@@ -88,7 +88,7 @@ def test_one_token_is_the_plain_decode(Hq, Hkv):
     torch.cuda.synchronize()
     assert torch.equal(bits(kc), bits(kc2))
     assert torch.equal(bits(vc), bits(vc2))
-    if Hq // Hkv <= 2:
+    if Hq // Hkv <= 4:
         assert torch.equal(bits(out[:, 0]), bits(ref))
     else:
         assert_attn_close(f64(out[:, 0]), f64(ref), "multi S=1 against the fused step")
