@@ -1,6 +1,8 @@
 // decode_kernels.cuh -- split-KV decode attention over a static KV cache with
-// GQA: the kernels and their launch, included by one translation unit per
-// group size g (decode_g1.cu ... decode_g8.cu).
+// GQA on CUDA cores, for group sizes g = 1, 2, 4: the kernels and their
+// launch, included by one translation unit per group size (decode_g1.cu ...
+// decode_g4.cu).  g = 8 runs on the tensor cores (decode_tc.cuh, which also
+// uses the segment walk, helpers and merges defined here).
 //
 // What it computes ("MiniCPM4 `forward_step` Attention Performance Fix",
 // sections 3 and 4.1): for every sequence b and query head h,
@@ -21,11 +23,8 @@
 //  * The attended rows of every (sequence, KV head) pair -- a "segment" -- are
 //    cut into 128-row tiles, streamed with 1-D bulk copies (TMA) into a
 //    2-stage shared-memory ring guarded by mbarriers (128 KB in flight per
-//    SM) by a producer warp (one thread).  For g = 8 there is no producer
-//    warp: one thread issues the first two tiles and the last consumer warp
-//    to finish with a stage refills it, so a CTA is 256 threads that may use
-//    248 registers each.  Each tile is read from HBM once and serves all g
-//    query heads of its KV head.
+//    SM) by a producer warp (one thread).  Each tile is read from HBM once
+//    and serves all g query heads of its KV head.
 //  * 8 consumer warps (16 for g=1) each take 16 (8) keys of a tile; a key's
 //    128 dims are spread over 16 lanes, 8 each, as fp32 pairs for the packed
 //    fma.rn.f32x2.  q.k partial sums of the g heads are reduced across the
@@ -36,7 +35,7 @@
 //  * Two ways to split a segment over CTAs, both computed on the device from
 //    `positions` (one launch serves any positions; graph-capturable):
 //    - cluster mode (few segments, e.g. B=1): one thread-block cluster of C
-//      CTAs (8..16, 8..12 for g = 8; the largest size that lets every
+//      CTAs (8..16; the largest size that lets every
 //      segment's cluster be resident at once) per segment; CTA rank r takes
 //      tiles [r*n/C, (r+1)*n/C).  Each CTA stores its partial (max, sum,
 //      unnormalised o) straight into rank 0's shared memory (distributed
@@ -101,18 +100,16 @@ __device__ __forceinline__ size_t head_row(const DecodeParams& p, int b, int kvh
 // (128*g/LPK each).  16 lanes for every g: with 8, g = 4 ran at the
 // register cap and spilled in its key loop (12% slower on the ragged batch),
 // and g = 1 and 2 gained nothing from the shorter reduction either.
+// These CUDA-core kernels serve g <= 4; g = 8 runs on the tensor cores
+// (decode_tc.cuh), where its FMA work becomes two small MMAs per tile.
 template <int G> struct Cfg {
+  static_assert(G == 1 || G == 2 || G == 4, "the CUDA-core decode serves g <= 4");
   static constexpr int LPK = 16;
   static constexpr int NW = (G == 1) ? 16 : 8;
-  // A producer warp streams the tiles for g <= 4.  For g = 8 the registers
-  // are worth more: with it, a CTA of 288 threads may use 168 registers a
-  // thread and the key loop spilled; without it, 256 threads get 248, and the
-  // last consumer warp to finish with a stage refills it (last_to_release).
-  static constexpr bool kProducer = G < 8;
   // largest cluster: rank 0 keeps a landing slot for every rank's partial
-  // (G x (kD + 2) floats each), and at g = 8 sixteen would not fit
-  static constexpr int kMaxC = G == 8 ? 12 : 16;
-  static constexpr int kThreads = (NW + (kProducer ? 1 : 0)) * 32;
+  // (G x (kD + 2) floats each)
+  static constexpr int kMaxC = 16;
+  static constexpr int kThreads = (NW + 1) * 32;  // + the producer warp
   static constexpr int kConsumers = NW * 32;
   static constexpr int kKeysPerWarp = kTile / NW;  // 16 or 8
   static constexpr int kKeysPerStep = 32 / LPK;    // 2
@@ -504,24 +501,6 @@ __device__ __forceinline__ void produce_tile(const Params& p, uint8_t* stages, u
   }
 }
 
-// A consumer warp's release of pipeline stage s once it is done with the
-// stage's tile (lane 0, after the warp synced).  The counter rel[s] picks
-// the last of the NW warps; that one rearms the counter and returns true, and
-// the caller refills the stage with the tile kStages ahead.  The acquire
-// orders every other warp's reads of the stage before the refill's bulk
-// copies, so no producer warp has to wait on the stage.
-__device__ __forceinline__ bool last_to_release(int* rel, int s, int nw) {
-  int old;
-  asm volatile("atom.acq_rel.cta.shared::cta.add.u32 %0, [%1], 1;"
-               : "=r"(old)
-               : "r"(smem_u32(&rel[s]))
-               : "memory");
-  if (old != nw - 1) return false;
-  rel[s] = 0;
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-  return true;
-}
-
 // Rotary embedding of one segment, by the consumers.  rope_segment (all NC
 // consumer threads, at the start of a segment, followed by a consumer
 // barrier): the G query rows of the segment, rotated, into q_rot [G][kD] fp32,
@@ -656,7 +635,6 @@ __global__ void __maxnreg__(Cfg<G>::kMaxRegs) decode_splitkv_kernel(const Params
   constexpr bool R = (M & kModeRope) != 0, A = (M & kModeAdvance) != 0;
   constexpr bool MT = (M & kModeMulti) != 0;
   constexpr int NW = Cfg<G>::NW;
-  constexpr bool kProducer = Cfg<G>::kProducer;
   constexpr int KPW = Cfg<G>::kKeysPerWarp;
   constexpr int NC = Cfg<G>::kConsumers;
   extern __shared__ __align__(1024) uint8_t smem[];
@@ -680,14 +658,12 @@ __global__ void __maxnreg__(Cfg<G>::kMaxRegs) decode_splitkv_kernel(const Params
 #pragma unroll
     for (int s = 0; s < kStages; ++s) {
       mbar_init(smem_u32(&bars[s]), 1);             // full: issuing thread's arrival + bytes
-      if (kProducer) mbar_init(smem_u32(&bars[kStages + s]), NW);  // empty: per consumer warp
+      mbar_init(smem_u32(&bars[kStages + s]), NW);  // empty: per consumer warp
     }
     mbar_init(smem_u32(&bars[2 * kStages]), NW);    // consumer barrier
-    mbar_init(smem_u32(&bars[2 * kStages + 1]), kProducer ? NW + 1 : NW);  // done with positions
+    mbar_init(smem_u32(&bars[2 * kStages + 1]), NW + 1);  // done with positions
     misc[0] = 0;
     misc[1] = 0;
-    misc[2] = 0;  // release counters of the stages
-    misc[3] = 0;
     fence_mbar_init();
   }
   // Launched with programmatic stream serialisation: everything above may run
@@ -752,43 +728,27 @@ __global__ void __maxnreg__(Cfg<G>::kMaxRegs) decode_splitkv_kernel(const Params
   const long long t0 = T * blockIdx.x / Gd;
   const long long t1 = T * (blockIdx.x + 1) / Gd;
 
-  // -------------------------------------------------------------- pipeline --
-  int* rel = misc + 2;
-  Walk ahead;  // without a producer: the tile kStages after the current one
-  if constexpr (kProducer) {
-    if (warp == NW) {
-      if (lane == 0) {
-        Walk w;
-        walk_init(w, t0, prefix, p.positions, B, Hkv, win, shift);
-        long long i = 0;
-        for (long long t = t0; t < t1; ++t, ++i) {
-          const int s = (int)(i % kStages);
-          const uint32_t u = (uint32_t)(i / kStages);
-          if (i >= kStages &&
-              !mbar_wait(smem_u32(&bars[kStages + s]), (u & 1u) ^ 1u, abort_flag)) {
-            *abort_flag = 1;
-            set_status(p.status, ATTN_DEV_TIMEOUT);
-            break;
-          }
-          produce_tile(p, stages, bars, s, w.b, w.kvh, w.k, w.ntiles, w.n, w.lo);
-          walk_next(w, prefix, p.positions, B, Hkv, win, shift);
+  // -------------------------------------------------------------- producer --
+  if (warp == NW) {
+    if (lane == 0) {
+      Walk w;
+      walk_init(w, t0, prefix, p.positions, B, Hkv, win, shift);
+      long long i = 0;
+      for (long long t = t0; t < t1; ++t, ++i) {
+        const int s = (int)(i % kStages);
+        const uint32_t u = (uint32_t)(i / kStages);
+        if (i >= kStages &&
+            !mbar_wait(smem_u32(&bars[kStages + s]), (u & 1u) ^ 1u, abort_flag)) {
+          *abort_flag = 1;
+          set_status(p.status, ATTN_DEV_TIMEOUT);
+          break;
         }
-        if (A) mbar_arrive(smem_u32(&bars[2 * kStages + 1]));  // no more reads of positions
+        produce_tile(p, stages, bars, s, w.b, w.kvh, w.k, w.ntiles, w.n, w.lo);
+        walk_next(w, prefix, p.positions, B, Hkv, win, shift);
       }
-      return;
+      if (A) mbar_arrive(smem_u32(&bars[2 * kStages + 1]));  // no more reads of positions
     }
-  } else {
-    // the first kStages tiles now; after that the last warp to release a
-    // stage refills it, so every warp is a consumer
-    if (tid == 0) {
-      Walk pw;
-      walk_init(pw, t0, prefix, p.positions, B, Hkv, win, shift);
-      for (long long t = t0; t < t1 && t < t0 + kStages; ++t) {
-        produce_tile(p, stages, bars, (int)(t - t0), pw.b, pw.kvh, pw.k, pw.ntiles, pw.n, pw.lo);
-        walk_next(pw, prefix, p.positions, B, Hkv, win, shift);
-      }
-    }
-    if (t0 + kStages < t1) walk_init(ahead, t0 + kStages, prefix, p.positions, B, Hkv, win, shift);
+    return;
   }
 
   // ------------------------------------------------------------ consumers --
@@ -822,14 +782,7 @@ __global__ void __maxnreg__(Cfg<G>::kMaxRegs) decode_splitkv_kernel(const Params
     cs.tile(Ks, Ks + kTileBytes, rows,
             MT ? min(rows, cs.head_last + 1 - (w.lo + w.k * kTile)) : rows, warp);
     __syncwarp();
-    if constexpr (kProducer) {
-      if (lane == 0) mbar_arrive(smem_u32(&bars[kStages + s]));
-    } else {
-      if (lane == 0 && last_to_release(rel, s, NW) && t + kStages < t1)
-        produce_tile(p, stages, bars, s, ahead.b, ahead.kvh, ahead.k, ahead.ntiles, ahead.n,
-                   ahead.lo);
-      if (t + kStages < t1) walk_next(ahead, prefix, p.positions, B, Hkv, win, shift);
-    }
+    if (lane == 0) mbar_arrive(smem_u32(&bars[kStages + s]));  // the stage may be refilled
     const bool seg_end = (w.k == w.ntiles - 1) || (t == t1 - 1);
 
     // ---- end of this CTA's part of the segment: merge and emit ------------
@@ -971,7 +924,6 @@ __global__ void __maxnreg__(Cfg<G>::kMaxRegs) decode_cluster_kernel(const Params
   constexpr bool R = (M & kModeRope) != 0, A = (M & kModeAdvance) != 0;
   constexpr bool MT = (M & kModeMulti) != 0;
   constexpr int NW = Cfg<G>::NW;
-  constexpr bool kProducer = Cfg<G>::kProducer;
   constexpr int KPW = Cfg<G>::kKeysPerWarp;
   constexpr int NC = Cfg<G>::kConsumers;
   extern __shared__ __align__(1024) uint8_t smem[];
@@ -1000,12 +952,10 @@ __global__ void __maxnreg__(Cfg<G>::kMaxRegs) decode_cluster_kernel(const Params
 #pragma unroll
     for (int s = 0; s < kStages; ++s) {
       mbar_init(smem_u32(&bars[s]), 1);
-      if (kProducer) mbar_init(smem_u32(&bars[kStages + s]), NW);
+      mbar_init(smem_u32(&bars[kStages + s]), NW);
     }
     mbar_init(smem_u32(&bars[2 * kStages]), NW);
     misc[0] = 0;
-    misc[2] = 0;  // release counters of the stages
-    misc[3] = 0;
     fence_mbar_init();
   }
   grid_dependency_wait();
@@ -1033,14 +983,7 @@ __global__ void __maxnreg__(Cfg<G>::kMaxRegs) decode_cluster_kernel(const Params
   // shared memory, so rank 0 is known to have started by then
   asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
 
-  int* rel = misc + 2;
-  if constexpr (!kProducer) {
-    // the first kStages tiles now; the last warp to release a stage refills it
-    if (tid == 0)
-      for (int k = k0; k < k1 && k < k0 + kStages; ++k)
-        produce_tile(p, stages, bars, k - k0, b, kvh, k, ntiles, n, lo);
-  }
-  if (kProducer && warp == NW) {
+  if (warp == NW) {
     // ------------------------------------------------------------ producer --
     if (lane == 0) {
       for (int k = k0; k < k1; ++k) {
@@ -1086,12 +1029,7 @@ __global__ void __maxnreg__(Cfg<G>::kMaxRegs) decode_cluster_kernel(const Params
       cs.tile(Ks, Ks + kTileBytes, rows,
               MT ? min(rows, cs.head_last + 1 - (lo + k * kTile)) : rows, warp);
       __syncwarp();
-      if constexpr (kProducer) {
-        if (lane == 0) mbar_arrive(smem_u32(&bars[kStages + s]));
-      } else {
-        if (lane == 0 && last_to_release(rel, s, NW) && k + kStages < k1)
-          produce_tile(p, stages, bars, s, b, kvh, k + kStages, ntiles, n, lo);
-      }
+      if (lane == 0) mbar_arrive(smem_u32(&bars[kStages + s]));  // the stage may be refilled
     }
     // this CTA's warps' partials (max, sum, unnormalised o) merged below;
     // no tiles: (-inf, 0, 0)
