@@ -191,6 +191,26 @@ def test_max_batch_tiny_positions():
     _check(case, want, out, "B=8192")
 
 
+@pytest.mark.parametrize("fused", [False, True])
+def test_max_batch_tensor_cores(fused):
+    """B=8192 at g=8 (the tensor-core kernels): above B=4287 the stream-K
+    prefix array leaves room for two K/V stages only, so this runs the
+    2-stage ring.  Plain step, and the fused append step."""
+    B, L = 8192, 300
+    case = synth.decode_case(B=B, Hq=16, Hkv=2, D=128, L=L, positions="uniform", fill="all",
+                             poison=True, seed=13 + int(fused), device="cuda")
+    bs = [0, 1, 127, 2048, 4287, 4288, 8191]
+    want = _oracle_rows(case, bs)
+    if fused:
+        out = ga.attn_decode_step_append(case.q, case.k_new, case.v_new, case.positions,
+                                         case.k_cache, case.v_cache, case.scale)
+        torch.cuda.synchronize()
+    else:
+        out = _run_step(case)
+    assert torch.isfinite(out.float()).all()
+    _check(case, want, out, f"B=8192 g=8 fused={fused}")
+
+
 def test_single_row_cache_and_odd_scale():
     case = synth.decode_case(B=2, Hq=4, Hkv=1, D=128, L=1, positions=[0, 0], fill="all",
                              seed=13, device="cuda", scale=3.7)
