@@ -82,6 +82,9 @@ int decode_append(const void* q, const void* k_new, const void* v_new, const flo
       (reinterpret_cast<uintptr_t>(positions) & 3u))
     return ATTN_ERR_INVALID_ARG;
   if (!gqa::decode_supported(B, Hq, Hkv, L, D)) return ATTN_ERR_UNSUPPORTED;
+  // the rotated query takes two operand rows per head (bf16 high and low
+  // parts) in the tensor-core kernels' 16 rows: g <= 8 with the rotation
+  if (rope_cos && Hq / Hkv > 8) return ATTN_ERR_UNSUPPORTED;
   if (!workspace || !aligned16(workspace) ||
       workspace_bytes < gqa::decode_workspace_layout(B, Hq, Hkv, D).total)
     return ATTN_ERR_WORKSPACE;
@@ -135,7 +138,7 @@ int attn_decode_multi(const void* q, const void* k_new, const void* v_new,
       (reinterpret_cast<uintptr_t>(positions) & 3u))
     return ATTN_ERR_INVALID_ARG;
   if ((long long)S * Hq > 65536 || !gqa::decode_supported(B, S * Hq, Hkv, L, D))
-    return ATTN_ERR_UNSUPPORTED;  // S * g must be 1, 2, 4 or 8
+    return ATTN_ERR_UNSUPPORTED;  // S * g must be 1, 2, 4, 8 or 16
   if (!workspace || !aligned16(workspace) ||
       workspace_bytes < gqa::decode_workspace_layout(B, S * Hq, Hkv, D).total)
     return ATTN_ERR_WORKSPACE;

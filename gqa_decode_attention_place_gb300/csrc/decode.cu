@@ -30,7 +30,7 @@ DecodeWorkspace decode_workspace_layout(int B, int Hq, int Hkv, int D) {
 
 bool decode_supported(int B, int Hq, int Hkv, int L, int D) {
   const int g = Hq / Hkv;
-  return D == kDecodeD && (g == 1 || g == 2 || g == 4 || g == 8) && B >= 1 &&
+  return D == kDecodeD && (g == 1 || g == 2 || g == 4 || g == 8 || g == 16) && B >= 1 &&
          B <= kDecodeMaxB && L >= 1 && L <= (1 << 24);
 }
 
@@ -71,6 +71,7 @@ cudaError_t launch_decode(const void* q, const void* k_new, const void* v_new,
     case 2: return launch_decode_group2(p, stream);
     case 4: return launch_decode_group4(p, stream);
     case 8: return launch_decode_group8(p, stream);
+    case 16: return launch_decode_group16(p, stream);
   }
   return cudaErrorInvalidValue;
 }

@@ -202,6 +202,7 @@ template <> struct Log2<2> { static constexpr int v = 1; };
 template <> struct Log2<4> { static constexpr int v = 2; };
 template <> struct Log2<8> { static constexpr int v = 3; };
 template <> struct Log2<16> { static constexpr int v = 4; };
+template <> struct Log2<32> { static constexpr int v = 5; };
 
 // Sum of acc[h] over the LPK lanes holding one key, for every head at once.
 // A step with offset `off` keeps half of the heads and ships the other half

@@ -44,5 +44,6 @@ cudaError_t launch_decode_group1(const DecodeParams& p, cudaStream_t stream);
 cudaError_t launch_decode_group2(const DecodeParams& p, cudaStream_t stream);
 cudaError_t launch_decode_group4(const DecodeParams& p, cudaStream_t stream);
 cudaError_t launch_decode_group8(const DecodeParams& p, cudaStream_t stream);
+cudaError_t launch_decode_group16(const DecodeParams& p, cudaStream_t stream);
 
 }  // namespace gqa

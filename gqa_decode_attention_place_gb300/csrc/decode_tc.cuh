@@ -71,6 +71,9 @@ constexpr uint32_t kTcTmemCols = 64;
 constexpr uint32_t kTcTmemS = 0;               // S^T of tile parity x: columns 16x .. 16x+15
 constexpr uint32_t kTcTmemO = 32;              // O^T: columns 32 .. 47
 constexpr float kTcTau = 8.0f;                 // a stale running max may lag by 2^8
+// The rotation needs two operand rows per head (bf16 high and low parts of
+// the rotated q): g <= 8.  g = 16 fills the 16 rows with plain q.
+template <int G> constexpr bool kTcRope = 2 * G <= kTcN;
 
 // mbarriers
 constexpr int kTbFull = 0;                     // + stage: the tile's K and V landed
@@ -845,7 +848,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     if (rank == 0) {
       // weights 2^(m_r - M) / L per (rank, head): a warp per head reduces
       // over the ranks, lane r holding rank r's (max, sum)
-      float* wr = tmax;  // [C][G]
+      static_assert(kMaxCluster * G <= 2 * kTcSW * kTcN + kTcSW * 2 * kTcN,
+                    "the weights fit the tile-maxima and sums buffers");
+      float* wr = tmax;  // [C][G], over tmax and red (both free by now)
       for (int h = warp; h < G; h += kTcThreads / 32) {
         const bool in = lane < C;
         const float m = in ? land_ml[(lane * G + h) * 2] : -INFINITY;
@@ -933,10 +938,12 @@ TcDevInfo g_tc_dev[64];
 
 template <int G>
 int tc_max_clusters(int C) {
+  // rank 0 holds a landing slot per rank: at g = 16 that limits C to 9
+  if (tc_smem_bytes<G>(2, C, 0) > (size_t)kTcMaxSmem) return 0;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(C * 64);
   cfg.blockDim = dim3(kTcThreads);
-  cfg.dynamicSmemBytes = tc_smem_bytes<G>(2, kMaxCluster, 0);
+  cfg.dynamicSmemBytes = tc_smem_bytes<G>(2, C, 0);
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = C;
@@ -969,11 +976,13 @@ cudaError_t tc_set_attributes(bool* big) {
 template <int G>
 cudaError_t tc_configure(TcDevInfo& d) {
   if (d.configured[G]) return cudaSuccess;
-  bool big[6] = {};
+  bool big[6] = {true, true, true, true, true, true};
   cudaError_t e = tc_set_attributes<G, 0>(&big[0]);
-  if (e == cudaSuccess) e = tc_set_attributes<G, kModeRope>(&big[1]);
+  if constexpr (kTcRope<G>) {
+    if (e == cudaSuccess) e = tc_set_attributes<G, kModeRope>(&big[1]);
+    if (e == cudaSuccess) e = tc_set_attributes<G, kModeRope | kModeAdvance>(&big[3]);
+  }
   if (e == cudaSuccess) e = tc_set_attributes<G, kModeAdvance>(&big[2]);
-  if (e == cudaSuccess) e = tc_set_attributes<G, kModeRope | kModeAdvance>(&big[3]);
   if (e == cudaSuccess) e = tc_set_attributes<G, kModeWindow>(&big[4]);
   if (e == cudaSuccess) e = tc_set_attributes<G, kModeMulti>(&big[5]);
   if (e != cudaSuccess) return e;
@@ -1036,15 +1045,19 @@ cudaError_t launch_group_tc(const Params& p, cudaStream_t stream) {
   const int mode = (p.rope_cos != nullptr ? kModeRope : 0) |
                    (p.advance != nullptr ? kModeAdvance : 0) | (p.window > 0 ? kModeWindow : 0) |
                    (p.S > 1 ? kModeMulti : 0);
+  if constexpr (kTcRope<G>) {
+    if (mode == kModeRope) return launch_tc_g<G, kModeRope>(p, stream);
+    if (mode == (kModeRope | kModeAdvance))
+      return launch_tc_g<G, kModeRope | kModeAdvance>(p, stream);
+  }
   switch (mode) {
     case 0: return launch_tc_g<G, 0>(p, stream);
-    case kModeRope: return launch_tc_g<G, kModeRope>(p, stream);
     case kModeAdvance: return launch_tc_g<G, kModeAdvance>(p, stream);
-    case kModeRope | kModeAdvance: return launch_tc_g<G, kModeRope | kModeAdvance>(p, stream);
     case kModeWindow: return launch_tc_g<G, kModeWindow>(p, stream);
     case kModeMulti: return launch_tc_g<G, kModeMulti>(p, stream);
   }
-  return cudaErrorInvalidValue;
+  return cudaErrorInvalidValue;  // a combination no entry point makes, or the
+                                 // rotation at g = 16 (the entry points refuse it)
 }
 
 }  // namespace

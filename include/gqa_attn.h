@@ -113,7 +113,8 @@ size_t attn_decode_workspace_size(int B, int Hq, int Hkv, int L, int D);
  *   workspace : device buffer of at least attn_decode_workspace_size(...)
  *               bytes, zero-filled before first use (see above).
  *
- * Supported: D == 128; g = Hq / Hkv in {1, 2, 4, 8}; 1 <= B <= 8192;
+ * Supported: D == 128; g = Hq / Hkv in {1, 2, 4, 8, 16} (g = 16 on the
+ * tensor cores, like g = 8); 1 <= B <= 8192;
  * 1 <= L <= 2^24.  Work is split over the attended rows only, so the cost of
  * a step follows sum_b (positions[b] + 1), not B * L.
  */
@@ -169,7 +170,9 @@ int attn_decode_step_append(const void* q, const void* k_new, const void* v_new,
  *              it, so any frequency base or scaling works).  Read only.
  *   all other arguments, sizes and errors: as attn_decode_step_append.
  *
- * Errors: ATTN_ERR_INVALID_ARG also for a null or misaligned cos or sin.
+ * Errors: ATTN_ERR_INVALID_ARG also for a null or misaligned cos or sin;
+ * ATTN_ERR_UNSUPPORTED for g = 16 (the rotation serves g <= 8: the
+ * tensor-core kernels carry the rotated query as two bf16 rows per head).
  */
 int attn_decode_step_rope_append(const void* q, const void* k_new, const void* v_new,
                                  const float* cos, const float* sin,
@@ -221,14 +224,14 @@ int attn_decode_step_window(const void* q, const void* k_new, const void* v_new,
  *   out          : [B, S, Hq, D] bf16.
  *   workspace    : at least attn_decode_workspace_size(B, S * Hq, Hkv, L, D)
  *                  bytes, zero-filled before first use.
- *   Supported: D == 128; S * g in {1, 2, 4, 8}; other limits as
+ *   Supported: D == 128; S * g in {1, 2, 4, 8, 16}; other limits as
  *   attn_decode_step.  S == 1 is attn_decode_step (after the append).
  *
  * A sequence whose positions[b] + S - 1 falls outside [0, L) gets NaN in all
  * of its output rows, no cache write, and ATTN_DEV_BAD_POSITION.
  * Errors: ATTN_ERR_INVALID_ARG for null or misaligned pointers, exactly one
  * of k_new and v_new null, or non-positive sizes; ATTN_ERR_UNSUPPORTED when
- * S * g is not 1, 2, 4 or 8; ATTN_ERR_WORKSPACE as above.
+ * S * g is not 1, 2, 4, 8 or 16; ATTN_ERR_WORKSPACE as above.
  */
 int attn_decode_multi(const void* q, const void* k_new, const void* v_new,
                       const int32_t* positions, void* k_cache, void* v_cache,
@@ -259,7 +262,8 @@ int attn_decode_multi(const void* q, const void* k_new, const void* v_new,
  *   step uses a counter in the workspace and leaves it at zero again.
  *
  * Errors: ATTN_ERR_INVALID_ARG also when exactly one of cos_table and
- * sin_table is null, or either is misaligned.
+ * sin_table is null, or either is misaligned; ATTN_ERR_UNSUPPORTED for the
+ * rotation at g = 16 (as attn_decode_step_rope_append).
  */
 int attn_decode_stream_step(const void* q, const void* k_new, const void* v_new,
                             const float* cos_table, const float* sin_table,

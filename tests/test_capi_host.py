@@ -67,7 +67,8 @@ def test_workspace_size_rules(lib):
     assert ga.attn_decode_workspace_size(1, 16, 8, 1 << 20, 128) == n1
     assert ga.attn_decode_workspace_size(1, 16, 8, 8192, 64) == 0      # D unsupported
     assert ga.attn_decode_workspace_size(1, 12, 8, 8192, 128) == 0     # Hq % Hkv
-    assert ga.attn_decode_workspace_size(1, 48, 3, 8192, 128) == 0     # g = 16
+    assert ga.attn_decode_workspace_size(1, 48, 3, 8192, 128) > 0      # g = 16
+    assert ga.attn_decode_workspace_size(1, 96, 3, 8192, 128) == 0     # g = 32
     assert ga.attn_decode_workspace_size(0, 16, 8, 8192, 128) == 0
 
 
@@ -83,7 +84,7 @@ def test_host_validation_happens_before_any_launch(lib):
     assert lib.attn_kv_append(P, P, P, P, P, 0, 8, 16, 128, None) == 1
     # unsupported D / g
     assert lib.attn_decode_step(P, P, P, P, 1, 16, 8, 16, 96, 1.0, P, P, 1 << 20, None) == 2
-    assert lib.attn_decode_step(P, P, P, P, 1, 32, 2, 16, 128, 1.0, P, P, 1 << 20, None) == 2
+    assert lib.attn_decode_step(P, P, P, P, 1, 64, 2, 16, 128, 1.0, P, P, 1 << 20, None) == 2
     assert lib.attn_kv_append(P, P, P, P, P, 1, 8, 16, 12, None) == 2
     # workspace too small / missing
     need = ga.attn_decode_workspace_size(1, 16, 8, 16, 128)
@@ -100,7 +101,9 @@ def test_host_validation_happens_before_any_launch(lib):
     assert rope(P, P, P, None, P, P, P, P, 1, 16, 8, 16, 128, 1.0, P, P, 1 << 20, None) == 1
     assert rope(P, P, P, P, P + 4, P, P, P, 1, 16, 8, 16, 128, 1.0, P, P, 1 << 20, None) == 1
     assert rope(P, None, P, P, P, P, P, P, 1, 16, 8, 16, 128, 1.0, P, P, 1 << 20, None) == 1
+    # g = 16 decodes, but not with the rotation (two operand rows per head)
     assert rope(P, P, P, P, P, P, P, P, 1, 32, 2, 16, 128, 1.0, P, P, 1 << 20, None) == 2
+    assert rope(P, P, P, P, P, P, P, P, 1, 64, 2, 16, 128, 1.0, P, P, 1 << 20, None) == 2
     assert rope(P, P, P, P, P, P, P, P, 1, 16, 8, 16, 128, 1.0, P, P, need - 1, None) == 3
     # streaming step: tables both or neither, aligned; then the append step's checks
     stream = lib.attn_decode_stream_step
@@ -109,6 +112,7 @@ def test_host_validation_happens_before_any_launch(lib):
     assert stream(P, P, P, None, None, None, P, P, 1, 16, 8, 16, 128, 1.0, P, P, 1 << 20,
                   None) == 1
     assert stream(P, P, P, None, None, P, P, P, 1, 16, 8, 16, 96, 1.0, P, P, 1 << 20, None) == 2
+    assert stream(P, P, P, P, P, P, P, P, 1, 32, 2, 16, 128, 1.0, P, P, 1 << 20, None) == 2
     assert stream(P, P, P, None, None, P, P, P, 1, 16, 8, 16, 128, 1.0, P, None, need,
                   None) == 3
     assert stream(P, None, None, None, None, P, P, P, 1, 16, 8, 16, 128, 1.0, P, P, need,
@@ -117,13 +121,14 @@ def test_host_validation_happens_before_any_launch(lib):
     win = lib.attn_decode_step_window
     assert win(P, None, None, P, P, P, 1, 16, 8, 16, 128, 0, 1.0, P, P, need, None) == 1
     assert win(P, P, None, P, P, P, 1, 16, 8, 16, 128, 4, 1.0, P, P, need, None) == 1
-    assert win(P, None, None, P, P, P, 1, 32, 2, 16, 128, 4, 1.0, P, P, need, None) == 2
+    assert win(P, None, None, P, P, P, 1, 64, 2, 16, 128, 4, 1.0, P, P, need, None) == 2
     assert win(P, None, None, P, P, P, 1, 16, 8, 16, 128, 4, 1.0, P, P, need - 1, None) == 3
-    # multi-token decode: S * g must be 1, 2, 4 or 8; workspace for S * Hq heads
+    # multi-token decode: S * g must be 1, 2, 4, 8 or 16; workspace for S * Hq heads
     multi = lib.attn_decode_multi
     need2 = ga.attn_decode_workspace_size(1, 32, 8, 16, 128)
     assert need2 > need
     assert multi(P, None, None, P, P, P, 1, 3, 16, 8, 16, 128, 1.0, P, P, 1 << 24, None) == 2
+    assert multi(P, None, None, P, P, P, 1, 4, 64, 8, 16, 128, 1.0, P, P, 1 << 24, None) == 2
     assert multi(P, None, None, P, P, P, 1, 0, 16, 8, 16, 128, 1.0, P, P, 1 << 24, None) == 1
     assert multi(P, P, None, P, P, P, 1, 2, 16, 8, 16, 128, 1.0, P, P, 1 << 24, None) == 1
     assert multi(P, None, None, P, P, P, 1, 2, 16, 8, 16, 128, 1.0, P, P, need2 - 1, None) == 3

@@ -64,7 +64,7 @@ def test_single_step_workload():
     _check(case, want, out, "single_step")
 
 
-@pytest.mark.parametrize("g", [1, 2, 4, 8])
+@pytest.mark.parametrize("g", [1, 2, 4, 8, 16])
 def test_tile_and_split_boundaries_poisoned(g):
     Hkv = 2
     positions = [0, 1, 62, 63, 64, 65, 127, 128, 129, 255, 256, 257, 1000, 4095, 4096, 8191]
@@ -232,7 +232,7 @@ def _fused_step(case, workspace=None):
     return out
 
 
-@pytest.mark.parametrize("g", [1, 2, 4, 8])
+@pytest.mark.parametrize("g", [1, 2, 4, 8, 16])
 def test_fused_append_decode_boundaries_poisoned(g):
     Hkv = 2
     positions = [0, 1, 62, 63, 64, 65, 127, 128, 129, 255, 256, 257, 1000, 4095, 4096, 8191]
@@ -299,6 +299,8 @@ def test_fused_streaming_loop_matches_two_call_loop():
     # tensor-core kernels: position 0 (with the fused append the tile holds
     # only the appended row) and the first tile boundaries
     (4, 8, [0]), (8, 8, [0]), (8, 2, [127, 128]), (4, 4, [1, 8191]),
+    # g = 16: clusters of at most 9 (rank 0's 16-head landing slots)
+    (16, 2, [5000]), (16, 1, [0, 8191]), (16, 4, [127, 128, 3000]),
 ])
 def test_small_batches_one_cluster_per_segment(g, Hkv, positions):
     """Few (sequence, KV head) segments: each gets a cluster of CTAs that

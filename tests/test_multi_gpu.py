@@ -59,14 +59,15 @@ def _run_and_check(B, S, Hq, Hkv, positions, seed, what):
 POS16 = [0, 1, 60, 124, 125, 126, 127, 128, 250, 253, 1000, 4093, 4094, 8000, 7, 3001]
 
 
-@pytest.mark.parametrize("S,Hq,Hkv", [(2, 4, 2), (4, 4, 2), (8, 2, 2), (2, 8, 2), (4, 2, 2)])
+@pytest.mark.parametrize("S,Hq,Hkv", [(2, 4, 2), (4, 4, 2), (8, 2, 2), (2, 8, 2), (4, 2, 2),
+                                      (2, 16, 2), (4, 8, 2), (16, 2, 2)])
 def test_multi_stream_k(S, Hq, Hkv):
-    """16 sequences (stream-K); S x g = 4, 8, 8, 8, 4."""
+    """16 sequences (stream-K); S x g = 4, 8, 8, 8, 4, 16, 16, 16."""
     _run_and_check(16, S, Hq, Hkv, [min(p, 8192 - S) for p in POS16], 300 + S * Hq,
                    f"multi S={S} Hq={Hq} Hkv={Hkv} stream-K")
 
 
-@pytest.mark.parametrize("S,Hq,Hkv", [(2, 16, 8), (4, 16, 8), (2, 32, 8)])
+@pytest.mark.parametrize("S,Hq,Hkv", [(2, 16, 8), (4, 16, 8), (2, 32, 8), (2, 64, 8)])
 def test_multi_clusters(S, Hq, Hkv):
     """One or two sequences at the decode shapes (cluster mode)."""
     _run_and_check(1, S, Hq, Hkv, [4094], 310 + S, f"multi S={S} Hq={Hq} B=1")

@@ -48,7 +48,7 @@ def _want(case, window, bs=None):
     return out
 
 
-@pytest.mark.parametrize("g", [1, 2, 4, 8])
+@pytest.mark.parametrize("g", [1, 2, 4, 8, 16])
 @pytest.mark.parametrize("window", [1, 7, 128, 129, 1000])
 def test_window_stream_k(g, window):
     """16 sequences x 2 KV heads (stream-K)."""
