@@ -14,10 +14,9 @@ q and out) / device time of the step, in GB/s; `steps_per_s` is decode steps
 per second.  Extra legs: per-position decode time (warm and cold L2), the
 ragged B=64 batch, the B=256 g=8 stress batch, the ragged batch as a fused
 append step with and without the rotary embedding, the ragged batch over a
-1024-row local window and with two new tokens per sequence, and the causal
-prefill
-workloads (TFLOP/s; also GQA prompt chunks at d_head=128), each against its
-roofline.  The cross-checks time the
+1024-row local window, the ragged and stress batches with two new tokens per
+sequence, and the causal prefill workloads (TFLOP/s; also GQA prompt chunks
+at d_head=128), each against its roofline.  The cross-checks time the
 same 8192 positions as separate append/decode launches, as decode launches
 alone, and as fused steps with the rotary embedding.
 
@@ -775,6 +774,8 @@ def run_ours(args):
                                                  rope=True)
         legs["ragged_window1024"] = _window_leg(torch, ga, synth, "ragged", flush, hbm, 1024)
         legs["ragged_multi_s2"] = _multi_leg(torch, ga, synth, "ragged", flush, hbm, 2)
+        # the stress shapes (g = 8) with 2 new tokens: 16 heads per KV head
+        legs["stress_multi_s2"] = _multi_leg(torch, ga, synth, "stress", flush, hbm, 2)
         for name in ("prefill_prefix", "prefill", "prefill_d128_chunk", "prefill_d128"):
             legs[name] = _prefill_leg(torch, ga, synth, name, flush, tf_burst)
         line["legs"] = legs
