@@ -1,6 +1,7 @@
 // decode_tc.cuh -- split-KV decode attention with both contractions of a
-// tile on the tcgen05 tensor cores: the kernels and their launch, included
-// by one translation unit per group size g (decode_g1.cu ... decode_g8.cu).
+// tile on the tcgen05 tensor cores, for group sizes g = 8 and 16 (g <= 4 runs
+// on CUDA cores, decode_kernels.cuh): the kernels and their launch, included
+// by decode_g8.cu and decode_g16.cu.
 //
 // What it computes ("MiniCPM4 `forward_step` Attention Performance Fix",
 // sections 3 and 4.1): for every sequence b and query head h,
@@ -16,20 +17,21 @@
 // so one 128-key tile is two small dense contractions,
 //   S^T [128 keys x g] = K [128 x 128 dims] . Q^T [128 dims x g]
 //   O^T [128 dims x g] += V^T [128 dims x 128 keys] . P^T [128 keys x g].
-// On CUDA cores their multiply-adds, bf16 unpacking and lane reductions are
-// about 28 warp instructions per key at g = 2, which caps one SM near one
-// tile per 0.45 us -- below what the SM can fetch.  Here each is eight
-// tcgen05.mma (M = 128, N = 16: the g heads padded to 16, K = 16), so a
-// tile costs the CUDA cores only its softmax.
+// On CUDA cores their multiply-adds, bf16 unpacking and lane reductions grow
+// with g; at g = 8 they made that kernel issue-bound (0.66 of HBM on a large
+// batch).  Here each is eight tcgen05.mma (M = 128, N = 16: the g heads
+// padded to 16, K = 16), so a tile costs the CUDA cores only its softmax.
 //
 // Layout per CTA (one per SM):
 //  * warp 4, one thread: 2-D TMA loads (cp.async.bulk.tensor, 128-byte
-//    swizzle) of each tile's K and V into a 2-stage ring, as two 64-dim
-//    column blocks each: exactly the canonical K-major layout of K as the A
-//    operand of S^T, and the MN-major layout of V as the A operand of O^T.
-//  * warp 5, one thread: the MMAs.  Per tile i: S^T_i into tensor memory
-//    (two buffers), then O^T += V^T_{i-1} P^T_{i-1} for the previous tile,
-//    so the softmax of one tile overlaps the tensor core's work on the next.
+//    swizzle) of each tile's K and V into a ring of 3 stages (2 where shared
+//    memory is short), as two 64-dim column blocks each: exactly the
+//    canonical K-major layout of K as the A operand of S^T, and the MN-major
+//    layout of V as the A operand of O^T.
+//  * warp 5, one thread: S^T_i into tensor memory (two buffers); warp 6,
+//    one thread: O^T += V^T_i P^T_i once the softmax wrote P_i, which frees
+//    the tile's stage.  Each blocks on its own barriers, so the softmax of
+//    one tile overlaps the tensor core's work on the next.
 //  * warps 0-3, thread t: key t of a tile (TMEM lane t of S^T) and dim t of
 //    O^T.  A thread reads its key's g scores, the four warps agree on each
 //    head's tile maximum through shared memory, and P (bf16) goes to shared
