@@ -5,7 +5,7 @@ waits for that tile never complete.  Every wait in the
 kernels gives up after 500 ms: the launch must end by itself with
 ATTN_DEV_TIMEOUT in the status word, and the CUDA context must stay usable --
 a normal step right after gives the oracle's result.  Covers cluster mode
-(B=1), stream-K (a batch) and the g=8 kernel without a producer warp.
+and stream-K on both kernels: CUDA cores (g <= 4) and tensor cores (g >= 8).
 """
 
 import numpy as np
@@ -20,7 +20,10 @@ from _helpers import assert_attn_close, f64
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("B,Hq,Hkv", [(1, 16, 8), (16, 8, 2), (16, 16, 2)])
+# CUDA cores: clusters (g=2), stream-K (g=4); tensor cores: stream-K (g=8),
+# clusters (g=8), clusters at g=16 (at most 9 CTAs)
+@pytest.mark.parametrize("B,Hq,Hkv", [(1, 16, 8), (16, 8, 2), (16, 16, 2), (1, 64, 8),
+                                      (4, 32, 2)])
 def test_wait_runs_out_and_the_context_stays_usable(B, Hq, Hkv):
     positions = [700 + 37 * b for b in range(B)]
     case = synth.decode_case(B=B, Hq=Hq, Hkv=Hkv, D=128, L=2048, positions=positions,
