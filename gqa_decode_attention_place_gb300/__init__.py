@@ -21,7 +21,7 @@ __all__ = [
     "AttnError", "load_library", "library_path",
     "attn_kv_append", "attn_decode_workspace_size", "attn_decode_step",
     "attn_prefill_causal", "attn_read_device_status", "attn_status_string",
-    "attn_last_cuda_error", "decode_workspace", "attn_decode_step_noalloc",
+    "attn_read_prefill_status", "attn_last_cuda_error", "decode_workspace", "attn_decode_step_noalloc",
     "attn_decode_step_append", "attn_decode_step_rope_append", "attn_decode_stream_step",
     "attn_decode_step_window", "attn_decode_multi", "attn_test_skip_tile",
 ]
@@ -86,6 +86,8 @@ def load_library(build_if_missing: bool = True) -> ctypes.CDLL:
     lib.attn_prefill_causal.restype = i32
     lib.attn_read_device_status.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32), vp]
     lib.attn_read_device_status.restype = i32
+    lib.attn_read_prefill_status.argtypes = [ctypes.POINTER(ctypes.c_uint32), vp]
+    lib.attn_read_prefill_status.restype = i32
     lib.attn_status_string.argtypes = [i32]
     lib.attn_status_string.restype = ctypes.c_char_p
     lib.attn_last_cuda_error.argtypes = []
@@ -389,6 +391,15 @@ def attn_test_skip_tile(tile: int) -> None:
     """Failure-path tests only: the next decode launches never issue tile
     ``tile`` of the first segment, so the waits for it run out (-1: off)."""
     _raise(load_library().attn_test_skip_tile(int(tile)), "attn_test_skip_tile")
+
+
+def attn_read_prefill_status(stream=None) -> int:
+    """Synchronise, read and clear the count of prefill waits that gave up."""
+    n = ctypes.c_uint32(0)
+    code = load_library().attn_read_prefill_status(ctypes.byref(n), _stream(stream))
+    if code not in (0, 5):
+        raise AttnError(code, "attn_read_prefill_status")
+    return int(n.value)
 
 
 def attn_read_device_status(workspace, stream=None) -> int:

@@ -194,6 +194,14 @@ int attn_prefill_causal(const void* q, const void* k, const void* v, int S, int 
       gqa::launch_prefill(q, k, v, S, start_pos, Hq, Hkv, d, scale, out, stream));
 }
 
+int attn_read_prefill_status(uint32_t* timeouts, cudaStream_t stream) {
+  uint32_t n = 0;
+  const cudaError_t e = gqa::prefill_read_timeouts(&n, stream);
+  if (e != cudaSuccess) return cuda_status(e);
+  if (timeouts) *timeouts = n;
+  return n ? ATTN_ERR_DEVICE : ATTN_OK;
+}
+
 int attn_read_device_status(void* workspace, uint32_t* bits, cudaStream_t stream) {
   if (!workspace) return ATTN_ERR_INVALID_ARG;
   uint32_t word = 0;

@@ -45,5 +45,7 @@ cudaError_t launch_decode_noalloc(const void* q, const int32_t* positions, const
 cudaError_t launch_prefill(const void* q, const void* k, const void* v, int S, int start_pos,
                            int Hq, int Hkv, int d, float scale, void* out,
                            cudaStream_t stream);
+// Prefill waits that gave up since the last call (synchronises the stream).
+cudaError_t prefill_read_timeouts(uint32_t* count, cudaStream_t stream);
 
 }  // namespace gqa

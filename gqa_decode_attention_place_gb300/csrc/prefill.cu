@@ -83,7 +83,7 @@ constexpr int kBarOFree = kBarPVDone + kQT;   // + tile: epilogue has read O
 constexpr int kBarQFree = kBarOFree + kQT;    // QK^T of the item has read Q
 constexpr int kNumBars = kBarQFree + 1;
 
-__device__ unsigned int g_prefill_timeouts;   // diagnostic: waits that gave up
+__device__ unsigned int g_prefill_timeouts;   // CTAs whose wait gave up; read by prefill_read_timeouts
 
 struct PrefillParams {
   uint16_t* out;
@@ -511,6 +511,20 @@ cudaError_t launch_prefill_hd(const CUtensorMap& mq, const CUtensorMap& mk, cons
 }
 
 }  // namespace
+
+// The prefill waits that gave up since the last call (their kernels stopped
+// early, so some output rows were not written); clears the count.
+cudaError_t prefill_read_timeouts(uint32_t* count, cudaStream_t stream) {
+  cudaError_t e = cudaStreamSynchronize(stream);
+  unsigned v = 0;
+  if (e == cudaSuccess) e = cudaMemcpyFromSymbol(&v, g_prefill_timeouts, sizeof(v));
+  if (e == cudaSuccess && v != 0) {
+    const unsigned zero = 0;
+    e = cudaMemcpyToSymbol(g_prefill_timeouts, &zero, sizeof(zero));
+  }
+  *count = v;
+  return e;
+}
 
 cudaError_t launch_prefill(const void* q, const void* k, const void* v, int S, int start_pos,
                            int Hq, int Hkv, int d, float scale, void* out,

@@ -313,10 +313,22 @@ int attn_decode_step_noalloc(const void* q, const int32_t* positions,
  * Supported: d == 64 or d == 128; g = Hq / Hkv >= 1; S >= 0 (S == 0 does nothing);
  * start_pos >= 0; start_pos + S < 2^31.  QK^T and PV run on the tcgen05
  * tensor cores (bf16 operands, fp32 accumulation in tensor memory).
+ *
+ * Every wait in the kernel is bounded: one that runs out ends the launch
+ * early, leaves some output rows unwritten, and is counted on the device;
+ * attn_read_prefill_status reads (and clears) that count.
  */
 int attn_prefill_causal(const void* q, const void* k, const void* v,
                         int S, int start_pos, int Hq, int Hkv, int d, float scale,
                         void* out, cudaStream_t stream);
+
+/*
+ * attn_read_prefill_status -- synchronise `stream`, read into *timeouts the
+ * number of prefill waits that gave up since the last call on this device,
+ * clear it, and return ATTN_OK if there were none, ATTN_ERR_DEVICE if there
+ * were, or ATTN_ERR_CUDA.  `timeouts` may be NULL.
+ */
+int attn_read_prefill_status(uint32_t* timeouts, cudaStream_t stream);
 
 /*
  * attn_read_device_status -- synchronise `stream`, read the device status

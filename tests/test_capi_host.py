@@ -40,7 +40,7 @@ def test_header_declares_the_boundary():
                  "attn_last_cuda_error", "attn_decode_step_append",
                  "attn_decode_step_rope_append", "attn_decode_step_noalloc",
                  "attn_decode_stream_step", "attn_decode_step_window", "attn_decode_multi",
-                 "attn_test_skip_tile"]:
+                 "attn_test_skip_tile", "attn_read_prefill_status"]:
         assert want in names
 
 
