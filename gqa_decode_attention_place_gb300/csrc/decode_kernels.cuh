@@ -1,7 +1,7 @@
 // decode_kernels.cuh -- split-KV decode attention over a static KV cache with
-// GQA on CUDA cores, for group sizes g = 1, 2, 4: the kernels and their
-// launch, included by one translation unit per group size (decode_g1.cu ...
-// decode_g4.cu).  g = 8 runs on the tensor cores (decode_tc.cuh, which also
+// GQA, for group sizes g = 1, 2, 4: the kernels and their launch, included by
+// one translation unit per group size (decode_g1.cu ... decode_g4.cu).
+// g = 8 and 16 run on the tcgen05 tensor cores (decode_tc.cuh, which also
 // uses the segment walk, helpers and merges defined here).
 //
 // What it computes ("MiniCPM4 `forward_step` Attention Performance Fix",
@@ -21,26 +21,33 @@
 //
 // How (GB300 design, not the page's: the page calls PyTorch SDPA):
 //  * The attended rows of every (sequence, KV head) pair -- a "segment" -- are
-//    cut into 128-row tiles, streamed with 1-D bulk copies (TMA) into a
-//    2-stage shared-memory ring guarded by mbarriers (128 KB in flight per
-//    SM) by a producer warp (one thread).  Each tile is read from HBM once
-//    and serves all g query heads of its KV head.
-//  * 8 consumer warps (16 for g=1) each take 16 (8) keys of a tile; a key's
-//    128 dims are spread over 16 lanes, 8 each, as fp32 pairs for the packed
-//    fma.rn.f32x2.  q.k partial sums of the g heads are reduced across the
-//    16 lanes with a transposing butterfly (each shuffle step halves the
-//    number of heads still carried), and the softmax is kept
-//    online in fp32 (running max and sum per head, in base 2 with
-//    scale*log2(e) folded into q).
+//    cut into 128-row tiles, streamed by tiled TMA copies (two 64-dim boxes
+//    per operand, 128-byte swizzle) into a 2-stage shared-memory ring
+//    guarded by mbarriers (128 KB in flight per SM), issued by one producer
+//    thread.  Each tile is read from HBM once and serves all g query heads
+//    of its KV head.
+//  * 8 consumer warps each take 16 keys of a tile and do both products with
+//    warp-level tensor-core MMAs (mma.sync m16n8k16, bf16 in, fp32 out):
+//    S = K q^T with the 16 keys as rows and the g heads as columns, then
+//    O^T += V^T P^T with 16 dims per MMA.  The swizzle makes every
+//    shared-memory read of both products conflict-free; P is moved from the
+//    score layout to the operand layout by an 8x8 transpose in registers
+//    (movmatrix) and enters as two bf16 parts (high and remainder), so the
+//    product keeps about 16 bits of P.  The softmax is kept online in fp32
+//    (running max and sum per head, base 2, scale*log2(e) applied to the fp32
+//    scores).  On CUDA cores the same work took about 28 warp instructions
+//    per key; on these MMAs it takes about 8.
 //  * Two ways to split a segment over CTAs, both computed on the device from
 //    `positions` (one launch serves any positions; graph-capturable):
 //    - cluster mode (few segments, e.g. B=1): one thread-block cluster of C
 //      CTAs (8..16; the largest size that lets every
 //      segment's cluster be resident at once) per segment; CTA rank r takes
-//      tiles [r*n/C, (r+1)*n/C).  Each CTA stores its partial (max, sum,
-//      unnormalised o) straight into rank 0's shared memory (distributed
-//      shared memory); after one cluster barrier rank 0 merges them locally
-//      -- no global scratch, no atomics.
+//      tiles r, r+C, r+2C, ...  Tile r is then rank r's first whatever the
+//      position, so its copy (and the q loads) go out before the position
+//      is read.  Each CTA stores its partial (max, sum, unnormalised o)
+//      straight into rank 0's shared memory (distributed shared memory);
+//      after one cluster barrier rank 0 merges them locally in one pass --
+//      no global scratch, no atomics.
 //    - stream-K mode (many segments): all tiles of all segments form one flat
 //      list; CTA c of a persistent grid (one per SM) takes
 //      [c*T/G, (c+1)*T/G), balanced to one tile however ragged the batch is.
@@ -55,6 +62,7 @@
 #include "common.cuh"
 #include "internal.h"
 #include "decode_params.h"
+#include "tcgen05.cuh"
 
 namespace gqa {
 namespace {
@@ -66,6 +74,7 @@ constexpr int kTile = 128;                         // keys per pipeline stage
 constexpr int kStages = 2;
 constexpr int kRowBytes = kD * 2;
 constexpr int kTileBytes = kTile * kRowBytes;      // 32 KB per operand
+constexpr int kHalf = kTile * 128;                 // one 64-dim box of an operand (16 KB)
 constexpr int kMaxB = kDecodeMaxB;
 constexpr int kMaxGrid = kDecodeMaxGrid;
 constexpr int kMiscInts = 32;                      // [0] abort [1] last [8..8+NW) scan
@@ -94,26 +103,16 @@ __device__ __forceinline__ size_t head_row(const DecodeParams& p, int b, int kvh
   return ((size_t)b * p.S + (h >> lg)) * p.Hq + (size_t)(kvh << lg) + (h & (gr - 1));
 }
 
-// Lanes per key (LPK): a key's 128 dims are spread over LPK lanes of a warp
-// (128/LPK dims each), so a warp takes 32/LPK keys per step.  Fewer lanes
-// per key means fewer shuffle-reduction steps but more q and o registers
-// (128*g/LPK each).  16 lanes for every g: with 8, g = 4 ran at the
-// register cap and spilled in its key loop (12% slower on the ragged batch),
-// and g = 1 and 2 gained nothing from the shorter reduction either.
-// These CUDA-core kernels serve g <= 4; g = 8 runs on the tensor cores
-// (decode_tc.cuh), where its FMA work becomes two small MMAs per tile.
+// The consumers: NW warps of 16 keys each per tile.
 template <int G> struct Cfg {
-  static_assert(G == 1 || G == 2 || G == 4, "the CUDA-core decode serves g <= 4");
-  static constexpr int LPK = 16;
-  static constexpr int NW = (G == 1) ? 16 : 8;
+  static_assert(G == 1 || G == 2 || G == 4, "these decode kernels serve g <= 4");
+  static constexpr int NW = kTile / 16;
   // largest cluster: rank 0 keeps a landing slot for every rank's partial
   // (G x (kD + 2) floats each)
   static constexpr int kMaxC = 16;
   static constexpr int kThreads = (NW + 1) * 32;  // + the producer warp
   static constexpr int kConsumers = NW * 32;
-  static constexpr int kKeysPerWarp = kTile / NW;  // 16 or 8
-  static constexpr int kKeysPerStep = 32 / LPK;    // 2
-  static constexpr int kIters = kKeysPerWarp / kKeysPerStep;
+  static constexpr int kKeysPerWarp = kTile / NW;  // 16
   // registers per thread that still let one CTA of kThreads fit the SM
   // (the register file is handed out as if the block were a multiple of
   // 128 threads)
@@ -204,39 +203,6 @@ template <> struct Log2<8> { static constexpr int v = 3; };
 template <> struct Log2<16> { static constexpr int v = 4; };
 template <> struct Log2<32> { static constexpr int v = 5; };
 
-// Sum of acc[h] over the LPK lanes holding one key, for every head at once.
-// A step with offset `off` keeps half of the heads and ships the other half
-// to the partner lane, so after log2(G) steps each lane carries one head:
-// head = lk >> (log2 LPK - log2 G).  The remaining steps are a plain butterfly.
-template <int G, int LPK>
-__device__ __forceinline__ float reduce_key(float (&acc)[G], int lk) {
-  constexpr int LG = Log2<G>::v;
-#pragma unroll
-  for (int st = 0; st < LG; ++st) {
-    const int off = (LPK / 2) >> st;
-    const int n = G >> (st + 1);
-    const bool upper = (lk & off) != 0;
-#pragma unroll
-    for (int i = 0; i < n; ++i) {
-      const float keep = upper ? acc[n + i] : acc[i];
-      const float send = upper ? acc[i] : acc[n + i];
-      acc[i] = keep + __shfl_xor_sync(0xffffffffu, send, off);
-    }
-  }
-  float v = acc[0];
-#pragma unroll
-  for (int off = (LPK / 2) >> LG; off >= 1; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
-  return v;
-}
-
-// 8 bf16 (one 16-byte vector) -> 4 fp32 pairs (dims 2i, 2i+1).
-__device__ __forceinline__ void unpack8x2(const uint4& u, f2 (&f)[4]) {
-  f[0] = mk2(bf16lo(u.x), bf16hi(u.x));
-  f[1] = mk2(bf16lo(u.y), bf16hi(u.y));
-  f[2] = mk2(bf16lo(u.z), bf16hi(u.z));
-  f[3] = mk2(bf16lo(u.w), bf16hi(u.w));
-}
-
 // Rotary embedding, rotate-half form, on N consecutive dims x of a row whose
 // partner dims (64 away) are y: x' = x*cos + r*sin with r = -y in the first
 // half of the row and r = y in the second.  Each product and the sum are
@@ -248,205 +214,251 @@ __device__ __forceinline__ float rope1(float x, float partner, float c, float sn
   return __fadd_rn(__fmul_rn(x, c), __fmul_rn(r, sn));
 }
 
-// Per-warp consumer state and math: one KV head's g query heads.  Lane
-// `lane` works on key group grp = lane / LPK (32/LPK keys per step) and holds
-// 128/LPK dims of that key: VPL 16-byte vectors, vector v covering dims
-// 8*(lk + LPK*v) .. +8 (lk = lane % LPK), as fp32 pairs for fma.rn.f32x2.
+// ---- warp-level tensor-core products (mma.sync m16n8k16, bf16 -> fp32) ----
+// Fragment layouts (lane = 4*g + t): A (16x16, row-major) holds
+// {A[g][2t..2t+1], A[g+8][2t..2t+1], A[g][2t+8..2t+9], A[g+8][2t+8..2t+9]};
+// B (16x8, column-major) holds {B[2t..2t+1][g], B[2t+8..2t+9][g]}; the
+// accumulator holds {C[g][2t], C[g][2t+1], C[g+8][2t], C[g+8][2t+1]}.  Each
+// 32-bit register carries two bf16, the lower index in the low half.
+__device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                         uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+// Transpose of an 8x8 matrix of 16-bit values held as one row pair per lane
+// (lane 4r + c holds row r, columns 2c and 2c+1).
+__device__ __forceinline__ uint32_t movm_trans(uint32_t x) {
+  uint32_t y;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+  return y;
+}
+// Bytes of a and b picked by `sel` (prmt): 0x5410 gives {a.lo, b.lo},
+// 0x7632 gives {a.hi, b.hi}.
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t d;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+  return d;
+}
+__device__ __forceinline__ uint4 lds128(const uint8_t* p) {
+  return *reinterpret_cast<const uint4*>(p);
+}
+__device__ __forceinline__ uint32_t word(const uint4& u, int i) {
+  return i == 0 ? u.x : i == 1 ? u.y : i == 2 ? u.z : u.w;
+}
+// Byte offset of row r, dims 8c..8c+7 within one 64-dim box of a tile, as the
+// 128-byte swizzle of the tiled copy lays it out (16-byte chunk c of row r
+// sits at chunk c ^ (r mod 8); the stage buffers are 1024-byte aligned).
+__device__ __forceinline__ int sw128(int r, int c) { return r * 128 + ((c ^ (r & 7)) << 4); }
+// Byte offset of dims 8q..8q+7 (q = 0..15) of row r of a K or V tile.
+__device__ __forceinline__ int tile_chunk(int r, int q) { return (q >> 3) * kHalf + sw128(r, q & 7); }
+
+// Per-warp consumer state and math: one KV head's g query heads, 16 keys
+// (kw .. kw+15) of each tile.  Lane 4g+t.
+//  * Scores: S = K q^T, an m16n8k16 per 16 dims: the 16 keys are the rows,
+//    heads the 8 columns (column h < g is head h; with the rotary embedding
+//    column g+h carries the low bf16 part of rotated head h).  The 16 dims of
+//    MMA step 2j+s are dims 64*(j/2) + 8*((j%2)*4 + t) + 4s .. +4 in lane t,
+//    the same for the key rows (A) and for q (B), so one 16-byte read per key
+//    row and lane feeds two MMAs and the 8 rows of each read hit 8 different
+//    swizzle chunks.  Lane 4g+t ends with the scores of keys kw+g and
+//    kw+g+8 for heads 2t and 2t+1.
+//  * P^T (keys x heads) is that score layout transposed in 8x8 blocks.
+//  * Output: O^T += V^T P^T, m-block mb (0..7) holding dims 8g+mb (row g)
+//    and 64+8g+mb (row g+8): lane 4g+t reads 16 bytes of dims 8g.. and
+//    64+8g.. of keys kw+2t, kw+2t+1, kw+2t+8, kw+2t+9 and pairs the keys
+//    with prmt.  It accumulates O^T for those dims and heads 2t, 2t+1.
 template <int G>
 struct Consumer {
-  static constexpr int LG = Log2<G>::v;
-  static constexpr int LPK = Cfg<G>::LPK;
-  static constexpr int LL = Log2<LPK>::v;
-  static constexpr int VPL = 16 / LPK;             // 16-byte vectors per lane per row
-  static constexpr int NP = 4 * VPL;               // fp32 pairs per lane per row
-  static constexpr int KPS = Cfg<G>::kKeysPerStep;
-  static constexpr int KPW = Cfg<G>::kKeysPerWarp;
-  static constexpr int IT = Cfg<G>::kIters;
   static constexpr float kTau = 8.0f;  // a stale running max may lag by 2^8
-  f2 qf[G][NP];  // q[h][lane dims], pre-scaled by scale*log2(e)
-  f2 o[G][NP];   // unnormalised output accumulators, same layout
-  float m_run, l_run;  // for head hd (the same in every key group)
-  int grp, lk, hd;
-  int head_last;       // multi-token decode: last row head hd's token may see
+  uint32_t qb[4][4];   // q^T as B operand, [dim group j][register]
+  float o[8][4];       // O^T accumulators per m-block
+  float m_run[2], l_run[2];  // heads 2t, 2t+1; l_run sums this lane's keys only
+  int g, t;
+  int head_last[2];    // multi-token decode: last row heads 2t, 2t+1 may see
+  float qs;            // scale * log2(e), applied to the fp32 scores
 
   __device__ __forceinline__ void init(int lane) {
-    grp = lane >> LL;
-    lk = lane & (LPK - 1);
-    hd = lk >> (LL - LG);  // head whose score this lane ends up with
+    g = lane >> 2;
+    t = lane & 3;
   }
-  __device__ __forceinline__ int dim_off(int v) const { return (lk + LPK * v) * 16; }  // bytes
-  // the G query rows of KV head kvh of sequence b (head_row)
+  // the G query rows of KV head kvh of sequence b (head_row), bf16 as stored
   template <bool MT>
   __device__ __forceinline__ void load_q(const DecodeParams& p, int b, int kvh, float qscale) {
+    qs = qscale;
 #pragma unroll
-    for (int h = 0; h < G; ++h)
-#pragma unroll
-      for (int v = 0; v < VPL; ++v) {
-        const uint4 u = *reinterpret_cast<const uint4*>(
-            reinterpret_cast<const uint8_t*>(p.q + head_row<G, MT>(p, b, kvh, h) * kD) +
-            dim_off(v));
-        const uint32_t wd[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-          qf[h][4 * v + j] = mk2(bf16lo(wd[j]) * qscale, bf16hi(wd[j]) * qscale);
-      }
+    for (int j = 0; j < 4; ++j) {
+      uint4 u = make_uint4(0u, 0u, 0u, 0u);
+      if (g < G)
+        u = *reinterpret_cast<const uint4*>(
+            reinterpret_cast<const uint8_t*>(p.q + head_row<G, MT>(p, b, kvh, g) * kD) +
+            (j >> 1) * 128 + (((j & 1) * 4 + t) << 4));
+      qb[j][0] = u.x;
+      qb[j][1] = u.y;
+      qb[j][2] = u.z;
+      qb[j][3] = u.w;
+    }
   }
-  // The same from the rotated query, q_rot [G][kD] fp32 in shared memory.
+  // The rotated query, q_rot [G][kD] fp32 in shared memory: column h < G
+  // takes its bf16 rounding, column G+h the rounding of what is left.
   __device__ __forceinline__ void load_q_rot(const float* q_rot, float qscale) {
+    qs = qscale;
+    const int h = g < G ? g : g - G;
 #pragma unroll
-    for (int h = 0; h < G; ++h)
+    for (int j = 0; j < 4; ++j) {
+      const int d0 = (j >> 1) * 64 + ((j & 1) * 4 + t) * 8;
 #pragma unroll
-      for (int v = 0; v < VPL; ++v) {
-        const float* src = q_rot + h * kD + dim_off(v) / 2;
-        const float4 a = *reinterpret_cast<const float4*>(src);
-        const float4 c = *reinterpret_cast<const float4*>(src + 4);
-        qf[h][4 * v + 0] = mk2(a.x * qscale, a.y * qscale);
-        qf[h][4 * v + 1] = mk2(a.z * qscale, a.w * qscale);
-        qf[h][4 * v + 2] = mk2(c.x * qscale, c.y * qscale);
-        qf[h][4 * v + 3] = mk2(c.z * qscale, c.w * qscale);
+      for (int r = 0; r < 4; ++r) {
+        uint32_t w = 0u;
+        if (g < 2 * G) {
+          const float x0 = q_rot[h * kD + d0 + 2 * r], x1 = q_rot[h * kD + d0 + 2 * r + 1];
+          const uint32_t hi = pack_bf16x2(x0, x1);
+          w = g < G ? hi : pack_bf16x2(x0 - bf16lo(hi), x1 - bf16hi(hi));
+        }
+        qb[j][r] = w;
       }
+    }
+  }
+  // multi-token decode: head h (token h / (G/S)) sees rows up to base + token
+  __device__ __forceinline__ void set_last(int base, int S) {
+#pragma unroll
+    for (int e = 0; e < 2; ++e) head_last[e] = base + (2 * t + e) / (G / S);
   }
   __device__ __forceinline__ void reset() {
-    m_run = -INFINITY;
-    l_run = 0.f;
 #pragma unroll
-    for (int h = 0; h < G; ++h)
-#pragma unroll
-      for (int j = 0; j < NP; ++j) o[h][j] = mk2(0.f, 0.f);
-  }
-  // Scores (log2 domain) of this warp's keys of a tile; keys >= rows
-  // are invalid (the rest of the stage may hold anything) and get -inf.
-  // rows: keys of the tile this lane's head may see (all valid rows, or fewer
-  // for an early token of a multi-token step)
-  __device__ __forceinline__ void qk(const uint8_t* Ks, int rows, int warp, float (&sc)[IT]) {
-#pragma unroll
-    for (int it = 0; it < IT; ++it) {
-      const int key = warp * KPW + it * KPS + grp;
-      f2 a[G];
-#pragma unroll
-      for (int v = 0; v < VPL; ++v) {
-        const uint4 kv = *reinterpret_cast<const uint4*>(Ks + key * kRowBytes + dim_off(v));
-        f2 kf[4];
-        unpack8x2(kv, kf);
-#pragma unroll
-        for (int h = 0; h < G; ++h)
-#pragma unroll
-          for (int j = 0; j < 4; ++j)
-            a[h] = (v == 0 && j == 0) ? mul2(qf[h][0], kf[0]) : fma2(qf[h][4 * v + j], kf[j], a[h]);
-      }
-      float acc[G];
-#pragma unroll
-      for (int h = 0; h < G; ++h) {
-        float lo, hi;
-        brk2(a[h], lo, hi);
-        acc[h] = lo + hi;
-      }
-      const float sv = reduce_key<G, LPK>(acc, lk);
-      sc[it] = (key < rows) ? sv : -INFINITY;
-    }
-  }
-  // Online softmax for head hd over the tile's scores -> probabilities pr.
-  __device__ __forceinline__ void softmax(const float (&sc)[IT], float (&pr)[IT]) {
-    float mx = sc[0];
-#pragma unroll
-    for (int it = 1; it < IT; ++it) mx = fmaxf(mx, sc[it]);
-#pragma unroll
-    for (int off = LPK; off < 32; off <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-    // Raise the running max only when it grows by more than 2^kTau (the
-    // first valid tile always does): p may then reach 2^kTau, harmless in
-    // fp32, and most tiles skip the rescale of o.
-    const bool grow = mx > m_run + kTau;
-    if (__any_sync(0xffffffffu, grow)) {
-      const float alpha = grow ? ex2(m_run - mx) : 1.f;  // m_run = -inf: 0
-      if (grow) m_run = mx;
-      l_run *= alpha;
-#pragma unroll
-      for (int h = 0; h < G; ++h) {
-        const float ah = __shfl_sync(0xffffffffu, alpha, h << (LL - LG));
-        const f2 a2 = mk2(ah, ah);
-#pragma unroll
-        for (int j = 0; j < NP; ++j) o[h][j] = mul2(o[h][j], a2);
-      }
-    }
-    const float m_use = (m_run == -INFINITY) ? 0.f : m_run;  // no valid key yet
-    float ps = 0.f;
-#pragma unroll
-    for (int it = 0; it < IT; ++it) {
-      pr[it] = ex2(sc[it] - m_use);
-      ps += pr[it];
+    for (int e = 0; e < 2; ++e) {
+      m_run[e] = -INFINITY;
+      l_run[e] = 0.f;
     }
 #pragma unroll
-    for (int off = LPK; off < 32; off <<= 1) ps += __shfl_xor_sync(0xffffffffu, ps, off);
-    l_run += ps;
+    for (int mb = 0; mb < 8; ++mb)
+#pragma unroll
+      for (int c = 0; c < 4; ++c) o[mb][c] = 0.f;
   }
-  // o += p * v over this warp's keys of a tile.
-  __device__ __forceinline__ void pv(const uint8_t* Vs, int rows, int warp, const float (&pr)[IT]) {
-#pragma unroll
-    for (int it = 0; it < IT; ++it) {
-      const int key = warp * KPW + it * KPS + grp;
-      float ph[G];
-#pragma unroll
-      for (int h = 0; h < G; ++h)
-        ph[h] = __shfl_sync(0xffffffffu, pr[it], (grp << LL) | (h << (LL - LG)));
-      const bool valid = key < rows;  // invalid: p = 0, and v forced to 0 (stale smem)
-#pragma unroll
-      for (int v = 0; v < VPL; ++v) {
-        uint4 vv = *reinterpret_cast<const uint4*>(Vs + key * kRowBytes + dim_off(v));
-        vv.x = valid ? vv.x : 0u;
-        vv.y = valid ? vv.y : 0u;
-        vv.z = valid ? vv.z : 0u;
-        vv.w = valid ? vv.w : 0u;
-        f2 vf[4];
-        unpack8x2(vv, vf);
-#pragma unroll
-        for (int h = 0; h < G; ++h) {
-          const f2 p2 = mk2(ph[h], ph[h]);
-#pragma unroll
-          for (int j = 0; j < 4; ++j) o[h][4 * v + j] = fma2(p2, vf[j], o[h][4 * v + j]);
-        }
-      }
-    }
-  }
-  // One tile: scores, online softmax, P.V.
-  __device__ __forceinline__ void tile(const uint8_t* Ks, const uint8_t* Vs, int rows, int rows_h,
+  // One tile: rows valid rows from absolute row row0 (multi-token decode:
+  // head 2t+e only up to head_last[e]).  Rows past `rows` may hold anything.
+  template <bool MT, bool R>
+  __device__ __forceinline__ void tile(const uint8_t* Ks, const uint8_t* Vs, int rows, int row0,
                                        int warp) {
-    float sc[IT], pr[IT];
-    qk(Ks, rows_h, warp, sc);
-    softmax(sc, pr);
-    pv(Vs, rows, warp, pr);
+    const int kw = warp * 16;
+    if (kw >= rows) return;  // no valid key for this warp (warp-uniform)
+    float s[4] = {0.f, 0.f, 0.f, 0.f}, s2[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int c = (j & 1) * 4 + t;
+      const uint8_t* base = Ks + (j >> 1) * kHalf;
+      const uint4 ka = lds128(base + sw128(kw + g, c));
+      const uint4 kb = lds128(base + sw128(kw + g + 8, c));
+      mma16816(s, ka.x, kb.x, ka.y, kb.y, qb[j][0], qb[j][1]);
+      mma16816(s2, ka.z, kb.z, ka.w, kb.w, qb[j][2], qb[j][3]);
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) s[i] += s2[i];
+    if (R) {  // add the low parts' column G+h onto head h
+      if (G == 1) {
+        s[0] += s[1];
+        s[2] += s[3];
+      } else {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) s[i] += __shfl_xor_sync(0xffffffffu, s[i], G / 2);
+      }
+    }
+    float x[4];  // log2-domain scores; invalid keys -inf
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int key = kw + g + (i >> 1) * 8;
+      const int lim = MT ? min(rows, head_last[i & 1] + 1 - row0) : rows;
+      x[i] = key < lim ? s[i] * qs : -INFINITY;
+    }
+    float mx[2];
+    bool grow[2];
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      mx[e] = fmaxf(x[e], x[2 + e]);
+#pragma unroll
+      for (int off = 4; off < 32; off <<= 1)
+        mx[e] = fmaxf(mx[e], __shfl_xor_sync(0xffffffffu, mx[e], off));
+      // raise the running max only when it grows by more than 2^kTau (the
+      // first valid tile always does); columns past the heads never do
+      grow[e] = (2 * t + e < G) && mx[e] > m_run[e] + kTau;
+    }
+    if (__any_sync(0xffffffffu, grow[0] || grow[1])) {
+      float alpha[2];
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        alpha[e] = grow[e] ? ex2(m_run[e] - mx[e]) : 1.f;  // m_run = -inf: 0
+        if (grow[e]) m_run[e] = mx[e];
+        l_run[e] *= alpha[e];
+      }
+#pragma unroll
+      for (int mb = 0; mb < 8; ++mb) {
+        o[mb][0] *= alpha[0];
+        o[mb][1] *= alpha[1];
+        o[mb][2] *= alpha[0];
+        o[mb][3] *= alpha[1];
+      }
+    }
+    float pr[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float mu = m_run[i & 1] == -INFINITY ? 0.f : m_run[i & 1];  // no valid key yet
+      pr[i] = ex2(x[i] - mu);
+    }
+    l_run[0] += pr[0] + pr[2];
+    l_run[1] += pr[1] + pr[3];
+    // P^T as B operands: bf16 high parts and the bf16 rounding of the rest
+    const uint32_t h0 = pack_bf16x2(pr[0], pr[1]), h1 = pack_bf16x2(pr[2], pr[3]);
+    const uint32_t l0 = pack_bf16x2(pr[0] - bf16lo(h0), pr[1] - bf16hi(h0));
+    const uint32_t l1 = pack_bf16x2(pr[2] - bf16lo(h1), pr[3] - bf16hi(h1));
+    const uint32_t bh0 = movm_trans(h0), bh1 = movm_trans(h1);
+    const uint32_t bl0 = movm_trans(l0), bl1 = movm_trans(l1);
+    const int r0 = kw + 2 * t;
+    uint4 v[4][2];  // keys r0, r0+1, r0+8, r0+9; dims 8g.. and 64+8g..
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+#pragma unroll
+      for (int h = 0; h < 2; ++h)
+        v[k][h] = lds128(Vs + h * kHalf + sw128(r0 + (k & 1) + (k >> 1) * 8, g));
+    if (kw + 16 > rows) {  // V rows past the valid ones may be NaN: 0 * NaN would spread
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        if (r0 + (k & 1) + (k >> 1) * 8 >= rows) v[k][0] = v[k][1] = make_uint4(0u, 0u, 0u, 0u);
+    }
+#pragma unroll
+    for (int mb = 0; mb < 8; ++mb) {
+      const uint32_t sel = (mb & 1) ? 0x7632u : 0x5410u;
+      const int w = mb >> 1;
+      const uint32_t a0 = prmt(word(v[0][0], w), word(v[1][0], w), sel);
+      const uint32_t a1 = prmt(word(v[0][1], w), word(v[1][1], w), sel);
+      const uint32_t a2 = prmt(word(v[2][0], w), word(v[3][0], w), sel);
+      const uint32_t a3 = prmt(word(v[2][1], w), word(v[3][1], w), sel);
+      mma16816(o[mb], a0, a1, a2, a3, bh0, bh1);
+      mma16816(o[mb], a0, a1, a2, a3, bl0, bl1);
+    }
   }
-  // This warp's (m, l, o) -> merge buffers [warp][G][...]: the key groups
-  // hold partial o for the same (m, l), so they are added first.
+  // This warp's (m, l, o) -> merge buffers [warp][G][...]
   __device__ __forceinline__ void stash(float* merge_o, float* merge_ml, int warp) {
 #pragma unroll
-    for (int h = 0; h < G; ++h)
+    for (int e = 0; e < 2; ++e)
 #pragma unroll
-      for (int j = 0; j < NP; ++j) {
-        float lo, hi;
-        brk2(o[h][j], lo, hi);
+      for (int off = 4; off < 32; off <<= 1)
+        l_run[e] += __shfl_xor_sync(0xffffffffu, l_run[e], off);
 #pragma unroll
-        for (int off = LPK; off < 32; off <<= 1) {
-          lo += __shfl_xor_sync(0xffffffffu, lo, off);
-          hi += __shfl_xor_sync(0xffffffffu, hi, off);
+    for (int e = 0; e < 2; ++e) {
+      const int h = 2 * t + e;
+      if (h < G) {
+        float* dst = merge_o + (warp * G + h) * kD + 8 * g;
+        reinterpret_cast<float4*>(dst)[0] = make_float4(o[0][e], o[1][e], o[2][e], o[3][e]);
+        reinterpret_cast<float4*>(dst)[1] = make_float4(o[4][e], o[5][e], o[6][e], o[7][e]);
+        reinterpret_cast<float4*>(dst + 64)[0] =
+            make_float4(o[0][2 + e], o[1][2 + e], o[2][2 + e], o[3][2 + e]);
+        reinterpret_cast<float4*>(dst + 64)[1] =
+            make_float4(o[4][2 + e], o[5][2 + e], o[6][2 + e], o[7][2 + e]);
+        if (g == 0) {
+          merge_ml[(warp * G + h) * 2 + 0] = m_run[e];
+          merge_ml[(warp * G + h) * 2 + 1] = l_run[e];
         }
-        o[h][j] = mk2(lo, hi);
-      }
-    if (grp == 0) {
-#pragma unroll
-      for (int h = 0; h < G; ++h)
-#pragma unroll
-        for (int v = 0; v < VPL; ++v) {
-          float f[8];
-#pragma unroll
-          for (int j = 0; j < 4; ++j) brk2(o[h][4 * v + j], f[2 * j], f[2 * j + 1]);
-          float4* dst = reinterpret_cast<float4*>(
-              reinterpret_cast<uint8_t*>(merge_o + (warp * G + h) * kD) + dim_off(v) * 2);
-          dst[0] = make_float4(f[0], f[1], f[2], f[3]);
-          dst[1] = make_float4(f[4], f[5], f[6], f[7]);
-        }
-      if (lk == (hd << (LL - LG))) {
-        merge_ml[(warp * G + hd) * 2 + 0] = m_run;
-        merge_ml[(warp * G + hd) * 2 + 1] = l_run;
       }
     }
   }
@@ -471,35 +483,25 @@ __device__ __forceinline__ void merge_warps(const float* merge_o, const float* m
   }
 }
 
-// Producer (one thread): one tile's bulk copies.  With the fused append the
-// segment's last tile ends with row pos = n-1, taken from k_new/v_new instead
-// of the cache; a consumer warp rotates it if asked and writes it to the
-// cache (fresh_row).  No other CTA reads that row.
-__device__ __forceinline__ void produce_tile(const Params& p, uint8_t* stages, uint64_t* bars,
-                                             int s, int b, int kvh, int k, int ntiles, int n,
-                                             int lo) {
+// Producer (one thread): tile k of a segment, rows lo + k*kTile .. +kTile of
+// sequence b, KV head kvh, as four tiled copies (K and V, two 64-dim boxes
+// each).  Rows past the cache's end arrive as zeros; rows past the attended
+// ones are masked by the consumers.  The transaction count is the full box.
+__device__ __forceinline__ void produce_tile(const CUtensorMap* tmk, const CUtensorMap* tmv,
+                                             const Params& p, uint8_t* stages, uint64_t* bars,
+                                             int s, int b, int kvh, int k, int lo) {
   // failure-path tests only: tile test_skip of the first segment is never
   // issued, so the bounded waits for it run out (ATTN_DEV_TIMEOUT)
   if (p.test_skip >= 0 && b == 0 && kvh == 0 && k == p.test_skip) return;
-  const int rows = min(kTile, n - k * kTile);
-  const size_t row0 = ((size_t)b * p.Hkv + kvh) * (size_t)p.L + (size_t)lo + (size_t)k * kTile;
-  const bool fresh = p.k_new != nullptr && k == ntiles - 1;
-  const int cache_rows = fresh ? rows - 1 : rows;
   const uint32_t full = smem_u32(&bars[s]);
   const uint32_t sK = smem_u32(stages + (size_t)s * 2 * kTileBytes);
   const uint32_t sV = sK + kTileBytes;
-  mbar_arrive_expect_tx(full, 2u * (uint32_t)rows * kRowBytes);
-  if (cache_rows > 0) {
-    const uint32_t bytes = (uint32_t)cache_rows * kRowBytes;
-    bulk_g2s(sK, p.k_cache + row0 * kRowBytes, bytes, full);
-    bulk_g2s(sV, p.v_cache + row0 * kRowBytes, bytes, full);
-  }
-  if (fresh) {
-    const size_t src = ((size_t)b * p.Hkv + kvh) * kRowBytes;
-    const uint32_t off = (uint32_t)cache_rows * kRowBytes;
-    bulk_g2s(sK + off, p.k_new + src, kRowBytes, full);
-    bulk_g2s(sV + off, p.v_new + src, kRowBytes, full);
-  }
+  const int row = lo + k * kTile, z = b * p.Hkv + kvh;
+  mbar_arrive_expect_tx(full, 2u * kTileBytes);
+  tma_load_3d(sK, tmk, 0, row, z, full);
+  tma_load_3d(sK + kHalf, tmk, 64, row, z, full);
+  tma_load_3d(sV, tmv, 0, row, z, full);
+  tma_load_3d(sV + kHalf, tmv, 64, row, z, full);
 }
 
 // Rotary embedding of one segment, by the consumers.  rope_segment (all NC
@@ -524,23 +526,6 @@ __device__ __forceinline__ void rope_segment(const uint16_t* qb, const float* rc
   for (int i = ct; i < 2 * kD; i += NC) rope_cs[i] = i < kD ? rc[i] : rs[i - kD];
 }
 
-__device__ __forceinline__ void rope_fresh_key(uint8_t* row, const float* rope_cs, int lane) {
-  const int d0 = 4 * lane;
-  const uint2 a = *reinterpret_cast<const uint2*>(row + d0 * 2);
-  const uint2 y2 = *reinterpret_cast<const uint2*>(row + (d0 ^ 64) * 2);
-  __syncwarp();
-  const float4 c4 = *reinterpret_cast<const float4*>(rope_cs + d0);
-  const float4 s4 = *reinterpret_cast<const float4*>(rope_cs + kD + d0);
-  float x[4] = {bf16lo(a.x), bf16hi(a.x), bf16lo(a.y), bf16hi(a.y)};
-  const float y[4] = {bf16lo(y2.x), bf16hi(y2.x), bf16lo(y2.y), bf16hi(y2.y)};
-  const float c[4] = {c4.x, c4.y, c4.z, c4.w};
-  const float sn[4] = {s4.x, s4.y, s4.z, s4.w};
-#pragma unroll
-  for (int j = 0; j < 4; ++j) x[j] = rope1(x[j], y[j], c[j], sn[j], d0 < kD / 2);
-  *reinterpret_cast<uint2*>(row + d0 * 2) =
-      make_uint2(pack_bf16x2(x[0], x[1]), pack_bf16x2(x[2], x[3]));
-}
-
 // A consumer warp's wait for a tile, with the outcome made warp-uniform (the
 // tile math uses full-warp shuffles, so either every lane goes on or every
 // lane leaves the loop).
@@ -555,31 +540,50 @@ __device__ __forceinline__ bool consumer_wait(uint32_t bar, uint32_t parity,
   return false;
 }
 
-// The fused append's cache write: once a segment's last tile has landed, the
-// appended K and V rows (its last row, rotated key included) go from shared
-// memory to cache row pos = n-1, one 16-byte store per lane of one warp
-// (lanes 0-15 the K row, 16-31 the V row).
-__device__ __forceinline__ void write_fresh_rows(const Params& p, const uint8_t* Ks, int rows,
-                                                 int b, int kvh, int pos, int lane) {
-  const int c = lane & 15;
-  const bool is_v = lane >= 16;
-  const uint8_t* src = Ks + (is_v ? kTileBytes : 0) + (size_t)(rows - 1) * kRowBytes + c * 16;
-  uint8_t* dst = (is_v ? p.v_cache : p.k_cache) +
-                 (((size_t)b * p.Hkv + kvh) * (size_t)p.L + (size_t)pos) * kRowBytes + c * 16;
-  *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<const uint4*>(src);
+// The fused append.  Lane l of the one consumer warp whose keys include the
+// segment's last row (row pos = n-1 of the last tile) holds 16 bytes of the
+// new rows: lanes 0-15 dims 8l..8l+7 of k_new, lanes 16-31 those of v_new
+// (load_fresh, issued when the segment starts).  Once the tile has landed
+// (its copy brought the stale cache row), fresh_row rotates the key if asked
+// (the partner dims, 64 away, are in lane l^8), writes the row into the
+// tile's shared memory and to cache row pos.  No other warp reads that row
+// and no other CTA reads it in this launch.
+__device__ __forceinline__ uint4 load_fresh(const Params& p, int b, int kvh, int lane) {
+  const uint8_t* src = (lane < 16 ? p.k_new : p.v_new) +
+                       ((size_t)b * p.Hkv + kvh) * kRowBytes + (lane & 15) * 16;
+  return *reinterpret_cast<const uint4*>(src);
 }
 
-// The appended row of a segment's last tile, by the one consumer warp whose
-// keys include it (row rows-1): rotated in place first with the rotary
-// embedding, then written to the cache.  No other warp reads the K row.
 template <bool R>
 __device__ __forceinline__ void fresh_row(const Params& p, uint8_t* Ks, int rows, int b, int kvh,
-                                          int pos, const float* rope_cs, int lane) {
+                                         int pos, const float* rope_cs, uint4 u, int lane) {
+  const int q = lane & 15;  // 16-byte chunk of the row: dims 8q..8q+7
   if (R) {
-    rope_fresh_key(Ks + (size_t)(rows - 1) * kRowBytes, rope_cs, lane);
-    __syncwarp();
+    uint4 y;
+    y.x = __shfl_xor_sync(0xffffffffu, u.x, 8);
+    y.y = __shfl_xor_sync(0xffffffffu, u.y, 8);
+    y.z = __shfl_xor_sync(0xffffffffu, u.z, 8);
+    y.w = __shfl_xor_sync(0xffffffffu, u.w, 8);
+    if (lane < 16) {
+      const int d0 = 8 * q;
+      const uint32_t xs[4] = {u.x, u.y, u.z, u.w}, ys[4] = {y.x, y.y, y.z, y.w};
+      uint32_t r[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int d = d0 + 2 * i;
+        r[i] = pack_bf16x2(
+            rope1(bf16lo(xs[i]), bf16lo(ys[i]), rope_cs[d], rope_cs[kD + d], d < kD / 2),
+            rope1(bf16hi(xs[i]), bf16hi(ys[i]), rope_cs[d + 1], rope_cs[kD + d + 1], d < kD / 2));
+      }
+      u = make_uint4(r[0], r[1], r[2], r[3]);
+    }
   }
-  write_fresh_rows(p, Ks, rows, b, kvh, pos, lane);
+  const bool is_v = lane >= 16;
+  *reinterpret_cast<uint4*>(Ks + (is_v ? kTileBytes : 0) + tile_chunk(rows - 1, q)) = u;
+  *reinterpret_cast<uint4*>((is_v ? p.v_cache : p.k_cache) +
+                            (((size_t)b * p.Hkv + kvh) * (size_t)p.L + (size_t)pos) * kRowBytes +
+                            q * 16) = u;
+  __syncwarp();
 }
 
 // The rotation row of sequence b at position pos: row b of a [B, D] table,
@@ -632,7 +636,9 @@ size_t smem_bytes(int B) {
 
 // ---------------------------------------------------------- stream-K mode --
 template <int G, int M>
-__global__ void __maxnreg__(Cfg<G>::kMaxRegs) decode_splitkv_kernel(const Params p) {
+__global__ void __maxnreg__(Cfg<G>::kMaxRegs) decode_splitkv_kernel(const __grid_constant__ CUtensorMap tm_k,
+                                                                   const __grid_constant__ CUtensorMap tm_v,
+                                                                   const Params p) {
   constexpr bool R = (M & kModeRope) != 0, A = (M & kModeAdvance) != 0;
   constexpr bool MT = (M & kModeMulti) != 0;
   constexpr int NW = Cfg<G>::NW;
@@ -744,7 +750,7 @@ __global__ void __maxnreg__(Cfg<G>::kMaxRegs) decode_splitkv_kernel(const Params
           set_status(p.status, ATTN_DEV_TIMEOUT);
           break;
         }
-        produce_tile(p, stages, bars, s, w.b, w.kvh, w.k, w.ntiles, w.n, w.lo);
+        produce_tile(&tm_k, &tm_v, p, stages, bars, s, w.b, w.kvh, w.k, w.lo);
         walk_next(w, prefix, p.positions, B, Hkv, win, shift);
       }
       if (A) mbar_arrive(smem_u32(&bars[2 * kStages + 1]));  // no more reads of positions
@@ -759,7 +765,15 @@ __global__ void __maxnreg__(Cfg<G>::kMaxRegs) decode_splitkv_kernel(const Params
   Walk w;
   walk_init(w, t0, prefix, p.positions, B, Hkv, win, shift);
   const uint16_t* qb = p.q + ((size_t)w.b * p.Hq + (size_t)w.kvh * G) * kD;
-  if (MT) cs.head_last = w.lo + w.n - 1 - shift + cs.hd / (G / p.S);
+  if (MT) cs.set_last(w.lo + w.n - 1 - shift, p.S);
+  // fused append: this warp writes the segment's new rows if the segment's
+  // last tile is in this CTA's range and its last row among the warp's keys
+  auto owns_fresh = [&](long long t) {
+    return p.k_new != nullptr && t + (w.ntiles - 1 - w.k) < t1 &&
+           warp == (w.n - 1 - (w.ntiles - 1) * kTile) / KPW;
+  };
+  bool own_fresh = owns_fresh(t0);
+  uint4 fk = own_fresh ? load_fresh(p, w.b, w.kvh, lane) : make_uint4(0u, 0u, 0u, 0u);
   if (R) {
     rope_segment<G, NC>(qb, rope_row<R>(p, p.rope_cos, w.b, w.lo + w.n - 1),
                         rope_row<R>(p, p.rope_sin, w.b, w.lo + w.n - 1), q_rot,
@@ -778,10 +792,9 @@ __global__ void __maxnreg__(Cfg<G>::kMaxRegs) decode_splitkv_kernel(const Params
     if (!consumer_wait(smem_u32(&bars[s]), u & 1u, abort_flag, p.status, lane)) break;
     const int rows = min(kTile, w.n - w.k * kTile);
     uint8_t* Ks = stages + (size_t)s * 2 * kTileBytes;
-    if (p.k_new != nullptr && w.k == w.ntiles - 1 && warp == (rows - 1) / KPW)
-      fresh_row<R>(p, Ks, rows, w.b, w.kvh, w.lo + w.n - 1, rope_cs, lane);
-    cs.tile(Ks, Ks + kTileBytes, rows,
-            MT ? min(rows, cs.head_last + 1 - (w.lo + w.k * kTile)) : rows, warp);
+    if (own_fresh && w.k == w.ntiles - 1)
+      fresh_row<R>(p, Ks, rows, w.b, w.kvh, w.lo + w.n - 1, rope_cs, fk, lane);
+    cs.template tile<MT, R>(Ks, Ks + kTileBytes, rows, w.lo + w.k * kTile, warp);
     __syncwarp();
     if (lane == 0) mbar_arrive(smem_u32(&bars[kStages + s]));  // the stage may be refilled
     const bool seg_end = (w.k == w.ntiles - 1) || (t == t1 - 1);
@@ -886,7 +899,9 @@ __global__ void __maxnreg__(Cfg<G>::kMaxRegs) decode_splitkv_kernel(const Params
       } else {
         cs.template load_q<MT>(p, w.b, w.kvh, p.qscale);
       }
-      if (MT) cs.head_last = w.lo + w.n - 1 - shift + cs.hd / (G / p.S);
+      if (MT) cs.set_last(w.lo + w.n - 1 - shift, p.S);
+      own_fresh = owns_fresh(t + 1);
+      if (own_fresh) fk = load_fresh(p, w.b, w.kvh, lane);
     }
   }
 
@@ -921,7 +936,9 @@ size_t cluster_smem_bytes() {
 // Grid = B*Hkv clusters of C CTAs; cluster s handles segment s (sequence
 // s / Hkv, KV head s % Hkv).
 template <int G, int M>
-__global__ void __maxnreg__(Cfg<G>::kMaxRegs) decode_cluster_kernel(const Params p) {
+__global__ void __maxnreg__(Cfg<G>::kMaxRegs)
+    decode_cluster_kernel(const __grid_constant__ CUtensorMap tm_k,
+                          const __grid_constant__ CUtensorMap tm_v, const Params p) {
   constexpr bool R = (M & kModeRope) != 0, A = (M & kModeAdvance) != 0;
   constexpr bool MT = (M & kModeMulti) != 0;
   constexpr int NW = Cfg<G>::NW;
@@ -947,9 +964,10 @@ __global__ void __maxnreg__(Cfg<G>::kMaxRegs) decode_cluster_kernel(const Params
   const int shift = MT ? p.S - 1 : 0;  // positions[b] + shift: the last new token's row
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
+  const bool producer = tid == NW * 32;
   volatile int* abort_flag = misc;
 
-  if (tid == 0) {
+  if (producer) {
 #pragma unroll
     for (int s = 0; s < kStages; ++s) {
       mbar_init(smem_u32(&bars[s]), 1);
@@ -961,9 +979,21 @@ __global__ void __maxnreg__(Cfg<G>::kMaxRegs) decode_cluster_kernel(const Params
   }
   grid_dependency_wait();
   grid_dependents_launch();
+  // Rank r's first tile is tile r whatever the position (rows from 0 without
+  // a local window), so its copy goes out before the position is read, and
+  // so do the q loads.  If the position leaves rank r without tiles, the
+  // copy only has to land before the CTA exits.
+  const bool early = !(M & kModeWindow) && rank * kTile < p.L;
+  if (early && producer) produce_tile(&tm_k, &tm_v, p, stages, bars, 0, b, kvh, rank, 0);
+  Consumer<G> cs;
+  if (warp < NW) {
+    cs.init(lane);
+    if (!R) cs.template load_q<MT>(p, b, kvh, p.qscale);
+  }
   const int pos = p.positions[b] + shift;
   if (pos - shift < 0 || pos >= p.L) {
     // the same for every CTA of the cluster: all leave, no cluster barrier
+    if (early && producer) mbar_wait(smem_u32(&bars[0]), 0u, abort_flag);
     if (rank == 0 && kvh == 0 && tid == 0) {
       set_status(p.status, ATTN_DEV_BAD_POSITION);
       write_nan_rows(p, b, MT ? p.S : 1);
@@ -977,8 +1007,6 @@ __global__ void __maxnreg__(Cfg<G>::kMaxRegs) decode_cluster_kernel(const Params
   int lo, n;
   attended_rows(pos, win, lo, n);
   const int ntiles = (n - 1) / kTile + 1;
-  const int k0 = (int)((long long)rank * ntiles / C);
-  const int k1 = (int)((long long)(rank + 1) * ntiles / C);
   __syncthreads();  // barriers initialised
   // this CTA runs: the matching wait comes before any write into rank 0's
   // shared memory, so rank 0 is known to have started by then
@@ -987,8 +1015,9 @@ __global__ void __maxnreg__(Cfg<G>::kMaxRegs) decode_cluster_kernel(const Params
   if (warp == NW) {
     // ------------------------------------------------------------ producer --
     if (lane == 0) {
-      for (int k = k0; k < k1; ++k) {
-        const int i = k - k0;
+      int i = 0;
+      for (int k = rank; k < ntiles; k += C, ++i) {
+        if (i == 0 && early) continue;  // issued above
         const int s = i % kStages;
         const uint32_t u = (uint32_t)(i / kStages);
         if (i >= kStages && !mbar_wait(smem_u32(&bars[kStages + s]), (u & 1u) ^ 1u, abort_flag)) {
@@ -996,14 +1025,14 @@ __global__ void __maxnreg__(Cfg<G>::kMaxRegs) decode_cluster_kernel(const Params
           set_status(p.status, ATTN_DEV_TIMEOUT);
           break;
         }
-        produce_tile(p, stages, bars, s, b, kvh, k, ntiles, n, lo);
+        produce_tile(&tm_k, &tm_v, p, stages, bars, s, b, kvh, k, lo);
       }
+      // a first copy that no consumer waits for lands before the CTA exits
+      if (early && rank >= ntiles) mbar_wait(smem_u32(&bars[0]), 0u, abort_flag);
     }
     __syncwarp();
   } else {
     // ----------------------------------------------------------- consumers --
-    Consumer<G> cs;
-    cs.init(lane);
     ConsumerSync csync{smem_u32(&bars[2 * kStages]), abort_flag, p.status, 0u};
     const uint16_t* qb = p.q + ((size_t)b * p.Hq + (size_t)kvh * G) * kD;
     if (R) {
@@ -1012,23 +1041,25 @@ __global__ void __maxnreg__(Cfg<G>::kMaxRegs) decode_cluster_kernel(const Params
                           rope_cs, tid);
       consumer_bar<NC>();  // before any tile wait: every consumer warp gets here
       cs.load_q_rot(q_rot, p.qscale);
-    } else {
-      cs.template load_q<MT>(p, b, kvh, p.qscale);
     }
-    if (MT) cs.head_last = pos - shift + cs.hd / (G / p.S);
+    if (MT) cs.set_last(pos - shift, p.S);
+    // fused append: the warp whose keys include the last row of the last
+    // tile, in the rank that takes that tile, writes the new rows
+    const bool own_fresh = p.k_new != nullptr && (ntiles - 1) % C == rank &&
+                           warp == (n - 1 - (ntiles - 1) * kTile) / KPW;
+    const uint4 fk = own_fresh ? load_fresh(p, b, kvh, lane) : make_uint4(0u, 0u, 0u, 0u);
     cs.reset();
-    for (int k = k0; k < k1; ++k) {
-      const int i = k - k0;
+    int i = 0;
+    for (int k = rank; k < ntiles; k += C, ++i) {
       const int s = i % kStages;
       if (!consumer_wait(smem_u32(&bars[s]), (uint32_t)(i / kStages) & 1u, abort_flag, p.status,
                          lane))
         break;
       const int rows = min(kTile, n - k * kTile);
       uint8_t* Ks = stages + (size_t)s * 2 * kTileBytes;
-      if (p.k_new != nullptr && k == ntiles - 1 && warp == (rows - 1) / KPW)
-        fresh_row<R>(p, Ks, rows, b, kvh, pos, rope_cs, lane);
-      cs.tile(Ks, Ks + kTileBytes, rows,
-              MT ? min(rows, cs.head_last + 1 - (lo + k * kTile)) : rows, warp);
+      if (own_fresh && k == ntiles - 1)
+        fresh_row<R>(p, Ks, rows, b, kvh, pos, rope_cs, fk, lane);
+      cs.template tile<MT, R>(Ks, Ks + kTileBytes, rows, lo + k * kTile, warp);
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&bars[kStages + s]));  // the stage may be refilled
     }
@@ -1059,30 +1090,29 @@ __global__ void __maxnreg__(Cfg<G>::kMaxRegs) decode_cluster_kernel(const Params
 
   cluster.sync();  // every rank's partial is in rank 0's shared memory
   if (rank == 0) {
-    // weights 2^(m_r - M) / L per (rank, head): warp h reduces over the
-    // ranks, lane r holding rank r's (max, sum); merge_ml is free by now
-    float* wr = merge_ml;  // [C][G]
-    if (warp < G) {
-      const int h = warp;
-      const bool in = lane < C;
-      const float m = in ? land_ml[(lane * G + h) * 2] : -INFINITY;
-      const float l = in ? land_ml[(lane * G + h) * 2 + 1] : 0.f;
-      float Mx = m;
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) Mx = fmaxf(Mx, __shfl_xor_sync(0xffffffffu, Mx, off));
-      const float e = in ? ex2(m - Mx) : 0.f;  // a rank without tiles: 2^-inf = 0
-      float Ls = l * e;
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) Ls += __shfl_xor_sync(0xffffffffu, Ls, off);
-      if (in) wr[lane * G + h] = e / Ls;
-    }
-    __syncthreads();
+    // One pass per output element: the max over the ranks, then the C
+    // weights 2^(m_r - M) (independent of one another, so they issue back to
+    // back), the sum and the weighted partials.  A rank without tiles has
+    // m = -inf and weighs 0; some rank always has a valid key.
     for (int idx = tid; idx < G * kD; idx += blockDim.x) {
       const int h = idx / kD, d = idx % kD;
-      float Os = 0.f;
-#pragma unroll 4
-      for (int r = 0; r < C; ++r) Os = fmaf(land_o[(r * G + h) * kD + d], wr[r * G + h], Os);
-      store_bf16(p.out + head_row<G, MT>(p, b, kvh, h) * kD + d, Os);
+      float m[Cfg<G>::kMaxC];
+      float Mx = -INFINITY;
+#pragma unroll
+      for (int r = 0; r < Cfg<G>::kMaxC; ++r) {
+        m[r] = r < C ? land_ml[(r * G + h) * 2] : -INFINITY;
+        Mx = fmaxf(Mx, m[r]);
+      }
+      float Ls = 0.f, Os = 0.f;
+#pragma unroll
+      for (int r = 0; r < Cfg<G>::kMaxC; ++r) {
+        if (r < C) {
+          const float e = ex2(m[r] - Mx);
+          Ls = fmaf(land_ml[(r * G + h) * 2 + 1], e, Ls);
+          Os = fmaf(land_o[(r * G + h) * kD + d], e, Os);
+        }
+      }
+      store_bf16(p.out + head_row<G, MT>(p, b, kvh, h) * kD + d, Os / Ls);
     }
   }
   // no second cluster barrier: no CTA reads another's shared memory any more
@@ -1196,14 +1226,49 @@ cudaError_t cluster_size(const Params& p, int* C) {
   return cudaSuccess;
 }
 
+// A cache [B*Hkv, L, 128] bf16 as a 3-D tensor map (dims, rows, segments);
+// box 64 dims x 128 rows x 1, 128-byte swizzle: one column block of a tile.
+// Rows past L read as zeros.  The last few maps are kept per host thread.
+bool cache_map(CUtensorMap* m, const void* ptr, int L, long long segs) {
+  struct Entry {
+    const void* ptr;
+    int L;
+    long long segs;
+    CUtensorMap map;
+  };
+  static thread_local Entry cache[4] = {};
+  static thread_local int next = 0;
+  for (const Entry& e : cache)
+    if (e.ptr == ptr && e.L == L && e.segs == segs) {
+      *m = e.map;
+      return true;
+    }
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)kD, (cuuint64_t)L, (cuuint64_t)segs};
+  cuuint64_t strides[2] = {(cuuint64_t)kRowBytes, (cuuint64_t)kRowBytes * (cuuint64_t)L};
+  cuuint32_t box[3] = {64, (cuuint32_t)kTile, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  if (enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box,
+          estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return false;
+  cache[next] = Entry{ptr, L, segs, *m};
+  next = (next + 1) % 4;
+  return true;
+}
+
 template <int G, int M>
 cudaError_t launch_g(const Params& p, cudaStream_t stream) {
   int dev = 0;
   DevInfo& d = dev_info(&dev);
+  const long long nseg = (long long)p.B * p.Hkv;
+  CUtensorMap mk, mv;
+  if (!cache_map(&mk, p.k_cache, p.L, nseg) || !cache_map(&mv, p.v_cache, p.L, nseg))
+    return cudaErrorInvalidValue;
   int C = 0;
   cudaError_t e = cluster_size<G>(p, &C);
   if (e != cudaSuccess) return e;
-  const long long nseg = (long long)p.B * p.Hkv;
   if (C > 0) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(nseg * C));
@@ -1219,11 +1284,11 @@ cudaError_t launch_g(const Params& p, cudaStream_t stream) {
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    e = cudaLaunchKernelEx(&cfg, decode_cluster_kernel<G, M>, p);
+    e = cudaLaunchKernelEx(&cfg, decode_cluster_kernel<G, M>, mk, mv, p);
     return e != cudaSuccess ? e : cudaGetLastError();
   }
   return launch_pdl(decode_splitkv_kernel<G, M>, dim3(min(kMaxGrid, d.num_sms)),
-                    dim3(Cfg<G>::kThreads), smem_bytes<G>(p.B), stream, p);
+                    dim3(Cfg<G>::kThreads), smem_bytes<G>(p.B), stream, mk, mv, p);
 }
 
 // The variant for this launch.  The entry points use six combinations:

@@ -900,38 +900,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
 // ------------------------------------------------------------------ host --
 
-// A cache [B*Hkv, L, 128] bf16 as a 3-D tensor map (dims, rows, segments);
-// box 64 dims x 128 rows x 1, 128-byte swizzle: one column block of a tile.
-// Rows past L read as zeros.  The last few maps are kept per host thread.
-bool cache_map(CUtensorMap* m, const void* ptr, int L, long long segs) {
-  struct Entry {
-    const void* ptr;
-    int L;
-    long long segs;
-    CUtensorMap map;
-  };
-  static thread_local Entry cache[4] = {};
-  static thread_local int next = 0;
-  for (const Entry& e : cache)
-    if (e.ptr == ptr && e.L == L && e.segs == segs) {
-      *m = e.map;
-      return true;
-    }
-  EncodeTiledFn enc = encode_fn();
-  if (!enc) return false;
-  cuuint64_t dims[3] = {(cuuint64_t)kD, (cuuint64_t)L, (cuuint64_t)segs};
-  cuuint64_t strides[2] = {(cuuint64_t)kRowBytes, (cuuint64_t)kRowBytes * (cuuint64_t)L};
-  cuuint32_t box[3] = {64, (cuuint32_t)kTile, 1};
-  cuuint32_t estr[3] = {1, 1, 1};
-  if (enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box,
-          estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-    return false;
-  cache[next] = Entry{ptr, L, segs, *m};
-  next = (next + 1) % 4;
-  return true;
-}
-
 struct TcDevInfo {
   bool configured[9] = {};                // per g
   int clusters[9][kMaxCluster + 1] = {};  // [g][C]: co-resident clusters of C CTAs
