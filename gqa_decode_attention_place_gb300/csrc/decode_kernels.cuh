@@ -254,6 +254,14 @@ __device__ __forceinline__ int sw128(int r, int c) { return r * 128 + ((c ^ (r &
 // Byte offset of dims 8q..8q+7 (q = 0..15) of row r of a K or V tile.
 __device__ __forceinline__ int tile_chunk(int r, int q) { return (q >> 3) * kHalf + sw128(r, q & 7); }
 
+// Key (0..7, plus 8 for rows 8..15) that MMA row m of a warp's 16 stands
+// for.  A 16-byte shared load is served per quarter warp (lanes 8i..8i+7,
+// rows g = 2i and 2i+1): the K reads of those two rows must fall on opposite
+// halves of the swizzle, so their keys differ in bit 2 (key_of(2i+1) =
+// key_of(2i) ^ 4); the V reads of keys key_of(2t) (and of key_of(2t+1)),
+// t = 0..3, must cover the four pairs {2k, 2k+1} once each.
+__device__ __forceinline__ int key_of(int m) { return ((m & 6) | (m >> 2)) ^ ((m & 1) << 2); }
+
 // Per-warp consumer state and math: one KV head's g query heads, 16 keys
 // (kw .. kw+15) of each tile.  Lane 4g+t.
 //  * Scores: S = K q^T, an m16n8k16 per 16 dims: the 16 keys are the rows,
@@ -262,13 +270,15 @@ __device__ __forceinline__ int tile_chunk(int r, int q) { return (q >> 3) * kHal
 //    MMA step 2j+s are dims 64*(j/2) + 8*((j%2)*4 + t) + 4s .. +4 in lane t,
 //    the same for the key rows (A) and for q (B), so one 16-byte read per key
 //    row and lane feeds two MMAs and the 8 rows of each read hit 8 different
-//    swizzle chunks.  Lane 4g+t ends with the scores of keys kw+g and
-//    kw+g+8 for heads 2t and 2t+1.
+//    swizzle chunks.  MMA row m is key kw + key_of(m) (rows m+8: + 8), an
+//    order that keeps these reads free of bank conflicts.  Lane 4g+t ends
+//    with the scores of keys kw+key_of(g) and kw+8+key_of(g) for heads 2t
+//    and 2t+1.
 //  * P^T (keys x heads) is that score layout transposed in 8x8 blocks.
 //  * Output: O^T += V^T P^T, m-block mb (0..7) holding dims 8g+mb (row g)
 //    and 64+8g+mb (row g+8): lane 4g+t reads 16 bytes of dims 8g.. and
-//    64+8g.. of keys kw+2t, kw+2t+1, kw+2t+8, kw+2t+9 and pairs the keys
-//    with prmt.  It accumulates O^T for those dims and heads 2t, 2t+1.
+//    64+8g.. of the keys of MMA rows 2t, 2t+1, 2t+8, 2t+9 and pairs the
+//    keys with prmt.  It accumulates O^T for those dims and heads 2t, 2t+1.
 template <int G>
 struct Consumer {
   static constexpr float kTau = 8.0f;  // a stale running max may lag by 2^8
@@ -343,13 +353,14 @@ struct Consumer {
                                        int warp) {
     const int kw = warp * 16;
     if (kw >= rows) return;  // no valid key for this warp (warp-uniform)
+    const int pg = key_of(g);
     float s[4] = {0.f, 0.f, 0.f, 0.f}, s2[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       const int c = (j & 1) * 4 + t;
       const uint8_t* base = Ks + (j >> 1) * kHalf;
-      const uint4 ka = lds128(base + sw128(kw + g, c));
-      const uint4 kb = lds128(base + sw128(kw + g + 8, c));
+      const uint4 ka = lds128(base + sw128(kw + pg, c));
+      const uint4 kb = lds128(base + sw128(kw + pg + 8, c));
       mma16816(s, ka.x, kb.x, ka.y, kb.y, qb[j][0], qb[j][1]);
       mma16816(s2, ka.z, kb.z, ka.w, kb.w, qb[j][2], qb[j][3]);
     }
@@ -367,7 +378,7 @@ struct Consumer {
     float x[4];  // log2-domain scores; invalid keys -inf
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      const int key = kw + g + (i >> 1) * 8;
+      const int key = kw + pg + (i >> 1) * 8;
       const int lim = MT ? min(rows, head_last[i & 1] + 1 - row0) : rows;
       x[i] = key < lim ? s[i] * qs : -INFINITY;
     }
@@ -413,17 +424,18 @@ struct Consumer {
     const uint32_t l1 = pack_bf16x2(pr[2] - bf16lo(h1), pr[3] - bf16hi(h1));
     const uint32_t bh0 = movm_trans(h0), bh1 = movm_trans(h1);
     const uint32_t bl0 = movm_trans(l0), bl1 = movm_trans(l1);
-    const int r0 = kw + 2 * t;
-    uint4 v[4][2];  // keys r0, r0+1, r0+8, r0+9; dims 8g.. and 64+8g..
+    // MMA keys 2t, 2t+1, 2t+8, 2t+9
+    const int vr[4] = {kw + key_of(2 * t), kw + key_of(2 * t + 1), kw + 8 + key_of(2 * t),
+                       kw + 8 + key_of(2 * t + 1)};
+    uint4 v[4][2];  // those keys' dims 8g.. and 64+8g..
 #pragma unroll
     for (int k = 0; k < 4; ++k)
 #pragma unroll
-      for (int h = 0; h < 2; ++h)
-        v[k][h] = lds128(Vs + h * kHalf + sw128(r0 + (k & 1) + (k >> 1) * 8, g));
+      for (int h = 0; h < 2; ++h) v[k][h] = lds128(Vs + h * kHalf + sw128(vr[k], g));
     if (kw + 16 > rows) {  // V rows past the valid ones may be NaN: 0 * NaN would spread
 #pragma unroll
       for (int k = 0; k < 4; ++k)
-        if (r0 + (k & 1) + (k >> 1) * 8 >= rows) v[k][0] = v[k][1] = make_uint4(0u, 0u, 0u, 0u);
+        if (vr[k] >= rows) v[k][0] = v[k][1] = make_uint4(0u, 0u, 0u, 0u);
     }
 #pragma unroll
     for (int mb = 0; mb < 8; ++mb) {
