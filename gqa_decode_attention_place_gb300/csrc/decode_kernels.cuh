@@ -35,8 +35,9 @@
 //    (movmatrix) and enters as two bf16 parts (high and remainder), so the
 //    product keeps about 16 bits of P.  The softmax is kept online in fp32
 //    (running max and sum per head, base 2, scale*log2(e) applied to the fp32
-//    scores).  On CUDA cores the same work took about 28 warp instructions
-//    per key; on these MMAs it takes about 8.
+//    scores).  On CUDA cores (fp32 FMAs, 16 lanes per key, shuffle
+//    reductions) the same work took about 28 warp instructions per key;
+//    here it takes about 7.
 //  * Two ways to split a segment over CTAs, both computed on the device from
 //    `positions` (one launch serves any positions; graph-capturable):
 //    - cluster mode (few segments, e.g. B=1): one thread-block cluster of C

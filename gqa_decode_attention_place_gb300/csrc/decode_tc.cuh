@@ -1,7 +1,7 @@
 // decode_tc.cuh -- split-KV decode attention with both contractions of a
 // tile on the tcgen05 tensor cores, for group sizes g = 8 and 16 (g <= 4 runs
-// on CUDA cores, decode_kernels.cuh): the kernels and their launch, included
-// by decode_g8.cu and decode_g16.cu.
+// on per-warp mma.sync MMAs, decode_kernels.cuh): the kernels and their
+// launch, included by decode_g8.cu and decode_g16.cu.
 //
 // What it computes ("MiniCPM4 `forward_step` Attention Performance Fix",
 // sections 3 and 4.1): for every sequence b and query head h,
@@ -9,18 +9,19 @@
 // over cache rows j = 0..positions[b] only (or the last W of them with a
 // local window), optionally after appending the step's new K/V row (rotated
 // by the rotary embedding if asked) and optionally advancing every position
-// by one afterwards -- the same operation and options as the CUDA-core
-// kernels of decode_kernels.cuh, whose segment walk, partial merges and
-// helpers this file shares.
+// by one afterwards -- the same operation and options as the kernels of
+// decode_kernels.cuh, whose segment walk, helpers and tensor maps this file
+// shares.
 //
 // Why tensor cores: the g query heads of a KV head share every K and V row,
 // so one 128-key tile is two small dense contractions,
 //   S^T [128 keys x g] = K [128 x 128 dims] . Q^T [128 dims x g]
 //   O^T [128 dims x g] += V^T [128 dims x 128 keys] . P^T [128 keys x g].
 // On CUDA cores their multiply-adds, bf16 unpacking and lane reductions grow
-// with g; at g = 8 they made that kernel issue-bound (0.66 of HBM on a large
-// batch).  Here each is eight tcgen05.mma (M = 128, N = 16: the g heads
-// padded to 16, K = 16), so a tile costs the CUDA cores only its softmax.
+// with g; at g = 8 they made a CUDA-core kernel issue-bound (0.66 of HBM on
+// a large batch).  Here each is eight tcgen05.mma (M = 128, N = 16: the g
+// heads padded to 16, K = 16), so a tile costs the CUDA cores only its
+// softmax, and the large g = 8 batch streams at the copy rate.
 //
 // Layout per CTA (one per SM):
 //  * warp 4, one thread: 2-D TMA loads (cp.async.bulk.tensor, 128-byte
@@ -45,9 +46,10 @@
 //    the CTA whose part ends the segment writes it to the cache and folds its
 //    score and value (fp32, CUDA cores) into its partial at the end.  So no
 //    load has to wait for that write.
-//  * Segment splitting and merging are the CUDA-core kernels' (cluster mode:
-//    partials pushed into rank 0's shared memory; stream-K: partials through
-//    the workspace, merged by the last CTA to arrive).
+//  * Segment splitting and merging follow decode_kernels.cuh (cluster mode:
+//    partials pushed into rank 0's shared memory, here over contiguous tile
+//    ranges; stream-K: partials through the workspace, merged by the last
+//    CTA to arrive).
 //  * Every wait is bounded (ATTN_DEV_TIMEOUT); the softmax warps' named
 //    barriers sit where all four warps always arrive, whatever a wait gave.
 #pragma once
@@ -1008,8 +1010,8 @@ cudaError_t launch_tc_g(const Params& p, cudaStream_t stream) {
                     dim3(kTcThreads), tc_smem_bytes<G>(ns, 0, p.B), stream, mk, mv, p, ns);
 }
 
-// The variant for this launch (the same six combinations as the CUDA-core
-// kernels).
+// The variant for this launch (the same six combinations as the kernels of
+// decode_kernels.cuh).
 template <int G>
 cudaError_t launch_group_tc(const Params& p, cudaStream_t stream) {
   const int mode = (p.rope_cos != nullptr ? kModeRope : 0) |

@@ -105,11 +105,12 @@ size_t attn_decode_workspace_size(int B, int Hq, int Hkv, int L, int D);
  *   v_cache   : [B, Hkv, L, D] bf16.
  *   scale     : fp32 score scale (the page's default is 1/sqrt(D)).
  *   out       : [B, Hq, D] bf16 (= [B, Hq*D]), fp32 softmax and accumulation,
- *               rounded to nearest even.  For g <= 4 the products run on
- *               CUDA cores in fp32; for g = 8 both contractions of a tile
- *               run on the tcgen05 tensor cores (bf16 operands, fp32
- *               accumulation), with the probabilities rounded to bf16
- *               before P.V.
+ *               rounded to nearest even.  Both contractions of a tile run
+ *               on tensor cores with bf16 operands and fp32 accumulation:
+ *               per warp (mma.sync) for g <= 4, with the probabilities
+ *               entering P.V as two bf16 parts (about 16 bits); on the
+ *               tcgen05 tensor cores for g = 8 and 16, with the
+ *               probabilities rounded to bf16 before P.V.
  *   workspace : device buffer of at least attn_decode_workspace_size(...)
  *               bytes, zero-filled before first use (see above).
  *
@@ -131,10 +132,11 @@ int attn_decode_step(const void* q, const int32_t* positions,
  * row positions[b] of every KV head of sequence b becomes k_new/v_new
  * (bit-exact) and out is attention over rows 0..positions[b], the new row
  * included.  The new rows are fed to the attention straight from k_new/v_new
- * and written to the cache in the same launch.  On the CUDA-core kernels out
- * is bit-identical to the two calls; on the tensor-core ones (see
- * attn_decode_step) the new row's score and value are folded in fp32 beside
- * the tile, so out agrees with the two calls to rounding.
+ * and written to the cache in the same launch.  For g <= 4 the new row goes
+ * through the tile like any cache row, so out is bit-identical to the two
+ * calls; for g = 8 and 16 (the tcgen05 kernels) its score and value are
+ * folded in fp32 beside the tile, so out agrees with the two calls to
+ * rounding.
  *
  *   q            : [B, Hq, D] bf16.
  *   k_new, v_new : [B, Hkv, D] bf16.

@@ -77,7 +77,7 @@ def test_multi_clusters(S, Hq, Hkv):
 @pytest.mark.parametrize("Hq,Hkv", [(16, 8), (64, 8)])
 def test_one_token_is_the_plain_decode(Hq, Hkv):
     """S = 1 writes the same cache bits as the fused append step.  At g = 2
-    (CUDA-core kernels) the outputs are the same bits too.  At g = 8
+    (the per-warp MMA kernels) the outputs are the same bits too.  At g = 8
     (tensor-core kernels) the fused step folds its new row in fp32 on the
     side, while the multi-token path reads it back through the tile, so
     there the two agree to rounding, within the attention tolerance."""

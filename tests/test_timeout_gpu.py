@@ -5,7 +5,8 @@ waits for that tile never complete.  Every wait in the
 kernels gives up after 500 ms: the launch must end by itself with
 ATTN_DEV_TIMEOUT in the status word, and the CUDA context must stay usable --
 a normal step right after gives the oracle's result.  Covers cluster mode
-and stream-K on both kernels: CUDA cores (g <= 4) and tensor cores (g >= 8).
+and stream-K on both kernel families: per-warp MMAs (g <= 4) and tcgen05
+(g >= 8).
 """
 
 import numpy as np
@@ -20,7 +21,7 @@ from _helpers import assert_attn_close, f64
 pytestmark = pytest.mark.gpu
 
 
-# CUDA cores: clusters (g=2), stream-K (g=4); tensor cores: stream-K (g=8),
+# per-warp MMAs: clusters (g=2), stream-K (g=4); tcgen05: stream-K (g=8),
 # clusters (g=8), clusters at g=16 (at most 9 CTAs)
 @pytest.mark.parametrize("B,Hq,Hkv", [(1, 16, 8), (16, 8, 2), (16, 16, 2), (1, 64, 8),
                                       (4, 32, 2)])
