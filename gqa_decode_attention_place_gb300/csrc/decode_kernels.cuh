@@ -528,15 +528,27 @@ template <int G, int NC>
 __device__ __forceinline__ void rope_segment(const uint16_t* qb, const float* rc, const float* rs,
                                              float* q_rot, float* rope_cs, int ct) {
   constexpr int kH = kD / 2;
-  for (int i = ct; i < G * kH; i += NC) {
-    const int h = i / kH, d = i % kH;
+  static_assert(G * kH <= NC && 2 * kD <= NC, "one rotation and one table value per thread");
+  // every load first, so they share one round trip (q and the rotation rows
+  // are fresh inputs of the step, often not in L2), then the stores
+  const bool rot = ct < G * kH, tab = ct < 2 * kD;
+  const int h = ct / kH, d = ct % kH;
+  float x0 = 0.f, x1 = 0.f, c0 = 0.f, c1 = 0.f, s0 = 0.f, s1 = 0.f, cs = 0.f;
+  if (rot) {
     const uint16_t* qh = qb + (size_t)h * kD;
-    const float x0 = __uint_as_float((uint32_t)qh[d] << 16);
-    const float x1 = __uint_as_float((uint32_t)qh[d + kH] << 16);
-    q_rot[h * kD + d] = rope1(x0, x1, rc[d], rs[d], true);
-    q_rot[h * kD + d + kH] = rope1(x1, x0, rc[d + kH], rs[d + kH], false);
+    x0 = __uint_as_float((uint32_t)qh[d] << 16);
+    x1 = __uint_as_float((uint32_t)qh[d + kH] << 16);
+    c0 = rc[d];
+    c1 = rc[d + kH];
+    s0 = rs[d];
+    s1 = rs[d + kH];
   }
-  for (int i = ct; i < 2 * kD; i += NC) rope_cs[i] = i < kD ? rc[i] : rs[i - kD];
+  if (tab) cs = ct < kD ? rc[ct] : rs[ct - kD];
+  if (rot) {
+    q_rot[h * kD + d] = rope1(x0, x1, c0, s0, true);
+    q_rot[h * kD + d + kH] = rope1(x1, x0, c1, s1, false);
+  }
+  if (tab) rope_cs[ct] = cs;
 }
 
 // A consumer warp's wait for a tile, with the outcome made warp-uniform (the
@@ -994,16 +1006,26 @@ __global__ void __maxnreg__(Cfg<G>::kMaxRegs)
   grid_dependents_launch();
   // Rank r's first tile is tile r whatever the position (rows from 0 without
   // a local window), so its copy goes out before the position is read, and
-  // so do the q loads.  If the position leaves rank r without tiles, the
-  // copy only has to land before the CTA exits.
+  // so does q: loaded, or rotated when the rotation rows are per sequence.
+  // If the position leaves rank r without tiles, the copy only has to land
+  // before the CTA exits.
   const bool early = !(M & kModeWindow) && rank * kTile < p.L;
   if (early && producer) produce_tile(&tm_k, &tm_v, p, stages, bars, 0, b, kvh, rank, 0);
+  // the position's load goes out first; its value is used after the q setup
+  const int pos = p.positions[b] + shift;
+  const uint16_t* qb = p.q + ((size_t)b * p.Hq + (size_t)kvh * G) * kD;
   Consumer<G> cs;
   if (warp < NW) {
     cs.init(lane);
-    if (!R) cs.template load_q<MT>(p, b, kvh, p.qscale);
+    if (!R) {
+      cs.template load_q<MT>(p, b, kvh, p.qscale);
+    } else if (!p.rope_by_pos) {
+      rope_segment<G, NC>(qb, rope_row<R>(p, p.rope_cos, b, 0), rope_row<R>(p, p.rope_sin, b, 0),
+                          q_rot, rope_cs, tid);
+      consumer_bar<NC>();  // every consumer warp gets here
+      cs.load_q_rot(q_rot, p.qscale);
+    }
   }
-  const int pos = p.positions[b] + shift;
   if (pos - shift < 0 || pos >= p.L) {
     // the same for every CTA of the cluster: all leave, no cluster barrier
     if (early && producer) mbar_wait(smem_u32(&bars[0]), 0u, abort_flag);
@@ -1047,8 +1069,7 @@ __global__ void __maxnreg__(Cfg<G>::kMaxRegs)
   } else {
     // ----------------------------------------------------------- consumers --
     ConsumerSync csync{smem_u32(&bars[2 * kStages]), abort_flag, p.status, 0u};
-    const uint16_t* qb = p.q + ((size_t)b * p.Hq + (size_t)kvh * G) * kD;
-    if (R) {
+    if (R && p.rope_by_pos) {  // the rotation row is the position's
       rope_segment<G, NC>(qb, rope_row<R>(p, p.rope_cos, b, pos),
                           rope_row<R>(p, p.rope_sin, b, pos), q_rot,
                           rope_cs, tid);

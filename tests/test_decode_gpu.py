@@ -312,3 +312,29 @@ def test_small_batches_one_cluster_per_segment(g, Hkv, positions):
         want = _oracle_rows(case, range(B))
         out = _fused_step(case) if fused else _run_step(case)
         _check(case, want, out, f"small batch g={g} fused={fused}")
+
+
+@pytest.mark.parametrize("g", [1, 2, 4])
+@pytest.mark.parametrize("L,positions", [(100, [99, 0]), (300, [299, 255]), (1500, [1499, 1407])])
+def test_short_caches_in_cluster_mode(g, L, positions):
+    """Caches whose length is not a multiple of the 128-row tile, few
+    segments (one cluster each): a rank's first tile is copied before the
+    position is known when it starts inside the cache, its box may reach past
+    L (those rows arrive as zeros), and ranks that the position leaves without
+    tiles drop that copy.  Plain and fused calls, rows past each position
+    NaN-poisoned, the appended rows checked bit for bit."""
+    B, Hkv = len(positions), 2
+    for fused in (False, True):
+        case = synth.decode_case(B=B, Hq=g * Hkv, Hkv=Hkv, D=128, L=L, positions=positions,
+                                 fill="all", poison=True, seed=70 + g + L + int(fused),
+                                 device="cuda")
+        want = _oracle_rows(case, range(B))
+        pos = case.positions.cpu().numpy()
+        wk, wv = oracle.kv_append(bits(case.k_cache).cpu().numpy(),
+                                  bits(case.v_cache).cpu().numpy(),
+                                  bits(case.k_new).cpu().numpy(), bits(case.v_new).cpu().numpy(),
+                                  pos)
+        out = _fused_step(case) if fused else _run_step(case)
+        _check(case, want, out, f"L={L} g={g} fused={fused}")
+        assert np.array_equal(bits(case.k_cache).cpu().numpy(), wk)
+        assert np.array_equal(bits(case.v_cache).cpu().numpy(), wv)
