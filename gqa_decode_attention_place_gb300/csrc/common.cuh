@@ -72,17 +72,6 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
 
 // ------------------------------------------------------------ bulk copies --
 
-// 1-D bulk copy global -> shared (the TMA unit), completion counted in bytes on
-// the mbarrier.  dst, src and bytes must be multiples of 16.
-__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes,
-                                         uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-          dst),
-      "l"(src), "r"(bytes), "r"(bar)
-      : "memory");
-}
-
 // ------------------------------------------------------------- conversions --
 
 // Two bf16 values packed in a 32-bit word -> two exact fp32 values.
@@ -123,11 +112,6 @@ __device__ __forceinline__ f2 mk2(float lo, float hi) {
 }
 __device__ __forceinline__ void brk2(f2 x, float& lo, float& hi) {
   asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(x.r));
-}
-__device__ __forceinline__ f2 fma2(f2 a, f2 b, f2 c) {
-  f2 d;
-  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d.r) : "l"(a.r), "l"(b.r), "l"(c.r));
-  return d;
 }
 __device__ __forceinline__ f2 mul2(f2 a, f2 b) {
   f2 d;
