@@ -826,6 +826,18 @@ __global__ void __maxnreg__(Cfg<G>::kMaxRegs) decode_splitkv_kernel(const __grid
 
     // ---- end of this CTA's part of the segment: merge and emit ------------
     if (seg_end) {
+      if (!R && (w.k == w.ntiles - 1) && t + 1 < t1) {
+        // the next segment's q (and new rows) only need loads: they go out
+        // now and land while this segment's partials are merged (the merge
+        // reads m, l and o, not q)
+        Walk wn = w;
+        walk_next(wn, prefix, p.positions, B, Hkv, win, shift);
+        cs.template load_q<MT>(p, wn.b, wn.kvh, p.qscale);
+        if (MT) cs.set_last(wn.lo + wn.n - 1 - shift, p.S);
+        own_fresh = p.k_new != nullptr && t + wn.ntiles < t1 &&
+                    warp == (wn.n - 1 - (wn.ntiles - 1) * kTile) / KPW;
+        if (own_fresh) fk = load_fresh(p, wn.b, wn.kvh, lane);
+      }
       const int seg = w.b * Hkv + w.kvh;
       const long long seg_t0 = (long long)Hkv * prefix[w.b] + (long long)w.kvh * w.ntiles;
       const long long seg_t1 = seg_t0 + w.ntiles;
@@ -921,12 +933,10 @@ __global__ void __maxnreg__(Cfg<G>::kMaxRegs) decode_splitkv_kernel(const __grid
                             q_rot, rope_cs, tid);
         csync(lane);
         cs.load_q_rot(q_rot, p.qscale);
-      } else {
-        cs.template load_q<MT>(p, w.b, w.kvh, p.qscale);
+        if (MT) cs.set_last(w.lo + w.n - 1 - shift, p.S);
+        own_fresh = owns_fresh(t + 1);
+        if (own_fresh) fk = load_fresh(p, w.b, w.kvh, lane);
       }
-      if (MT) cs.set_last(w.lo + w.n - 1 - shift, p.S);
-      own_fresh = owns_fresh(t + 1);
-      if (own_fresh) fk = load_fresh(p, w.b, w.kvh, lane);
     }
   }
 
