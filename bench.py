@@ -67,6 +67,9 @@ def _args():
     ap.add_argument("--batch", type=int, default=None,
                     help="--only with a decode workload: use this batch size instead "
                          "(a smaller capture of the same kernel)")
+    ap.add_argument("--heads", type=int, default=None,
+                    help="--only with a decode workload: use this many query heads "
+                         "(another group size on the same cache shape)")
     ap.add_argument("--cpu-worker", type=str, default=None, help=argparse.SUPPRESS)
     return ap.parse_args()
 
@@ -521,7 +524,7 @@ def _decode_leg(torch, ga, synth, name, flush, hbm):
     pos = case.positions.cpu().tolist()
     nb = oracle.decode_bytes(pos, Hq, Hkv, Dd)
     fl = oracle.decode_flops(pos, Hq, Dd)
-    tc = Hq // Hkv == 8  # g = 8 runs on the tcgen05 kernel, g <= 4 on warp-level MMAs
+    tc = Hq // Hkv == 16  # g = 16 runs on the tcgen05 kernel, g <= 8 on warp-level MMAs
     r = {"us": round(ms * 1e3, 2), "GBs": round(nb / (ms * 1e-3) / 1e9, 1),
          "frac_hbm": round(nb / (ms * 1e-3) / 1e9 / hbm, 3),
          "TFLOPs_tensor": round(fl / (ms * 1e-3) / 1e12, 2),
@@ -851,8 +854,9 @@ def run_only(args):
         print(json.dumps({"only": name, "launches_per_rep": len(sample)}))
         return
     w = dict(synth.generators.WORKLOADS[name])
-    if args.batch and w["kind"] == "decode":
-        w["B"] = args.batch
+    if (args.batch or args.heads) and w["kind"] == "decode":
+        w["B"] = args.batch or w["B"]
+        w["Hq"] = args.heads or w["Hq"]
         kind = w.pop("kind")
         case = synth.generators.decode_case(seed=0, device="cuda", name=name, **w)
         w["kind"] = kind

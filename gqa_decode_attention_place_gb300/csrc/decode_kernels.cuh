@@ -1,8 +1,9 @@
 // decode_kernels.cuh -- split-KV decode attention over a static KV cache with
-// GQA, for group sizes g = 1, 2, 4: the kernels and their launch, included by
-// one translation unit per group size (decode_g1.cu ... decode_g4.cu).
-// g = 8 and 16 run on the tcgen05 tensor cores (decode_tc.cuh, which also
-// uses the segment walk, helpers and merges defined here).
+// GQA, for group sizes g = 1, 2, 4 and 8 (8 without the rotary embedding):
+// the kernels and their launch, included by one translation unit per group
+// size (decode_g1.cu ... decode_g8.cu).  g = 16, and g = 8 with the rotary
+// embedding, run on the tcgen05 tensor cores (decode_tc.cuh, which also uses
+// the segment walk, helpers and tensor maps defined here).
 //
 // What it computes ("MiniCPM4 `forward_step` Attention Performance Fix",
 // sections 3 and 4.1): for every sequence b and query head h,
@@ -106,11 +107,14 @@ __device__ __forceinline__ size_t head_row(const DecodeParams& p, int b, int kvh
 
 // The consumers: NW warps of 16 keys each per tile.
 template <int G> struct Cfg {
-  static_assert(G == 1 || G == 2 || G == 4, "these decode kernels serve g <= 4");
+  static_assert(G == 1 || G == 2 || G == 4 || G == 8, "these decode kernels serve g <= 8");
   static constexpr int NW = kTile / 16;
   // largest cluster: rank 0 keeps a landing slot for every rank's partial
-  // (G x (kD + 2) floats each)
-  static constexpr int kMaxC = 16;
+  // (G x (kD + 2) floats each); 16 slots of 8 heads would not fit beside the
+  // ring
+  static constexpr int kMaxC = G == 8 ? 12 : 16;
+  // the rotated query takes two MMA columns per head: g <= 4 only
+  static constexpr bool kRope = 2 * G <= 8;
   static constexpr int kThreads = (NW + 1) * 32;  // + the producer warp
   static constexpr int kConsumers = NW * 32;
   static constexpr int kKeysPerWarp = kTile / NW;  // 16
@@ -528,25 +532,31 @@ template <int G, int NC>
 __device__ __forceinline__ void rope_segment(const uint16_t* qb, const float* rc, const float* rs,
                                              float* q_rot, float* rope_cs, int ct) {
   constexpr int kH = kD / 2;
-  static_assert(G * kH <= NC && 2 * kD <= NC, "one rotation and one table value per thread");
-  // every load first, so they share one round trip (q and the rotation rows
-  // are fresh inputs of the step, often not in L2), then the stores
-  const bool rot = ct < G * kH, tab = ct < 2 * kD;
-  const int h = ct / kH, d = ct % kH;
-  float x0 = 0.f, x1 = 0.f, c0 = 0.f, c1 = 0.f, s0 = 0.f, s1 = 0.f, cs = 0.f;
-  if (rot) {
-    const uint16_t* qh = qb + (size_t)h * kD;
-    x0 = __uint_as_float((uint32_t)qh[d] << 16);
-    x1 = __uint_as_float((uint32_t)qh[d + kH] << 16);
-    c0 = rc[d];
-    c1 = rc[d + kH];
-    s0 = rs[d];
-    s1 = rs[d + kH];
-  }
-  if (tab) cs = ct < kD ? rc[ct] : rs[ct - kD];
-  if (rot) {
-    q_rot[h * kD + d] = rope1(x0, x1, c0, s0, true);
-    q_rot[h * kD + d + kH] = rope1(x1, x0, c1, s1, false);
+  static_assert(2 * kD <= NC, "one table value per thread");
+  // every load of a pass first, so they share one round trip (q and the
+  // rotation rows are fresh inputs of the step, often not in L2), then the
+  // stores; g <= 4 takes one pass
+  const bool tab = ct < 2 * kD;
+  const float cs = tab ? (ct < kD ? rc[ct] : rs[ct - kD]) : 0.f;
+#pragma unroll
+  for (int i0 = 0; i0 < G * kH; i0 += NC) {
+    const int i = i0 + ct;
+    const bool rot = i < G * kH;
+    const int h = i / kH, d = i % kH;
+    float x0 = 0.f, x1 = 0.f, c0 = 0.f, c1 = 0.f, s0 = 0.f, s1 = 0.f;
+    if (rot) {
+      const uint16_t* qh = qb + (size_t)h * kD;
+      x0 = __uint_as_float((uint32_t)qh[d] << 16);
+      x1 = __uint_as_float((uint32_t)qh[d + kH] << 16);
+      c0 = rc[d];
+      c1 = rc[d + kH];
+      s0 = rs[d];
+      s1 = rs[d + kH];
+    }
+    if (rot) {
+      q_rot[h * kD + d] = rope1(x0, x1, c0, s0, true);
+      q_rot[h * kD + d + kH] = rope1(x1, x0, c1, s1, false);
+    }
   }
   if (tab) rope_cs[ct] = cs;
 }
@@ -1238,9 +1248,13 @@ cudaError_t configure(DevInfo& d) {
   if (d.configured[G]) return cudaSuccess;
   bool big[6] = {};
   cudaError_t e = set_attributes<G, 0>(&big[0]);
-  if (e == cudaSuccess) e = set_attributes<G, kModeRope>(&big[1]);
+  if constexpr (Cfg<G>::kRope) {
+    if (e == cudaSuccess) e = set_attributes<G, kModeRope>(&big[1]);
+    if (e == cudaSuccess) e = set_attributes<G, kModeRope | kModeAdvance>(&big[3]);
+  } else {
+    big[1] = big[3] = true;
+  }
   if (e == cudaSuccess) e = set_attributes<G, kModeAdvance>(&big[2]);
-  if (e == cudaSuccess) e = set_attributes<G, kModeRope | kModeAdvance>(&big[3]);
   if (e == cudaSuccess) e = set_attributes<G, kModeWindow>(&big[4]);
   if (e == cudaSuccess) e = set_attributes<G, kModeMulti>(&big[5]);
   if (e != cudaSuccess) return e;
@@ -1345,13 +1359,15 @@ cudaError_t launch_group(const Params& p, cudaStream_t stream) {
                    (p.S > 1 ? kModeMulti : 0);
   switch (mode) {
     case 0: return launch_g<G, 0>(p, stream);
-    case kModeRope: return launch_g<G, kModeRope>(p, stream);
     case kModeAdvance: return launch_g<G, kModeAdvance>(p, stream);
-    case kModeRope | kModeAdvance: return launch_g<G, kModeRope | kModeAdvance>(p, stream);
     case kModeWindow: return launch_g<G, kModeWindow>(p, stream);
     case kModeMulti: return launch_g<G, kModeMulti>(p, stream);
   }
-  return cudaErrorInvalidValue;  // a combination no entry point makes
+  if constexpr (Cfg<G>::kRope) {
+    if (mode == kModeRope) return launch_g<G, kModeRope>(p, stream);
+    if (mode == (kModeRope | kModeAdvance)) return launch_g<G, kModeRope | kModeAdvance>(p, stream);
+  }
+  return cudaErrorInvalidValue;  // a combination no entry point makes (or rotation at g = 8)
 }
 
 }  // namespace

@@ -1,7 +1,9 @@
 // decode_tc.cuh -- split-KV decode attention with both contractions of a
-// tile on the tcgen05 tensor cores, for group sizes g = 8 and 16 (g <= 4 runs
-// on per-warp mma.sync MMAs, decode_kernels.cuh): the kernels and their
-// launch, included by decode_g8.cu and decode_g16.cu.
+// tile on the tcgen05 tensor cores, for g = 16 and for g = 8 with the rotary
+// embedding (whose rotated query takes 16 operand rows); every other g <= 8
+// runs on per-warp mma.sync MMAs (decode_kernels.cuh), which measured faster
+// there.  The kernels and their launch, included by decode_g8.cu and
+// decode_g16.cu.
 //
 // What it computes ("MiniCPM4 `forward_step` Attention Performance Fix",
 // sections 3 and 4.1): for every sequence b and query head h,
@@ -21,7 +23,7 @@
 // with g; at g = 8 they made a CUDA-core kernel issue-bound (0.66 of HBM on
 // a large batch).  Here each is eight tcgen05.mma (M = 128, N = 16: the g
 // heads padded to 16, K = 16), so a tile costs the CUDA cores only its
-// softmax, and the large g = 8 batch streams at the copy rate.
+// softmax, and a large g = 8 batch streams at the copy rate.
 //
 // Layout per CTA (one per SM):
 //  * warp 4, one thread: 2-D TMA loads (cp.async.bulk.tensor, 128-byte

@@ -107,15 +107,16 @@ size_t attn_decode_workspace_size(int B, int Hq, int Hkv, int L, int D);
  *   out       : [B, Hq, D] bf16 (= [B, Hq*D]), fp32 softmax and accumulation,
  *               rounded to nearest even.  Both contractions of a tile run
  *               on tensor cores with bf16 operands and fp32 accumulation:
- *               per warp (mma.sync) for g <= 4, with the probabilities
+ *               per warp (mma.sync) for g <= 8, with the probabilities
  *               entering P.V as two bf16 parts (about 16 bits); on the
- *               tcgen05 tensor cores for g = 8 and 16, with the
- *               probabilities rounded to bf16 before P.V.
+ *               tcgen05 tensor cores for g = 16 (and for the rotary entry
+ *               points at g = 8), with the probabilities rounded to bf16
+ *               before P.V.
  *   workspace : device buffer of at least attn_decode_workspace_size(...)
  *               bytes, zero-filled before first use (see above).
  *
  * Supported: D == 128; g = Hq / Hkv in {1, 2, 4, 8, 16} (g = 16 on the
- * tensor cores, like g = 8); 1 <= B <= 8192;
+ * tcgen05 tensor cores); 1 <= B <= 8192;
  * 1 <= L <= 2^24.  Work is split over the attended rows only, so the cost of
  * a step follows sum_b (positions[b] + 1), not B * L.
  */
@@ -132,11 +133,10 @@ int attn_decode_step(const void* q, const int32_t* positions,
  * row positions[b] of every KV head of sequence b becomes k_new/v_new
  * (bit-exact) and out is attention over rows 0..positions[b], the new row
  * included.  The new rows are fed to the attention straight from k_new/v_new
- * and written to the cache in the same launch.  For g <= 4 the new row goes
+ * and written to the cache in the same launch.  For g <= 8 the new row goes
  * through the tile like any cache row, so out is bit-identical to the two
- * calls; for g = 8 and 16 (the tcgen05 kernels) its score and value are
- * folded in fp32 beside the tile, so out agrees with the two calls to
- * rounding.
+ * calls; on the tcgen05 kernels (g = 16) its score and value are folded in
+ * fp32 beside the tile, so out agrees with the two calls to rounding.
  *
  *   q            : [B, Hq, D] bf16.
  *   k_new, v_new : [B, Hkv, D] bf16.

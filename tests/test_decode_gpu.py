@@ -192,13 +192,15 @@ def test_max_batch_tiny_positions():
 
 
 @pytest.mark.parametrize("fused", [False, True])
-def test_max_batch_tensor_cores(fused):
-    """B=8192 at g=8 (the tensor-core kernels): above B=4287 the stream-K
-    prefix array leaves room for two K/V stages only, so this runs the
-    2-stage ring.  Plain step, and the fused append step."""
+@pytest.mark.parametrize("Hq", [16, 32])
+def test_max_batch_eight_and_sixteen_heads(fused, Hq):
+    """B=8192 with 8 heads per KV head (per-warp MMA kernels) and 16 (the
+    tcgen05 kernels; there, above B=4287 the stream-K prefix array leaves
+    room for two K/V stages only, so this runs the 2-stage ring).  Plain
+    step, and the fused append step."""
     B, L = 8192, 300
-    case = synth.decode_case(B=B, Hq=16, Hkv=2, D=128, L=L, positions="uniform", fill="all",
-                             poison=True, seed=13 + int(fused), device="cuda")
+    case = synth.decode_case(B=B, Hq=Hq, Hkv=2, D=128, L=L, positions="uniform", fill="all",
+                             poison=True, seed=13 + int(fused) + Hq, device="cuda")
     bs = [0, 1, 127, 2048, 4287, 4288, 8191]
     want = _oracle_rows(case, bs)
     if fused:
@@ -208,7 +210,7 @@ def test_max_batch_tensor_cores(fused):
     else:
         out = _run_step(case)
     assert torch.isfinite(out.float()).all()
-    _check(case, want, out, f"B=8192 g=8 fused={fused}")
+    _check(case, want, out, f"B=8192 g={Hq // 2} fused={fused}")
 
 
 def test_single_row_cache_and_odd_scale():

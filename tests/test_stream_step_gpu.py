@@ -29,7 +29,8 @@ def _tables(L, D=128, base=10000.0):
 def test_graph_replayed_stream_b1(rope, Hq):
     """B=1, Hkv=8: one captured step replayed 200 times from position 0, fresh
     q/k/v copied in before each replay.  Hq=16 (g=2, the streaming shapes)
-    runs the per-warp MMA kernels, Hq=64 (g=8) the tcgen05 ones."""
+    runs the per-warp MMA kernels; Hq=64 (g=8) runs them too without the
+    rotation, and the tcgen05 kernels with it."""
     steps, Hkv, D, L = 200, 8, 128, 1024
     q, kn, vn, _ = synth.streaming_inputs(steps=steps, B=1, Hq=Hq, Hkv=Hkv, D=D, seed=90,
                                           device="cuda")

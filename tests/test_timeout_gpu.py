@@ -5,8 +5,8 @@ waits for that tile never complete.  Every wait in the
 kernels gives up after 500 ms: the launch must end by itself with
 ATTN_DEV_TIMEOUT in the status word, and the CUDA context must stay usable --
 a normal step right after gives the oracle's result.  Covers cluster mode
-and stream-K on both kernel families: per-warp MMAs (g <= 4) and tcgen05
-(g >= 8).
+and stream-K on both kernel families: per-warp MMAs (g <= 8) and tcgen05
+(g = 16).
 """
 
 import numpy as np
@@ -21,10 +21,10 @@ from _helpers import assert_attn_close, f64
 pytestmark = pytest.mark.gpu
 
 
-# per-warp MMAs: clusters (g=2), stream-K (g=4); tcgen05: stream-K (g=8),
-# clusters (g=8), clusters at g=16 (at most 9 CTAs)
+# per-warp MMAs: clusters (g=2), stream-K (g=4), stream-K (g=8), clusters
+# (g=8); tcgen05: clusters at g=16 (at most 9 CTAs), stream-K at g=16
 @pytest.mark.parametrize("B,Hq,Hkv", [(1, 16, 8), (16, 8, 2), (16, 16, 2), (1, 64, 8),
-                                      (4, 32, 2)])
+                                      (4, 32, 2), (16, 32, 2)])
 def test_wait_runs_out_and_the_context_stays_usable(B, Hq, Hkv):
     positions = [700 + 37 * b for b in range(B)]
     case = synth.decode_case(B=B, Hq=Hq, Hkv=Hkv, D=128, L=2048, positions=positions,
