@@ -125,14 +125,7 @@ template <int G> struct Cfg {
   static constexpr int kMaxRegs = (kRegsFit > 255 ? 255 : kRegsFit) & ~7;
 };
 
-// A named barrier among the consumers, only for the one place every consumer
-// warp reaches unconditionally: before the first tile wait.
-template <int NC>
-__device__ __forceinline__ void consumer_bar() {
-  asm volatile("bar.sync 1, %0;" ::"n"(NC) : "memory");
-}
-
-// Barrier among the NW consumer warps everywhere else.  It sits on an
+// Barrier among the NW consumer warps.  It sits on an
 // mbarrier (count NW, one arrival per warp from lane 0 once the warp's lanes
 // have synced) so that its wait is bounded like every other: a named barrier
 // has no time limit, and a warp that gave up on a tile after a timeout would
@@ -315,23 +308,51 @@ struct Consumer {
       qb[j][3] = u.w;
     }
   }
-  // The rotated query, q_rot [G][kD] fp32 in shared memory: column h < G
-  // takes its bf16 rounding, column G+h the rounding of what is left.
-  __device__ __forceinline__ void load_q_rot(const float* q_rot, float qscale) {
+  // The rotated query, straight from the segment's G query rows and the
+  // rotation row (rc, rs: cos and sin, fp32): lane 4g+t rotates the 32 dims
+  // it feeds to the MMA, each with its partner 64 dims away (rotate-half
+  // form, one rounding per operation).  Column h < G takes the bf16
+  // rounding of rotated head h, column G+h the rounding of what is left.
+  // All of a lane's loads are independent: one round trip, no barrier.
+  __device__ __forceinline__ void load_q_rope(const uint16_t* qrows, const float* rc,
+                                              const float* rs, float qscale) {
     qs = qscale;
-    const int h = g < G ? g : g - G;
+    const bool on = g < 2 * G;
+    const uint16_t* qh = qrows + (size_t)(g < G ? g : g - G) * kD;
+    // every load first (the compiler would otherwise interleave them with
+    // the arithmetic, one round trip per dim group), then the rotations
+    uint4 xv[4], yv[4];
+    float4 cv[4][2], sv[4][2];
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       const int d0 = (j >> 1) * 64 + ((j & 1) * 4 + t) * 8;
+      xv[j] = yv[j] = make_uint4(0u, 0u, 0u, 0u);
+      cv[j][0] = cv[j][1] = sv[j][0] = sv[j][1] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (on) {
+        xv[j] = *reinterpret_cast<const uint4*>(qh + d0);
+        yv[j] = *reinterpret_cast<const uint4*>(qh + (d0 ^ 64));
+        cv[j][0] = *reinterpret_cast<const float4*>(rc + d0);
+        cv[j][1] = *reinterpret_cast<const float4*>(rc + d0 + 4);
+        sv[j][0] = *reinterpret_cast<const float4*>(rs + d0);
+        sv[j][1] = *reinterpret_cast<const float4*>(rs + d0 + 4);
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int d0 = (j >> 1) * 64 + ((j & 1) * 4 + t) * 8;
+      const uint32_t xw[4] = {xv[j].x, xv[j].y, xv[j].z, xv[j].w};
+      const uint32_t yw[4] = {yv[j].x, yv[j].y, yv[j].z, yv[j].w};
+      const float cc[8] = {cv[j][0].x, cv[j][0].y, cv[j][0].z, cv[j][0].w,
+                           cv[j][1].x, cv[j][1].y, cv[j][1].z, cv[j][1].w};
+      const float ss[8] = {sv[j][0].x, sv[j][0].y, sv[j][0].z, sv[j][0].w,
+                           sv[j][1].x, sv[j][1].y, sv[j][1].z, sv[j][1].w};
+      const bool first = d0 < kD / 2;
 #pragma unroll
       for (int r = 0; r < 4; ++r) {
-        uint32_t w = 0u;
-        if (g < 2 * G) {
-          const float x0 = q_rot[h * kD + d0 + 2 * r], x1 = q_rot[h * kD + d0 + 2 * r + 1];
-          const uint32_t hi = pack_bf16x2(x0, x1);
-          w = g < G ? hi : pack_bf16x2(x0 - bf16lo(hi), x1 - bf16hi(hi));
-        }
-        qb[j][r] = w;
+        const float lo = rope1(bf16lo(xw[r]), bf16lo(yw[r]), cc[2 * r], ss[2 * r], first);
+        const float hi = rope1(bf16hi(xw[r]), bf16hi(yw[r]), cc[2 * r + 1], ss[2 * r + 1], first);
+        const uint32_t w = pack_bf16x2(lo, hi);
+        qb[j][r] = !on ? 0u : g < G ? w : pack_bf16x2(lo - bf16lo(w), hi - bf16hi(w));
       }
     }
   }
@@ -521,44 +542,19 @@ __device__ __forceinline__ void produce_tile(const CUtensorMap* tmk, const CUten
   tma_load_3d(sV + kHalf, tmv, 64, row, z, full);
 }
 
-// Rotary embedding of one segment, by the consumers.  rope_segment (all NC
-// consumer threads, at the start of a segment, followed by a consumer
-// barrier): the G query rows of the segment, rotated, into q_rot [G][kD] fp32,
-// and the sequence's cos/sin row into rope_cs [2][kD].  rope_fresh_key (one
-// warp, once the segment's last tile has landed): the appended key row of
-// the tile rotated in place, lane l taking dims 4l..4l+3 and reading its
-// partner dims 64 away before any lane writes.
-template <int G, int NC>
-__device__ __forceinline__ void rope_segment(const uint16_t* qb, const float* rc, const float* rs,
-                                             float* q_rot, float* rope_cs, int ct) {
-  constexpr int kH = kD / 2;
-  static_assert(2 * kD <= NC, "one table value per thread");
-  // every load of a pass first, so they share one round trip (q and the
-  // rotation rows are fresh inputs of the step, often not in L2), then the
-  // stores; g <= 4 takes one pass
-  const bool tab = ct < 2 * kD;
-  const float cs = tab ? (ct < kD ? rc[ct] : rs[ct - kD]) : 0.f;
-#pragma unroll
-  for (int i0 = 0; i0 < G * kH; i0 += NC) {
-    const int i = i0 + ct;
-    const bool rot = i < G * kH;
-    const int h = i / kH, d = i % kH;
-    float x0 = 0.f, x1 = 0.f, c0 = 0.f, c1 = 0.f, s0 = 0.f, s1 = 0.f;
-    if (rot) {
-      const uint16_t* qh = qb + (size_t)h * kD;
-      x0 = __uint_as_float((uint32_t)qh[d] << 16);
-      x1 = __uint_as_float((uint32_t)qh[d + kH] << 16);
-      c0 = rc[d];
-      c1 = rc[d + kH];
-      s0 = rs[d];
-      s1 = rs[d + kH];
-    }
-    if (rot) {
-      q_rot[h * kD + d] = rope1(x0, x1, c0, s0, true);
-      q_rot[h * kD + d + kH] = rope1(x1, x0, c1, s1, false);
-    }
+// The rotation of the fused append's new key: the warp that writes the new
+// rows stages, at the segment's start, the cos and sin values each of its
+// lanes 0-15 will use (dims 8l..8l+7), in that lane's own 16 floats of
+// rope_cs [2][kD].  No other lane reads them, so no barrier is needed.
+__device__ __forceinline__ void stage_fresh_rope(float* rope_cs, const float* rc, const float* rs,
+                                                 int lane) {
+  if (lane < 16) {
+    float4* dst = reinterpret_cast<float4*>(rope_cs + 16 * lane);
+    dst[0] = *reinterpret_cast<const float4*>(rc + 8 * lane);
+    dst[1] = *reinterpret_cast<const float4*>(rc + 8 * lane + 4);
+    dst[2] = *reinterpret_cast<const float4*>(rs + 8 * lane);
+    dst[3] = *reinterpret_cast<const float4*>(rs + 8 * lane + 4);
   }
-  if (tab) rope_cs[ct] = cs;
 }
 
 // A consumer warp's wait for a tile, with the outcome made warp-uniform (the
@@ -606,9 +602,10 @@ __device__ __forceinline__ void fresh_row(const Params& p, uint8_t* Ks, int rows
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         const int d = d0 + 2 * i;
+        const float* cs = rope_cs + 16 * q;  // this lane's staged cos (0-7) and sin (8-15)
         r[i] = pack_bf16x2(
-            rope1(bf16lo(xs[i]), bf16lo(ys[i]), rope_cs[d], rope_cs[kD + d], d < kD / 2),
-            rope1(bf16hi(xs[i]), bf16hi(ys[i]), rope_cs[d + 1], rope_cs[kD + d + 1], d < kD / 2));
+            rope1(bf16lo(xs[i]), bf16lo(ys[i]), cs[2 * i], cs[8 + 2 * i], d < kD / 2),
+            rope1(bf16hi(xs[i]), bf16hi(ys[i]), cs[2 * i + 1], cs[8 + 2 * i + 1], d < kD / 2));
       }
       u = make_uint4(r[0], r[1], r[2], r[3]);
     }
@@ -665,7 +662,7 @@ size_t smem_bytes(int B) {
   constexpr int NW = Cfg<G>::NW;
   return (size_t)kStages * 2 * kTileBytes + (2 * kStages + 2) * sizeof(uint64_t) +
          kMiscInts * sizeof(int) + (size_t)NW * G * 2 * sizeof(float) +
-         (size_t)NW * G * kD * sizeof(float) + (2 + G) * kD * sizeof(float) +
+         (size_t)NW * G * kD * sizeof(float) + 2 * kD * sizeof(float) +
          (size_t)(B + 1) * sizeof(int);
 }
 
@@ -685,9 +682,8 @@ __global__ void __maxnreg__(Cfg<G>::kMaxRegs) decode_splitkv_kernel(const __grid
   int* misc = reinterpret_cast<int*>(bars + 2 * kStages + 2);  // after full, empty, csync, done
   float* merge_ml = reinterpret_cast<float*>(misc + kMiscInts);  // [NW][G][2]
   float* merge_o = merge_ml + NW * G * 2;                         // [NW][G][kD]
-  float* rope_cs = merge_o + NW * G * kD;                         // [2][kD] cos, sin
-  float* q_rot = rope_cs + 2 * kD;                                 // [G][kD]
-  int* prefix = reinterpret_cast<int*>(q_rot + G * kD);            // [B+1]
+  float* rope_cs = merge_o + NW * G * kD;                         // [2][kD] staged cos, sin
+  int* prefix = reinterpret_cast<int*>(rope_cs + 2 * kD);          // [B+1]
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
@@ -810,11 +806,10 @@ __global__ void __maxnreg__(Cfg<G>::kMaxRegs) decode_splitkv_kernel(const __grid
   bool own_fresh = owns_fresh(t0);
   uint4 fk = own_fresh ? load_fresh(p, w.b, w.kvh, lane) : make_uint4(0u, 0u, 0u, 0u);
   if (R) {
-    rope_segment<G, NC>(qb, rope_row<R>(p, p.rope_cos, w.b, w.lo + w.n - 1),
-                        rope_row<R>(p, p.rope_sin, w.b, w.lo + w.n - 1), q_rot,
-                        rope_cs, tid);
-    consumer_bar<NC>();  // before any tile wait: every consumer warp gets here
-    cs.load_q_rot(q_rot, p.qscale);
+    const float* rc = rope_row<R>(p, p.rope_cos, w.b, w.lo + w.n - 1);
+    const float* rs = rope_row<R>(p, p.rope_sin, w.b, w.lo + w.n - 1);
+    cs.load_q_rope(qb, rc, rs, p.qscale);
+    if (own_fresh) stage_fresh_rope(rope_cs, rc, rs, lane);
   } else {
     cs.template load_q<MT>(p, w.b, w.kvh, p.qscale);
   }
@@ -836,13 +831,18 @@ __global__ void __maxnreg__(Cfg<G>::kMaxRegs) decode_splitkv_kernel(const __grid
 
     // ---- end of this CTA's part of the segment: merge and emit ------------
     if (seg_end) {
-      if (!R && (w.k == w.ntiles - 1) && t + 1 < t1) {
-        // the next segment's q (and new rows) only need loads: they go out
-        // now and land while this segment's partials are merged (the merge
-        // reads m, l and o, not q)
+      if ((w.k == w.ntiles - 1) && t + 1 < t1) {
+        // the next segment's q (rotated if asked) and new rows only need
+        // loads: they go out now and land while this segment's partials are
+        // merged (the merge reads m, l and o, not q)
         Walk wn = w;
         walk_next(wn, prefix, p.positions, B, Hkv, win, shift);
-        cs.template load_q<MT>(p, wn.b, wn.kvh, p.qscale);
+        if (R)
+          cs.load_q_rope(p.q + ((size_t)wn.b * p.Hq + (size_t)wn.kvh * G) * kD,
+                         rope_row<R>(p, p.rope_cos, wn.b, wn.lo + wn.n - 1),
+                         rope_row<R>(p, p.rope_sin, wn.b, wn.lo + wn.n - 1), p.qscale);
+        else
+          cs.template load_q<MT>(p, wn.b, wn.kvh, p.qscale);
         if (MT) cs.set_last(wn.lo + wn.n - 1 - shift, p.S);
         own_fresh = p.k_new != nullptr && t + wn.ntiles < t1 &&
                     warp == (wn.n - 1 - (wn.ntiles - 1) * kTile) / KPW;
@@ -933,20 +933,11 @@ __global__ void __maxnreg__(Cfg<G>::kMaxRegs) decode_splitkv_kernel(const __grid
       cs.reset();
     }
     walk_next(w, prefix, p.positions, B, Hkv, win, shift);
-    if (w.k == 0 && t + 1 < t1) {
-      // a new segment; every consumer has read q_rot and rope_cs of the last
-      // one (seg_end's barriers came after), so they may be overwritten
-      const uint16_t* qn = p.q + ((size_t)w.b * p.Hq + (size_t)w.kvh * G) * kD;
-      if (R) {
-        rope_segment<G, NC>(qn, rope_row<R>(p, p.rope_cos, w.b, w.lo + w.n - 1),
-                            rope_row<R>(p, p.rope_sin, w.b, w.lo + w.n - 1),
-                            q_rot, rope_cs, tid);
-        csync(lane);
-        cs.load_q_rot(q_rot, p.qscale);
-        if (MT) cs.set_last(w.lo + w.n - 1 - shift, p.S);
-        own_fresh = owns_fresh(t + 1);
-        if (own_fresh) fk = load_fresh(p, w.b, w.kvh, lane);
-      }
+    if (R && own_fresh && w.k == 0 && t + 1 < t1) {
+      // a new segment whose new key this warp rotates: the last segment's
+      // writer has read its staged values (seg_end's barriers came after)
+      stage_fresh_rope(rope_cs, rope_row<R>(p, p.rope_cos, w.b, w.lo + w.n - 1),
+                       rope_row<R>(p, p.rope_sin, w.b, w.lo + w.n - 1), lane);
     }
   }
 
@@ -974,7 +965,7 @@ size_t cluster_smem_bytes() {
   constexpr int NW = Cfg<G>::NW;
   return (size_t)kStages * 2 * kTileBytes + (2 * kStages + 2) * sizeof(uint64_t) +
          kMiscInts * sizeof(int) + (size_t)NW * G * 2 * sizeof(float) +
-         (size_t)NW * G * kD * sizeof(float) + (2 + G) * kD * sizeof(float) +
+         (size_t)NW * G * kD * sizeof(float) + 2 * kD * sizeof(float) +
          (size_t)Cfg<G>::kMaxC * G * (kD + 2) * sizeof(float);
 }
 
@@ -995,9 +986,8 @@ __global__ void __maxnreg__(Cfg<G>::kMaxRegs)
   int* misc = reinterpret_cast<int*>(bars + 2 * kStages + 2);  // after full, empty, csync, done
   float* merge_ml = reinterpret_cast<float*>(misc + kMiscInts);  // [NW][G][2]
   float* merge_o = merge_ml + NW * G * 2;                         // [NW][G][kD]
-  float* rope_cs = merge_o + NW * G * kD;                         // [2][kD] cos, sin
-  float* q_rot = rope_cs + 2 * kD;                                 // [G][kD]
-  float* land_o = q_rot + G * kD;                    // [kMaxC][G][kD]: rank r's partial o
+  float* rope_cs = merge_o + NW * G * kD;                         // [2][kD] staged cos, sin
+  float* land_o = rope_cs + 2 * kD;                  // [kMaxC][G][kD]: rank r's partial o
   float* land_ml = land_o + Cfg<G>::kMaxC * G * kD;  // [kMaxC][G][2]: its (max, sum)
 
   cg::cluster_group cluster = cg::this_cluster();
@@ -1040,10 +1030,8 @@ __global__ void __maxnreg__(Cfg<G>::kMaxRegs)
     if (!R) {
       cs.template load_q<MT>(p, b, kvh, p.qscale);
     } else if (!p.rope_by_pos) {
-      rope_segment<G, NC>(qb, rope_row<R>(p, p.rope_cos, b, 0), rope_row<R>(p, p.rope_sin, b, 0),
-                          q_rot, rope_cs, tid);
-      consumer_bar<NC>();  // every consumer warp gets here
-      cs.load_q_rot(q_rot, p.qscale);
+      cs.load_q_rope(qb, rope_row<R>(p, p.rope_cos, b, 0), rope_row<R>(p, p.rope_sin, b, 0),
+                     p.qscale);
     }
   }
   if (pos - shift < 0 || pos >= p.L) {
@@ -1089,19 +1077,18 @@ __global__ void __maxnreg__(Cfg<G>::kMaxRegs)
   } else {
     // ----------------------------------------------------------- consumers --
     ConsumerSync csync{smem_u32(&bars[2 * kStages]), abort_flag, p.status, 0u};
-    if (R && p.rope_by_pos) {  // the rotation row is the position's
-      rope_segment<G, NC>(qb, rope_row<R>(p, p.rope_cos, b, pos),
-                          rope_row<R>(p, p.rope_sin, b, pos), q_rot,
-                          rope_cs, tid);
-      consumer_bar<NC>();  // before any tile wait: every consumer warp gets here
-      cs.load_q_rot(q_rot, p.qscale);
-    }
+    if (R && p.rope_by_pos)  // the rotation row is the position's
+      cs.load_q_rope(qb, rope_row<R>(p, p.rope_cos, b, pos), rope_row<R>(p, p.rope_sin, b, pos),
+                     p.qscale);
     if (MT) cs.set_last(pos - shift, p.S);
     // fused append: the warp whose keys include the last row of the last
     // tile, in the rank that takes that tile, writes the new rows
     const bool own_fresh = p.k_new != nullptr && (ntiles - 1) % C == rank &&
                            warp == (n - 1 - (ntiles - 1) * kTile) / KPW;
     const uint4 fk = own_fresh ? load_fresh(p, b, kvh, lane) : make_uint4(0u, 0u, 0u, 0u);
+    if (R && own_fresh)
+      stage_fresh_rope(rope_cs, rope_row<R>(p, p.rope_cos, b, pos),
+                       rope_row<R>(p, p.rope_sin, b, pos), lane);
     cs.reset();
     int i = 0;
     for (int k = rank; k < ntiles; k += C, ++i) {
