@@ -16,11 +16,14 @@
 //    the two Q tiles once and streams 128-key K and V tiles through a 3-stage
 //    ring (4 stages).
 //  * warp 1, one thread: issues tcgen05.mma (bf16 in, fp32 accumulate in
-//    tensor memory).  Per K/V tile i: S_A = Q_A K^T and S_B = Q_B K^T (128
-//    TMEM columns each), then O_A += P_A V and O_B += P_B V for tile i-1,
+//    tensor memory) for S_A = Q_A K^T and S_B = Q_B K^T (128 TMEM columns
+//    each) per K/V tile; warp 10, one thread: O_A += P_A V and O_B += P_B V,
 //    with P read from tensor memory (64 columns of bf16 pairs per tile) and
-//    O kept in tensor memory for the whole key loop.  While one query tile's
-//    softmax runs, the tensor core works on the other tile.
+//    O kept in tensor memory for the whole key loop.  Two issuing threads
+//    took the 2048-token prefill from 28.9 to 24.9 us; for one-tile items
+//    at HD = 64 one thread issuing both streams measured faster (22.4 against
+//    23.5 us), so that launch keeps it.  While one query tile's softmax
+//    runs, the tensor core works on the other tile.
 //  * warps 2-5 (tile A) and 6-9 (tile B), thread r owns query row r (TMEM
 //    lane quarter warp % 4): read the whole S row from TMEM into registers in
 //    one round trip, mask the causal diagonal, keep the online softmax in
@@ -44,7 +47,8 @@ constexpr int kBM = 128;   // query rows per tile (MMA M)
 constexpr int kBN = 128;   // keys per tile (MMA N of QK^T, K of PV)
 constexpr int kQT = 2;     // query-tile slots per CTA (softmax warpgroups)
 constexpr int kMaxKVStages = 4;
-constexpr int kPThreads = 320;             // 10 warps
+constexpr int kPThreads = 352;             // 11 warps
+constexpr int kPVWarp = 10;                // the PV issuer
 constexpr int kChunkBytes = kBM * 64 * 2;  // 16 KB: 128 rows x 128 bytes, one swizzle column block
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemP = 256;           // P of tile x at 256 + 64x (bf16 pairs)
@@ -108,7 +112,7 @@ __device__ __forceinline__ bool warp_wait_or_abort(uint32_t bar, uint32_t parity
   return __all_sync(0xffffffffu, wait_or_abort(bar, parity, abort_flag));
 }
 
-template <int HD>
+template <int HD, bool kSplit>
 __global__ void __launch_bounds__(kPThreads, 1)
     prefill_tcgen05_kernel(const __grid_constant__ CUtensorMap tm_q,
                            const __grid_constant__ CUtensorMap tm_k,
@@ -219,8 +223,8 @@ __global__ void __launch_bounds__(kPThreads, 1)
         if (!ok) break;
       }
     }
-  } else if (warp == 1) {
-    // ------------------------------------------------------- MMA issuer --
+  } else if (warp == 1 && !kSplit) {
+    // ------------------------------------ MMA issuer, both streams (S, O) --
     if (lane == 0) {
       constexpr uint32_t idesc_qk = make_idesc(kBM, kBN, false);
       // O (+)= P V at N = HD: V's HD/64 column blocks, kChunkBytes apart
@@ -289,6 +293,92 @@ __global__ void __launch_bounds__(kPThreads, 1)
         for (int x = 0; ok && x < kQT; ++x)
           if (it.n - 1 < it.nt[x]) ok = issue_pv(x, it.n - 1, gk0);
         tc_commit(bar(kBarKVEmpty + (gk0 + it.n - 1) % kKVStages));  // last tile released
+        gk = gk0 + it.n;
+      }
+    }
+  } else if (warp == 1) {
+    // ----------------------------------------------- QK^T issuer (S_x) --
+    if (lane == 0) {
+      constexpr uint32_t idesc_qk = make_idesc(kBM, kBN, false);
+      uint32_t gk = 0;             // K/V tiles consumed so far
+      uint32_t cs[kQT] = {0, 0};   // S_x issued so far
+      bool ok = true;
+      for (int r = 0; ok && item_of(r) < n_items; ++r) {
+        const Item it = item(item_of(r));
+        if (!wait_or_abort(bar(kBarQ), (uint32_t)r & 1u, abort_flag)) break;
+        const uint32_t gk0 = gk;
+        for (int i = 0; ok && i < it.n; ++i) {
+          const uint32_t g = gk0 + i;
+          const int s = g % kKVStages;
+          if (!wait_or_abort(bar(kBarKVFull + s), (g / kKVStages) & 1u, abort_flag)) {
+            ok = false;
+            break;
+          }
+          const uint32_t sK = base + L::kOffKV + s * 2 * kTileBytes;
+          for (int x = 0; ok && x < kQT; ++x) {
+            if (i >= it.nt[x]) continue;
+            // the softmax has read the previous S_x
+            if (cs[x] > 0 &&
+                !wait_or_abort(bar(kBarSFree + x), (cs[x] - 1) & 1u, abort_flag)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+#pragma unroll
+            for (int k = 0; k < HD / 16; ++k) {  // 4 K-steps per 128-byte column block
+              const uint32_t off = (k >> 2) * kChunkBytes + (k & 3) * 32;
+              tc_mma(tmem + 128 * x, sw128_desc(sQ + x * kTileBytes + off), sw128_desc(sK + off),
+                     idesc_qk, k > 0);
+            }
+            tc_commit(bar(kBarSFull + x));
+            ++cs[x];
+          }
+          if (ok && i + 1 == it.n) tc_commit(bar(kBarQFree));  // last QK^T of this item
+        }
+        gk = gk0 + it.n;
+      }
+    }
+  } else if (warp == kPVWarp) {
+    // ------------------------------------------------ PV issuer (O_x) --
+    // Its own thread (kSplit), so that the two streams of MMAs are issued
+    // in parallel.  P_x of tile j is written after S_x of tile j was read,
+    // so the QK^T that read the stage's K is done once P_x is; the commit
+    // after the tile's last PV therefore releases the whole stage.  Without
+    // kSplit the combined issuer does this and the warp idles.
+    if (kSplit && lane == 0) {
+      // O (+)= P V at N = HD: V's HD/64 column blocks, kChunkBytes apart
+      constexpr uint32_t idesc_pv = make_idesc(kBM, HD, true);
+      uint32_t gk = 0;             // K/V tiles consumed so far
+      uint32_t cp[kQT] = {0, 0};   // P_x consumed (PV_x issued) so far
+      bool ok = true;
+      for (int r = 0; ok && item_of(r) < n_items; ++r) {
+        const Item it = item(item_of(r));
+        const uint32_t gk0 = gk;
+        for (int j = 0; ok && j < it.n; ++j) {
+          for (int x = 0; ok && x < kQT; ++x) {
+            if (j >= it.nt[x]) continue;
+            if (j == 0 && r > 0 &&  // the previous item's epilogue has read O_x
+                !wait_or_abort(bar(kBarOFree + x), (uint32_t)(r - 1) & 1u, abort_flag)) {
+              ok = false;
+              break;
+            }
+            if (!wait_or_abort(bar(kBarPFull + x), cp[x] & 1u, abort_flag)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t sV =
+                base + L::kOffKV + ((gk0 + j) % kKVStages) * 2 * kTileBytes + kTileBytes;
+#pragma unroll
+            for (int k = 0; k < kBN / 16; ++k)
+              tc_mma_ts(tmem + kTmemO + HD * x, tmem + kTmemP + 64 * x + 8 * k,
+                        sw128_desc(sV + k * 16 * 128, HD > 64 ? kChunkBytes : 16), idesc_pv,
+                        (j > 0 || k > 0) ? 1u : 0u);
+            tc_commit(bar(kBarPVDone + x));
+            ++cp[x];
+          }
+          if (ok) tc_commit(bar(kBarKVEmpty + (gk0 + j) % kKVStages));  // tile j released
+        }
         gk = gk0 + it.n;
       }
     }
@@ -488,9 +578,12 @@ cudaError_t launch_prefill_hd(const CUtensorMap& mq, const CUtensorMap& mk, cons
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev >= 0 && dev < 64 && !configured[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(prefill_tcgen05_kernel<HD>,
+    cudaError_t e = cudaFuncSetAttribute(prefill_tcgen05_kernel<HD, true>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          L::kSmemBytes);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(prefill_tcgen05_kernel<HD, false>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmemBytes);
     if (e != cudaSuccess) return e;
     configured[dev] = true;
   }
@@ -506,7 +599,12 @@ cudaError_t launch_prefill_hd(const CUtensorMap& mq, const CUtensorMap& mk, cons
   const long long items = (long long)p.n_units * p.Hq;
   if (items > 0x7fffffffLL) return cudaErrorInvalidValue;
   const unsigned blocks = (unsigned)std::min<long long>(items, sms);  // one CTA per SM
-  prefill_tcgen05_kernel<HD><<<blocks, kPThreads, L::kSmemBytes, stream>>>(mq, mk, mv, p);
+  // QK^T and PV issued from two threads, except for one-tile items at
+  // HD = 64, where one thread issuing both measured faster
+  if (HD == 64 && p.tpi == 1)
+    prefill_tcgen05_kernel<HD, false><<<blocks, kPThreads, L::kSmemBytes, stream>>>(mq, mk, mv, p);
+  else
+    prefill_tcgen05_kernel<HD, true><<<blocks, kPThreads, L::kSmemBytes, stream>>>(mq, mk, mv, p);
   return cudaGetLastError();
 }
 
