@@ -1172,7 +1172,7 @@ __global__ void __maxnreg__(Cfg<G>::kMaxRegs)
 
 struct DevInfo {
   int num_sms = 0;
-  bool configured[9] = {};               // per g
+  bool configured[9] = {};               // per g (1, 2, 4 and 8)
   int clusters[9][kMaxCluster + 1] = {};  // [g][C]: co-resident clusters of C CTAs
 };
 DevInfo g_dev[64];

@@ -905,8 +905,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 // ------------------------------------------------------------------ host --
 
 struct TcDevInfo {
-  bool configured[9] = {};                // per g
-  int clusters[9][kMaxCluster + 1] = {};  // [g][C]: co-resident clusters of C CTAs
+  bool configured[17] = {};                // per g (8 and 16)
+  int clusters[17][kMaxCluster + 1] = {};  // [g][C]: co-resident clusters of C CTAs
 };
 TcDevInfo g_tc_dev[64];
 
