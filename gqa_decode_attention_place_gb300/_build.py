@@ -25,7 +25,7 @@ LIBNAME = "libgqa_attn.so"
 LIBPATH = os.path.join(LIBDIR, LIBNAME)
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
+NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-Wall,-Wextra",
                      "--expt-relaxed-constexpr", "-Xptxas", "-v", "-I", INCLUDE, "-I", CSRC]
 
 
@@ -76,6 +76,10 @@ def build(force: bool = False, verbose: bool = False) -> str:
         if rc != 0:
             failed = True
             sys.stderr.write(f"nvcc failed on {src}:\n{out}\n")
+        else:
+            warnings = [ln for ln in out.splitlines() if "warning" in ln.lower()]
+            if warnings:  # host-compiler warnings (-Wall -Wextra) are shown, not hidden
+                sys.stderr.write(f"{os.path.basename(src)}:\n" + "\n".join(warnings) + "\n")
     with open(os.path.join(BUILD, "ptxas.log"), "w") as f:
         f.write("\n".join(logs))
     if failed:
