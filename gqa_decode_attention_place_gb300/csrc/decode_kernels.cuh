@@ -239,6 +239,9 @@ __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
   asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
   return d;
 }
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
 __device__ __forceinline__ uint4 lds128(const uint8_t* p) {
   return *reinterpret_cast<const uint4*>(p);
 }
@@ -1011,6 +1014,21 @@ __global__ void __maxnreg__(Cfg<G>::kMaxRegs)
     mbar_init(smem_u32(&bars[2 * kStages]), NW);
     misc[0] = 0;
     fence_mbar_init();
+  }
+  // The step's own small inputs (this segment's q rows, new rows and
+  // position) are often cold in HBM: warm them into L2 while the previous
+  // kernel finishes.  An L2 prefetch returns no data, and L2 is where every
+  // write lands first, so anything the previous kernel still writes there
+  // is what the loads after the wait see.
+  if (warp == 0 && lane < 8) {
+    const uint8_t* qrow = reinterpret_cast<const uint8_t*>(
+        p.q + head_row<G, MT>(p, b, kvh, 0) * kD);
+    if (!MT && lane < G * 2) prefetch_l2(qrow + lane * 128);  // G contiguous rows of 256 bytes
+    if (p.k_new != nullptr && lane < 4) {
+      const size_t off = ((size_t)b * p.Hkv + kvh) * kRowBytes + (lane & 1) * 128;
+      prefetch_l2((lane < 2 ? p.k_new : p.v_new) + off);
+    }
+    if (lane == 7) prefetch_l2(p.positions + b);
   }
   grid_dependency_wait();
   grid_dependents_launch();
