@@ -1030,6 +1030,8 @@ __global__ void __maxnreg__(Cfg<G>::kMaxRegs)
     }
     if (lane == 7) prefetch_l2(p.positions + b);
   }
+  if (R && warp == 1 && lane < 8 && !p.rope_by_pos)  // per-sequence rotation rows: 2 x 512 bytes
+    prefetch_l2((lane < 4 ? p.rope_cos : p.rope_sin) + (size_t)b * kD + (lane & 3) * 32);
   grid_dependency_wait();
   grid_dependents_launch();
   // Rank r's first tile is tile r whatever the position (rows from 0 without
