@@ -49,6 +49,9 @@ TRAFFIC_BYTES_PER_LAUNCH = 17.617e6
 HQ, HKV, D, L = 16, 8, 128, 8192
 METRIC = "decode-attn HBM GB/s (% of peak) & steps/s; causal prefill TFLOP/s"
 FLUSH_BYTES = 512 << 20
+# the nominal HBM3e bandwidth of the part (a second denominator beside the
+# measured copy rate, which both reads and writes)
+NOMINAL_HBM_GBS = 8000.0
 
 
 def _args():
@@ -468,19 +471,21 @@ def _time_graph(torch, fn, flush, reps, warm):
     return times
 
 
-def _per_position(torch, ga, st, flush, hbm):
-    """Decode time at fixed positions: warm (graph of R back-to-back launches,
-    cache in L2) and cold (each launch preceded by an L2 flush; flush-only
-    time subtracted)."""
+def _time_positions(torch, ga, q_of, kc, vc, ws, positions, flush, hbm, scale):
+    """B=1 decode time at fixed positions: warm (graph of R back-to-back
+    launches, cache in L2) and cold (each launch preceded by an L2 flush;
+    flush-only time subtracted).  q_of(p) gives the query rows for p."""
     import oracle
     R = 50
+    Hq, Hkv, Dd = q_of(0).shape[1], kc.shape[1], kc.shape[3]
     res = {}
-    for p in (100, 1000, 4000, 8000):
+    for p in positions:
         pos = torch.full((1,), p, dtype=torch.int32, device="cuda")
-        out = torch.empty((1, HQ, D), dtype=torch.bfloat16, device="cuda")
+        out = torch.empty((1, Hq, Dd), dtype=torch.bfloat16, device="cuda")
+        q = q_of(p)
 
         def one():
-            ga.attn_decode_step(st.q[p], pos, st.kc, st.vc, st.scale, out=out, workspace=st.ws)
+            ga.attn_decode_step(q, pos, kc, vc, scale, out=out, workspace=ws)
         one()
         torch.cuda.synchronize()
         g_warm = torch.cuda.CUDAGraph()
@@ -496,14 +501,48 @@ def _per_position(torch, ga, st, flush, hbm):
         with torch.cuda.graph(g_flush):
             for _ in range(R):
                 flush()
-        warm = statistics.median(_time_graph(torch, g_warm.replay, flush, 5, 2)) / R
-        cold = (statistics.median(_time_graph(torch, g_cold.replay, flush, 5, 2)) -
-                statistics.median(_time_graph(torch, g_flush.replay, flush, 5, 2))) / R
-        nb = oracle.decode_bytes([p], HQ, HKV, D)
+        warm = statistics.median(_time_graph(torch, g_warm.replay, flush, 7, 2)) / R
+        cold = (statistics.median(_time_graph(torch, g_cold.replay, flush, 7, 2)) -
+                statistics.median(_time_graph(torch, g_flush.replay, flush, 7, 2))) / R
+        nb = oracle.decode_bytes([p], Hq, Hkv, Dd)
         res[str(p)] = {"us_warm_l2": round(warm * 1e3, 3), "us_cold_l2": round(cold * 1e3, 3),
                        "GBs_cold": round(nb / (cold * 1e-3) / 1e9, 1),
                        "frac_cold": round(nb / (cold * 1e-3) / 1e9 / hbm, 3),
+                       "frac_cold_8tbs": round(nb / (cold * 1e-3) / 1e9 / NOMINAL_HBM_GBS, 3),
                        "bytes": nb}
+    return res
+
+
+def _per_position(torch, ga, st, flush, hbm):
+    """The streaming workload's cache at positions 100/1000/4000/8000."""
+    return _time_positions(torch, ga, lambda p: st.q[p], st.kc, st.vc, st.ws,
+                           (100, 1000, 4000, 8000), flush, hbm, st.scale)
+
+
+def _max_len_leg(torch, ga, flush, hbm):
+    """Per-step cost against max_len: B=1, Hq=16, Hkv=8 at positions
+    100/4000/8000 with max_len 8192 and with max_len 2^20 (two 2 GiB
+    caches).  The step reads rows 0..pos only, so the times should agree."""
+    g = torch.Generator(device="cuda")
+    g.manual_seed(11)
+    q = torch.randn((1, HQ, D), generator=g, device="cuda").to(torch.bfloat16)
+    res = {}
+    for Lx in (L, 1 << 20):
+        kc = torch.empty((1, HKV, Lx, D), dtype=torch.bfloat16, device="cuda")
+        vc = torch.empty_like(kc)
+        for t in (kc, vc):  # N(0,1) rows, drawn in 64 Mi-element chunks
+            flat = t.view(-1)
+            for i in range(0, flat.numel(), 1 << 26):
+                n = min(1 << 26, flat.numel() - i)
+                flat[i:i + n] = torch.randn(n, generator=g, device="cuda").to(torch.bfloat16)
+        ws = ga.decode_workspace(1, HQ, HKV, Lx, D)
+        res[f"max_len_{Lx}"] = _time_positions(torch, ga, lambda p: q, kc, vc, ws,
+                                               (100, 4000, 8000), flush, hbm, 1.0 / math.sqrt(D))
+        del kc, vc
+        torch.cuda.empty_cache()
+    a, b = res[f"max_len_{L}"], res[f"max_len_{1 << 20}"]
+    res["ratio_warm"] = {p: round(b[p]["us_warm_l2"] / a[p]["us_warm_l2"], 3) for p in a}
+    res["ratio_cold"] = {p: round(b[p]["us_cold_l2"] / a[p]["us_cold_l2"], 3) for p in a}
     return res
 
 
@@ -527,6 +566,7 @@ def _decode_leg(torch, ga, synth, name, flush, hbm):
     tc = Hq // Hkv == 16  # g = 16 runs on the tcgen05 kernel, g <= 8 on warp-level MMAs
     r = {"us": round(ms * 1e3, 2), "GBs": round(nb / (ms * 1e-3) / 1e9, 1),
          "frac_hbm": round(nb / (ms * 1e-3) / 1e9 / hbm, 3),
+         "frac_hbm_8tbs": round(nb / (ms * 1e-3) / 1e9 / NOMINAL_HBM_GBS, 3),
          "TFLOPs_tensor": round(fl / (ms * 1e-3) / 1e12, 2),
          "kernel": "decode_tc_kernel (tcgen05)" if tc else "decode kernel (mma.sync per warp)",
          "bytes": nb, "shape": {"B": B, "Hq": Hq, "Hkv": Hkv, "D": Dd, "L": Ll}}
@@ -560,7 +600,8 @@ def _append_leg(torch, ga, synth, name, flush, hbm, rope):
     pos = case.positions.cpu().tolist()
     nb = oracle.decode_bytes(pos, Hq, Hkv, Dd) + 2 * 2 * B * Hkv * Dd * 2
     r = {"us": round(ms * 1e3, 2), "GBs": round(nb / (ms * 1e-3) / 1e9, 1),
-         "frac_hbm": round(nb / (ms * 1e-3) / 1e9 / hbm, 3), "bytes": nb,
+         "frac_hbm": round(nb / (ms * 1e-3) / 1e9 / hbm, 3),
+         "frac_hbm_8tbs": round(nb / (ms * 1e-3) / 1e9 / NOMINAL_HBM_GBS, 3), "bytes": nb,
          "shape": {"B": B, "Hq": Hq, "Hkv": Hkv, "D": Dd, "L": Ll}}
     del case, ws, out
     torch.cuda.empty_cache()
@@ -584,7 +625,8 @@ def _window_leg(torch, ga, synth, name, flush, hbm, window):
     rows_pos = [min(int(p), window - 1) for p in case.positions.cpu().tolist()]
     nb = oracle.decode_bytes(rows_pos, Hq, Hkv, Dd)
     r = {"us": round(ms * 1e3, 2), "GBs": round(nb / (ms * 1e-3) / 1e9, 1),
-         "frac_hbm": round(nb / (ms * 1e-3) / 1e9 / hbm, 3), "bytes": nb, "window": window,
+         "frac_hbm": round(nb / (ms * 1e-3) / 1e9 / hbm, 3),
+         "frac_hbm_8tbs": round(nb / (ms * 1e-3) / 1e9 / NOMINAL_HBM_GBS, 3), "bytes": nb, "window": window,
          "shape": {"B": B, "Hq": Hq, "Hkv": Hkv, "D": Dd, "L": Ll}}
     del case, ws, out
     torch.cuda.empty_cache()
@@ -611,7 +653,8 @@ def _multi_leg(torch, ga, synth, name, flush, hbm, S):
     last = [int(p) + S - 1 for p in pos.cpu().tolist()]
     nb = oracle.decode_bytes(last, Hq, Hkv, Dd) + 2 * (S - 1) * B * Hq * Dd * 2
     r = {"us": round(ms * 1e3, 2), "GBs": round(nb / (ms * 1e-3) / 1e9, 1),
-         "frac_hbm": round(nb / (ms * 1e-3) / 1e9 / hbm, 3), "bytes": nb, "S": S,
+         "frac_hbm": round(nb / (ms * 1e-3) / 1e9 / hbm, 3),
+         "frac_hbm_8tbs": round(nb / (ms * 1e-3) / 1e9 / NOMINAL_HBM_GBS, 3), "bytes": nb, "S": S,
          "shape": {"B": B, "Hq": Hq, "Hkv": Hkv, "D": Dd, "L": Ll}}
     del case, ws, out, q
     torch.cuda.empty_cache()
@@ -772,6 +815,7 @@ def run_ours(args):
         legs = {"per_position": _per_position(torch, ga, st, flush, hbm)}
         del st
         torch.cuda.empty_cache()
+        legs["max_len"] = _max_len_leg(torch, ga, flush, hbm)
         for name in ("ragged", "stress"):
             legs[name] = _decode_leg(torch, ga, synth, name, flush, hbm)
         legs["ragged_append"] = _append_leg(torch, ga, synth, "ragged", flush, hbm, rope=False)

@@ -1,6 +1,7 @@
 // common.cuh -- small sm_103a building blocks shared by the kernels:
-// mbarrier pipeline waits with a time limit, 1-D bulk (TMA) copies,
-// bf16 <-> fp32 conversion and the ex2 instruction.
+// mbarrier pipeline waits with a time limit, bf16 <-> fp32 conversion, the
+// ex2 instruction, packed fp32 pairs and the launch with programmatic
+// dependent launch.
 #pragma once
 
 #include <cstdint>
@@ -70,8 +71,6 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
   }
 }
 
-// ------------------------------------------------------------ bulk copies --
-
 // ------------------------------------------------------------- conversions --
 
 // Two bf16 values packed in a 32-bit word -> two exact fp32 values.
@@ -122,6 +121,15 @@ __device__ __forceinline__ f2 add2(f2 a, f2 b) {
   f2 d;
   asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d.r) : "l"(a.r), "l"(b.r));
   return d;
+}
+
+// Whether rows p0 .. p0 + shift (a sequence's position and the shift - 1
+// further rows of a multi-token step) lie inside a cache of L rows.  p0 comes
+// from the caller and may be any int, so the test is written without a sum
+// that could overflow (L >= 1 and 0 <= shift < 2^31 - L keep L - 1 - shift
+// in range).
+__device__ __forceinline__ bool rows_in_cache(int p0, int shift, int L) {
+  return p0 >= 0 && p0 <= L - 1 - shift;
 }
 
 __device__ __forceinline__ void set_status(uint32_t* status, uint32_t bits) {

@@ -2,6 +2,10 @@
 // decode_kernels.cuh, compiled per group size in decode_g<g>.cu): workspace
 // layout, supported sizes, parameter set-up and dispatch, and the
 // allocation-free variant's built-in scratch.
+#include <cuda.h>
+
+#include <mutex>
+
 #include "decode_params.h"
 #include "internal.h"
 
@@ -93,21 +97,71 @@ namespace {
 constexpr size_t kNoAllocScratchBytes = (size_t)16 << 20;
 static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
 
-// Device address of g_noalloc_scratch, looked up once per device (with that
-// device current).  In host code the array's name is only a stand-in, never a
-// usable device address.
+// The current context's id (0 if none is current or the driver cannot say).
+// A device reset (cudaDeviceReset) replaces the context and reloads the
+// library's device code, so the array may then sit at another address.
+unsigned long long current_context_id() {
+  typedef CUresult (*GetCurrentFn)(CUcontext*);
+  typedef CUresult (*GetIdFn)(CUcontext, unsigned long long*);
+  static GetCurrentFn get_current = nullptr;
+  static GetIdFn get_id = nullptr;
+  static bool resolved = false;
+  if (!resolved) {  // called with the lookup mutex held
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<GetCurrentFn>(f);
+    f = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<GetIdFn>(f);
+    resolved = true;
+  }
+  CUcontext c = nullptr;
+  unsigned long long id = 0;
+  if (!get_current || !get_id || get_current(&c) != CUDA_SUCCESS || !c ||
+      get_id(c, &id) != CUDA_SUCCESS)
+    return 0;
+  return id;
+}
+
+// Device address of g_noalloc_scratch for the current device.  In host code
+// the array's name is only a stand-in, never a usable device address, so the
+// address is looked up (cudaGetSymbolAddress, with the device current) once
+// per device and context and kept.  The lookup table is guarded by a mutex,
+// so host threads making their first calls at the same time are safe; a new
+// context on the device (after a reset) triggers a fresh lookup.
 void* noalloc_scratch(cudaError_t* err) {
-  static void* addr[64] = {};
+  struct Entry {
+    unsigned long long ctx;
+    void* addr;
+  };
+  static std::mutex mu;
+  static Entry table[64] = {};
+  std::lock_guard<std::mutex> lock(mu);
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e == cudaSuccess && (dev < 0 || dev >= 64)) e = cudaErrorInvalidDevice;
-  if (e == cudaSuccess && !addr[dev]) {
+  if (e != cudaSuccess) {
+    *err = e;
+    return nullptr;
+  }
+  Entry& t = table[dev];
+  const unsigned long long ctx = current_context_id();
+  if (!t.addr || ctx == 0 || ctx != t.ctx) {
     void* p = nullptr;
     e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-    if (e == cudaSuccess) addr[dev] = p;
+    if (e != cudaSuccess) {
+      *err = e;
+      return nullptr;
+    }
+    // the lookup made the device's context current if none was
+    t.ctx = current_context_id();
+    t.addr = p;
   }
-  *err = e;
-  return e == cudaSuccess ? addr[dev] : nullptr;
+  *err = cudaSuccess;
+  return t.addr;
 }
 
 }  // namespace

@@ -643,7 +643,9 @@ __device__ __forceinline__ void advance_ticket(const Params& p, int lane) {
   last = __shfl_sync(0xffffffffu, last, 0);
   __syncwarp();
   if (!last) return;
-  for (int b = lane; b < p.B; b += 32) p.advance[b] += 1;
+  // unsigned add: a position at INT_MAX wraps to a negative (rejected) one
+  for (int b = lane; b < p.B; b += 32)
+    p.advance[b] = (int32_t)((uint32_t)p.advance[b] + 1u);
   if (lane == 0) *p.ticket = 0u;
 }
 
@@ -719,10 +721,10 @@ __global__ void __maxnreg__(Cfg<G>::kMaxRegs) decode_splitkv_kernel(const __grid
     const int b = base + tid;
     int v = 0;
     if (tid < NC && b < B) {
-      const int pos = p.positions[b] + shift;
-      if (pos - shift >= 0 && pos < L) {
+      const int p0 = p.positions[b];
+      if (rows_in_cache(p0, shift, L)) {
         int lo, n;
-        attended_rows(pos, win, lo, n);
+        attended_rows(p0 + shift, win, lo, n);
         v = (n - 1) / kTile + 1;  // ceil(n / kTile)
       } else if (b % gridDim.x == blockIdx.x) {
         // out-of-range position: flag it and make the sequence's output NaN
@@ -1042,7 +1044,7 @@ __global__ void __maxnreg__(Cfg<G>::kMaxRegs)
   const bool early = !(M & kModeWindow) && rank * kTile < p.L;
   if (early && producer) produce_tile(&tm_k, &tm_v, p, stages, bars, 0, b, kvh, rank, 0);
   // the position's load goes out first; its value is used after the q setup
-  const int pos = p.positions[b] + shift;
+  const int pos0 = p.positions[b];
   const uint16_t* qb = p.q + ((size_t)b * p.Hq + (size_t)kvh * G) * kD;
   Consumer<G> cs;
   if (warp < NW) {
@@ -1054,7 +1056,7 @@ __global__ void __maxnreg__(Cfg<G>::kMaxRegs)
                      p.qscale);
     }
   }
-  if (pos - shift < 0 || pos >= p.L) {
+  if (!rows_in_cache(pos0, shift, p.L)) {
     // the same for every CTA of the cluster: all leave, no cluster barrier
     if (early && producer) mbar_wait(smem_u32(&bars[0]), 0u, abort_flag);
     if (rank == 0 && kvh == 0 && tid == 0) {
@@ -1067,6 +1069,7 @@ __global__ void __maxnreg__(Cfg<G>::kMaxRegs)
     }
     return;
   }
+  const int pos = pos0 + shift;
   int lo, n;
   attended_rows(pos, win, lo, n);
   const int ntiles = (n - 1) / kTile + 1;

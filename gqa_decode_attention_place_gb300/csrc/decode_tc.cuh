@@ -278,8 +278,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     rank = (int)cluster.block_rank();
     const int seg = blockIdx.x / C;
     const int b = seg / Hkv, kvh = seg % Hkv;
-    const int pos = p.positions[b] + shift;
-    if (pos - shift < 0 || pos >= L) {
+    const int pos0 = p.positions[b];
+    if (!rows_in_cache(pos0, shift, L)) {
       // the same for every CTA of the cluster: all leave, no cluster barrier
       if (rank == 0 && kvh == 0 && tid == 0) {
         set_status(p.status, ATTN_DEV_BAD_POSITION);
@@ -292,7 +292,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       return;
     }
     int lo, n;
-    attended_rows(pos, win, lo, n);
+    attended_rows(pos0 + shift, win, lo, n);
     const int ntiles = (n - 1) / kTile + 1;
     const int k0 = (int)((long long)rank * ntiles / C);
     const int k1 = (int)((long long)(rank + 1) * ntiles / C);
@@ -310,10 +310,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const int b = b0 + tid;
       int v = 0;
       if (tid < kTcNC && b < B) {
-        const int pos = p.positions[b] + shift;
-        if (pos - shift >= 0 && pos < L) {
+        const int p0 = p.positions[b];
+        if (rows_in_cache(p0, shift, L)) {
           int lo, n;
-          attended_rows(pos, win, lo, n);
+          attended_rows(p0 + shift, win, lo, n);
           v = (n - 1) / kTile + 1;
         } else if (b % gridDim.x == blockIdx.x) {
           set_status(p.status, ATTN_DEV_BAD_POSITION);

@@ -26,7 +26,7 @@ __global__ void __launch_bounds__(256) kv_append_kernel(
   const long long bt = row / Hkv;
   const int b = (int)(bt / S), t = (int)(bt % S);
   const int p0 = positions[b];
-  if (p0 < 0 || p0 + S - 1 >= L) return;  // reported by the decode call
+  if (!rows_in_cache(p0, S - 1, L)) return;  // reported by the decode call
   const long long dst = (((long long)b * Hkv + h) * L + p0 + t) * vec_per_row + c;
   k_cache[dst] = k_new[i];
   v_cache[dst] = v_new[i];

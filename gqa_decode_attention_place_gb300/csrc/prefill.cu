@@ -13,8 +13,8 @@
 // order (CTA c takes items c, 2G-1-c, 2G+c, ...) so the causal work per CTA
 // evens out.  Each K/V tile loaded serves both query tiles of an item.
 //  * warp 0, one thread: TMA (cp.async.bulk.tensor, 128-byte swizzle) loads
-//    the two Q tiles once and streams 128-key K and V tiles through a 3-stage
-//    ring (4 stages).
+//    the two Q tiles once and streams 128-key K and V tiles through a ring
+//    of 4 stages (d = 64) or 3 (d = 128).
 //  * warp 1, one thread: issues tcgen05.mma (bf16 in, fp32 accumulate in
 //    tensor memory) for S_A = Q_A K^T and S_B = Q_B K^T (128 TMEM columns
 //    each) per K/V tile; warp 10, one thread: O_A += P_A V and O_B += P_B V,

@@ -277,25 +277,26 @@ int attn_decode_stream_step(const void* q, const void* k_new, const void* v_new,
 /*
  * attn_decode_step_noalloc -- attn_decode_step without a workspace argument.
  * The decode page has no counterpart: this entry point exists for callers
- * that cannot call cudaMalloc, for example code running while a CUDA graph is
- * being captured (allocation is not allowed there), real-time streaming loops
- * where the device-wide synchronisation of cudaMalloc would stall playback,
- * and plugin or embedded hosts that own all device memory and hand the
- * library none.  It allocates nothing: its split-KV scratch is a fixed
- * 16 MiB device array inside the library, which every GPU that loads the
- * library holds until the process exits.
+ * that cannot call cudaMalloc, for example plugin or embedded hosts that own
+ * all device memory and hand the library none, and real-time streaming loops
+ * where the device-wide synchronisation an allocation can imply would stall
+ * playback.  It allocates nothing: its split-KV scratch is a fixed 16 MiB
+ * device array inside the library, which every GPU that loads the library
+ * holds until the process exits.
  *
  * Arguments, supported sizes and results are those of attn_decode_step.
  * Sizes whose attn_decode_workspace_size() exceeds 16 MiB (16777216 bytes)
  * are rejected with ATTN_ERR_WORKSPACE (B=256, Hq=64, Hkv=8, D=128 needs about
  * 12.8 MB and fits).  The first call on a device looks up the array's device
- * address (cudaGetSymbolAddress) while that device is current; make that
- * first call before any stream capture.  Every call first clears the array's
- * status word and arrival counters with cudaMemsetAsync on `stream`.  All
- * calls share the one array, so calls that overlap on the GPU (other
- * streams, other host threads) race and give wrong results; serialise them.
- * The device status word is not readable for this variant: an out-of-range
- * position still gives NaN output rows.
+ * address (cudaGetSymbolAddress) while that device is current, and so does
+ * the first call after the device's context was replaced (cudaDeviceReset);
+ * make those calls before any stream capture.  The lookup is guarded by a
+ * mutex, so host threads may make their first calls at the same time.  Every
+ * call first clears the array's status word and arrival counters with
+ * cudaMemsetAsync on `stream`.  All calls share the one array, so calls that
+ * overlap on the GPU (other streams, other host threads) race and give wrong
+ * results; serialise them.  The device status word is not readable for this
+ * variant: an out-of-range position still gives NaN output rows.
  */
 int attn_decode_step_noalloc(const void* q, const int32_t* positions,
                              const void* k_cache, const void* v_cache,

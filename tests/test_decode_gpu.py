@@ -340,3 +340,20 @@ def test_short_caches_in_cluster_mode(g, L, positions):
         _check(case, want, out, f"L={L} g={g} fused={fused}")
         assert np.array_equal(bits(case.k_cache).cpu().numpy(), wk)
         assert np.array_equal(bits(case.v_cache).cpu().numpy(), wv)
+
+
+@pytest.mark.parametrize("B,Hq,positions", [(1, 16, [70000]), (3, 16, [100, 8000, 70000]),
+                                            (1, 128, [4000])])
+def test_max_len_of_a_million_rows(B, Hq, positions):
+    """max_len = 2^20 with short positions: the step reads rows 0..pos only
+    (every row past each position is NaN, so a read of any of them would show
+    in the output) and matches the oracle, on a cluster launch (B=1), on
+    stream-K (B=3) and on the tensor-core kernels (g = 16)."""
+    L = 1 << 20
+    case = synth.decode_case(B=B, Hq=Hq, Hkv=8, D=128, L=L, positions=positions, fill="all",
+                             poison=True, seed=77 + B + Hq, device="cuda")
+    want = _oracle_rows(case, range(B))
+    out = _run_step(case)
+    _check(case, want, out, f"L=2^20 B={B} Hq={Hq}")
+    del case
+    torch.cuda.empty_cache()

@@ -108,3 +108,32 @@ def test_multi_out_of_range_and_unsupported():
     with pytest.raises(ga.AttnError):
         ga.attn_decode_multi(torch.zeros(1, 3, 16, 128, dtype=torch.bfloat16, device="cuda"),
                              pos[:1], kc[:1], vc[:1], 0.088)
+
+
+@pytest.mark.parametrize("B,S,Hq,Hkv", [(1, 2, 16, 8), (1, 4, 16, 8), (12, 2, 8, 4),
+                                        (12, 2, 16, 2)])
+def test_multi_positions_near_int_max(B, S, Hq, Hkv):
+    """A first-token position so large that position + S - 1 overflows a
+    32-bit int must be rejected like any other out-of-range position: status
+    bit, NaN output rows, and no byte of the cache written (the row index
+    of such a token, taken in 64 bits, would lie far outside the cache).
+    Covers a cluster launch (B=1), stream-K (B=12) and the tensor-core
+    kernels (S x g = 16)."""
+    L = 1024
+    big = [2 ** 31 - 1, 2 ** 31 - 2, 2 ** 31 - S + 1]
+    positions = [(big[b % 3] if b % 2 == 0 else 100 + 37 * b) for b in range(B)]
+    q, kn, vn, pos, kc, vc = _case(B, S, Hq, Hkv, [min(p, L - S) for p in positions], 340 + B,
+                                   L=L)
+    pos.copy_(torch.tensor(positions, dtype=torch.int32, device="cuda"))
+    k_before, v_before = kc.clone(), vc.clone()
+    ws = ga.decode_workspace(B, S * Hq, Hkv, L, 128)
+    out = ga.attn_decode_multi(q, pos, kc, vc, 0.088, k_new=kn, v_new=vn, workspace=ws)
+    assert ga.attn_read_device_status(ws) & ga.ATTN_DEV_BAD_POSITION
+    for b, p in enumerate(positions):
+        if p >= L:
+            assert torch.isnan(out[b].float()).all(), f"b={b}"
+            assert torch.equal(bits(kc[b]), bits(k_before[b])), f"k b={b}"
+            assert torch.equal(bits(vc[b]), bits(v_before[b])), f"v b={b}"
+        else:
+            assert torch.isfinite(out[b].float()).all(), f"b={b}"
+            assert torch.equal(bits(kc[b, :, p:p + S].transpose(0, 1)), bits(kn[b])), f"b={b}"

@@ -301,6 +301,46 @@ def test_kv_append_writes_only_the_target_rows():
     assert np.all(kc == 7.0)  # inputs not modified
 
 
+def test_kv_append_hand_written_case():
+    """A 2-sequence, 2-head, 3-row, D=2 cache written out by hand: sequence 0
+    takes its new rows at position 2, sequence 1 at position 0; every other
+    entry keeps its value."""
+    kc = np.array([[[[1, 2], [3, 4], [5, 6]], [[7, 8], [9, 10], [11, 12]]],
+                   [[[13, 14], [15, 16], [17, 18]], [[19, 20], [21, 22], [23, 24]]]],
+                  dtype=np.float64)
+    vc = -kc
+    kn = np.array([[[101, 102], [103, 104]], [[105, 106], [107, 108]]], dtype=np.float64)
+    vn = -kn
+    k2, v2 = oracle.kv_append(kc, vc, kn, vn, [2, 0])
+    want_k = np.array([[[[1, 2], [3, 4], [101, 102]], [[7, 8], [9, 10], [103, 104]]],
+                       [[[105, 106], [15, 16], [17, 18]], [[107, 108], [21, 22], [23, 24]]]],
+                      dtype=np.float64)
+    assert np.array_equal(k2, want_k)
+    assert np.array_equal(v2, -want_k)
+
+
+def test_kv_append_matches_library_indexed_assignment():
+    """The same write as PyTorch's index_put_ with (sequence, head, position)
+    index tensors on the CPU, on bf16 bit patterns."""
+    g = torch.Generator().manual_seed(5)
+    B, Hkv, L, D = 4, 3, 11, 8
+    kc = torch.randn(B, Hkv, L, D, generator=g).to(torch.bfloat16)
+    vc = torch.randn(B, Hkv, L, D, generator=g).to(torch.bfloat16)
+    kn = torch.randn(B, Hkv, D, generator=g).to(torch.bfloat16)
+    vn = torch.randn(B, Hkv, D, generator=g).to(torch.bfloat16)
+    positions = torch.tensor([10, 0, 5, 5])
+    bi = torch.arange(B).repeat_interleave(Hkv)
+    hi = torch.arange(Hkv).repeat(B)
+    pi = positions.repeat_interleave(Hkv)
+    want_k = kc.clone().index_put_((bi, hi, pi), kn.reshape(B * Hkv, D))
+    want_v = vc.clone().index_put_((bi, hi, pi), vn.reshape(B * Hkv, D))
+    k2, v2 = oracle.kv_append(kc.view(torch.int16).numpy(), vc.view(torch.int16).numpy(),
+                              kn.view(torch.int16).numpy(), vn.view(torch.int16).numpy(),
+                              positions.tolist())
+    assert np.array_equal(k2, want_k.view(torch.int16).numpy())
+    assert np.array_equal(v2, want_v.view(torch.int16).numpy())
+
+
 def test_work_counts():
     """Algorithmic bytes/flops used by the roofline: hand-counted small cases."""
     # one sequence at position 3: 4 rows of K and V, 2 KV heads, D=2, bf16
