@@ -2,6 +2,8 @@
 // these have been validated by capi.cu.
 #pragma once
 
+#include <cuda.h>
+
 #include <cstddef>
 #include <cstdint>
 #include <cuda_runtime.h>
@@ -45,6 +47,14 @@ cudaError_t launch_decode_noalloc(const void* q, const int32_t* positions, const
 cudaError_t launch_prefill(const void* q, const void* k, const void* v, int S, int start_pos,
                            int Hq, int Hkv, int d, float scale, void* out,
                            cudaStream_t stream);
+// Prefill at head dim 64 with one query tile per work item, its keys split
+// between the CTA's two softmax warpgroups (prefill_split.cu); maps of
+// [tokens, heads, 64] bf16 with a 64 x 1 x 128 box.  scale_log2 = scale *
+// log2(e).
+cudaError_t launch_prefill_split(const CUtensorMap& mq, const CUtensorMap& mk,
+                                 const CUtensorMap& mv, int S, int start_pos, int Hq, int Hkv,
+                                 float scale_log2, void* out, int sms, cudaStream_t stream);
+cudaError_t prefill_split_read_timeouts(uint32_t* count);
 // Prefill waits that gave up since the last call (synchronises the stream).
 cudaError_t prefill_read_timeouts(uint32_t* count, cudaStream_t stream);
 

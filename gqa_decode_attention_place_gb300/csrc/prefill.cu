@@ -9,21 +9,23 @@
 // h reads KV head h/g.  out [S,Hq,d] bf16.
 //
 // How: work items are (pair of 128-token query tiles, query head) -- or a
-// single tile when pairs would leave SMs idle -- sorted longest first; a persistent grid (one CTA per SM) walks them in snake
+// single tile at HD = 128, where tensor memory holds one tile's O -- sorted
+// longest first; a persistent grid (one CTA per SM) walks them in snake
 // order (CTA c takes items c, 2G-1-c, 2G+c, ...) so the causal work per CTA
-// evens out.  Each K/V tile loaded serves both query tiles of an item.
+// evens out.  Each K/V tile loaded serves both query tiles of an item.  At
+// HD = 64, when pairs would leave SMs idle, the launch goes to
+// prefill_split.cu instead (one query tile per item, its keys split between
+// the two softmax warpgroups).
 //  * warp 0, one thread: TMA (cp.async.bulk.tensor, 128-byte swizzle) loads
-//    the two Q tiles once and streams 128-key K and V tiles through a ring
-//    of 4 stages (d = 64) or 3 (d = 128).
+//    the Q tile(s) once and streams 128-key K and V tiles through a ring of
+//    4 stages (d = 64) or 3 (d = 128).
 //  * warp 1, one thread: issues tcgen05.mma (bf16 in, fp32 accumulate in
 //    tensor memory) for S_A = Q_A K^T and S_B = Q_B K^T (128 TMEM columns
 //    each) per K/V tile; warp 10, one thread: O_A += P_A V and O_B += P_B V,
 //    with P read from tensor memory (64 columns of bf16 pairs per tile) and
 //    O kept in tensor memory for the whole key loop.  Two issuing threads
-//    took the 2048-token prefill from 28.9 to 24.9 us; for one-tile items
-//    at HD = 64 one thread issuing both streams measured faster (22.4 against
-//    23.5 us), so that launch keeps it.  While one query tile's softmax
-//    runs, the tensor core works on the other tile.
+//    took the 2048-token prefill from 28.9 to 24.9 us.  While one query
+//    tile's softmax runs, the tensor core works on the other tile.
 //  * warps 2-5 (tile A) and 6-9 (tile B), thread r owns query row r (TMEM
 //    lane quarter warp % 4): read the whole S row from TMEM into registers in
 //    one round trip, mask the causal diagonal, keep the online softmax in
@@ -112,7 +114,7 @@ __device__ __forceinline__ bool warp_wait_or_abort(uint32_t bar, uint32_t parity
   return __all_sync(0xffffffffu, wait_or_abort(bar, parity, abort_flag));
 }
 
-template <int HD, bool kSplit>
+template <int HD>
 __global__ void __launch_bounds__(kPThreads, 1)
     prefill_tcgen05_kernel(const __grid_constant__ CUtensorMap tm_q,
                            const __grid_constant__ CUtensorMap tm_k,
@@ -223,79 +225,6 @@ __global__ void __launch_bounds__(kPThreads, 1)
         if (!ok) break;
       }
     }
-  } else if (warp == 1 && !kSplit) {
-    // ------------------------------------ MMA issuer, both streams (S, O) --
-    if (lane == 0) {
-      constexpr uint32_t idesc_qk = make_idesc(kBM, kBN, false);
-      // O (+)= P V at N = HD: V's HD/64 column blocks, kChunkBytes apart
-      constexpr uint32_t idesc_pv = make_idesc(kBM, HD, true);
-      uint32_t gk = 0;             // K/V tiles consumed so far
-      uint32_t cs[kQT] = {0, 0};   // S_x issued so far
-      uint32_t cp[kQT] = {0, 0};   // P_x consumed (PV_x issued) so far
-      bool ok = true;
-      for (int r = 0; ok && item_of(r) < n_items; ++r) {
-        const Item it = item(item_of(r));
-        // O_x (+)= P_x V_j; gk0 is the item's first K/V tile in the ring order
-        auto issue_pv = [&](int x, int j, uint32_t gk0) -> bool {
-          if (j == 0 && r > 0 &&  // the previous item's epilogue has read O_x
-              !wait_or_abort(bar(kBarOFree + x), (uint32_t)(r - 1) & 1u, abort_flag))
-            return false;
-          if (!wait_or_abort(bar(kBarPFull + x), cp[x] & 1u, abort_flag)) return false;
-          tc_fence_after();
-          const uint32_t sV =
-              base + L::kOffKV + ((gk0 + j) % kKVStages) * 2 * kTileBytes + kTileBytes;
-#pragma unroll
-          for (int k = 0; k < kBN / 16; ++k)
-            tc_mma_ts(tmem + kTmemO + HD * x, tmem + kTmemP + 64 * x + 8 * k,
-                      sw128_desc(sV + k * 16 * 128, HD > 64 ? kChunkBytes : 16), idesc_pv,
-                      (j > 0 || k > 0) ? 1u : 0u);
-          tc_commit(bar(kBarPVDone + x));
-          ++cp[x];
-          return true;
-        };
-        if (!wait_or_abort(bar(kBarQ), (uint32_t)r & 1u, abort_flag)) { ok = false; break; }
-        const uint32_t gk0 = gk;
-        for (int i = 0; ok && i < it.n; ++i) {
-          const uint32_t g = gk0 + i;
-          const int s = g % kKVStages;
-          if (!wait_or_abort(bar(kBarKVFull + s), (g / kKVStages) & 1u, abort_flag)) {
-            ok = false;
-            break;
-          }
-          const uint32_t sK = base + L::kOffKV + s * 2 * kTileBytes;
-          for (int x = 0; ok && x < kQT; ++x) {
-            if (i >= it.nt[x]) continue;
-            // the softmax has read the previous S_x
-            if (cs[x] > 0 &&
-                !wait_or_abort(bar(kBarSFree + x), (cs[x] - 1) & 1u, abort_flag)) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
-#pragma unroll
-            for (int k = 0; k < HD / 16; ++k) {  // 4 K-steps per 128-byte column block
-              const uint32_t off = (k >> 2) * kChunkBytes + (k & 3) * 32;
-              tc_mma(tmem + 128 * x, sw128_desc(sQ + x * kTileBytes + off), sw128_desc(sK + off),
-                     idesc_qk, k > 0);
-            }
-            tc_commit(bar(kBarSFull + x));
-            ++cs[x];
-          }
-          if (!ok) break;
-          if (i + 1 == it.n) tc_commit(bar(kBarQFree));  // last QK^T of this item
-          if (i > 0) {
-            for (int x = 0; ok && x < kQT; ++x)
-              if (i - 1 < it.nt[x]) ok = issue_pv(x, i - 1, gk0);
-            tc_commit(bar(kBarKVEmpty + (g - 1) % kKVStages));  // tile i-1 released
-          }
-        }
-        if (!ok) break;
-        for (int x = 0; ok && x < kQT; ++x)
-          if (it.n - 1 < it.nt[x]) ok = issue_pv(x, it.n - 1, gk0);
-        tc_commit(bar(kBarKVEmpty + (gk0 + it.n - 1) % kKVStages));  // last tile released
-        gk = gk0 + it.n;
-      }
-    }
   } else if (warp == 1) {
     // ----------------------------------------------- QK^T issuer (S_x) --
     if (lane == 0) {
@@ -340,12 +269,11 @@ __global__ void __launch_bounds__(kPThreads, 1)
     }
   } else if (warp == kPVWarp) {
     // ------------------------------------------------ PV issuer (O_x) --
-    // Its own thread (kSplit), so that the two streams of MMAs are issued
-    // in parallel.  P_x of tile j is written after S_x of tile j was read,
-    // so the QK^T that read the stage's K is done once P_x is; the commit
-    // after the tile's last PV therefore releases the whole stage.  Without
-    // kSplit the combined issuer does this and the warp idles.
-    if (kSplit && lane == 0) {
+    // Its own thread, so that the two streams of MMAs are issued in
+    // parallel.  P_x of tile j is written after S_x of tile j was read, so
+    // the QK^T that read the stage's K is done once P_x is; the commit after
+    // the tile's last PV therefore releases the whole stage.
+    if (lane == 0) {
       // O (+)= P V at N = HD: V's HD/64 column blocks, kChunkBytes apart
       constexpr uint32_t idesc_pv = make_idesc(kBM, HD, true);
       uint32_t gk = 0;             // K/V tiles consumed so far
@@ -578,12 +506,9 @@ cudaError_t launch_prefill_hd(const CUtensorMap& mq, const CUtensorMap& mk, cons
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev >= 0 && dev < 64 && !configured[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(prefill_tcgen05_kernel<HD, true>,
+    cudaError_t e = cudaFuncSetAttribute(prefill_tcgen05_kernel<HD>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          L::kSmemBytes);
-    if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(prefill_tcgen05_kernel<HD, false>,
-                               cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmemBytes);
     if (e != cudaSuccess) return e;
     configured[dev] = true;
   }
@@ -591,20 +516,20 @@ cudaError_t launch_prefill_hd(const CUtensorMap& mq, const CUtensorMap& mk, cons
   if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
     sms = 148;
   // Two query tiles per item share each K/V tile and keep both softmax
-  // warpgroups busy; when that leaves SMs idle, or tensor memory holds only
-  // one tile's O (HD = 128), one tile per item instead.
+  // warpgroups busy.  When that leaves SMs idle at HD = 64, one tile per
+  // item with its keys split between the two softmax warpgroups
+  // (prefill_split.cu); at HD = 128, where tensor memory holds one tile's O,
+  // one tile per item here.
   const long long n_qt = (p.S + kBM - 1) / kBM;
-  p.tpi = (L::kQTiles == 1 || (n_qt + 1) / 2 * (long long)p.Hq < sms) ? 1 : kQT;
+  if (HD == 64 && (n_qt + 1) / 2 * (long long)p.Hq < sms)
+    return launch_prefill_split(mq, mk, mv, p.S, p.start_pos, p.Hq, p.Hkv, p.scale_log2, p.out,
+                                sms, stream);
+  p.tpi = L::kQTiles == 1 ? 1 : kQT;
   p.n_units = (int)((n_qt + p.tpi - 1) / p.tpi);
   const long long items = (long long)p.n_units * p.Hq;
   if (items > 0x7fffffffLL) return cudaErrorInvalidValue;
   const unsigned blocks = (unsigned)std::min<long long>(items, sms);  // one CTA per SM
-  // QK^T and PV issued from two threads, except for one-tile items at
-  // HD = 64, where one thread issuing both measured faster
-  if (HD == 64 && p.tpi == 1)
-    prefill_tcgen05_kernel<HD, false><<<blocks, kPThreads, L::kSmemBytes, stream>>>(mq, mk, mv, p);
-  else
-    prefill_tcgen05_kernel<HD, true><<<blocks, kPThreads, L::kSmemBytes, stream>>>(mq, mk, mv, p);
+  prefill_tcgen05_kernel<HD><<<blocks, kPThreads, L::kSmemBytes, stream>>>(mq, mk, mv, p);
   return cudaGetLastError();
 }
 
@@ -614,13 +539,14 @@ cudaError_t launch_prefill_hd(const CUtensorMap& mq, const CUtensorMap& mk, cons
 // early, so some output rows were not written); clears the count.
 cudaError_t prefill_read_timeouts(uint32_t* count, cudaStream_t stream) {
   cudaError_t e = cudaStreamSynchronize(stream);
-  unsigned v = 0;
+  unsigned v = 0, v_split = 0;
   if (e == cudaSuccess) e = cudaMemcpyFromSymbol(&v, g_prefill_timeouts, sizeof(v));
   if (e == cudaSuccess && v != 0) {
     const unsigned zero = 0;
     e = cudaMemcpyToSymbol(g_prefill_timeouts, &zero, sizeof(zero));
   }
-  *count = v;
+  if (e == cudaSuccess) e = prefill_split_read_timeouts(&v_split);
+  *count = v + v_split;
   return e;
 }
 

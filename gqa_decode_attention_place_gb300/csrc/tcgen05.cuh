@@ -59,6 +59,54 @@ __device__ __forceinline__ void tc_mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint
       : "memory");
 }
 
+// The issuing lane of a converged warp (elect.sync): non-zero in exactly one
+// lane.  The whole warp runs a warp-uniform issue loop (descriptors and
+// waits are warp-uniform values) and only that lane issues the
+// single-thread instructions (tcgen05.mma, tcgen05.commit).  Measured on
+// this part: an M=128, N=64 MMA with A in tensor memory issues at 32 cycles
+// (its tensor-core time) this way, against 46-49 cycles from a loop that
+// one thread runs alone in a divergent branch.
+__device__ __forceinline__ uint32_t elect_one() {
+  uint32_t pred = 0;
+  asm volatile(
+      "{\n\t.reg .pred P;\n\t"
+      "elect.sync _|P, 0xffffffff;\n\t"
+      "selp.u32 %0, 1, 0, P;\n\t}"
+      : "=r"(pred));
+  return pred;
+}
+
+// tc_mma, tc_mma_ts and tc_commit issued by the lane whose `leader` is
+// non-zero only.
+__device__ __forceinline__ void tc_mma_by(uint32_t leader, uint32_t d_tmem, uint64_t adesc,
+                                          uint64_t bdesc, uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "setp.ne.b32 q, %5, 0;\n\t"
+      "@q tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate), "r"(leader)
+      : "memory");
+}
+__device__ __forceinline__ void tc_mma_ts_by(uint32_t leader, uint32_t d_tmem, uint32_t a_tmem,
+                                             uint64_t bdesc, uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "setp.ne.b32 q, %5, 0;\n\t"
+      "@q tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate), "r"(leader)
+      : "memory");
+}
+__device__ __forceinline__ void tc_commit_by(uint32_t leader, uint32_t bar) {
+  asm volatile(
+      "{\n\t.reg .pred q;\n\t"
+      "setp.ne.b32 q, %1, 0;\n\t"
+      "@q tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(
+          bar), "r"(leader)
+      : "memory");
+}
+
 // 32 consecutive TMEM columns of this warp's 32 lanes -> 32 registers per thread.
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
   uint32_t r[32];

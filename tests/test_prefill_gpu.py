@@ -96,6 +96,31 @@ def test_prefill_matches_decode_path():
     assert_attn_close(f64(out), want, "S=1 prefill")
 
 
+def test_pair_items_with_a_ragged_last_tile():
+    """Enough heads that work items hold two query tiles (each K/V tile
+    serves both softmax lanes): 300 tokens are three query tiles, so the
+    second item of each head has one tile and its second lane no work; GQA
+    g=4 over a prefix that is not tile aligned."""
+    case = synth.prefill_case(S=300, start_pos=37, Hq=160, Hkv=40, d=64, seed=91, device="cuda")
+    rng = np.random.default_rng(91)
+    rows = [(int(i), int(h)) for i, h in zip(rng.integers(0, 300, 700), rng.integers(0, 160, 700))]
+    rows += [(i, 7) for i in range(300)] + [(i, 159) for i in range(0, 300, 7)]
+    rows += [(0, h) for h in range(160)] + [(299, h) for h in range(160)]
+    _sampled_check(case, rows, "pair items, ragged last tile")
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("sign", [0.0, -1.0])
+def test_zero_and_negative_scale(d, sign):
+    """A zero scale weighs every visible key alike; a negative one (the
+    usual 1/sqrt(d), sign flipped) reverses the order of the scores, so the
+    row's largest scaled score is the smallest raw one."""
+    scale = sign / d ** 0.5
+    case = synth.prefill_case(S=260, start_pos=70, Hq=4, Hkv=2, d=d, seed=93 + d, device="cuda",
+                              scale=scale)
+    _full_check(case, f"d={d} scale={scale}")
+
+
 # ------------------------------------------------------------- d_head = 128 ---
 # The decode model's head size: prompt chunks of a GQA model with D=128 go
 # through the same kernel, each 128-wide row as two 128-byte column blocks.
