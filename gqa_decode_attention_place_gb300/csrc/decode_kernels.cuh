@@ -242,6 +242,7 @@ __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
 __device__ __forceinline__ void prefetch_l2(const void* p) {
   asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
 }
+
 __device__ __forceinline__ uint4 lds128(const uint8_t* p) {
   return *reinterpret_cast<const uint4*>(p);
 }
@@ -354,6 +355,30 @@ struct Consumer {
       for (int r = 0; r < 4; ++r) {
         const float lo = rope1(bf16lo(xw[r]), bf16lo(yw[r]), cc[2 * r], ss[2 * r], first);
         const float hi = rope1(bf16hi(xw[r]), bf16hi(yw[r]), cc[2 * r + 1], ss[2 * r + 1], first);
+        const uint32_t w = pack_bf16x2(lo, hi);
+        qb[j][r] = !on ? 0u : g < G ? w : pack_bf16x2(lo - bf16lo(w), hi - bf16hi(w));
+      }
+    }
+  }
+  // The same operand from q already rotated (fp32 rows [G][kD], one per
+  // head, in shared memory): column h < G gets the bf16 rounding of head h,
+  // column G+h the rounding of what is left.  Bit-identical to load_q_rope.
+  __device__ __forceinline__ void load_q_rotated(const float* rot, float qscale) {
+    qs = qscale;
+    const bool on = g < 2 * G;
+    const float* qh = rot + (size_t)(g < G ? g : g - G) * kD;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int d0 = (j >> 1) * 64 + ((j & 1) * 4 + t) * 8;
+      float4 a = make_float4(0.f, 0.f, 0.f, 0.f), b = a;
+      if (on) {
+        a = *reinterpret_cast<const float4*>(qh + d0);
+        b = *reinterpret_cast<const float4*>(qh + d0 + 4);
+      }
+      const float v[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        const float lo = v[2 * r], hi = v[2 * r + 1];
         const uint32_t w = pack_bf16x2(lo, hi);
         qb[j][r] = !on ? 0u : g < G ? w : pack_bf16x2(lo - bf16lo(w), hi - bf16hi(w));
       }
@@ -627,6 +652,84 @@ __device__ __forceinline__ void fresh_row(const Params& p, uint8_t* Ks, int rows
 template <bool R>
 __device__ __forceinline__ const float* rope_row(const Params& p, const float* t, int b, int pos) {
   return R ? t + (size_t)(p.rope_by_pos ? pos : b) * kD : nullptr;
+}
+
+// 1-D bulk copy global -> shared (the TMA engine; both addresses 16-byte
+// aligned, size a multiple of 16), completing on mbarrier `bar`.
+__device__ __forceinline__ void bulk_copy(void* dst, const void* src, uint32_t bytes,
+                                          uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
+// Shared memory of the rotary embedding in cluster mode: the inputs staged
+// by bulk copies (G query rows, the new key row, the cos row, the sin row),
+// then q rotated to fp32 rows [G][kD], then the new key rotated to bf16.
+template <int G>
+struct RopeStage {
+  static constexpr int kIn = (G + 1) * kRowBytes + 2 * kD * 4;
+  static constexpr int kRotQ = kIn;
+  static constexpr int kRotK = kRotQ + G * kD * 4;
+  static constexpr int kBytes = kRotK + kRowBytes;
+};
+
+// Copy the rotation's inputs into shared memory (one thread; bulk copies on
+// the TMA engine, like the tiles: plain loads issued beside a tile's copy
+// were measured to hold that copy back by about 1400 cycles).
+template <int G>
+__device__ __forceinline__ void stage_rope_inputs(uint8_t* area, const Params& p, int b, int kvh,
+                                                  const float* rc, const float* rs, uint32_t bar) {
+  mbar_arrive_expect_tx(bar, RopeStage<G>::kIn);
+  bulk_copy(area, p.q + ((size_t)b * p.Hq + (size_t)kvh * G) * kD, G * kRowBytes, bar);
+  bulk_copy(area + G * kRowBytes, p.k_new + ((size_t)b * p.Hkv + kvh) * kRowBytes, kRowBytes, bar);
+  bulk_copy(area + (G + 1) * kRowBytes, rc, kD * 4, bar);
+  bulk_copy(area + (G + 1) * kRowBytes + kD * 4, rs, kD * 4, bar);
+}
+
+// The producer warp's share of the rotary embedding, from the staged inputs:
+// the G query rows rotated to fp32 (for the consumers' MMA operands) and the
+// new key row rotated and rounded to bf16 (for the CTA whose part ends the
+// segment).  Lane l takes dims 8(l%16)..+7 of rows l/16, l/16 + 2, ... (row
+// G is the key); the partner dims are 64 away.  The same rounding, one IEEE
+// operation at a time, as every other rotation here.
+template <int G>
+__device__ __forceinline__ void rotate_rows(uint8_t* area, int lane) {
+  const int d0 = 8 * (lane & 15);
+  const bool first = d0 < kD / 2;
+  const float* rc = reinterpret_cast<const float*>(area + (G + 1) * kRowBytes);
+  const float* rs = rc + kD;
+  float* rot = reinterpret_cast<float*>(area + RopeStage<G>::kRotQ);
+  uint8_t* rotk = area + RopeStage<G>::kRotK;
+  const float4 c0 = *reinterpret_cast<const float4*>(rc + d0);
+  const float4 c1 = *reinterpret_cast<const float4*>(rc + d0 + 4);
+  const float4 s0 = *reinterpret_cast<const float4*>(rs + d0);
+  const float4 s1 = *reinterpret_cast<const float4*>(rs + d0 + 4);
+  const float cc[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+  const float ss[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
+  for (int r = lane >> 4; r <= G; r += 2) {
+    const uint16_t* src = reinterpret_cast<const uint16_t*>(area + r * kRowBytes);
+    const uint4 xv = *reinterpret_cast<const uint4*>(src + d0);
+    const uint4 yv = *reinterpret_cast<const uint4*>(src + (d0 ^ 64));
+    const uint32_t xs[4] = {xv.x, xv.y, xv.z, xv.w}, ys[4] = {yv.x, yv.y, yv.z, yv.w};
+    float v[8];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      v[2 * i] = rope1(bf16lo(xs[i]), bf16lo(ys[i]), cc[2 * i], ss[2 * i], first);
+      v[2 * i + 1] = rope1(bf16hi(xs[i]), bf16hi(ys[i]), cc[2 * i + 1], ss[2 * i + 1], first);
+    }
+    if (r < G) {
+      float4* dst = reinterpret_cast<float4*>(rot + r * kD + d0);
+      dst[0] = make_float4(v[0], v[1], v[2], v[3]);
+      dst[1] = make_float4(v[4], v[5], v[6], v[7]);
+    } else {
+      *reinterpret_cast<uint4*>(rotk + 2 * d0) =
+          make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]), pack_bf16x2(v[4], v[5]),
+                     pack_bf16x2(v[6], v[7]));
+    }
+  }
 }
 
 // The position advance of a streaming step (p.advance non-null): called by
@@ -971,7 +1074,8 @@ size_t cluster_smem_bytes() {
   return (size_t)kStages * 2 * kTileBytes + (2 * kStages + 2) * sizeof(uint64_t) +
          kMiscInts * sizeof(int) + (size_t)NW * G * 2 * sizeof(float) +
          (size_t)NW * G * kD * sizeof(float) + 2 * kD * sizeof(float) +
-         (size_t)Cfg<G>::kMaxC * G * (kD + 2) * sizeof(float);
+         (size_t)Cfg<G>::kMaxC * G * (kD + 2) * sizeof(float) +
+         (Cfg<G>::kRope ? (size_t)RopeStage<G>::kBytes : 0) + 2 * sizeof(uint64_t);
 }
 
 // Grid = B*Hkv clusters of C CTAs; cluster s handles segment s (sequence
@@ -994,6 +1098,14 @@ __global__ void __maxnreg__(Cfg<G>::kMaxRegs)
   float* rope_cs = merge_o + NW * G * kD;                         // [2][kD] staged cos, sin
   float* land_o = rope_cs + 2 * kD;                  // [kMaxC][G][kD]: rank r's partial o
   float* land_ml = land_o + Cfg<G>::kMaxC * G * kD;  // [kMaxC][G][2]: its (max, sum)
+  // rotation (RopeStage): staged inputs, q and the new key rotated, and two
+  // mbarriers: the staging copies landed; the producer warp wrote the rotations
+  uint8_t* q_stage = reinterpret_cast<uint8_t*>(land_ml + Cfg<G>::kMaxC * G * 2);
+  const float* rot_q = reinterpret_cast<const float*>(q_stage + RopeStage<G>::kRotQ);
+  const uint8_t* rot_k = q_stage + RopeStage<G>::kRotK;
+  uint64_t* stage_bar = reinterpret_cast<uint64_t*>(
+      q_stage + (Cfg<G>::kRope ? RopeStage<G>::kBytes : 0));
+  uint64_t* q_stage_bar = stage_bar + 1;
 
   cg::cluster_group cluster = cg::this_cluster();
   const int C = (int)cluster.num_blocks();
@@ -1014,6 +1126,8 @@ __global__ void __maxnreg__(Cfg<G>::kMaxRegs)
       mbar_init(smem_u32(&bars[kStages + s]), NW);
     }
     mbar_init(smem_u32(&bars[2 * kStages]), NW);
+    mbar_init(smem_u32(stage_bar), 1);
+    mbar_init(smem_u32(q_stage_bar), 1);
     misc[0] = 0;
     fence_mbar_init();
   }
@@ -1038,26 +1152,28 @@ __global__ void __maxnreg__(Cfg<G>::kMaxRegs)
   grid_dependents_launch();
   // Rank r's first tile is tile r whatever the position (rows from 0 without
   // a local window), so its copy goes out before the position is read, and
-  // so does q: loaded, or rotated when the rotation rows are per sequence.
-  // If the position leaves rank r without tiles, the copy only has to land
+  // so does q, loaded; with the rotary embedding and per-sequence rotation
+  // rows the rotation's inputs are copied in just before it, and the producer
+  // warp rotates q and the new key once it has issued the next tile.  If the
+  // position leaves rank r without tiles, the copies only have to land
   // before the CTA exits.
   const bool early = !(M & kModeWindow) && rank * kTile < p.L;
+  // the rotation's inputs (a few KB) go ahead of the tile, so that they land,
+  // and are rotated, while the tile is still in flight
+  if (R && !p.rope_by_pos && producer)  // rotation rows known before the position
+    stage_rope_inputs<G>(q_stage, p, b, kvh, rope_row<R>(p, p.rope_cos, b, 0),
+                         rope_row<R>(p, p.rope_sin, b, 0), smem_u32(stage_bar));
   if (early && producer) produce_tile(&tm_k, &tm_v, p, stages, bars, 0, b, kvh, rank, 0);
   // the position's load goes out first; its value is used after the q setup
   const int pos0 = p.positions[b];
-  const uint16_t* qb = p.q + ((size_t)b * p.Hq + (size_t)kvh * G) * kD;
   Consumer<G> cs;
   if (warp < NW) {
     cs.init(lane);
-    if (!R) {
-      cs.template load_q<MT>(p, b, kvh, p.qscale);
-    } else if (!p.rope_by_pos) {
-      cs.load_q_rope(qb, rope_row<R>(p, p.rope_cos, b, 0), rope_row<R>(p, p.rope_sin, b, 0),
-                     p.qscale);
-    }
+    if (!R) cs.template load_q<MT>(p, b, kvh, p.qscale);
   }
   if (!rows_in_cache(pos0, shift, p.L)) {
     // the same for every CTA of the cluster: all leave, no cluster barrier
+    if (R && !p.rope_by_pos && producer) mbar_wait(smem_u32(stage_bar), 0u, abort_flag);
     if (early && producer) mbar_wait(smem_u32(&bars[0]), 0u, abort_flag);
     if (rank == 0 && kvh == 0 && tid == 0) {
       set_status(p.status, ATTN_DEV_BAD_POSITION);
@@ -1080,13 +1196,33 @@ __global__ void __maxnreg__(Cfg<G>::kMaxRegs)
 
   if (warp == NW) {
     // ------------------------------------------------------------ producer --
+    // the tiles of the first round (free stages, no wait), then the rotation,
+    // then the rest
     if (lane == 0) {
+      if (R && p.rope_by_pos)  // the rotation rows are the position's
+        stage_rope_inputs<G>(q_stage, p, b, kvh, rope_row<R>(p, p.rope_cos, b, pos),
+                             rope_row<R>(p, p.rope_sin, b, pos), smem_u32(stage_bar));
       int i = 0;
-      for (int k = rank; k < ntiles; k += C, ++i) {
-        if (i == 0 && early) continue;  // issued above
+      for (int k = rank; k < ntiles && i < kStages; k += C, ++i)
+        if (i > 0 || !early) produce_tile(&tm_k, &tm_v, p, stages, bars, i, b, kvh, k, lo);
+    }
+    __syncwarp();
+    if (R) {
+      if (__all_sync(0xffffffffu, mbar_wait(smem_u32(stage_bar), 0u, abort_flag))) {
+        rotate_rows<G>(q_stage, lane);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(q_stage_bar));  // the consumers may read them
+      } else if (lane == 0) {
+        *abort_flag = 1;
+        set_status(p.status, ATTN_DEV_TIMEOUT);
+      }
+    }
+    if (lane == 0) {
+      int i = kStages;
+      for (int k = rank + kStages * C; k < ntiles; k += C, ++i) {
         const int s = i % kStages;
         const uint32_t u = (uint32_t)(i / kStages);
-        if (i >= kStages && !mbar_wait(smem_u32(&bars[kStages + s]), (u & 1u) ^ 1u, abort_flag)) {
+        if (!mbar_wait(smem_u32(&bars[kStages + s]), (u & 1u) ^ 1u, abort_flag)) {
           *abort_flag = 1;
           set_status(p.status, ATTN_DEV_TIMEOUT);
           break;
@@ -1100,18 +1236,12 @@ __global__ void __maxnreg__(Cfg<G>::kMaxRegs)
   } else {
     // ----------------------------------------------------------- consumers --
     ConsumerSync csync{smem_u32(&bars[2 * kStages]), abort_flag, p.status, 0u};
-    if (R && p.rope_by_pos)  // the rotation row is the position's
-      cs.load_q_rope(qb, rope_row<R>(p, p.rope_cos, b, pos), rope_row<R>(p, p.rope_sin, b, pos),
-                     p.qscale);
     if (MT) cs.set_last(pos - shift, p.S);
     // fused append: the warp whose keys include the last row of the last
     // tile, in the rank that takes that tile, writes the new rows
     const bool own_fresh = p.k_new != nullptr && (ntiles - 1) % C == rank &&
                            warp == (n - 1 - (ntiles - 1) * kTile) / KPW;
     const uint4 fk = own_fresh ? load_fresh(p, b, kvh, lane) : make_uint4(0u, 0u, 0u, 0u);
-    if (R && own_fresh)
-      stage_fresh_rope(rope_cs, rope_row<R>(p, p.rope_cos, b, pos),
-                       rope_row<R>(p, p.rope_sin, b, pos), lane);
     cs.reset();
     int i = 0;
     for (int k = rank; k < ntiles; k += C, ++i) {
@@ -1119,10 +1249,16 @@ __global__ void __maxnreg__(Cfg<G>::kMaxRegs)
       if (!consumer_wait(smem_u32(&bars[s]), (uint32_t)(i / kStages) & 1u, abort_flag, p.status,
                          lane))
         break;
+      if (R && i == 0) {  // the operand from the producer warp's rotated q
+        if (!consumer_wait(smem_u32(q_stage_bar), 0u, abort_flag, p.status, lane)) break;
+        cs.load_q_rotated(rot_q, p.qscale);
+      }
       const int rows = min(kTile, n - k * kTile);
       uint8_t* Ks = stages + (size_t)s * 2 * kTileBytes;
-      if (own_fresh && k == ntiles - 1)
-        fresh_row<R>(p, Ks, rows, b, kvh, pos, rope_cs, fk, lane);
+      if (own_fresh && k == ntiles - 1)  // with the rotation: the key rotated by the producer
+        fresh_row<false>(p, Ks, rows, b, kvh, pos, rope_cs,
+                         (R && lane < 16) ? reinterpret_cast<const uint4*>(rot_k)[lane] : fk,
+                         lane);
       cs.template tile<MT, R>(Ks, Ks + kTileBytes, rows, lo + k * kTile, warp);
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&bars[kStages + s]));  // the stage may be refilled
