@@ -5,6 +5,10 @@ their dtype, shape, contiguity and device, and passes raw device pointers and
 the current CUDA stream to the C entry point of the same name.  All compute
 runs in the library's CUDA kernels; there is no fallback path, and a missing
 or unloadable library raises immediately.
+
+With ``GQA_ATTN_DEBUG=1`` in the environment the range-checked build
+(``lib/libgqa_attn_debug.so``, compiled with ``-DGQA_DEBUG``) is loaded
+instead; ``attn_debug_build()`` says which one is in use.
 """
 
 from __future__ import annotations
@@ -24,13 +28,20 @@ __all__ = [
     "attn_read_prefill_status", "attn_last_cuda_error", "decode_workspace", "attn_decode_step_noalloc",
     "attn_decode_step_append", "attn_decode_step_rope_append", "attn_decode_stream_step",
     "attn_decode_step_window", "attn_decode_multi", "attn_test_skip_tile",
+    "attn_debug_build", "attn_read_prefill_skips", "debug_collect_range_bits",
 ]
 
 ATTN_OK = 0
 ATTN_DEV_BAD_POSITION = 0x1
 ATTN_DEV_TIMEOUT = 0x2
+ATTN_DEV_RANGE = 0x4
 
 _LIB: Optional[ctypes.CDLL] = None
+# Range-checked builds only: every workspace handed out by decode_workspace()
+# (kept alive until debug_collect_range_bits() reads it), and any
+# ATTN_DEV_RANGE bit a caller's own attn_read_device_status() saw.
+_DEBUG_WORKSPACES: list = []
+_DEBUG_RANGE_SEEN = 0
 
 
 class AttnError(RuntimeError):
@@ -42,20 +53,27 @@ class AttnError(RuntimeError):
         super().__init__(msg)
 
 
+def _debug_requested() -> bool:
+    return os.environ.get("GQA_ATTN_DEBUG", "0") not in ("", "0")
+
+
 def library_path() -> str:
-    return _build.LIBPATH
+    return _build.lib_path(_debug_requested())
 
 
 def load_library(build_if_missing: bool = True) -> ctypes.CDLL:
-    """Load libgqa_attn.so (building it in-tree first if allowed and needed)."""
+    """Load libgqa_attn.so, or libgqa_attn_debug.so under GQA_ATTN_DEBUG=1
+    (building it in-tree first if allowed and needed)."""
     global _LIB
     if _LIB is not None:
         return _LIB
-    if not os.path.exists(_build.LIBPATH) or (build_if_missing and not _build.up_to_date()):
+    debug = _debug_requested()
+    path = _build.lib_path(debug)
+    if not os.path.exists(path) or (build_if_missing and not _build.up_to_date(debug)):
         if not build_if_missing:
-            raise RuntimeError(f"{_build.LIBPATH} is missing; run __graft_entry__.build()")
-        _build.build()
-    lib = ctypes.CDLL(_build.LIBPATH)
+            raise RuntimeError(f"{path} is missing; run __graft_entry__.build()")
+        _build.build(debug=debug)
+    lib = ctypes.CDLL(path)
     vp, i32, sz, f32 = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t, ctypes.c_float
     lib.attn_kv_append.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, vp]
     lib.attn_kv_append.restype = i32
@@ -92,6 +110,10 @@ def load_library(build_if_missing: bool = True) -> ctypes.CDLL:
     lib.attn_status_string.restype = ctypes.c_char_p
     lib.attn_last_cuda_error.argtypes = []
     lib.attn_last_cuda_error.restype = i32
+    lib.attn_debug_build.argtypes = []
+    lib.attn_debug_build.restype = i32
+    lib.attn_read_prefill_skips.argtypes = [ctypes.POINTER(ctypes.c_uint32), vp]
+    lib.attn_read_prefill_skips.restype = i32
     _LIB = lib
     return lib
 
@@ -157,7 +179,29 @@ def decode_workspace(B: int, Hq: int, Hkv: int, L: int, D: int, device=None) -> 
     n = attn_decode_workspace_size(B, Hq, Hkv, L, D)
     if n == 0:
         raise AttnError(2, "attn_decode_workspace_size")
-    return torch.zeros(n, dtype=torch.uint8, device=device or "cuda")
+    ws = torch.zeros(n, dtype=torch.uint8, device=device or "cuda")
+    if attn_debug_build():
+        _DEBUG_WORKSPACES.append(ws)
+    return ws
+
+
+def debug_collect_range_bits() -> int:
+    """Range-checked builds: synchronise, then return ATTN_DEV_RANGE if any
+    decode launch since the last call skipped an access (read from every
+    workspace decode_workspace() handed out, and from the status reads callers
+    made themselves) or if a prefill launch did; clears all of it.  Always 0
+    in release builds."""
+    global _DEBUG_RANGE_SEEN
+    if not attn_debug_build():
+        return 0
+    bits = _DEBUG_RANGE_SEEN
+    for ws in _DEBUG_WORKSPACES:
+        bits |= attn_read_device_status(ws)
+    _DEBUG_WORKSPACES.clear()
+    _DEBUG_RANGE_SEEN = 0
+    if attn_read_prefill_skips():
+        bits |= ATTN_DEV_RANGE
+    return bits & ATTN_DEV_RANGE
 
 
 def attn_decode_step(q, positions, k_cache, v_cache, scale: float, out=None, workspace=None,
@@ -402,11 +446,28 @@ def attn_read_prefill_status(stream=None) -> int:
     return int(n.value)
 
 
+def attn_debug_build() -> bool:
+    """True if the loaded library has the device range checks."""
+    return bool(load_library().attn_debug_build())
+
+
+def attn_read_prefill_skips(stream=None) -> int:
+    """Synchronise, read and clear the count of prefill accesses that failed
+    a range check (range-checked builds; always 0 otherwise)."""
+    n = ctypes.c_uint32(0)
+    code = load_library().attn_read_prefill_skips(ctypes.byref(n), _stream(stream))
+    if code not in (0, 5):
+        raise AttnError(code, "attn_read_prefill_skips")
+    return int(n.value)
+
+
 def attn_read_device_status(workspace, stream=None) -> int:
     """Synchronise, read and clear the decode workspace's device status bits."""
+    global _DEBUG_RANGE_SEEN
     bits = ctypes.c_uint32(0)
     code = load_library().attn_read_device_status(workspace.data_ptr(), ctypes.byref(bits),
                                                   _stream(stream))
     if code not in (0, 5):
         raise AttnError(code, "attn_read_device_status")
+    _DEBUG_RANGE_SEEN |= int(bits.value) & ATTN_DEV_RANGE
     return int(bits.value)

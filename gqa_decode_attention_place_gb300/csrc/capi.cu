@@ -202,6 +202,22 @@ int attn_read_prefill_status(uint32_t* timeouts, cudaStream_t stream) {
   return n ? ATTN_ERR_DEVICE : ATTN_OK;
 }
 
+int attn_read_prefill_skips(uint32_t* skips, cudaStream_t stream) {
+  uint32_t n = 0;
+  const cudaError_t e = gqa::prefill_read_skips(&n, stream);
+  if (e != cudaSuccess) return cuda_status(e);
+  if (skips) *skips = n;
+  return n ? ATTN_ERR_DEVICE : ATTN_OK;
+}
+
+int attn_debug_build(void) {
+#ifdef GQA_DEBUG
+  return 1;
+#else
+  return 0;
+#endif
+}
+
 int attn_read_device_status(void* workspace, uint32_t* bits, cudaStream_t stream) {
   if (!workspace) return ATTN_ERR_INVALID_ARG;
   uint32_t word = 0;

@@ -154,6 +154,27 @@ __device__ __forceinline__ void set_status(uint32_t* status, uint32_t bits) {
   if (status) atomicOr(status, bits);
 }
 
+// Debug builds (-DGQA_DEBUG) check the kernels' index-derived accesses:
+// tile coordinates of the bulk copies, landing and partial slots, output and
+// cache rows.  A failed check sets ATTN_DEV_RANGE in *status (decode) or
+// counts in *counter (prefill), and the caller skips the access; nothing
+// traps.  Release builds compile every check away.
+#ifdef GQA_DEBUG
+constexpr bool kDebugChecks = true;
+#else
+constexpr bool kDebugChecks = false;
+#endif
+__device__ __forceinline__ bool range_ok(bool ok, uint32_t* status) {
+  if (!kDebugChecks || ok) return true;
+  set_status(status, ATTN_DEV_RANGE);
+  return false;
+}
+__device__ __forceinline__ bool range_ok_count(bool ok, unsigned int* counter) {
+  if (!kDebugChecks || ok) return true;
+  atomicAdd(counter, 1u);
+  return false;
+}
+
 // Launch `kernel` on `stream` with programmatic stream serialisation, so it
 // may begin while the previous kernel on the stream drains (the kernel calls
 // grid_dependency_wait() before touching anything that kernel wrote).

@@ -563,6 +563,9 @@ __device__ __forceinline__ void produce_tile(const CUtensorMap* tmk, const CUten
   const uint32_t sK = smem_u32(stages + (size_t)s * 2 * kTileBytes);
   const uint32_t sV = sK + kTileBytes;
   const int row = lo + k * kTile, z = b * p.Hkv + kvh;
+  if (!range_ok(s >= 0 && s < kStages && z >= 0 && z < p.B * p.Hkv && row >= 0 && row < p.L,
+                p.status))
+    return;
   mbar_arrive_expect_tx(full, 2u * kTileBytes);
   tma_load_3d(sK, tmk, 0, row, z, full);
   tma_load_3d(sK + kHalf, tmk, 64, row, z, full);
@@ -639,6 +642,10 @@ __device__ __forceinline__ void fresh_row(const Params& p, uint8_t* Ks, int rows
     }
   }
   const bool is_v = lane >= 16;
+  if (!range_ok(rows >= 1 && rows <= kTile && pos >= 0 && pos < p.L && b >= 0 && b < p.B &&
+                    kvh >= 0 && kvh < p.Hkv,
+                p.status))
+    return;
   *reinterpret_cast<uint4*>(Ks + (is_v ? kTileBytes : 0) + tile_chunk(rows - 1, q)) = u;
   *reinterpret_cast<uint4*>((is_v ? p.v_cache : p.k_cache) +
                             (((size_t)b * p.Hkv + kvh) * (size_t)p.L + (size_t)pos) * kRowBytes +
@@ -763,6 +770,12 @@ __device__ __forceinline__ void write_nan_rows(const Params& p, int b, int S) {
 __device__ __forceinline__ void store_bf16(uint16_t* dst, float v) {
   __nv_bfloat16 r = __float2bfloat16_rn(v);
   *dst = *reinterpret_cast<uint16_t*>(&r);
+}
+
+// Element d of output row `row` (a head_row), checked in debug builds.
+__device__ __forceinline__ void store_out(const Params& p, size_t row, int d, float v) {
+  if (range_ok(row < (size_t)p.B * p.S * p.Hq && d >= 0 && d < kD, p.status))
+    store_bf16(p.out + row * kD + d, v);
 }
 
 template <int G>
@@ -965,14 +978,15 @@ __global__ void __maxnreg__(Cfg<G>::kMaxRegs) decode_splitkv_kernel(const __grid
       csync(lane);
 
       const int slot = blockIdx.x + seg;
+      const bool slot_ok = range_ok(slot < kMaxGrid + B * Hkv, p.status);
       const int ob = w.b, okvh = w.kvh;  // the segment whose output this is
       for (int idx = ct; idx < G * kD; idx += NC) {
         const int h = idx / kD, d = idx % kD;
         float Mx, Ls, Os;
         merge_warps<NW, G>(merge_o, merge_ml, h, d, Mx, Ls, Os);
         if (whole) {
-          store_bf16(p.out + head_row<G, MT>(p, ob, okvh, h) * kD + d, Os / Ls);
-        } else {
+          store_out(p, head_row<G, MT>(p, ob, okvh, h), d, Os / Ls);
+        } else if (slot_ok) {
           p.part_o[((size_t)slot * G + h) * kD + d] = Os;
           if (d == 0) {
             p.part_ml[((size_t)slot * G + h) * 2 + 0] = Mx;
@@ -1007,7 +1021,7 @@ __global__ void __maxnreg__(Cfg<G>::kMaxRegs) decode_splitkv_kernel(const __grid
 #pragma unroll
               for (int uu = 0; uu < 8; ++uu) {
                 const int c = c0 + uu;
-                if (c <= c_last) {
+                if (c <= c_last && range_ok(c + seg < kMaxGrid + B * Hkv, p.status)) {
                   const size_t sl = (size_t)(c + seg) * G + h;
                   mm[uu] = __ldcg(&p.part_ml[sl * 2]);
                   ll[uu] = __ldcg(&p.part_ml[sl * 2 + 1]);
@@ -1032,7 +1046,7 @@ __global__ void __maxnreg__(Cfg<G>::kMaxRegs) decode_splitkv_kernel(const __grid
               }
               Mm = Mb;
             }
-            store_bf16(p.out + head_row<G, MT>(p, ob, okvh, h) * kD + d, Os / Ls);
+            store_out(p, head_row<G, MT>(p, ob, okvh, h), d, Os / Ls);
           }
           if (ct == 0) p.counters[seg] = 0u;  // ready for the next launch
         }
@@ -1273,7 +1287,7 @@ __global__ void __maxnreg__(Cfg<G>::kMaxRegs)
   // memory (remote stores; nobody waits for them but the barrier below), so
   // rank 0 then merges from local memory and no CTA reads another's.
   asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
-  if (tid < NC) {
+  if (tid < NC && range_ok(rank < Cfg<G>::kMaxC && C <= Cfg<G>::kMaxC, p.status)) {
     float* to_o = cluster.map_shared_rank(land_o, 0) + rank * G * kD;
     float* to_ml = cluster.map_shared_rank(land_ml, 0) + rank * G * 2;
     for (int idx = tid; idx < G * kD; idx += NC) {
@@ -1312,7 +1326,7 @@ __global__ void __maxnreg__(Cfg<G>::kMaxRegs)
           Os = fmaf(land_o[(r * G + h) * kD + d], e, Os);
         }
       }
-      store_bf16(p.out + head_row<G, MT>(p, b, kvh, h) * kD + d, Os / Ls);
+      store_out(p, head_row<G, MT>(p, b, kvh, h), d, Os / Ls);
     }
   }
   // no second cluster barrier: no CTA reads another's shared memory any more

@@ -374,11 +374,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const uint32_t full = bar(kTbFull + ps);
         const uint32_t sK = base + (uint32_t)(ps * 2 * kTileBytes);
         const int row = pw.lo + pw.k * kTile, z = pw.b * Hkv + pw.kvh;
-        mbar_arrive_expect_tx(full, 2u * kTileBytes);
-        tma_load_3d(sK, &tm_k, 0, row, z, full);
-        tma_load_3d(sK + kTcHalf, &tm_k, 64, row, z, full);
-        tma_load_3d(sK + kTileBytes, &tm_v, 0, row, z, full);
-        tma_load_3d(sK + kTileBytes + kTcHalf, &tm_v, 64, row, z, full);
+        if (range_ok(z >= 0 && z < p.B * Hkv && row >= 0 && row < L, p.status)) {
+          mbar_arrive_expect_tx(full, 2u * kTileBytes);
+          tma_load_3d(sK, &tm_k, 0, row, z, full);
+          tma_load_3d(sK + kTcHalf, &tm_k, 64, row, z, full);
+          tma_load_3d(sK + kTileBytes, &tm_v, 0, row, z, full);
+          tma_load_3d(sK + kTileBytes + kTcHalf, &tm_v, 64, row, z, full);
+        }
       }
       tiles_next<CL>(pw, p, prefix, win, shift);
       if (++ps == ns) {
@@ -737,8 +739,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           cg::cluster_group cluster = cg::this_cluster();
           float* to_o = cluster.map_shared_rank(land_o, 0) + rank * G * kD;
           float* to_ml = cluster.map_shared_rank(land_ml, 0) + rank * G * 2;
+          const bool land_ok = range_ok(rank < kMaxCluster && C <= kMaxCluster, p.status);
 #pragma unroll
-          for (int h = 0; h < G; ++h) {
+          for (int h = 0; h < G && land_ok; ++h) {
             to_o[h * kD + t] = oo[h];
             if (t == 0) {
               to_ml[h * 2 + 0] = mo[h];
@@ -753,11 +756,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           if (whole) {
 #pragma unroll
             for (int h = 0; h < G; ++h)
-              store_bf16(p.out + head_row<G, MT>(p, w.b, w.kvh, h) * kD + t, oo[h] / lo_[h]);
+              store_out(p, head_row<G, MT>(p, w.b, w.kvh, h), t, oo[h] / lo_[h]);
           } else {
             const int slot = blockIdx.x + seg;
+            const bool slot_ok = range_ok(slot < kMaxGrid + B * Hkv, p.status);
 #pragma unroll
-            for (int h = 0; h < G; ++h) {
+            for (int h = 0; h < G && slot_ok; ++h) {
               p.part_o[((size_t)slot * G + h) * kD + t] = oo[h];
               if (t == 0) {
                 p.part_ml[((size_t)slot * G + h) * 2 + 0] = mo[h];
@@ -789,7 +793,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
                   for (int uu = 0; uu < 8; ++uu) {
                     const int c = c0 + uu;
-                    if (c <= c_last) {
+                    if (c <= c_last && range_ok(c + seg < kMaxGrid + B * Hkv, p.status)) {
                       const size_t sl = (size_t)(c + seg) * G + h;
                       mm[uu] = __ldcg(&p.part_ml[sl * 2]);
                       ll[uu] = __ldcg(&p.part_ml[sl * 2 + 1]);
@@ -814,7 +818,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                   }
                   Mm = Mb;
                 }
-                store_bf16(p.out + head_row<G, MT>(p, w.b, w.kvh, h) * kD + d, Os / Ls);
+                store_out(p, head_row<G, MT>(p, w.b, w.kvh, h), d, Os / Ls);
               }
               if (t == 0) p.counters[seg] = 0u;  // ready for the next launch
             }
@@ -835,8 +839,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       cg::cluster_group cluster = cg::this_cluster();
       float* to_o = cluster.map_shared_rank(land_o, 0) + rank * G * kD;
       float* to_ml = cluster.map_shared_rank(land_ml, 0) + rank * G * 2;
+      const bool land_ok = range_ok(rank < kMaxCluster && C <= kMaxCluster, p.status);
 #pragma unroll
-      for (int h = 0; h < G; ++h) {
+      for (int h = 0; h < G && land_ok; ++h) {
         to_o[h * kD + t] = 0.f;
         if (t == 0) {
           to_ml[h * 2 + 0] = -INFINITY;
@@ -877,7 +882,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         float Os = 0.f;
 #pragma unroll 4
         for (int r = 0; r < C; ++r) Os = fmaf(land_o[(r * G + h) * kD + d], wr[r * G + h], Os);
-        store_bf16(p.out + head_row<G, MT>(p, w0.b, w0.kvh, h) * kD + d, Os);
+        store_out(p, head_row<G, MT>(p, w0.b, w0.kvh, h), d, Os);
       }
     }
     // no second cluster barrier: no CTA reads another's shared memory again

@@ -55,7 +55,11 @@ cudaError_t launch_prefill_split(const CUtensorMap& mq, const CUtensorMap& mk,
                                  const CUtensorMap& mv, int S, int start_pos, int Hq, int Hkv,
                                  float scale_log2, void* out, int sms, cudaStream_t stream);
 cudaError_t prefill_split_read_timeouts(uint32_t* count);
+cudaError_t prefill_split_read_skips(uint32_t* count);
 // Prefill waits that gave up since the last call (synchronises the stream).
 cudaError_t prefill_read_timeouts(uint32_t* count, cudaStream_t stream);
+// Debug builds: prefill accesses a range check skipped since the last call
+// (synchronises the stream); 0 in other builds.
+cudaError_t prefill_read_skips(uint32_t* count, cudaStream_t stream);
 
 }  // namespace gqa

@@ -90,6 +90,7 @@ constexpr int kBarQFree = kBarOFree + kQT;    // QK^T of the item has read Q
 constexpr int kNumBars = kBarQFree + 1;
 
 __device__ unsigned int g_prefill_timeouts;   // CTAs whose wait gave up; read by prefill_read_timeouts
+__device__ unsigned int g_prefill_skips;      // debug builds: accesses a range check skipped
 
 struct PrefillParams {
   uint16_t* out;
@@ -191,7 +192,14 @@ __global__ void __launch_bounds__(kPThreads, 1)
   // O of tile x [384+64x, +64)
   const uint32_t sQ = base + L::kOffQ;
   // one 128-row tile: its HD/64 column blocks, each at +16 KB
-  auto tma_tile = [&](uint32_t dst, const CUtensorMap* map, int head, int row, uint32_t b) {
+  // (debug builds: a tile outside [0, heads) x [0, rows) is not loaded, and
+  // the CTA stops)
+  auto tma_tile = [&](uint32_t dst, const CUtensorMap* map, int head, int row, uint32_t b,
+                      int heads, int rows) {
+    if (!range_ok_count(head >= 0 && head < heads && row >= 0 && row < rows, &g_prefill_skips)) {
+      *abort_flag = 1;
+      return;
+    }
 #pragma unroll
     for (int c = 0; c < L::kChunks; ++c) tma_load_3d(dst + c * kChunkBytes, map, 64 * c, head, row, b);
   };
@@ -208,7 +216,9 @@ __global__ void __launch_bounds__(kPThreads, 1)
         if (r > 0 && !wait_or_abort(bar(kBarQFree), (uint32_t)(r - 1) & 1u, abort_flag)) break;
         mbar_arrive_expect_tx(bar(kBarQ), p.tpi * kTileBytes);
         for (int x = 0; x < p.tpi; ++x)
-          tma_tile(sQ + x * kTileBytes, &tm_q, it.h, it.q0 + x * kBM, bar(kBarQ));
+          // a second tile past the last query row is loaded (zero fill) but unused
+          tma_tile(sQ + x * kTileBytes, &tm_q, it.h, it.q0 + x * kBM, bar(kBarQ), p.Hq,
+                   it.nt[x] > 0 ? p.S : p.S + kBM);
         bool ok = true;
         for (int i = 0; i < it.n; ++i, ++gk) {
           const int s = gk % kKVStages;
@@ -219,8 +229,9 @@ __global__ void __launch_bounds__(kPThreads, 1)
           }
           const uint32_t sK = base + L::kOffKV + s * 2 * kTileBytes;
           mbar_arrive_expect_tx(bar(kBarKVFull + s), 2 * kTileBytes);
-          tma_tile(sK, &tm_k, it.kvh, i * kBN, bar(kBarKVFull + s));
-          tma_tile(sK + kTileBytes, &tm_v, it.kvh, i * kBN, bar(kBarKVFull + s));
+          tma_tile(sK, &tm_k, it.kvh, i * kBN, bar(kBarKVFull + s), p.Hkv, p.start_pos + p.S);
+          tma_tile(sK + kTileBytes, &tm_v, it.kvh, i * kBN, bar(kBarKVFull + s), p.Hkv,
+                   p.start_pos + p.S);
         }
         if (!ok) break;
       }
@@ -438,7 +449,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
           float o[32];
           tmem_ld32(tm_O + cc * 32, o);
           tmem_ld_wait();
-          if (row < p.S) {
+          if (row < p.S && range_ok_count(row >= 0 && it.h < p.Hq, &g_prefill_skips)) {
 #pragma unroll
             for (int q8 = 0; q8 < 4; ++q8) {
               uint4 w;
@@ -546,6 +557,21 @@ cudaError_t prefill_read_timeouts(uint32_t* count, cudaStream_t stream) {
     e = cudaMemcpyToSymbol(g_prefill_timeouts, &zero, sizeof(zero));
   }
   if (e == cudaSuccess) e = prefill_split_read_timeouts(&v_split);
+  *count = v + v_split;
+  return e;
+}
+
+// Debug builds: the accesses a range check skipped since the last call (both
+// prefill kernels); clears the count.  Always 0 in other builds.
+cudaError_t prefill_read_skips(uint32_t* count, cudaStream_t stream) {
+  cudaError_t e = cudaStreamSynchronize(stream);
+  unsigned v = 0, v_split = 0;
+  if (e == cudaSuccess) e = cudaMemcpyFromSymbol(&v, g_prefill_skips, sizeof(v));
+  if (e == cudaSuccess && v != 0) {
+    const unsigned zero = 0;
+    e = cudaMemcpyToSymbol(g_prefill_skips, &zero, sizeof(zero));
+  }
+  if (e == cudaSuccess) e = prefill_split_read_skips(&v_split);
   *count = v + v_split;
   return e;
 }

@@ -94,10 +94,11 @@ constexpr int kBarMerge = kBarQFree + 1;               // lane 1's (max, sum) ar
 constexpr int kNumBars = kBarMerge + 1;
 
 __device__ unsigned int g_split_timeouts;  // CTAs whose wait gave up
+__device__ unsigned int g_split_skips;     // debug builds: accesses a range check skipped
 
 struct SplitParams {
   uint16_t* out;
-  int S, start_pos, Hq, g;
+  int S, start_pos, Hq, Hkv, g;
   int n_qt;          // query tiles per head
   float scale_log2;  // scale * log2(e), never 0
 };
@@ -204,6 +205,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         const Item it = item(item_of(r));
         // the previous item's QK^T MMAs have finished reading Q
         if (r > 0 && !wait_or_abort(bar(kBarQFree), (uint32_t)(r - 1) & 1u, abort_flag)) break;
+        // (debug builds: a tile outside the query, key or value rows is not
+        // loaded, and the CTA stops)
+        if (!range_ok_count(it.h >= 0 && it.h < p.Hq && it.q0 >= 0 && it.q0 < p.S &&
+                                it.kvh >= 0 && it.kvh < p.Hkv &&
+                                (it.n - 1) * kBN < p.start_pos + p.S,
+                            &g_split_skips)) {
+          *abort_flag = 1;
+          break;
+        }
         mbar_arrive_expect_tx(bar(kBarQ), kTileBytes);
         tma_load_3d(sQ, &tm_q, 0, it.h, it.q0, bar(kBarQ));
         bool ok = true;
@@ -463,7 +473,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
               for (int q = 0; q < 32; ++q) o1[q] = 0.f;
             }
-            if (row < p.S) {
+            if (row < p.S && range_ok_count(row >= 0 && it.h < p.Hq, &g_split_skips)) {
 #pragma unroll
               for (int q8 = 0; q8 < 4; ++q8) {
                 float v[8];
@@ -529,6 +539,7 @@ cudaError_t launch_prefill_split(const CUtensorMap& mq, const CUtensorMap& mk,
   p.S = S;
   p.start_pos = start_pos;
   p.Hq = Hq;
+  p.Hkv = Hkv;
   p.g = Hq / Hkv;
   p.n_qt = (S + kBM - 1) / kBM;
   p.scale_log2 = scale_log2 == 0.f ? 1e-30f : scale_log2;
@@ -545,6 +556,17 @@ cudaError_t prefill_split_read_timeouts(uint32_t* count) {
   if (e == cudaSuccess && v != 0) {
     const unsigned zero = 0;
     e = cudaMemcpyToSymbol(g_split_timeouts, &zero, sizeof(zero));
+  }
+  *count = v;
+  return e;
+}
+
+cudaError_t prefill_split_read_skips(uint32_t* count) {
+  unsigned v = 0;
+  cudaError_t e = cudaMemcpyFromSymbol(&v, g_split_skips, sizeof(v));
+  if (e == cudaSuccess && v != 0) {
+    const unsigned zero = 0;
+    e = cudaMemcpyToSymbol(g_split_skips, &zero, sizeof(zero));
   }
   *count = v;
   return e;

@@ -58,6 +58,11 @@ extern "C" {
 /* Bits of the device status word (attn_read_device_status(..., &bits)). */
 #define ATTN_DEV_BAD_POSITION  0x1u  /* some positions[b] was outside [0, max_len) */
 #define ATTN_DEV_TIMEOUT       0x2u  /* a pipeline wait gave up (the kernel returned early) */
+#define ATTN_DEV_RANGE         0x4u  /* debug builds only (attn_debug_build() == 1): an
+                                        index-derived access (a bulk-copy tile coordinate,
+                                        a cluster landing slot, a partial-result slot, an
+                                        output or new-row address) failed its range check
+                                        and was skipped; the launch's outputs are undefined */
 
 /*
  * attn_kv_append -- the in-place cache write of the decode page, section 4.1
@@ -361,6 +366,25 @@ int attn_last_cuda_error(void);
  * Errors: ATTN_ERR_INVALID_ARG for tile < -1.
  */
 int attn_test_skip_tile(int tile);
+
+/*
+ * attn_debug_build -- 1 if this library was compiled with the device range
+ * checks (-DGQA_DEBUG), else 0.  In such a build every decode kernel checks
+ * the index-derived addresses named under ATTN_DEV_RANGE before it uses them,
+ * and both prefill kernels check their bulk-copy tile coordinates and output
+ * rows; a failed check skips the access and records it (no trap, no assert).
+ * Release builds contain no checks.
+ */
+int attn_debug_build(void);
+
+/*
+ * attn_read_prefill_skips -- synchronise `stream`, read into *skips the
+ * number of prefill accesses that failed a range check since the last call on
+ * this device, clear it, and return ATTN_OK if there were none,
+ * ATTN_ERR_DEVICE if there were, or ATTN_ERR_CUDA.  Always 0 in release
+ * builds.  `skips` may be NULL.
+ */
+int attn_read_prefill_skips(uint32_t* skips, cudaStream_t stream);
 
 #ifdef __cplusplus
 }

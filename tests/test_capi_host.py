@@ -40,13 +40,26 @@ def test_header_declares_the_boundary():
                  "attn_last_cuda_error", "attn_decode_step_append",
                  "attn_decode_step_rope_append", "attn_decode_step_noalloc",
                  "attn_decode_stream_step", "attn_decode_step_window", "attn_decode_multi",
-                 "attn_test_skip_tile", "attn_read_prefill_status"]:
+                 "attn_test_skip_tile", "attn_read_prefill_status", "attn_debug_build",
+                 "attn_read_prefill_skips"]:
         assert want in names
 
 
 def test_every_declared_symbol_is_exported(lib):
     for name in _declared_functions():
         assert hasattr(lib, name), f"{name} declared in include/ but not exported"
+
+
+def test_release_and_range_checked_builds():
+    """The default library has no range checks; the -DGQA_DEBUG build exports
+    the same functions and reports that it has them."""
+    from gqa_decode_attention_place_gb300 import _build
+    rel = ctypes.CDLL(_build.build())
+    dbg = ctypes.CDLL(_build.build(debug=True))
+    assert rel.attn_debug_build() == 0
+    assert dbg.attn_debug_build() == 1
+    for name in _declared_functions():
+        assert hasattr(dbg, name), f"{name} missing from the range-checked build"
 
 
 def test_status_strings(lib):
