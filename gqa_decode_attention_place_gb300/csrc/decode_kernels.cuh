@@ -55,7 +55,8 @@
 //      [c*T/G, (c+1)*T/G), balanced to one tile however ragged the batch is.
 //      A segment split over CTAs is merged by the CTA that arrives last at
 //      the segment's arrival counter (fp32 partials in the workspace; no
-//      spin-wait).
+//      spin-wait).  A merge warp does every merge, so the consumer warps
+//      only ever wait for tiles.
 #pragma once
 
 #include <cfloat>
@@ -116,12 +117,13 @@ template <int G> struct Cfg {
   // the rotated query takes two MMA columns per head: g <= 4 only
   static constexpr bool kRope = 2 * G <= 8;
   static constexpr int kThreads = (NW + 1) * 32;  // + the producer warp
+  static constexpr int kSKThreads = kThreads + 32;  // stream-K: + the merge warp
   static constexpr int kConsumers = NW * 32;
   static constexpr int kKeysPerWarp = kTile / NW;  // 16
-  // registers per thread that still let one CTA of kThreads fit the SM
+  // registers per thread that still let one CTA of kSKThreads fit the SM
   // (the register file is handed out as if the block were a multiple of
   // 128 threads)
-  static constexpr int kRegsFit = 65536 / ((kThreads + 127) / 128 * 128);
+  static constexpr int kRegsFit = 65536 / ((kSKThreads + 127) / 128 * 128);
   static constexpr int kMaxRegs = (kRegsFit > 255 ? 255 : kRegsFit) & ~7;
 };
 
@@ -778,33 +780,69 @@ __device__ __forceinline__ void store_out(const Params& p, size_t row, int d, fl
     store_bf16(p.out + row * kD + d, v);
 }
 
+// Elements d0..d0+3 (d0 a multiple of 4) of output row `row`, each times
+// `scale`: one 8-byte store.
+__device__ __forceinline__ void store_out4(const Params& p, size_t row, int d0, float4 v,
+                                           float scale) {
+  if (range_ok(row < (size_t)p.B * p.S * p.Hq && d0 >= 0 && d0 + 3 < kD, p.status))
+    *reinterpret_cast<uint2*>(p.out + row * kD + d0) =
+        make_uint2(pack_bf16x2(v.x * scale, v.y * scale), pack_bf16x2(v.z * scale, v.w * scale));
+}
+
+// Stream-K shared memory: the ring, barriers, two merge slots of the NW
+// warps' partials ([NW][G][kD] o, then [NW][G][2] max and sum), each warp's
+// staged rotation values (rotary variants), and the tile prefix sum.
+template <int G>
+struct SKLayout {
+  static constexpr int NW = Cfg<G>::NW;
+  static constexpr int kBars = 2 * kStages + 6;  // full, empty, done, spare, merge full[2], empty[2]
+  static constexpr int kBarDone = 2 * kStages;
+  static constexpr int kBarMFull = 2 * kStages + 2;
+  static constexpr int kBarMEmpty = 2 * kStages + 4;
+  static constexpr int kSlotFloats = NW * G * (kD + 2);
+  static constexpr int kRopeFloats = Cfg<G>::kRope ? NW * 256 : 0;  // [NW][16 lanes][16]
+};
+
 template <int G>
 size_t smem_bytes(int B) {
-  constexpr int NW = Cfg<G>::NW;
-  return (size_t)kStages * 2 * kTileBytes + (2 * kStages + 2) * sizeof(uint64_t) +
-         kMiscInts * sizeof(int) + (size_t)NW * G * 2 * sizeof(float) +
-         (size_t)NW * G * kD * sizeof(float) + 2 * kD * sizeof(float) +
-         (size_t)(B + 1) * sizeof(int);
+  using Ly = SKLayout<G>;
+  return (size_t)kStages * 2 * kTileBytes + Ly::kBars * sizeof(uint64_t) +
+         kMiscInts * sizeof(int) + 2 * (size_t)Ly::kSlotFloats * sizeof(float) +
+         (size_t)Ly::kRopeFloats * sizeof(float) + (size_t)(B + 1) * sizeof(int);
 }
 
 // ---------------------------------------------------------- stream-K mode --
+// Roles: warps 0..NW-1 consume tiles, warp NW issues the copies, warp NW+1
+// merges.  At the end of its part of a segment each consumer warp stashes
+// its (max, sum, o) into a merge slot and goes on with the next segment; the
+// merge warp combines the NW warps' partials and writes the output row, or,
+// for a segment split over CTAs, the CTA's partial and -- if this CTA is the
+// last to arrive -- the merge of all parts.  The consumers never wait for a
+// merge (two slots), so merges are off the path that streams the cache.
+//
+// Tile order within the CTA's range [t0, t1): if its last segment starts
+// inside the range and goes on past t1, that part comes first, the rest in
+// order after it.  The other CTA holding that segment starts with its own
+// part of it too, so the merge of every split segment happens early, and the
+// range ends on a whole segment.
 template <int G, int M>
 __global__ void __maxnreg__(Cfg<G>::kMaxRegs) decode_splitkv_kernel(const __grid_constant__ CUtensorMap tm_k,
                                                                    const __grid_constant__ CUtensorMap tm_v,
                                                                    const Params p) {
   constexpr bool R = (M & kModeRope) != 0, A = (M & kModeAdvance) != 0;
   constexpr bool MT = (M & kModeMulti) != 0;
+  using Ly = SKLayout<G>;
   constexpr int NW = Cfg<G>::NW;
   constexpr int KPW = Cfg<G>::kKeysPerWarp;
   constexpr int NC = Cfg<G>::kConsumers;
+  constexpr int kMergeWarp = NW + 1;
   extern __shared__ __align__(1024) uint8_t smem[];
   uint8_t* stages = smem;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kStages * 2 * kTileBytes);
-  int* misc = reinterpret_cast<int*>(bars + 2 * kStages + 2);  // after full, empty, csync, done
-  float* merge_ml = reinterpret_cast<float*>(misc + kMiscInts);  // [NW][G][2]
-  float* merge_o = merge_ml + NW * G * 2;                         // [NW][G][kD]
-  float* rope_cs = merge_o + NW * G * kD;                         // [2][kD] staged cos, sin
-  int* prefix = reinterpret_cast<int*>(rope_cs + 2 * kD);          // [B+1]
+  int* misc = reinterpret_cast<int*>(bars + Ly::kBars);                 // [0] abort [8..8+NW) scan
+  float* mslot = reinterpret_cast<float*>(misc + kMiscInts);            // [2][kSlotFloats]
+  float* rope_cs = mslot + 2 * Ly::kSlotFloats;                         // [NW][16][16]
+  int* prefix = reinterpret_cast<int*>(rope_cs + Ly::kRopeFloats);      // [B+1]
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
@@ -819,10 +857,13 @@ __global__ void __maxnreg__(Cfg<G>::kMaxRegs) decode_splitkv_kernel(const __grid
       mbar_init(smem_u32(&bars[s]), 1);             // full: issuing thread's arrival + bytes
       mbar_init(smem_u32(&bars[kStages + s]), NW);  // empty: per consumer warp
     }
-    mbar_init(smem_u32(&bars[2 * kStages]), NW);    // consumer barrier
-    mbar_init(smem_u32(&bars[2 * kStages + 1]), NW + 1);  // done with positions
+    mbar_init(smem_u32(&bars[Ly::kBarDone]), NW + 2);  // done with positions
+#pragma unroll
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(smem_u32(&bars[Ly::kBarMFull + s]), NW);  // every consumer warp stashed
+      mbar_init(smem_u32(&bars[Ly::kBarMEmpty + s]), 1);  // the merge warp has read the slot
+    }
     misc[0] = 0;
-    misc[1] = 0;
     fence_mbar_init();
   }
   // Launched with programmatic stream serialisation: everything above may run
@@ -886,14 +927,27 @@ __global__ void __maxnreg__(Cfg<G>::kMaxRegs) decode_splitkv_kernel(const __grid
   }
   const long long t0 = T * blockIdx.x / Gd;
   const long long t1 = T * (blockIdx.x + 1) / Gd;
+  const long long n_t = t1 - t0;
+  // processing order: tiles [tA, t1) first, then [t0, tA) (vJ = t1 - tA)
+  long long tA = t0;
+  {
+    Walk wl;
+    walk_init(wl, t1 - 1, prefix, p.positions, B, Hkv, win, shift);
+    const long long s0 = t1 - 1 - wl.k;  // first tile of the last segment
+    if (s0 > t0 && s0 + wl.ntiles > t1) tA = s0;
+  }
+  const long long vJ = t1 - tA;
+  auto step = [&](Walk& w, long long v_next) {  // the walk for order index v_next
+    if (v_next == vJ) walk_init(w, t0, prefix, p.positions, B, Hkv, win, shift);
+    else walk_next(w, prefix, p.positions, B, Hkv, win, shift);
+  };
 
   // -------------------------------------------------------------- producer --
   if (warp == NW) {
     if (lane == 0) {
       Walk w;
-      walk_init(w, t0, prefix, p.positions, B, Hkv, win, shift);
-      long long i = 0;
-      for (long long t = t0; t < t1; ++t, ++i) {
+      walk_init(w, tA, prefix, p.positions, B, Hkv, win, shift);
+      for (long long i = 0; i < n_t; ++i) {
         const int s = (int)(i % kStages);
         const uint32_t u = (uint32_t)(i / kStages);
         if (i >= kStages &&
@@ -903,9 +957,153 @@ __global__ void __maxnreg__(Cfg<G>::kMaxRegs) decode_splitkv_kernel(const __grid
           break;
         }
         produce_tile(&tm_k, &tm_v, p, stages, bars, s, w.b, w.kvh, w.k, w.lo);
-        walk_next(w, prefix, p.positions, B, Hkv, win, shift);
+        if (i + 1 < n_t) step(w, i + 1);
       }
-      if (A) mbar_arrive(smem_u32(&bars[2 * kStages + 1]));  // no more reads of positions
+      if (A) mbar_arrive(smem_u32(&bars[Ly::kBarDone]));  // no more reads of positions
+    }
+    return;
+  }
+
+  // ---------------------------------------------------------- merge warp --
+  if (warp == kMergeWarp) {
+    Walk w;
+    walk_init(w, tA, prefix, p.positions, B, Hkv, win, shift);
+    const int d0 = 4 * lane;  // this lane's 4 dims of every head
+    uint32_t k = 0;           // segment parts merged
+    for (long long v = 0; v < n_t; ++k) {
+      const long long v_end = v < vJ ? vJ : n_t;
+      const long long len = min((long long)(w.ntiles - w.k), v_end - v);
+      const int seg = w.b * Hkv + w.kvh;
+      const long long seg_t0 = (long long)Hkv * prefix[w.b] + (long long)w.kvh * w.ntiles;
+      const long long seg_t1 = seg_t0 + w.ntiles;
+      const bool whole = seg_t0 >= t0 && seg_t1 <= t1;
+      const int ob = w.b, okvh = w.kvh;
+      if (!consumer_wait(smem_u32(&bars[Ly::kBarMFull + (k & 1)]), (k >> 1) & 1u, abort_flag,
+                         p.status, lane))
+        break;
+      const float* so = mslot + (k & 1) * Ly::kSlotFloats;
+      const float* sml = so + NW * G * kD;
+      // combine the NW warps' partials of each head: max M, sum l, o (dims d0..d0+3)
+      float hm[G], hl[G];
+      float4 ho[G];
+#pragma unroll
+      for (int h = 0; h < G; ++h) {
+        float Mx = -INFINITY;
+#pragma unroll
+        for (int ww = 0; ww < NW; ++ww) Mx = fmaxf(Mx, sml[(ww * G + h) * 2]);
+        const float Mu = Mx == -INFINITY ? 0.f : Mx;
+        float l = 0.f;
+        float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int ww = 0; ww < NW; ++ww) {
+          const float e = ex2(sml[(ww * G + h) * 2] - Mu);
+          l = fmaf(sml[(ww * G + h) * 2 + 1], e, l);
+          const float4 x = *reinterpret_cast<const float4*>(so + (ww * G + h) * kD + d0);
+          o.x = fmaf(x.x, e, o.x);
+          o.y = fmaf(x.y, e, o.y);
+          o.z = fmaf(x.z, e, o.z);
+          o.w = fmaf(x.w, e, o.w);
+        }
+        hm[h] = Mx;
+        hl[h] = l;
+        ho[h] = o;
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&bars[Ly::kBarMEmpty + (k & 1)]));  // slot free
+      if (whole) {
+#pragma unroll
+        for (int h = 0; h < G; ++h)
+          store_out4(p, head_row<G, MT>(p, ob, okvh, h), d0, ho[h], 1.f / hl[h]);
+      } else {
+        // this CTA's partial, then the arrival; the last CTA to arrive merges
+        const int c_first = cta_of(seg_t0, T, Gd);
+        const int c_last = cta_of(seg_t1 - 1, T, Gd);
+        const int slot = blockIdx.x + seg;
+        if (range_ok(slot < kMaxGrid + B * Hkv, p.status)) {
+#pragma unroll
+          for (int h = 0; h < G; ++h) {
+            *reinterpret_cast<float4*>(&p.part_o[((size_t)slot * G + h) * kD + d0]) = ho[h];
+            if (lane == 0)
+              *reinterpret_cast<float2*>(&p.part_ml[((size_t)slot * G + h) * 2]) =
+                  make_float2(hm[h], hl[h]);
+          }
+        }
+        // release: the warp's partial stores (ordered before by the warp
+        // barrier) are visible to whoever acquires the counter; acquire: the
+        // last arrival sees every other CTA's partial
+        __threadfence();
+        __syncwarp();
+        uint32_t last = 0;
+        if (lane == 0) {
+          unsigned old;
+          asm volatile("atom.add.acq_rel.gpu.u32 %0, [%1], 1;"
+                       : "=r"(old)
+                       : "l"(&p.counters[seg])
+                       : "memory");
+          last = (old == (unsigned)(c_last - c_first)) ? 1u : 0u;
+        }
+        last = __shfl_sync(0xffffffffu, last, 0);
+        if (last) {
+          __threadfence();
+#pragma unroll 1
+          for (int h = 0; h < G; ++h) {
+            float Mm = -INFINITY, Ls = 0.f;
+            float4 Os = make_float4(0.f, 0.f, 0.f, 0.f);
+            // batches of 4 independent loads keep several L2 round trips in flight
+            for (int c0 = c_first; c0 <= c_last; c0 += 4) {
+              float2 ml[4];
+              float4 oo[4];
+#pragma unroll
+              for (int uu = 0; uu < 4; ++uu) {
+                const int c = c0 + uu;
+                if (c <= c_last && range_ok(c + seg < kMaxGrid + B * Hkv, p.status)) {
+                  const size_t sl = (size_t)(c + seg) * G + h;
+                  ml[uu] = __ldcg(reinterpret_cast<const float2*>(&p.part_ml[sl * 2]));
+                  oo[uu] = __ldcg(reinterpret_cast<const float4*>(&p.part_o[sl * kD + d0]));
+                } else {
+                  ml[uu] = make_float2(-INFINITY, 0.f);
+                  oo[uu] = make_float4(0.f, 0.f, 0.f, 0.f);
+                }
+              }
+              float Mb = Mm;
+#pragma unroll
+              for (int uu = 0; uu < 4; ++uu) Mb = fmaxf(Mb, ml[uu].x);
+              const float Mu = Mb == -INFINITY ? 0.f : Mb;
+              const float sc0 = ex2(Mm - Mu);  // Mm = -inf on the first batch: 0
+              Ls *= sc0;
+              Os.x *= sc0;
+              Os.y *= sc0;
+              Os.z *= sc0;
+              Os.w *= sc0;
+#pragma unroll
+              for (int uu = 0; uu < 4; ++uu) {
+                const float e = ex2(ml[uu].x - Mu);
+                Ls = fmaf(ml[uu].y, e, Ls);
+                Os.x = fmaf(oo[uu].x, e, Os.x);
+                Os.y = fmaf(oo[uu].y, e, Os.y);
+                Os.z = fmaf(oo[uu].z, e, Os.z);
+                Os.w = fmaf(oo[uu].w, e, Os.w);
+              }
+              Mm = Mb;
+            }
+            store_out4(p, head_row<G, MT>(p, ob, okvh, h), d0, Os, 1.f / Ls);
+          }
+          if (lane == 0) p.counters[seg] = 0u;  // ready for the next launch
+        }
+      }
+      v += len;
+      if (v < n_t) {
+        if (v == vJ) {
+          walk_init(w, t0, prefix, p.positions, B, Hkv, win, shift);
+        } else {
+          w.k = w.ntiles - 1;  // on to the next segment
+          walk_next(w, prefix, p.positions, B, Hkv, win, shift);
+        }
+      }
+    }
+    if (A) {
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&bars[Ly::kBarDone]));  // no more reads of positions
     }
     return;
   }
@@ -913,51 +1111,53 @@ __global__ void __maxnreg__(Cfg<G>::kMaxRegs) decode_splitkv_kernel(const __grid
   // ------------------------------------------------------------ consumers --
   Consumer<G> cs;
   cs.init(lane);
-  ConsumerSync csync{smem_u32(&bars[2 * kStages]), abort_flag, p.status, 0u};
+  float* my_rope_cs = rope_cs + (R ? warp * 256 : 0);  // this warp's staged cos, sin
   Walk w;
-  walk_init(w, t0, prefix, p.positions, B, Hkv, win, shift);
+  walk_init(w, tA, prefix, p.positions, B, Hkv, win, shift);
   const uint16_t* qb = p.q + ((size_t)w.b * p.Hq + (size_t)w.kvh * G) * kD;
   if (MT) cs.set_last(w.lo + w.n - 1 - shift, p.S);
   // fused append: this warp writes the segment's new rows if the segment's
   // last tile is in this CTA's range and its last row among the warp's keys
-  auto owns_fresh = [&](long long t) {
-    return p.k_new != nullptr && t + (w.ntiles - 1 - w.k) < t1 &&
-           warp == (w.n - 1 - (w.ntiles - 1) * kTile) / KPW;
+  // (a segment whose part comes first in the order ends past t1)
+  auto owns_fresh = [&](const Walk& ww, long long t) {
+    return p.k_new != nullptr && t + (ww.ntiles - 1 - ww.k) < t1 &&
+           warp == (ww.n - 1 - (ww.ntiles - 1) * kTile) / KPW;
   };
-  bool own_fresh = owns_fresh(t0);
+  bool own_fresh = owns_fresh(w, tA);
   uint4 fk = own_fresh ? load_fresh(p, w.b, w.kvh, lane) : make_uint4(0u, 0u, 0u, 0u);
   if (R) {
     const float* rc = rope_row<R>(p, p.rope_cos, w.b, w.lo + w.n - 1);
     const float* rs = rope_row<R>(p, p.rope_sin, w.b, w.lo + w.n - 1);
     cs.load_q_rope(qb, rc, rs, p.qscale);
-    if (own_fresh) stage_fresh_rope(rope_cs, rc, rs, lane);
+    if (own_fresh) stage_fresh_rope(my_rope_cs, rc, rs, lane);
   } else {
     cs.template load_q<MT>(p, w.b, w.kvh, p.qscale);
   }
   cs.reset();
 
-  long long i = 0;
-  for (long long t = t0; t < t1; ++t, ++i) {
+  uint32_t kseg = 0;  // segment parts stashed
+  for (long long i = 0; i < n_t; ++i) {
     const int s = (int)(i % kStages);
     const uint32_t u = (uint32_t)(i / kStages);
     if (!consumer_wait(smem_u32(&bars[s]), u & 1u, abort_flag, p.status, lane)) break;
     const int rows = min(kTile, w.n - w.k * kTile);
     uint8_t* Ks = stages + (size_t)s * 2 * kTileBytes;
     if (own_fresh && w.k == w.ntiles - 1)
-      fresh_row<R>(p, Ks, rows, w.b, w.kvh, w.lo + w.n - 1, rope_cs, fk, lane);
+      fresh_row<R>(p, Ks, rows, w.b, w.kvh, w.lo + w.n - 1, my_rope_cs, fk, lane);
     cs.template tile<MT, R>(Ks, Ks + kTileBytes, rows, w.lo + w.k * kTile, warp);
     __syncwarp();
     if (lane == 0) mbar_arrive(smem_u32(&bars[kStages + s]));  // the stage may be refilled
-    const bool seg_end = (w.k == w.ntiles - 1) || (t == t1 - 1);
+    const bool more = i + 1 < n_t;
+    const bool seg_end = (w.k == w.ntiles - 1) || i + 1 == vJ || !more;
+    Walk wn = w;
+    if (more) step(wn, i + 1);
 
-    // ---- end of this CTA's part of the segment: merge and emit ------------
+    // ---- end of this CTA's part of the segment: hand it to the merge warp --
     if (seg_end) {
-      if ((w.k == w.ntiles - 1) && t + 1 < t1) {
+      if (more) {
         // the next segment's q (rotated if asked) and new rows only need
-        // loads: they go out now and land while this segment's partials are
-        // merged (the merge reads m, l and o, not q)
-        Walk wn = w;
-        walk_next(wn, prefix, p.positions, B, Hkv, win, shift);
+        // loads: they go out now and land while this part is stashed
+        const long long tn = (i + 1) < vJ ? tA + i + 1 : t0 + (i + 1 - vJ);
         if (R)
           cs.load_q_rope(p.q + ((size_t)wn.b * p.Hq + (size_t)wn.kvh * G) * kD,
                          rope_row<R>(p, p.rope_cos, wn.b, wn.lo + wn.n - 1),
@@ -965,102 +1165,26 @@ __global__ void __maxnreg__(Cfg<G>::kMaxRegs) decode_splitkv_kernel(const __grid
         else
           cs.template load_q<MT>(p, wn.b, wn.kvh, p.qscale);
         if (MT) cs.set_last(wn.lo + wn.n - 1 - shift, p.S);
-        own_fresh = p.k_new != nullptr && t + wn.ntiles < t1 &&
-                    warp == (wn.n - 1 - (wn.ntiles - 1) * kTile) / KPW;
-        if (own_fresh) fk = load_fresh(p, wn.b, wn.kvh, lane);
-      }
-      const int seg = w.b * Hkv + w.kvh;
-      const long long seg_t0 = (long long)Hkv * prefix[w.b] + (long long)w.kvh * w.ntiles;
-      const long long seg_t1 = seg_t0 + w.ntiles;
-      const bool whole = seg_t0 >= t0 && seg_t1 <= t1;
-      const int ct = tid;
-      cs.stash(merge_o, merge_ml, warp);
-      csync(lane);
-
-      const int slot = blockIdx.x + seg;
-      const bool slot_ok = range_ok(slot < kMaxGrid + B * Hkv, p.status);
-      const int ob = w.b, okvh = w.kvh;  // the segment whose output this is
-      for (int idx = ct; idx < G * kD; idx += NC) {
-        const int h = idx / kD, d = idx % kD;
-        float Mx, Ls, Os;
-        merge_warps<NW, G>(merge_o, merge_ml, h, d, Mx, Ls, Os);
-        if (whole) {
-          store_out(p, head_row<G, MT>(p, ob, okvh, h), d, Os / Ls);
-        } else if (slot_ok) {
-          p.part_o[((size_t)slot * G + h) * kD + d] = Os;
-          if (d == 0) {
-            p.part_ml[((size_t)slot * G + h) * 2 + 0] = Mx;
-            p.part_ml[((size_t)slot * G + h) * 2 + 1] = Ls;
-          }
+        own_fresh = owns_fresh(wn, tn);
+        if (own_fresh) {
+          fk = load_fresh(p, wn.b, wn.kvh, lane);
+          if (R)
+            stage_fresh_rope(my_rope_cs, rope_row<R>(p, p.rope_cos, wn.b, wn.lo + wn.n - 1),
+                             rope_row<R>(p, p.rope_sin, wn.b, wn.lo + wn.n - 1), lane);
         }
       }
-      if (!whole) {
-        const int c_first = cta_of(seg_t0, T, Gd);
-        const int c_last = cta_of(seg_t1 - 1, T, Gd);
-        csync(lane);
-        if (ct == 0) {
-          // release: this CTA's partial (ordered before by the barrier) is
-          // visible to whoever acquires the counter; acquire: the last
-          // arrival sees every other CTA's partial
-          unsigned old;
-          asm volatile("atom.add.acq_rel.gpu.u32 %0, [%1], 1;"
-                       : "=r"(old)
-                       : "l"(&p.counters[seg])
-                       : "memory");
-          misc[1] = (old == (unsigned)(c_last - c_first)) ? 1 : 0;
-        }
-        csync(lane);
-        if (misc[1]) {
-          // last to arrive: merge the segment's partials.  Batches of 8
-          // independent loads keep several L2 round trips in flight.
-          for (int idx = ct; idx < G * kD; idx += NC) {
-            const int h = idx / kD, d = idx % kD;
-            float Mm = -INFINITY, Ls = 0.f, Os = 0.f;
-            for (int c0 = c_first; c0 <= c_last; c0 += 8) {
-              float mm[8], ll[8], oo[8];
-#pragma unroll
-              for (int uu = 0; uu < 8; ++uu) {
-                const int c = c0 + uu;
-                if (c <= c_last && range_ok(c + seg < kMaxGrid + B * Hkv, p.status)) {
-                  const size_t sl = (size_t)(c + seg) * G + h;
-                  mm[uu] = __ldcg(&p.part_ml[sl * 2]);
-                  ll[uu] = __ldcg(&p.part_ml[sl * 2 + 1]);
-                  oo[uu] = __ldcg(&p.part_o[sl * kD + d]);
-                } else {
-                  mm[uu] = -INFINITY;
-                  ll[uu] = 0.f;
-                  oo[uu] = 0.f;
-                }
-              }
-              float Mb = Mm;
-#pragma unroll
-              for (int uu = 0; uu < 8; ++uu) Mb = fmaxf(Mb, mm[uu]);
-              const float sc0 = ex2(Mm - Mb);  // Mm = -inf on the first batch: 0
-              Ls *= sc0;
-              Os *= sc0;
-#pragma unroll
-              for (int uu = 0; uu < 8; ++uu) {
-                const float e = ex2(mm[uu] - Mb);
-                Ls = fmaf(ll[uu], e, Ls);
-                Os = fmaf(oo[uu], e, Os);
-              }
-              Mm = Mb;
-            }
-            store_out(p, head_row<G, MT>(p, ob, okvh, h), d, Os / Ls);
-          }
-          if (ct == 0) p.counters[seg] = 0u;  // ready for the next launch
-        }
-      }
-      csync(lane);  // merge buffers are free again
+      // the slot's previous segment has been read by the merge warp
+      if (kseg >= 2 && !consumer_wait(smem_u32(&bars[Ly::kBarMEmpty + (kseg & 1)]),
+                                      ((kseg >> 1) - 1) & 1u, abort_flag, p.status, lane))
+        break;
+      float* so = mslot + (kseg & 1) * Ly::kSlotFloats;
+      cs.stash(so, so + NW * G * kD, warp);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&bars[Ly::kBarMFull + (kseg & 1)]));
+      ++kseg;
       cs.reset();
     }
-    walk_next(w, prefix, p.positions, B, Hkv, win, shift);
-    if (R && own_fresh && w.k == 0 && t + 1 < t1) {
-      // a new segment whose new key this warp rotates: the last segment's
-      // writer has read its staged values (seg_end's barriers came after)
-      stage_fresh_rope(rope_cs, rope_row<R>(p, p.rope_cos, w.b, w.lo + w.n - 1),
-                       rope_row<R>(p, p.rope_sin, w.b, w.lo + w.n - 1), lane);
-    }
+    w = wn;
   }
 
   if (*abort_flag) {
@@ -1070,12 +1194,12 @@ __global__ void __maxnreg__(Cfg<G>::kMaxRegs) decode_splitkv_kernel(const __grid
     }
   }
   if (A) {
-    // this warp is done with positions; warp 0 waits for the producer and the
-    // other consumers, then takes the CTA's ticket
+    // this warp is done with positions; warp 0 waits for the producer, the
+    // merge warp and the other consumers, then takes the CTA's ticket
     __syncwarp();
-    if (lane == 0) mbar_arrive(smem_u32(&bars[2 * kStages + 1]));
+    if (lane == 0) mbar_arrive(smem_u32(&bars[Ly::kBarDone]));
     if (warp == 0) {
-      mbar_wait(smem_u32(&bars[2 * kStages + 1]), 0u, abort_flag);
+      mbar_wait(smem_u32(&bars[Ly::kBarDone]), 0u, abort_flag);
       advance_ticket(p, lane);
     }
   }
@@ -1506,7 +1630,7 @@ cudaError_t launch_g(const Params& p, cudaStream_t stream) {
     return e != cudaSuccess ? e : cudaGetLastError();
   }
   return launch_pdl(decode_splitkv_kernel<G, M>, dim3(min(kMaxGrid, d.num_sms)),
-                    dim3(Cfg<G>::kThreads), smem_bytes<G>(p.B), stream, mk, mv, p);
+                    dim3(Cfg<G>::kSKThreads), smem_bytes<G>(p.B), stream, mk, mv, p);
 }
 
 // The variant for this launch.  The entry points use six combinations:
