@@ -471,6 +471,39 @@ def _time_graph(torch, fn, flush, reps, warm):
     return times
 
 
+def _launch_us(torch, one, flush, R=20):
+    """Device time of one launch of `one` with a cold L2, in us, two ways:
+    (a) a graph of R (flush, launch) pairs minus a graph of R flushes, over
+    R -- the launch's time in a stream of launches, free of the event clock's
+    coarse steps and of host launch latency; (b) the mean of R single
+    flushed launches, each between two events (includes the launch latency
+    and the event clock's granularity).  (a) is the leg's figure."""
+    one()
+    torch.cuda.synchronize()
+
+    def graph(fn):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            fn()
+        return g
+
+    def pairs():
+        for _ in range(R):
+            flush()
+            one()
+
+    def flushes():
+        for _ in range(R):
+            flush()
+    g_pairs, g_flush = graph(pairs), graph(flushes)
+    t_pairs = statistics.median(_time_graph(torch, g_pairs.replay, flush, 5, 1))
+    t_flush = statistics.median(_time_graph(torch, g_flush.replay, flush, 5, 1))
+    cold = (t_pairs - t_flush) * 1e3 / R
+    single = statistics.mean(_time_graph(torch, one, flush, R, 3)) * 1e3
+    del g_pairs, g_flush
+    return cold, single
+
+
 def _time_positions(torch, ga, q_of, kc, vc, ws, positions, flush, hbm, scale):
     """B=1 decode time at fixed positions: warm (graph of R back-to-back
     launches, cache in L2) and cold (each launch preceded by an L2 flush;
@@ -558,13 +591,14 @@ def _decode_leg(torch, ga, synth, name, flush, hbm):
     def one():
         ga.attn_decode_step(case.q, case.positions, case.k_cache, case.v_cache, case.scale,
                             out=out, workspace=ws)
-    times = _time_graph(torch, one, flush, 10, 3)
-    ms = statistics.median(times)
+    us, us1 = _launch_us(torch, one, flush)
+    ms = us * 1e-3
     pos = case.positions.cpu().tolist()
     nb = oracle.decode_bytes(pos, Hq, Hkv, Dd)
     fl = oracle.decode_flops(pos, Hq, Dd)
     tc = Hq // Hkv == 16  # g = 16 runs on the tcgen05 kernel, g <= 8 on warp-level MMAs
-    r = {"us": round(ms * 1e3, 2), "GBs": round(nb / (ms * 1e-3) / 1e9, 1),
+    r = {"us": round(us, 2), "us_single_launch": round(us1, 2),
+         "GBs": round(nb / (ms * 1e-3) / 1e9, 1),
          "frac_hbm": round(nb / (ms * 1e-3) / 1e9 / hbm, 3),
          "frac_hbm_8tbs": round(nb / (ms * 1e-3) / 1e9 / NOMINAL_HBM_GBS, 3),
          "TFLOPs_tensor": round(fl / (ms * 1e-3) / 1e12, 2),
@@ -596,10 +630,12 @@ def _append_leg(torch, ga, synth, name, flush, hbm, rope):
             ga.attn_decode_step_append(case.q, case.k_new, case.v_new, case.positions,
                                        case.k_cache, case.v_cache, case.scale, out=out,
                                        workspace=ws)
-    ms = statistics.median(_time_graph(torch, one, flush, 10, 3))
+    us, us1 = _launch_us(torch, one, flush)
+    ms = us * 1e-3
     pos = case.positions.cpu().tolist()
     nb = oracle.decode_bytes(pos, Hq, Hkv, Dd) + 2 * 2 * B * Hkv * Dd * 2
-    r = {"us": round(ms * 1e3, 2), "GBs": round(nb / (ms * 1e-3) / 1e9, 1),
+    r = {"us": round(us, 2), "us_single_launch": round(us1, 2),
+         "GBs": round(nb / (ms * 1e-3) / 1e9, 1),
          "frac_hbm": round(nb / (ms * 1e-3) / 1e9 / hbm, 3),
          "frac_hbm_8tbs": round(nb / (ms * 1e-3) / 1e9 / NOMINAL_HBM_GBS, 3), "bytes": nb,
          "shape": {"B": B, "Hq": Hq, "Hkv": Hkv, "D": Dd, "L": Ll}}
@@ -621,10 +657,12 @@ def _window_leg(torch, ga, synth, name, flush, hbm, window):
     def one():
         ga.attn_decode_step_window(case.q, case.positions, case.k_cache, case.v_cache,
                                    case.scale, window, out=out, workspace=ws)
-    ms = statistics.median(_time_graph(torch, one, flush, 10, 3))
+    us, us1 = _launch_us(torch, one, flush)
+    ms = us * 1e-3
     rows_pos = [min(int(p), window - 1) for p in case.positions.cpu().tolist()]
     nb = oracle.decode_bytes(rows_pos, Hq, Hkv, Dd)
-    r = {"us": round(ms * 1e3, 2), "GBs": round(nb / (ms * 1e-3) / 1e9, 1),
+    r = {"us": round(us, 2), "us_single_launch": round(us1, 2),
+         "GBs": round(nb / (ms * 1e-3) / 1e9, 1),
          "frac_hbm": round(nb / (ms * 1e-3) / 1e9 / hbm, 3),
          "frac_hbm_8tbs": round(nb / (ms * 1e-3) / 1e9 / NOMINAL_HBM_GBS, 3), "bytes": nb, "window": window,
          "shape": {"B": B, "Hq": Hq, "Hkv": Hkv, "D": Dd, "L": Ll}}
@@ -649,10 +687,12 @@ def _multi_leg(torch, ga, synth, name, flush, hbm, S):
     def one():
         ga.attn_decode_multi(q, pos, case.k_cache, case.v_cache, case.scale, out=out,
                              workspace=ws)
-    ms = statistics.median(_time_graph(torch, one, flush, 10, 3))
+    us, us1 = _launch_us(torch, one, flush)
+    ms = us * 1e-3
     last = [int(p) + S - 1 for p in pos.cpu().tolist()]
     nb = oracle.decode_bytes(last, Hq, Hkv, Dd) + 2 * (S - 1) * B * Hq * Dd * 2
-    r = {"us": round(ms * 1e3, 2), "GBs": round(nb / (ms * 1e-3) / 1e9, 1),
+    r = {"us": round(us, 2), "us_single_launch": round(us1, 2),
+         "GBs": round(nb / (ms * 1e-3) / 1e9, 1),
          "frac_hbm": round(nb / (ms * 1e-3) / 1e9 / hbm, 3),
          "frac_hbm_8tbs": round(nb / (ms * 1e-3) / 1e9 / NOMINAL_HBM_GBS, 3), "bytes": nb, "S": S,
          "shape": {"B": B, "Hq": Hq, "Hkv": Hkv, "D": Dd, "L": Ll}}
@@ -673,9 +713,11 @@ def _prefill_leg(torch, ga, synth, name, flush, tflops_peak):
 
     def one():
         ga.attn_prefill_causal(case.q, case.k, case.v, case.start_pos, case.scale, out=out)
-    ms = statistics.median(_time_graph(torch, one, flush, 10, 3))
+    us, us1 = _launch_us(torch, one, flush)
+    ms = us * 1e-3
     fl = oracle.prefill_flops(S, case.start_pos, Hq, d)
-    return {"us": round(ms * 1e3, 2), "TFLOPs": round(fl / (ms * 1e-3) / 1e12, 1),
+    return {"us": round(us, 2), "us_single_launch": round(us1, 2),
+            "TFLOPs": round(fl / (ms * 1e-3) / 1e12, 1),
             "frac_tensor": round(fl / (ms * 1e-3) / 1e12 / tflops_peak, 3), "flops": fl,
             "shape": {"S": S, "start_pos": case.start_pos, "Hq": Hq, "Hkv": case.k.shape[1],
                       "d": d}}
