@@ -579,9 +579,18 @@ def _max_len_leg(torch, ga, flush, hbm):
     return res
 
 
-def _decode_leg(torch, ga, synth, name, flush, hbm):
+def _decode_leg(torch, ga, synth, name, flush, hbm, B=None, Hq=None):
+    """A decode workload (optionally with another batch size or head count:
+    the cache shape, positions and value recipe stay the workload's)."""
     import oracle
-    case = synth.generators.workload_case(name, seed=0, device="cuda")
+    if B or Hq:
+        w = dict(synth.generators.WORKLOADS[name])
+        w.pop("kind")
+        w["B"] = B or w["B"]
+        w["Hq"] = Hq or w["Hq"]
+        case = synth.generators.decode_case(seed=0, device="cuda", name=name, **w)
+    else:
+        case = synth.generators.workload_case(name, seed=0, device="cuda")
     B, Hq, Dd = case.q.shape
     Hkv, Ll = case.k_cache.shape[1], case.k_cache.shape[2]
     ga.attn_kv_append(case.k_new, case.v_new, case.positions, case.k_cache, case.v_cache)
@@ -860,6 +869,8 @@ def run_ours(args):
         legs["max_len"] = _max_len_leg(torch, ga, flush, hbm)
         for name in ("ragged", "stress"):
             legs[name] = _decode_leg(torch, ga, synth, name, flush, hbm)
+        # 16 query heads per KV head: the tcgen05 decode kernel
+        legs["stress_g16_b32"] = _decode_leg(torch, ga, synth, "stress", flush, hbm, B=32, Hq=128)
         legs["ragged_append"] = _append_leg(torch, ga, synth, "ragged", flush, hbm, rope=False)
         legs["ragged_rope_append"] = _append_leg(torch, ga, synth, "ragged", flush, hbm,
                                                  rope=True)
