@@ -70,6 +70,9 @@ def _args():
     ap.add_argument("--batch", type=int, default=None,
                     help="--only with a decode workload: use this batch size instead "
                          "(a smaller capture of the same kernel)")
+    ap.add_argument("--window", type=int, default=None,
+                    help="--only with a decode workload: attend the last WINDOW rows "
+                         "(attn_decode_step_window)")
     ap.add_argument("--heads", type=int, default=None,
                     help="--only with a decode workload: use this many query heads "
                          "(another group size on the same cache shape)")
@@ -965,8 +968,12 @@ def run_only(args):
         out = torch.empty_like(case.q)
         ga.attn_kv_append(case.k_new, case.v_new, case.positions, case.k_cache, case.v_cache)
         for _ in range(args.reps):
-            ga.attn_decode_step(case.q, case.positions, case.k_cache, case.v_cache, case.scale,
-                                out=out, workspace=ws)
+            if args.window:
+                ga.attn_decode_step_window(case.q, case.positions, case.k_cache, case.v_cache,
+                                           case.scale, args.window, out=out, workspace=ws)
+            else:
+                ga.attn_decode_step(case.q, case.positions, case.k_cache, case.v_cache,
+                                    case.scale, out=out, workspace=ws)
     else:
         out = torch.empty_like(case.q)
         for _ in range(args.reps):
