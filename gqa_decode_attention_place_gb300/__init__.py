@@ -29,6 +29,7 @@ __all__ = [
     "attn_decode_step_append", "attn_decode_step_rope_append", "attn_decode_stream_step",
     "attn_decode_step_window", "attn_decode_multi", "attn_test_skip_tile",
     "attn_debug_build", "attn_read_prefill_skips", "debug_collect_range_bits",
+    "attn_test_force_schedule",
 ]
 
 ATTN_OK = 0
@@ -98,6 +99,8 @@ def load_library(build_if_missing: bool = True) -> ctypes.CDLL:
     lib.attn_decode_multi.restype = i32
     lib.attn_test_skip_tile.argtypes = [i32]
     lib.attn_test_skip_tile.restype = i32
+    lib.attn_test_force_schedule.argtypes = [i32]
+    lib.attn_test_force_schedule.restype = i32
     lib.attn_decode_step_noalloc.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, i32, f32, vp, vp]
     lib.attn_decode_step_noalloc.restype = i32
     lib.attn_prefill_causal.argtypes = [vp, vp, vp, i32, i32, i32, i32, i32, f32, vp, vp]
@@ -435,6 +438,13 @@ def attn_test_skip_tile(tile: int) -> None:
     """Failure-path tests only: the next decode launches never issue tile
     ``tile`` of the first segment, so the waits for it run out (-1: off)."""
     _raise(load_library().attn_test_skip_tile(int(tile)), "attn_test_skip_tile")
+
+
+def attn_test_force_schedule(cluster: int) -> None:
+    """Schedule tests only: split every segment by stream-K (0) or in
+    clusters of `cluster` CTAs (1..16) from the next decode launch on; -1
+    restores the automatic choice."""
+    _raise(load_library().attn_test_force_schedule(int(cluster)), "attn_test_force_schedule")
 
 
 def attn_read_prefill_status(stream=None) -> int:

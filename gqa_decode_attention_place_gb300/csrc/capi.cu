@@ -229,6 +229,12 @@ int attn_read_device_status(void* workspace, uint32_t* bits, cudaStream_t stream
   return word ? ATTN_ERR_DEVICE : ATTN_OK;
 }
 
+int attn_test_force_schedule(int cluster) {
+  if (cluster < -1 || cluster > 16) return ATTN_ERR_INVALID_ARG;
+  gqa::g_decode_test_cluster = cluster;
+  return ATTN_OK;
+}
+
 int attn_test_skip_tile(int tile) {
   if (tile < -1) return ATTN_ERR_INVALID_ARG;
   gqa::g_decode_test_skip = tile;

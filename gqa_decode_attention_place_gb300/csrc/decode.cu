@@ -12,6 +12,7 @@
 namespace gqa {
 
 int g_decode_test_skip = -1;
+int g_decode_test_cluster = -1;
 
 namespace {
 

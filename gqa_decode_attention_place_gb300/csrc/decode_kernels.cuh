@@ -1565,6 +1565,13 @@ cudaError_t cluster_size(const Params& p, int* C) {
   *C = 0;
   for (int c = Cfg<G>::kMaxC; c >= 8 && *C == 0; --c)
     if (nseg <= d.clusters[G][c]) *C = c;
+  const int force = g_decode_test_cluster;  // schedule tests only
+  if (force >= 0) {
+    // a cluster size these kernels cannot launch is refused, not replaced
+    if (force > Cfg<G>::kMaxC || (force > 8 && d.clusters[G][force] == 0))
+      return cudaErrorNotSupported;
+    *C = force;
+  }
   return cudaSuccess;
 }
 

@@ -38,6 +38,10 @@ struct DecodeParams {
 // Failure-path tests: a tile of the first segment the next decode launches
 // will not issue (-1: none).  Process-wide; set through attn_test_skip_tile.
 extern int g_decode_test_skip;
+// Schedule tests: -1 chooses the split of each segment automatically; 0
+// forces stream-K; C >= 1 forces cluster mode with clusters of C CTAs.
+// Process-wide; set through attn_test_force_schedule.
+extern int g_decode_test_cluster;
 
 // One launcher per group size g = Hq / Hkv (decode_g<g>.cu).
 cudaError_t launch_decode_group1(const DecodeParams& p, cudaStream_t stream);

@@ -991,6 +991,14 @@ cudaError_t launch_tc_g(const Params& p, cudaStream_t stream) {
   int C = 0;
   for (int c = kMaxCluster; c >= 8 && C == 0; --c)
     if (nseg <= d.clusters[G][c]) C = c;
+  const int force = g_decode_test_cluster;  // schedule tests only
+  if (force >= 0) {
+    // a cluster size this kernel cannot launch is refused, not replaced
+    if (force > kMaxCluster || tc_smem_bytes<G>(2, force, 0) > (size_t)kTcMaxSmem ||
+        (force > 8 && d.clusters[G][force] == 0))
+      return cudaErrorNotSupported;
+    C = force;
+  }
   // three K/V stages when they fit in shared memory, else two
   auto stages = [&](int c, int b) { return tc_smem_bytes<G>(3, c, b) <= (size_t)kTcMaxSmem ? 3 : 2; };
   if (C > 0) {

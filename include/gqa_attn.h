@@ -368,6 +368,23 @@ int attn_last_cuda_error(void);
 int attn_test_skip_tile(int tile);
 
 /*
+ * attn_test_force_schedule -- for tests of the split schedules only.  From
+ * the next decode launch on, every segment (sequence, KV head) is split the
+ * way `cluster` says instead of by the automatic choice: 0 = stream-K (all
+ * tiles of all segments in one flat list over a persistent grid, split
+ * segments merged through the workspace), C in 1..16 = cluster mode with
+ * clusters of C CTAs (one cluster per segment, partials merged in rank 0's
+ * shared memory), -1 (the default) = automatic.  Results agree with the
+ * automatic choice up to the rounding of a different merge order.  A decode
+ * call whose kernel cannot run clusters of C (too many landing slots for its
+ * shared memory, or more than 8 where the device allows no larger clusters)
+ * fails with ATTN_ERR_CUDA (cudaErrorNotSupported).  Process-wide and not
+ * thread-safe.
+ * Errors: ATTN_ERR_INVALID_ARG for cluster < -1 or > 16.
+ */
+int attn_test_force_schedule(int cluster);
+
+/*
  * attn_debug_build -- 1 if this library was compiled with the device range
  * checks (-DGQA_DEBUG), else 0.  In such a build every decode kernel checks
  * the index-derived addresses named under ATTN_DEV_RANGE before it uses them,

@@ -41,7 +41,7 @@ def test_header_declares_the_boundary():
                  "attn_decode_step_rope_append", "attn_decode_step_noalloc",
                  "attn_decode_stream_step", "attn_decode_step_window", "attn_decode_multi",
                  "attn_test_skip_tile", "attn_read_prefill_status", "attn_debug_build",
-                 "attn_read_prefill_skips"]:
+                 "attn_read_prefill_skips", "attn_test_force_schedule"]:
         assert want in names
 
 
@@ -147,6 +147,9 @@ def test_host_validation_happens_before_any_launch(lib):
     assert multi(P, None, None, P, P, P, 1, 2, 16, 8, 16, 128, 1.0, P, P, need2 - 1, None) == 3
     assert lib.attn_test_skip_tile(-2) == 1
     assert lib.attn_test_skip_tile(-1) == 0
+    assert lib.attn_test_force_schedule(-2) == 1
+    assert lib.attn_test_force_schedule(17) == 1
+    assert lib.attn_test_force_schedule(-1) == 0
     # the append entry points still refuse missing new rows
     assert lib.attn_decode_step_append(P, None, None, P, P, P, 1, 16, 8, 16, 128, 1.0, P, P,
                                        need, None) == 1
