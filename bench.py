@@ -337,18 +337,29 @@ class ClockSampler:
 
 # ------------------------------------------------------------ our arm ------
 
-def _dist():
+def _dist(set_device=None, backend="nccl"):
+    """Rank setup of a replica: the GPU is LOCAL_RANK (set_device is
+    torch.cuda.set_device unless a test passes its own), and with
+    WORLD_SIZE > 1 a process group (NCCL on the GPU; a test may use gloo)
+    for the barrier and the max-reduction of the step time only."""
     import torch
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
+    (set_device or torch.cuda.set_device)(local)
     if ws > 1:
         import torch.distributed as dist
-        torch.cuda.set_device(local)
-        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
-    else:
-        torch.cuda.set_device(local)
+        if backend == "nccl":
+            dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+        else:
+            dist.init_process_group(backend)
     return ws, rank, local
+
+
+def replica_seed(rank: int) -> int:
+    """Seed of a replica's synthetic inputs: every rank streams its own
+    sequence (weak scaling), not a copy of rank 0's."""
+    return 7919 * rank
 
 
 def _barrier(ws):
@@ -744,7 +755,7 @@ def run_ours(args):
     hbm, tf_burst, tf_sus, peak_src = _peaks()
     ga.load_library()
     flush = _L2Flush(torch, FLUSH_BYTES)
-    st = Stream(torch, ga, synth)
+    st = Stream(torch, ga, synth, seed=replica_seed(rank))
     nbytes = _decode_bytes_stream()
 
     # ---- timed region: K replays of the streaming step -------------------
