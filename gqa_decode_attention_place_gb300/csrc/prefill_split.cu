@@ -412,11 +412,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int a = 0; a < 4; ++a) rs2[a] = mk2(0.f, 0.f);
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          float pw[32];
+        for (int qt = 0; qt < 4; ++qt) {
+          float pw[16];
 #pragma unroll
-          for (int q = 0; q < 32; ++q) {
-            const int jj = half * 64 + 2 * q;
+          for (int q = 0; q < 16; ++q) {
+            const int jj = qt * 32 + 2 * q;
             float lo, hi;
             brk2(fma2(mk2(sv[jj], sv[jj + 1]), c2, m2), lo, hi);
             lo = ex2(lo);
@@ -424,7 +424,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             rs2[q & 3] = add2(rs2[q & 3], mk2(lo, hi));
             pw[q] = __uint_as_float(pack_bf16x2(lo, hi));
           }
-          tmem_st32(tm_P + half * 32, pw);
+          tmem_st16(tm_P + qt * 16, pw);
         }
         {
           f2 t = add2(add2(rs2[0], rs2[1]), add2(rs2[2], rs2[3]));
