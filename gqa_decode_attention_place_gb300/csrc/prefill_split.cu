@@ -125,6 +125,7 @@ struct Item {
   __device__ __forceinline__ int units(int x) const { return x == 0 ? (n + 1) >> 1 : n >> 1; }
 };
 
+template <bool kPos>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_split_kernel(const __grid_constant__ CUtensorMap tm_q,
                          const __grid_constant__ CUtensorMap tm_k,
@@ -314,7 +315,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tm_P = tmem + tmP(x) + lane_off;
     const uint32_t tm_O = tmem + tmO(x) + lane_off;
     const float c = p.scale_log2;  // non-zero (the host replaces 0 by a tiny value)
-    const bool c_pos = c > 0.f;
+    constexpr bool c_pos = kPos;  // the scale's sign, a launch choice
     const float mask_raw = c_pos ? -INFINITY : INFINITY;  // times c: -inf
     uint32_t cs = 0;   // S_x consumed so far (= P_x written = PV_x issued)
     bool ok = true;
@@ -522,16 +523,18 @@ cudaError_t launch_prefill_split(const CUtensorMap& mq, const CUtensorMap& mk,
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev >= 0 && dev < 64 && !configured[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(prefill_split_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-    if (e != cudaSuccess) return e;
-    // The kernel moves registers between its warpgroups (setmaxnreg); the
-    // block's launch allocation must cover the new split, or the softmax
-    // warpgroups would wait for registers for ever.
-    cudaFuncAttributes fa;
-    e = cudaFuncGetAttributes(&fa, prefill_split_kernel);
-    if (e != cudaSuccess) return e;
-    if ((long long)fa.numRegs * kThreads < kRegSplitTotal) return cudaErrorInvalidConfiguration;
+    for (auto kern : {prefill_split_kernel<true>, prefill_split_kernel<false>}) {
+      cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           kSmemBytes);
+      if (e != cudaSuccess) return e;
+      // The kernel moves registers between its warpgroups (setmaxnreg); the
+      // block's launch allocation must cover the new split, or the softmax
+      // warpgroups would wait for registers for ever.
+      cudaFuncAttributes fa;
+      e = cudaFuncGetAttributes(&fa, kern);
+      if (e != cudaSuccess) return e;
+      if ((long long)fa.numRegs * kThreads < kRegSplitTotal) return cudaErrorInvalidConfiguration;
+    }
     configured[dev] = true;
   }
   SplitParams p;
@@ -546,7 +549,10 @@ cudaError_t launch_prefill_split(const CUtensorMap& mq, const CUtensorMap& mk,
   const long long items = (long long)p.n_qt * Hq;
   if (items > 0x7fffffffLL) return cudaErrorInvalidValue;
   const unsigned blocks = (unsigned)std::min<long long>(items, sms);  // one CTA per SM
-  prefill_split_kernel<<<blocks, kThreads, kSmemBytes, stream>>>(mq, mk, mv, p);
+  if (p.scale_log2 > 0.f)
+    prefill_split_kernel<true><<<blocks, kThreads, kSmemBytes, stream>>>(mq, mk, mv, p);
+  else
+    prefill_split_kernel<false><<<blocks, kThreads, kSmemBytes, stream>>>(mq, mk, mv, p);
   return cudaGetLastError();
 }
 
