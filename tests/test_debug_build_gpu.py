@@ -7,7 +7,8 @@ addresses) and both prefill kernels check their tile coordinates and output
 rows before use; a failed check skips the access and is recorded
 (ATTN_DEV_RANGE in the decode status word, a count for prefill).  This test
 builds that library and runs the decode, append, rotary, window, multi-token,
-streaming and prefill parity tests against it in a child process
+streaming, prefill and split-schedule parity tests against it in a child
+process
 (GQA_ATTN_DEBUG=1): each must match the oracle as before, and the autouse
 fixture in conftest.py fails any test after which a check had failed.
 """
@@ -25,7 +26,8 @@ pytestmark = pytest.mark.gpu
 
 HERE = os.path.dirname(os.path.abspath(__file__))
 FILES = ["test_decode_gpu.py", "test_append_gpu.py", "test_rope_gpu.py", "test_window_gpu.py",
-         "test_multi_gpu.py", "test_stream_step_gpu.py", "test_prefill_gpu.py"]
+         "test_multi_gpu.py", "test_stream_step_gpu.py", "test_prefill_gpu.py",
+         "test_schedule_gpu.py"]
 # the 2^20-row caches are left out for memory and time; nothing else
 DESELECT = "not million"
 
