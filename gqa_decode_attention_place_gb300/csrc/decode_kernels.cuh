@@ -80,7 +80,7 @@ constexpr int kTileBytes = kTile * kRowBytes;      // 32 KB per operand
 constexpr int kHalf = kTile * 128;                 // one 64-dim box of an operand (16 KB)
 constexpr int kMaxB = kDecodeMaxB;
 constexpr int kMaxGrid = kDecodeMaxGrid;
-constexpr int kMiscInts = 32;                      // [0] abort [1] last [8..8+NW) scan
+constexpr int kMiscInts = 32;                      // [0] abort, [8..8+NW) scan
 constexpr int kWholeTiles = 4;                     // segments this short are not split
 constexpr int kMaxCluster = 16;                    // CTAs per cluster in cluster mode
 
