@@ -294,9 +294,9 @@ int attn_decode_stream_step(const void* q, const void* k_new, const void* v_new,
  * are rejected with ATTN_ERR_WORKSPACE (B=256, Hq=64, Hkv=8, D=128 needs about
  * 12.8 MB and fits).  The first call on a device looks up the array's device
  * address (cudaGetSymbolAddress) while that device is current, and so does
- * the first call after the device's context was replaced (cudaDeviceReset);
- * make those calls before any stream capture.  The lookup is guarded by a
- * mutex, so host threads may make their first calls at the same time.  Every
+ * the first call after the device's context was replaced (cudaDeviceReset).
+ * The lookup is guarded by a mutex, so host threads may make their first
+ * calls at the same time.  Every
  * call first clears the array's status word and arrival counters with
  * cudaMemsetAsync on `stream`.  All calls share the one array, so calls that
  * overlap on the GPU (other streams, other host threads) race and give wrong
