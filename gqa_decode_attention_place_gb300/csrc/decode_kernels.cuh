@@ -74,7 +74,8 @@ namespace cg = cooperative_groups;
 
 constexpr int kD = kDecodeD;
 constexpr int kTile = 128;                         // keys per pipeline stage
-constexpr int kStages = 2;
+constexpr int kStages = 2;                         // stream-K ring (cluster mode: Cfg)
+constexpr int kMaxRing = 3;                        // deepest ring of either mode
 constexpr int kRowBytes = kD * 2;
 constexpr int kTileBytes = kTile * kRowBytes;      // 32 KB per operand
 constexpr int kHalf = kTile * 128;                 // one 64-dim box of an operand (16 KB)
@@ -116,6 +117,9 @@ template <int G> struct Cfg {
   static constexpr int kMaxC = G == 8 ? 12 : 16;
   // the rotated query takes two MMA columns per head: g <= 4 only
   static constexpr bool kRope = 2 * G <= 8;
+  // cluster mode's K/V ring: 3 stages where they fit beside rank 0's landing
+  // slots (g <= 2), else 2
+  static constexpr int kClusterStages = G <= 2 ? 3 : 2;
   static constexpr int kThreads = (NW + 1) * 32;  // + the producer warp
   static constexpr int kSKThreads = kThreads + 32;  // stream-K: + the merge warp
   static constexpr int kConsumers = NW * 32;
@@ -565,7 +569,7 @@ __device__ __forceinline__ void produce_tile(const CUtensorMap* tmk, const CUten
   const uint32_t sK = smem_u32(stages + (size_t)s * 2 * kTileBytes);
   const uint32_t sV = sK + kTileBytes;
   const int row = lo + k * kTile, z = b * p.Hkv + kvh;
-  if (!range_ok(s >= 0 && s < kStages && z >= 0 && z < p.B * p.Hkv && row >= 0 && row < p.L,
+  if (!range_ok(s >= 0 && s < kMaxRing && z >= 0 && z < p.B * p.Hkv && row >= 0 && row < p.L,
                 p.status))
     return;
   mbar_arrive_expect_tx(full, 2u * kTileBytes);
@@ -1209,7 +1213,8 @@ __global__ void __maxnreg__(Cfg<G>::kMaxRegs) decode_splitkv_kernel(const __grid
 template <int G>
 size_t cluster_smem_bytes() {
   constexpr int NW = Cfg<G>::NW;
-  return (size_t)kStages * 2 * kTileBytes + (2 * kStages + 2) * sizeof(uint64_t) +
+  constexpr int NS = Cfg<G>::kClusterStages;
+  return (size_t)NS * 2 * kTileBytes + (2 * NS + 2) * sizeof(uint64_t) +
          kMiscInts * sizeof(int) + (size_t)NW * G * 2 * sizeof(float) +
          (size_t)NW * G * kD * sizeof(float) + 2 * kD * sizeof(float) +
          (size_t)Cfg<G>::kMaxC * G * (kD + 2) * sizeof(float) +
@@ -1225,12 +1230,16 @@ __global__ void __maxnreg__(Cfg<G>::kMaxRegs)
   constexpr bool R = (M & kModeRope) != 0, A = (M & kModeAdvance) != 0;
   constexpr bool MT = (M & kModeMulti) != 0;
   constexpr int NW = Cfg<G>::NW;
+  constexpr int NS = Cfg<G>::kClusterStages;  // ring stages in shared memory
+  // stages the ring uses: with the rotary embedding two, so that its staging
+  // copies meet a shorter TMA queue (a third stage measured slower there)
+  constexpr int NR = R ? 2 : NS;
   constexpr int KPW = Cfg<G>::kKeysPerWarp;
   constexpr int NC = Cfg<G>::kConsumers;
   extern __shared__ __align__(1024) uint8_t smem[];
   uint8_t* stages = smem;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kStages * 2 * kTileBytes);
-  int* misc = reinterpret_cast<int*>(bars + 2 * kStages + 2);  // after full, empty, csync, done
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + NS * 2 * kTileBytes);
+  int* misc = reinterpret_cast<int*>(bars + 2 * NS + 2);  // after full, empty, csync, done
   float* merge_ml = reinterpret_cast<float*>(misc + kMiscInts);  // [NW][G][2]
   float* merge_o = merge_ml + NW * G * 2;                         // [NW][G][kD]
   float* rope_cs = merge_o + NW * G * kD;                         // [2][kD] staged cos, sin
@@ -1259,11 +1268,11 @@ __global__ void __maxnreg__(Cfg<G>::kMaxRegs)
 
   if (producer) {
 #pragma unroll
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < NS; ++s) {
       mbar_init(smem_u32(&bars[s]), 1);
-      mbar_init(smem_u32(&bars[kStages + s]), NW);
+      mbar_init(smem_u32(&bars[NS + s]), NW);
     }
-    mbar_init(smem_u32(&bars[2 * kStages]), NW);
+    mbar_init(smem_u32(&bars[2 * NS]), NW);
     mbar_init(smem_u32(stage_bar), 1);
     mbar_init(smem_u32(q_stage_bar), 1);
     misc[0] = 0;
@@ -1341,7 +1350,7 @@ __global__ void __maxnreg__(Cfg<G>::kMaxRegs)
         stage_rope_inputs<G>(q_stage, p, b, kvh, rope_row<R>(p, p.rope_cos, b, pos),
                              rope_row<R>(p, p.rope_sin, b, pos), smem_u32(stage_bar));
       int i = 0;
-      for (int k = rank; k < ntiles && i < kStages; k += C, ++i)
+      for (int k = rank; k < ntiles && i < NR; k += C, ++i)
         if (i > 0 || !early) produce_tile(&tm_k, &tm_v, p, stages, bars, i, b, kvh, k, lo);
     }
     __syncwarp();
@@ -1356,11 +1365,11 @@ __global__ void __maxnreg__(Cfg<G>::kMaxRegs)
       }
     }
     if (lane == 0) {
-      int i = kStages;
-      for (int k = rank + kStages * C; k < ntiles; k += C, ++i) {
-        const int s = i % kStages;
-        const uint32_t u = (uint32_t)(i / kStages);
-        if (!mbar_wait(smem_u32(&bars[kStages + s]), (u & 1u) ^ 1u, abort_flag)) {
+      int i = NR;
+      for (int k = rank + NR * C; k < ntiles; k += C, ++i) {
+        const int s = i % NR;
+        const uint32_t u = (uint32_t)(i / NR);
+        if (!mbar_wait(smem_u32(&bars[NS + s]), (u & 1u) ^ 1u, abort_flag)) {
           *abort_flag = 1;
           set_status(p.status, ATTN_DEV_TIMEOUT);
           break;
@@ -1373,7 +1382,7 @@ __global__ void __maxnreg__(Cfg<G>::kMaxRegs)
     __syncwarp();
   } else {
     // ----------------------------------------------------------- consumers --
-    ConsumerSync csync{smem_u32(&bars[2 * kStages]), abort_flag, p.status, 0u};
+    ConsumerSync csync{smem_u32(&bars[2 * NS]), abort_flag, p.status, 0u};
     if (MT) cs.set_last(pos - shift, p.S);
     // fused append: the warp whose keys include the last row of the last
     // tile, in the rank that takes that tile, writes the new rows
@@ -1383,8 +1392,8 @@ __global__ void __maxnreg__(Cfg<G>::kMaxRegs)
     cs.reset();
     int i = 0;
     for (int k = rank; k < ntiles; k += C, ++i) {
-      const int s = i % kStages;
-      if (!consumer_wait(smem_u32(&bars[s]), (uint32_t)(i / kStages) & 1u, abort_flag, p.status,
+      const int s = i % NR;
+      if (!consumer_wait(smem_u32(&bars[s]), (uint32_t)(i / NR) & 1u, abort_flag, p.status,
                          lane))
         break;
       if (R && i == 0) {  // the operand from the producer warp's rotated q
@@ -1399,7 +1408,7 @@ __global__ void __maxnreg__(Cfg<G>::kMaxRegs)
                          lane);
       cs.template tile<MT, R>(Ks, Ks + kTileBytes, rows, lo + k * kTile, warp);
       __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&bars[kStages + s]));  // the stage may be refilled
+      if (lane == 0) mbar_arrive(smem_u32(&bars[NS + s]));  // the stage may be refilled
     }
     // this CTA's warps' partials (max, sum, unnormalised o) merged below;
     // no tiles: (-inf, 0, 0)
