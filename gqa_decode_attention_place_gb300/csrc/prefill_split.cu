@@ -21,7 +21,7 @@
 //
 //  * warp 8, one thread: TMA (cp.async.bulk.tensor, 128-byte swizzle) loads
 //    the item's query tile and streams 128-key K and V tiles through a
-//    4-stage ring.
+//    6-stage ring.
 //  * warp 9 issues S_x = Q K_i^T (M = 128, N = 128, 4 x K16; fp32 in tensor
 //    memory); warp 10 issues O_x += P_x V_i (A = P from tensor memory, B = V
 //    from shared memory, N = 64).  Each runs its loop warp-uniformly and one
@@ -50,7 +50,7 @@ constexpr int kHD = 64;
 constexpr int kBM = 128;   // query rows per tile (MMA M)
 constexpr int kBN = 128;   // keys per tile (MMA N of QK^T, K of PV)
 constexpr int kLanes = 2;  // softmax warpgroups
-constexpr int kStages = 4; // K/V ring depth
+constexpr int kStages = 6; // K/V ring depth
 constexpr int kThreads = 384;  // 12 warps
 constexpr int kTmaWarp = 8;
 constexpr int kQKWarp = 9;     // S issuer; allocates tensor memory
