@@ -16,23 +16,29 @@
 // HD = 64, when pairs would leave SMs idle, the launch goes to
 // prefill_split.cu instead (one query tile per item, its keys split between
 // the two softmax warpgroups).
-//  * warp 0, one thread: TMA (cp.async.bulk.tensor, 128-byte swizzle) loads
+//  * warp 8, one thread: TMA (cp.async.bulk.tensor, 128-byte swizzle) loads
 //    the Q tile(s) once and streams 128-key K and V tiles through a ring of
 //    4 stages (d = 64) or 3 (d = 128).
-//  * warp 1, one thread: issues tcgen05.mma (bf16 in, fp32 accumulate in
+//  * warp 9, one thread: issues tcgen05.mma (bf16 in, fp32 accumulate in
 //    tensor memory) for S_A = Q_A K^T and S_B = Q_B K^T (128 TMEM columns
 //    each) per K/V tile; warp 10, one thread: O_A += P_A V and O_B += P_B V,
 //    with P read from tensor memory (64 columns of bf16 pairs per tile) and
 //    O kept in tensor memory for the whole key loop.  Two issuing threads
 //    took the 2048-token prefill from 28.9 to 24.9 us.  While one query
-//    tile's softmax runs, the tensor core works on the other tile.
-//  * warps 2-5 (tile A) and 6-9 (tile B), thread r owns query row r (TMEM
+//    tile's softmax runs, the tensor core works on the other tile.  Warp 11
+//    has no role.
+//  * warps 0-3 (tile A) and 4-7 (tile B), thread r owns query row r (TMEM
 //    lane quarter warp % 4): read the whole S row from TMEM into registers in
-//    one round trip, mask the causal diagonal, keep the online softmax in
-//    base 2, write P as bf16 pairs into tensor memory (tcgen05.st).  The
-//    running max is raised only when a row's max grows by more than 2^8
-//    (then O is rescaled in TMEM); otherwise P may reach 2^8, harmless in
-//    fp32 sums and bf16 P.
+//    one round trip, mask the causal diagonal, find the row's largest scaled
+//    score from the raw scores (their maximum, or their minimum for a
+//    negative scale: the sign is a template parameter), keep the online
+//    softmax in base 2 with one fused multiply-add per pair of exponents,
+//    write P as bf16 pairs into tensor memory (tcgen05.st).  The running max
+//    is raised only when a row's max grows by more than 2^8 (then O is
+//    rescaled in TMEM); otherwise P may reach 2^8, harmless in fp32 sums and
+//    bf16 P.  The softmax warpgroups take 208 registers per thread from the
+//    issue warpgroup (setmaxnreg), which keeps the raw-score form free of
+//    spills.
 //  Scores never leave the SM (no S or P in HBM).
 #include <cuda.h>
 
@@ -49,8 +55,14 @@ constexpr int kBM = 128;   // query rows per tile (MMA M)
 constexpr int kBN = 128;   // keys per tile (MMA N of QK^T, K of PV)
 constexpr int kQT = 2;     // query-tile slots per CTA (softmax warpgroups)
 constexpr int kMaxKVStages = 4;
-constexpr int kPThreads = 352;             // 11 warps
+constexpr int kPThreads = 384;             // 12 warps
+constexpr int kPTmaWarp = 8;               // TMA
+constexpr int kPQKWarp = 9;                // QK^T issuer; allocates tensor memory
 constexpr int kPVWarp = 10;                // the PV issuer
+constexpr int kPRegsSoftmax = 208;
+constexpr int kPRegsOther = 88;
+constexpr int kPRegSplitTotal = 4 * 32 * (2 * kPRegsSoftmax + kPRegsOther);
+static_assert(kPRegSplitTotal <= kPThreads * 168, "register split above the launch allocation");
 constexpr int kChunkBytes = kBM * 64 * 2;  // 16 KB: 128 rows x 128 bytes, one swizzle column block
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemP = 256;           // P of tile x at 256 + 64x (bf16 pairs)
@@ -115,7 +127,7 @@ __device__ __forceinline__ bool warp_wait_or_abort(uint32_t bar, uint32_t parity
   return __all_sync(0xffffffffu, wait_or_abort(bar, parity, abort_flag));
 }
 
-template <int HD>
+template <int HD, bool kPos>
 __global__ void __launch_bounds__(kPThreads, 1)
     prefill_tcgen05_kernel(const __grid_constant__ CUtensorMap tm_q,
                            const __grid_constant__ CUtensorMap tm_k,
@@ -177,7 +189,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
     *abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == 1) {
+  if (warp == kPQKWarp) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                      smem_u32(tmem_holder)),
                  "r"(kTmemCols)
@@ -206,8 +218,11 @@ __global__ void __launch_bounds__(kPThreads, 1)
 
   // Every mbarrier completes one phase per use; parities below come from
   // running counts kept across this CTA's items.
-  if (warp == 0) {
+  auto regs_down = [] { asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kPRegsOther)); };
+  auto regs_up = [] { asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kPRegsSoftmax)); };
+  if (warp == kPTmaWarp) {
     // ------------------------------------------------------ TMA producer --
+    regs_down();
     if (lane == 0) {
       uint32_t gk = 0;  // K/V tiles issued so far
       for (int r = 0; item_of(r) < n_items; ++r) {
@@ -236,8 +251,9 @@ __global__ void __launch_bounds__(kPThreads, 1)
         if (!ok) break;
       }
     }
-  } else if (warp == 1) {
+  } else if (warp == kPQKWarp) {
     // ----------------------------------------------- QK^T issuer (S_x) --
+    regs_down();
     if (lane == 0) {
       constexpr uint32_t idesc_qk = make_idesc(kBM, kBN, false);
       uint32_t gk = 0;             // K/V tiles consumed so far
@@ -284,6 +300,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
     // parallel.  P_x of tile j is written after S_x of tile j was read, so
     // the QK^T that read the stage's K is done once P_x is; the commit after
     // the tile's last PV therefore releases the whole stage.
+    regs_down();
     if (lane == 0) {
       // O (+)= P V at N = HD: V's HD/64 column blocks, kChunkBytes apart
       constexpr uint32_t idesc_pv = make_idesc(kBM, HD, true);
@@ -321,16 +338,21 @@ __global__ void __launch_bounds__(kPThreads, 1)
         gk = gk0 + it.n;
       }
     }
+  } else if (warp > kPVWarp) {
+    regs_down();  // warp 11: no role
   } else {
     // ------------------------------------------- softmax / epilogue (r) --
-    const int x = (warp - 2) >> 2;                      // query tile of this warpgroup
+    regs_up();
+    const int x = warp >> 2;                            // query tile of this warpgroup
     const int sub = warp & 3;                           // TMEM lane quarter
     const int r = sub * 32 + lane;                      // row within the tile
     const uint32_t lane_off = (uint32_t)(sub * 32) << 16;
     const uint32_t tm_S = tmem + 128 * x + lane_off;
     const uint32_t tm_O = tmem + kTmemO + HD * x + lane_off;
     const uint32_t tm_P = tmem + kTmemP + 64 * x + lane_off;
-    const float c = p.scale_log2;
+    const float c = p.scale_log2;  // non-zero (the host replaces 0 by a tiny value)
+    constexpr bool c_pos = kPos;    // the scale's sign, a launch choice
+    const float mask_raw = c_pos ? -INFINITY : INFINITY;  // times c: -inf
     uint32_t cs = 0;   // S_x consumed so far
     uint32_t cpv = 0;  // PV_x issued before this item
     bool ok = true;
@@ -364,24 +386,26 @@ __global__ void __launch_bounds__(kPThreads, 1)
         tc_fence_before();
         mbar_arrive(bar(kBarSFree + x));       // S_x may be overwritten
 
-        // scale (packed pairs) and mask; 8 independent running maxima
-        const f2 c2 = mk2(c, c);
-#pragma unroll
-        for (int j = 0; j < kBN; j += 2) {
-          const f2 t = mul2(mk2(sv[j], sv[j + 1]), c2);
-          brk2(t, sv[j], sv[j + 1]);
-        }
+        // The row's largest scaled score from the raw scores: their maximum
+        // when the scale is positive, their minimum when it is negative (8
+        // independent three-input chains), times c.  Masked keys (diagonal
+        // tiles only) take the raw value that neither can pick.
         if (diag) {
 #pragma unroll
-          for (int j = 0; j < kBN; ++j) sv[j] = (kbase + j > qpos) ? -INFINITY : sv[j];
+          for (int j = 0; j < kBN; ++j) sv[j] = (kbase + j > qpos) ? mask_raw : sv[j];
         }
         float mx8[8];
 #pragma unroll
         for (int a = 0; a < 8; ++a) mx8[a] = sv[a];
 #pragma unroll
-        for (int j = 8; j < kBN; ++j) mx8[j & 7] = fmaxf(mx8[j & 7], sv[j]);
-        const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                               fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+        for (int j = 8; j < kBN; j += 2)
+          mx8[(j >> 1) & 7] = c_pos ? fmax3(mx8[(j >> 1) & 7], sv[j], sv[j + 1])
+                                    : fmin3(mx8[(j >> 1) & 7], sv[j], sv[j + 1]);
+        const float mr = c_pos ? fmax3(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(mx8[3], mx8[4], mx8[5]),
+                                       fmaxf(mx8[6], mx8[7]))
+                               : fmin3(fmin3(mx8[0], mx8[1], mx8[2]), fmin3(mx8[3], mx8[4], mx8[5]),
+                                       fminf(mx8[6], mx8[7]));
+        const float mx = mr * c;
 
         // PV of tile i-1 done: O is stable and P_x may be overwritten
         if (i > 0 && !wait_pv(i - 1)) { ok = false; break; }
@@ -409,7 +433,9 @@ __global__ void __launch_bounds__(kPThreads, 1)
 
         // P = 2^(s*c - m) (exactly 0 where masked: 2^-inf) as bf16 pairs into
         // TMEM: column q of P holds keys 2q (low half) and 2q+1 (high half)
-        const f2 m2 = mk2(-m_run, -m_run);
+        const float m_use = m_run == -INFINITY ? 0.f : m_run;
+        const f2 c2 = mk2(c, c);
+        const f2 m2 = mk2(-m_use, -m_use);
         f2 rs2[4];
 #pragma unroll
         for (int a = 0; a < 4; ++a) rs2[a] = mk2(0.f, 0.f);
@@ -420,7 +446,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
           for (int q = 0; q < 32; ++q) {
             const int j = half * 64 + 2 * q;
             float lo, hi;
-            brk2(add2(mk2(sv[j], sv[j + 1]), m2), lo, hi);
+            brk2(fma2(mk2(sv[j], sv[j + 1]), c2, m2), lo, hi);
             lo = ex2(lo);
             hi = ex2(hi);
             rs2[q & 3] = add2(rs2[q & 3], mk2(lo, hi));
@@ -477,7 +503,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
     while (globaltimer_ns() - t_start < 2000000ull) {
     }
   }
-  if (warp == 1) {
+  if (warp == kPQKWarp) {
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
                  "r"(kTmemCols)
@@ -517,10 +543,17 @@ cudaError_t launch_prefill_hd(const CUtensorMap& mq, const CUtensorMap& mk, cons
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev >= 0 && dev < 64 && !configured[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(prefill_tcgen05_kernel<HD>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         L::kSmemBytes);
-    if (e != cudaSuccess) return e;
+    for (auto kern : {prefill_tcgen05_kernel<HD, true>, prefill_tcgen05_kernel<HD, false>}) {
+      cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           L::kSmemBytes);
+      if (e != cudaSuccess) return e;
+      // registers move between warpgroups (setmaxnreg): the launch
+      // allocation must cover the split
+      cudaFuncAttributes fa;
+      e = cudaFuncGetAttributes(&fa, kern);
+      if (e != cudaSuccess) return e;
+      if ((long long)fa.numRegs * kPThreads < kPRegSplitTotal) return cudaErrorInvalidConfiguration;
+    }
     configured[dev] = true;
   }
   int sms = 0;
@@ -540,7 +573,10 @@ cudaError_t launch_prefill_hd(const CUtensorMap& mq, const CUtensorMap& mk, cons
   const long long items = (long long)p.n_units * p.Hq;
   if (items > 0x7fffffffLL) return cudaErrorInvalidValue;
   const unsigned blocks = (unsigned)std::min<long long>(items, sms);  // one CTA per SM
-  prefill_tcgen05_kernel<HD><<<blocks, kPThreads, L::kSmemBytes, stream>>>(mq, mk, mv, p);
+  if (p.scale_log2 > 0.f)
+    prefill_tcgen05_kernel<HD, true><<<blocks, kPThreads, L::kSmemBytes, stream>>>(mq, mk, mv, p);
+  else
+    prefill_tcgen05_kernel<HD, false><<<blocks, kPThreads, L::kSmemBytes, stream>>>(mq, mk, mv, p);
   return cudaGetLastError();
 }
 
@@ -592,6 +628,7 @@ cudaError_t launch_prefill(const void* q, const void* k, const void* v, int S, i
   p.Hkv = Hkv;
   p.g = Hq / Hkv;
   p.scale_log2 = scale * 1.4426950408889634f;
+  if (p.scale_log2 == 0.f) p.scale_log2 = 1e-30f;  // 2^(s*c - m) then rounds to exactly 1
   p.tpi = 1;
   p.n_units = 0;
   return d == 128 ? launch_prefill_hd<128>(mq, mk, mv, p, stream)
