@@ -200,6 +200,11 @@ __global__ void __launch_bounds__(kPThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_holder;
+  // Launched with programmatic stream serialisation: the set-up above may
+  // run while the previous kernel on the stream finishes; q, k, v and out
+  // are touched only after this wait.
+  grid_dependency_wait();
+  grid_dependents_launch();
   // TMEM columns: S of tile x [128x, +128); P of tile x [256+64x, +64);
   // O of tile x [384+64x, +64)
   const uint32_t sQ = base + L::kOffQ;
@@ -573,11 +578,11 @@ cudaError_t launch_prefill_hd(const CUtensorMap& mq, const CUtensorMap& mk, cons
   const long long items = (long long)p.n_units * p.Hq;
   if (items > 0x7fffffffLL) return cudaErrorInvalidValue;
   const unsigned blocks = (unsigned)std::min<long long>(items, sms);  // one CTA per SM
-  if (p.scale_log2 > 0.f)
-    prefill_tcgen05_kernel<HD, true><<<blocks, kPThreads, L::kSmemBytes, stream>>>(mq, mk, mv, p);
-  else
-    prefill_tcgen05_kernel<HD, false><<<blocks, kPThreads, L::kSmemBytes, stream>>>(mq, mk, mv, p);
-  return cudaGetLastError();
+  // programmatic dependent launch: the set-up overlaps the previous kernel
+  auto kern =
+      p.scale_log2 > 0.f ? prefill_tcgen05_kernel<HD, true> : prefill_tcgen05_kernel<HD, false>;
+  return launch_pdl(kern, dim3(blocks), dim3(kPThreads), (size_t)L::kSmemBytes, stream, mq, mk, mv,
+                    p);
 }
 
 }  // namespace

@@ -187,6 +187,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_holder;
+  // Launched with programmatic stream serialisation: the set-up above may
+  // run while the previous kernel on the stream finishes; q, k, v and out
+  // are touched only after this wait.
+  grid_dependency_wait();
+  grid_dependents_launch();
   const uint32_t sQ = base + kOffQ;
 
   // Registers move from the issue warpgroup (warps 8-11) to the two softmax
@@ -549,11 +554,9 @@ cudaError_t launch_prefill_split(const CUtensorMap& mq, const CUtensorMap& mk,
   const long long items = (long long)p.n_qt * Hq;
   if (items > 0x7fffffffLL) return cudaErrorInvalidValue;
   const unsigned blocks = (unsigned)std::min<long long>(items, sms);  // one CTA per SM
-  if (p.scale_log2 > 0.f)
-    prefill_split_kernel<true><<<blocks, kThreads, kSmemBytes, stream>>>(mq, mk, mv, p);
-  else
-    prefill_split_kernel<false><<<blocks, kThreads, kSmemBytes, stream>>>(mq, mk, mv, p);
-  return cudaGetLastError();
+  // programmatic dependent launch: the set-up overlaps the previous kernel
+  auto kern = p.scale_log2 > 0.f ? prefill_split_kernel<true> : prefill_split_kernel<false>;
+  return launch_pdl(kern, dim3(blocks), dim3(kThreads), (size_t)kSmemBytes, stream, mq, mk, mv, p);
 }
 
 cudaError_t prefill_split_read_timeouts(uint32_t* count) {

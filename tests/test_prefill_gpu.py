@@ -3,9 +3,10 @@
 Covers both prefill workloads (512 new tokens over a 2048-token prefix; 2048
 tokens from scratch; 32 heads of d=64), query tiles and prefixes that are not
 multiples of the 128-row tile, a single new token, GQA head sharing and the
-empty problem; and the same kernel at d_head=128 (small cases against the
-full oracle, a 512-token GQA prompt chunk at the decode shapes, and one new
-token through both the prefill and the decode kernel).
+empty problem; a launch that reads the previous launch's output on the same
+stream; and the same kernel at d_head=128 (small cases against the full
+oracle, a 512-token GQA prompt chunk at the decode shapes, and one new token
+through both the prefill and the decode kernel).
 """
 
 import numpy as np
@@ -107,6 +108,29 @@ def test_pair_items_with_a_ragged_last_tile():
     rows += [(i, 7) for i in range(300)] + [(i, 159) for i in range(0, 300, 7)]
     rows += [(0, h) for h in range(160)] + [(299, h) for h in range(160)]
     _sampled_check(case, rows, "pair items, ragged last tile")
+
+
+@pytest.mark.parametrize("S,start_pos,Hq,Hkv,d", [
+    (256, 300, 4, 2, 64),    # one query tile per item: the split-keys kernel
+    (1024, 0, 40, 8, 64),    # pairs of query tiles per item
+    (256, 100, 8, 2, 128),   # head dim 128
+])
+def test_back_to_back_launches_read_the_previous_output(S, start_pos, Hq, Hkv, d):
+    """The prefill kernels may start while the previous kernel on the stream
+    drains (programmatic dependent launch) and touch q, k, v and out only
+    after it is done: a second prefill whose queries are the first one's
+    output, queued without a synchronisation, sees all of that output."""
+    case = synth.prefill_case(S=S, start_pos=start_pos, Hq=Hq, Hkv=Hkv, d=d, seed=S + d,
+                              device="cuda")
+    out1 = ga.attn_prefill_causal(case.q, case.k, case.v, start_pos, case.scale)
+    out2 = ga.attn_prefill_causal(out1, case.k, case.v, start_pos, case.scale)
+    assert ga.attn_read_prefill_status() == 0
+    rng = np.random.default_rng(S + d)
+    rows = [(int(i), int(h)) for i, h in zip(rng.integers(0, S, 300), rng.integers(0, Hq, 300))]
+    rows += [(0, h) for h in range(Hq)] + [(S - 1, h) for h in range(Hq)]
+    want = oracle.prefill_rows(f64(out1), f64(case.k), f64(case.v), start_pos, case.scale, rows)
+    got = np.stack([f64(out2[i, h]) for i, h in rows])
+    assert_attn_close(got, want, f"chained S={S} d={d}")
 
 
 @pytest.mark.parametrize("d", [64, 128])
