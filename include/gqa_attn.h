@@ -50,7 +50,7 @@ extern "C" {
 #define ATTN_OK                0
 #define ATTN_ERR_INVALID_ARG   1  /* null pointer, non-positive size, Hq % Hkv != 0,
                                      pointer not 16-byte aligned, start_pos < 0 */
-#define ATTN_ERR_UNSUPPORTED   2  /* a size this build has no kernel for (see each call) */
+#define ATTN_ERR_UNSUPPORTED   2  /* a size the library has no kernel for (see each call) */
 #define ATTN_ERR_WORKSPACE     3  /* workspace null or smaller than attn_decode_workspace_size() */
 #define ATTN_ERR_CUDA          4  /* a CUDA runtime call or launch failed */
 #define ATTN_ERR_DEVICE        5  /* attn_read_device_status: the device flagged a fault */
